@@ -1,0 +1,129 @@
+"""Pins for the oracle's counter RNG and stochastic rounding (CPU only).
+
+Philox4x32-10 is checked against cuRAND's host-side Philox generator (a
+library routine: its block j of four outputs is Philox at counter (0,0,j,0)
+under key = seed), and statistically.  Stochastic rounding is checked against
+the fp4-train card's printed result for 2.3.
+"""
+import ctypes
+import ctypes.util
+import glob
+import os
+
+import numpy as np
+import pytest
+from scipy import stats
+
+import oracle as ora
+from golden_util import load
+
+
+def _curand():
+    cands = glob.glob("/usr/local/cuda/lib64/libcurand.so*")
+    name = ctypes.util.find_library("curand")
+    if name:
+        cands.append(name)
+    for c in cands:
+        try:
+            return ctypes.CDLL(c)
+        except OSError:
+            continue
+    return None
+
+
+def _curand_philox_host(seed: int, n: int) -> np.ndarray:
+    L = _curand()
+    if L is None:
+        pytest.skip("libcurand not available")
+    gen = ctypes.c_void_p()
+    PHILOX4_32_10 = 161  # curandRngType_t value for CURAND_RNG_PSEUDO_PHILOX4_32_10
+    rc = L.curandCreateGeneratorHost(ctypes.byref(gen), PHILOX4_32_10)
+    if rc != 0:
+        pytest.skip(f"curandCreateGeneratorHost failed ({rc})")
+    try:
+        assert L.curandSetPseudoRandomGeneratorSeed(gen, ctypes.c_ulonglong(seed)) == 0
+        out = np.empty(n, np.uint32)
+        assert L.curandGenerate(gen, out.ctypes.data_as(ctypes.c_void_p), ctypes.c_size_t(n)) == 0
+    finally:
+        L.curandDestroyGenerator(gen)
+    return out
+
+
+@pytest.mark.parametrize("seed", [0, 1, 0x123456789ABCDEF, 2 ** 64 - 1])
+def test_philox_matches_curand_host(seed):
+    n = 4 * 256
+    ref = _curand_philox_host(seed, n).reshape(-1, 4)
+    key = [seed & 0xFFFFFFFF, seed >> 32]
+    for j in range(ref.shape[0]):
+        got = ora.philox4x32_10([0, 0, j, 0], key)
+        assert np.array_equal(got, ref[j]), (j, got, ref[j])
+
+
+def test_rng_word_layout():
+    # element g draws word g & 3 of Philox(counter = (g>>2, step), key = seed)
+    seed, step = 0xDEADBEEF12345678, (7 << 32) | 3
+    g = np.array([0, 1, 2, 3, 4, 5, (1 << 33) + 2], np.uint64)
+    words = ora.rng_words(seed, step, g)
+    key = [seed & 0xFFFFFFFF, seed >> 32]
+    for gi, w in zip(g.tolist(), words.tolist()):
+        q = gi >> 2
+        blk = ora.philox4x32_10([q & 0xFFFFFFFF, q >> 32, step & 0xFFFFFFFF, step >> 32], key)
+        assert w == int(blk[gi & 3])
+
+
+def test_philox_uniformity_chi_square():
+    g = np.arange(1 << 18, dtype=np.uint64)
+    w = ora.rng_words(0, 0, g)
+    top = (w >> 24).astype(np.int64)          # 256 bins of the top byte
+    counts = np.bincount(top, minlength=256)
+    chi2, p = stats.chisquare(counts)
+    assert p > 1e-4, (chi2, p)
+    bits = np.unpackbits(w.view(np.uint8)).reshape(-1, 32).mean(axis=0)
+    assert np.all(np.abs(bits - 0.5) < 0.01)
+    # different steps give unrelated streams
+    w2 = ora.rng_words(0, 1, g)
+    assert np.mean(w == w2) < 1e-3
+
+
+def test_sr_grid_points_are_fixed_and_neighbours_only():
+    grid = ora.e2m1_value(np.arange(8)).astype(np.float32)
+    rng = np.random.default_rng(5)
+    words = rng.integers(0, 2 ** 32, 1000, dtype=np.uint64).astype(np.uint32)
+    for v in grid:
+        codes = ora.e2m1_sr(np.full(1000, v, np.float32), words)
+        assert np.all(ora.e2m1_value(codes) == v)
+    xs = rng.uniform(-6, 6, 20000).astype(np.float32)
+    w = rng.integers(0, 2 ** 32, xs.size, dtype=np.uint64).astype(np.uint32)
+    q = ora.e2m1_value(ora.e2m1_sr(xs, w))
+    pos = np.sort(grid)
+    lo = pos[np.searchsorted(pos, np.abs(xs), side="right") - 1]
+    hi = pos[np.minimum(np.searchsorted(pos, np.abs(xs), side="right"), 7)]
+    assert np.all((np.abs(q) == lo) | (np.abs(q) == hi))
+    assert np.all(np.sign(q)[q != 0] == np.sign(xs)[q != 0])
+    # saturation
+    assert np.all(ora.e2m1_value(ora.e2m1_sr(np.float32([6.5, -9.0]), 0)) == [6.0, -6.0])
+
+
+def test_sr_mean_of_2_3_matches_page():
+    """fp4-train "Correctness": the SR mean of 2.3 is 2.300 while RTN gives
+    2.000.  Block [6.0, 2.3 x 15] under tensor scale 1 has block scale 1, so
+    the quantized 2.3 is 2 or 3.  Over M draws the mean lies within 4 sigma."""
+    g = load("fp4train_correctness.txt")
+    x = float(g["value"][0])
+    nblocks = 70000
+    v = np.full((nblocks, 16), x, np.float32)
+    v[:, 0] = 6.0
+    draws = []
+    for step in range(3):
+        packed, scales, q = ora.nvfp4_blocks(v, 0, 1.0, rounding=ora.SR, seed=11, step=step)
+        assert np.all(scales == 0x38)             # e4m3 1.0
+        q = q.reshape(nblocks, 16)[:, 1:]
+        assert set(np.unique(q)) <= {2.0, 3.0}
+        draws.append(q.ravel())
+    d = np.concatenate(draws)
+    M = d.size
+    sigma = np.sqrt(0.3 * 0.7)
+    assert abs(d.mean() - x) < 4 * sigma / np.sqrt(M)
+    assert round(float(d.mean()), 2) == round(float(g["sr_mean"][0]), 2)
+    _, _, q_rtn = ora.nvfp4_blocks(v[:1], 0, 1.0, rounding=ora.RTN)
+    assert np.all(q_rtn[1:] == float(g["rtn"][0]))
