@@ -1,1 +1,16 @@
-"""Block-scaled FP4 (E2M1) codec for GB300 (sm_103a)."""
+"""Block-scaled FP4 (E2M1) codec for GB300 (sm_103a).
+
+The compute path is the CUDA library ``libfp4codec.so`` (C ABI in
+include/fp4codec.h); this package is its Python binding.  Importing the
+package does not load the library; the first call does, and raises if it has
+not been built (there is no CPU fallback).
+"""
+from .codec import (Segments, fp4_seg_scale_offsets, fp4_to_fp8_col, fp4_to_fp8_row,
+                    fp4quant_decode, fp4quant_encode, kernel_launches, mxfp4_quantize,
+                    nvfp4_amax, nvfp4_dequantize, nvfp4_qdq, nvfp4_qdq_amax, nvfp4_quantize)
+
+__all__ = [
+    "Segments", "fp4_seg_scale_offsets", "fp4_to_fp8_col", "fp4_to_fp8_row", "fp4quant_decode",
+    "fp4quant_encode", "kernel_launches", "mxfp4_quantize", "nvfp4_amax", "nvfp4_dequantize",
+    "nvfp4_qdq", "nvfp4_qdq_amax", "nvfp4_quantize",
+]

@@ -1,0 +1,183 @@
+// common.cuh -- device helpers shared by the codec kernels (sm_103a).
+//
+// All arithmetic that decides a code is written with explicit round-to-
+// nearest intrinsics (__fmul_rn, __fadd_rn, __fdiv_rn, __frcp_rn, __fsqrt_rn)
+// and the library is built with -fmad=false, so no multiply-add is ever
+// contracted: each operation is one correctly rounded fp32 operation.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fp4codec.h"
+
+namespace fp4 {
+
+// ------------------------------------------------------------ memory access
+
+struct U32x8 {
+  uint32_t w[8];
+};
+
+// 256-bit read-only load that does not allocate in L1 (streamed input).
+__device__ __forceinline__ U32x8 ld_stream_v8(const void* p) {
+  U32x8 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]), "=r"(r.w[4]),
+                 "=r"(r.w[5]), "=r"(r.w[6]), "=r"(r.w[7])
+               : "l"(p));
+  return r;
+}
+
+// 256-bit load of data this kernel may also write (no .nc).
+__device__ __forceinline__ U32x8 ld_v8(const void* p) {
+  U32x8 r;
+  asm volatile("ld.global.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]), "=r"(r.w[4]),
+                 "=r"(r.w[5]), "=r"(r.w[6]), "=r"(r.w[7])
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ void st_v8(void* p, const U32x8& v) {
+  asm volatile("st.global.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v.w[0]),
+               "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]),
+               "r"(v.w[7])
+               : "memory");
+}
+
+__device__ __forceinline__ uint2 ld_stream_v2(const void* p) {
+  uint2 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+               : "=r"(r.x), "=r"(r.y)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
+  uint32_t r;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t ld_stream_u8(const void* p) {
+  uint32_t r;
+  asm volatile("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+
+// ------------------------------------------------------------ bf16 <-> f32
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Two floats to a bf16 pair, round to nearest-even; lo in bits 15:0.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// --------------------------------------------------------------------- E2M1
+
+// Round-to-nearest-even, saturating E2M1 encode of two floats; lo -> bits 3:0.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+      "cvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Exact value of the E2M1 code in bits 3:0 of c: sign to bit 31, the three
+// magnitude bits to bits 24:22 of a binary32 pattern, which reads as
+// value * 2^-126 (a subnormal for 0.5); one exact multiply by 2^126 restores
+// the value.
+__device__ __forceinline__ float e2m1_value(uint32_t c) {
+  uint32_t bits = ((c & 8u) << 28) | ((c & 7u) << 22);
+  return __fmul_rn(__uint_as_float(bits), 0x1p126f);
+}
+
+// --------------------------------------------------------------------- E4M3
+
+// Round-to-nearest-even, saturating E4M3 (OCP E4M3FN) encode of one float.
+__device__ __forceinline__ uint32_t cvt_e4m3(float x) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(x));
+  return (uint32_t)(r & 0xFFu);
+}
+
+// Exact value of an E4M3FN byte (through f16, which holds every E4M3 value).
+__device__ __forceinline__ float e4m3_value(uint32_t b) {
+  uint32_t h2;
+  uint16_t in = (uint16_t)(b & 0xFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+  uint16_t h = (uint16_t)(h2 & 0xFFFFu);
+  float f;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(h));
+  return f;
+}
+
+// --------------------------------------------------------------- Philox4x32
+
+// Philox4x32 with 10 rounds (Salmon, Moraes, Dror, Shaw, SC'11): per round
+// the products of counter words 0 and 2 with the two multipliers are split
+// into high and low halves; the high halves are XORed with counter words 1
+// and 3 and the key; the key advances by the two Weyl increments.
+struct Philox4 {
+  uint32_t x, y, z, w;
+};
+
+__device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2,
+                                                  uint32_t c3, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t m0 = 0xD2511F53u, m1 = 0xCD9E8D57u;
+    uint32_t hi0 = __umulhi(m0, c0), lo0 = m0 * c0;
+    uint32_t hi1 = __umulhi(m1, c2), lo1 = m1 * c2;
+    uint32_t n0 = hi1 ^ c1 ^ k0;
+    uint32_t n2 = hi0 ^ c3 ^ k1;
+    c0 = n0;
+    c1 = lo1;
+    c2 = n2;
+    c3 = lo0;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return Philox4{c0, c1, c2, c3};
+}
+
+// Stochastic E2M1 encode of a with the 32-bit random word rw: between grid
+// neighbours lo <= |a| < hi the upper one is taken iff
+// (rw >> 8) * 2^-24 < (|a| - lo) / (hi - lo); |a| >= 6 gives 6.
+__device__ __forceinline__ uint32_t e2m1_sr(float a, uint32_t rw) {
+  uint32_t sign = (__float_as_uint(a) >> 28) & 8u;
+  float m = fabsf(a);
+  if (!(m < 6.0f)) return (m >= 6.0f) ? (sign | 7u) : 0u;  // NaN -> 0
+  uint32_t c = (uint32_t)(m >= 0.5f) + (uint32_t)(m >= 1.0f) + (uint32_t)(m >= 1.5f) +
+               (uint32_t)(m >= 2.0f) + (uint32_t)(m >= 3.0f) + (uint32_t)(m >= 4.0f);
+  float lo = e2m1_value(c);
+  // 1 / (hi - lo): 2 below 2, 1 in [2, 4), 0.5 in [4, 6)
+  float k = __uint_as_float((128u - (uint32_t)(c >= 4u) - (uint32_t)(c >= 6u)) << 23);
+  float frac = __fmul_rn(__fsub_rn(m, lo), k);
+  float u = __fmul_rn((float)(rw >> 8), 0x1p-24f);
+  return sign | (c + (uint32_t)(u < frac));
+}
+
+// ------------------------------------------------------------- reductions
+
+__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
+  return __reduce_max_sync(0xFFFFFFFFu, v);
+}
+
+}  // namespace fp4

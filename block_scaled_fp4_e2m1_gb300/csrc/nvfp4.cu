@@ -1,0 +1,487 @@
+// nvfp4.cu -- NVFP4 tensor amax, quantize (RTN / stochastic, optional error
+// feedback), dequantize, and the fused training-step qdq.
+//
+// [fp4-train] "How it works": 16-element blocks, scale block_absmax / 6
+// encoded to e4m3, every element divided by the decoded scale and encoded to
+// E2M1 by round-to-nearest or by stochastic rounding from a counter-based
+// (seed, step, global index) RNG, optional per-element error-feedback
+// residual.  [WP2] "Block scaling": one fp32 scale per tensor besides the
+// block scales (chosen as amax / (6 * 448)).
+//
+// Layout: one thread owns one 16-element block per grid-stride step: 32 B
+// of bf16 (one 256-bit load) or 64 B of fp32 (two), 8 B of packed codes and
+// 1 B of scale.  A warp's loads cover 1 or 2 KB of contiguous input, every
+// 256-bit load one full 32-byte sector.  HBM-bound; no shared memory.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "host_common.h"
+
+namespace fp4 {
+namespace {
+
+constexpr int kThreads = 256;
+
+// A tensor scale that is not finite or not > 0 is used as 1.
+__device__ __forceinline__ float sanitize_scale(float s) {
+  return (s > 0.0f && s <= 3.40282347e38f) ? s : 1.0f;
+}
+
+__device__ __forceinline__ float tensor_scale_from_amax(float amax) {
+  return sanitize_scale(__fdiv_rn(amax, 2688.0f));  // 6 * 448
+}
+
+template <bool kBF16>
+__device__ __forceinline__ void load_block(const void* x, int64_t b, float v[16]) {
+  if (kBF16) {
+    U32x8 r = ld_stream_v8(static_cast<const uint16_t*>(x) + 16 * b);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[2 * i] = bf16_lo(r.w[i]);
+      v[2 * i + 1] = bf16_hi(r.w[i]);
+    }
+  } else {
+    const float* p = static_cast<const float*>(x) + 16 * b;
+    U32x8 a = ld_stream_v8(p), c = ld_stream_v8(p + 8);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[i] = __uint_as_float(a.w[i]);
+      v[8 + i] = __uint_as_float(c.w[i]);
+    }
+  }
+}
+
+__device__ __forceinline__ void load_f32x16(const float* p, float v[16]) {
+  U32x8 a = ld_v8(p), c = ld_v8(p + 8);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    v[i] = __uint_as_float(a.w[i]);
+    v[8 + i] = __uint_as_float(c.w[i]);
+  }
+}
+
+__device__ __forceinline__ void load_f32x16_stream(const float* p, float v[16]) {
+  U32x8 a = ld_stream_v8(p), c = ld_stream_v8(p + 8);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    v[i] = __uint_as_float(a.w[i]);
+    v[8 + i] = __uint_as_float(c.w[i]);
+  }
+}
+
+__device__ __forceinline__ void store_f32x16(float* p, const float v[16]) {
+  U32x8 a, c;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    a.w[i] = __float_as_uint(v[i]);
+    c.w[i] = __float_as_uint(v[8 + i]);
+  }
+  st_v8(p, a);
+  st_v8(p + 8, c);
+}
+
+// Block-level max of non-negative floats into *out (atomic, order-free).
+__device__ __forceinline__ void block_max_to(float m, float* out) {
+  __shared__ uint32_t warp_max[kThreads / 32];
+  uint32_t u = warp_max_u32(__float_as_uint(m));
+  int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) warp_max[warp] = u;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t w = lane < kThreads / 32 ? warp_max[lane] : 0u;
+    w = warp_max_u32(w);
+    if (lane == 0 && w != 0u) atomicMax(reinterpret_cast<unsigned int*>(out), w);
+  }
+}
+
+// Quantize one block v[16] (residual already added) under tensor scale s_t.
+// Writes the 8 packed bytes as two words, returns the e4m3 scale byte, and
+// (kEF) leaves the dequantized values in q[16].
+template <bool kSR, bool kEF>
+__device__ __forceinline__ uint32_t quantize_block(const float v[16], float s_t, float den6,
+                                                   uint64_t g0, uint32_t key0, uint32_t key1,
+                                                   uint32_t step0, uint32_t step1, uint2& out,
+                                                   float q[16]) {
+  float bmax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(v[i]));
+  uint32_t sb = cvt_e4m3(__fdiv_rn(bmax, den6));
+  float eff = __fmul_rn(e4m3_value(sb), s_t);
+  float a[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) a[i] = (eff == 0.0f) ? __fmul_rn(v[i], 0.0f) : __fdiv_rn(v[i], eff);
+  uint32_t codes[16];
+  if (kSR) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint64_t quad = (g0 >> 2) + (uint64_t)k;
+      Philox4 r = philox4x32_10((uint32_t)quad, (uint32_t)(quad >> 32), step0, step1, key0, key1);
+      codes[4 * k + 0] = e2m1_sr(a[4 * k + 0], r.x);
+      codes[4 * k + 1] = e2m1_sr(a[4 * k + 1], r.y);
+      codes[4 * k + 2] = e2m1_sr(a[4 * k + 2], r.z);
+      codes[4 * k + 3] = e2m1_sr(a[4 * k + 3], r.w);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      uint32_t byte = cvt_e2m1x2(a[2 * i], a[2 * i + 1]);
+      codes[2 * i] = byte & 0xFu;
+      codes[2 * i + 1] = byte >> 4;
+    }
+  }
+  uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w0 |= codes[i] << (4 * i);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w1 |= codes[8 + i] << (4 * i);
+  out = make_uint2(w0, w1);
+  if (kEF) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) q[i] = __fmul_rn(e2m1_value(codes[i]), eff);
+  }
+  return sb;
+}
+
+template <bool kBF16, bool kRes>
+__global__ void __launch_bounds__(kThreads)
+    amax_kernel(const void* __restrict__ x, const float* __restrict__ residual, int64_t nblocks,
+                float* __restrict__ amax_ws) {
+  float m = 0.0f;
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  for (int64_t b = (int64_t)blockIdx.x * kThreads + threadIdx.x; b < nblocks; b += stride) {
+    float v[16];
+    load_block<kBF16>(x, b, v);
+    if (kRes) {
+      float r[16];
+      load_f32x16_stream(residual + 16 * b, r);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = __fadd_rn(v[i], r[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
+  }
+  block_max_to(m, amax_ws);
+}
+
+template <bool kBF16, bool kSR, bool kRes>
+__global__ void __launch_bounds__(kThreads)
+    quantize_kernel(const void* __restrict__ x, float* __restrict__ residual, int64_t nblocks,
+                    uint64_t seed, uint64_t step, int tscale_mode, float* __restrict__ tensor_scale,
+                    const float* __restrict__ amax_ws, uint8_t* __restrict__ packed,
+                    uint8_t* __restrict__ scales) {
+  float s_t;
+  if (tscale_mode == FP4_TSCALE_GIVEN) {
+    s_t = sanitize_scale(*tensor_scale);
+  } else {
+    s_t = tensor_scale_from_amax(*amax_ws);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *tensor_scale = s_t;
+  }
+  const float den6 = __fmul_rn(6.0f, s_t);
+  const uint32_t key0 = (uint32_t)seed, key1 = (uint32_t)(seed >> 32);
+  const uint32_t st0 = (uint32_t)step, st1 = (uint32_t)(step >> 32);
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  for (int64_t b = (int64_t)blockIdx.x * kThreads + threadIdx.x; b < nblocks; b += stride) {
+    float v[16], r[16], q[16];
+    load_block<kBF16>(x, b, v);
+    if (kRes) {
+      load_f32x16(residual + 16 * b, r);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = __fadd_rn(v[i], r[i]);
+    }
+    uint2 out;
+    uint32_t sb = quantize_block<kSR, kRes>(v, s_t, den6, (uint64_t)(16 * b), key0, key1, st0, st1,
+                                            out, q);
+    *reinterpret_cast<uint2*>(packed + 8 * b) = out;
+    scales[b] = (uint8_t)sb;
+    if (kRes) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) r[i] = __fsub_rn(v[i], q[i]);
+      store_f32x16(residual + 16 * b, r);
+    }
+  }
+}
+
+template <bool kBF16Out>
+__global__ void __launch_bounds__(kThreads)
+    dequantize_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ scales,
+                      const float* __restrict__ tensor_scale, int64_t nblocks, void* __restrict__ y) {
+  const float s_t = tensor_scale ? sanitize_scale(*tensor_scale) : 1.0f;
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  for (int64_t b = (int64_t)blockIdx.x * kThreads + threadIdx.x; b < nblocks; b += stride) {
+    uint2 p = ld_stream_v2(packed + 8 * b);
+    uint32_t sb = ld_stream_u8(scales + b);
+    float eff = __fmul_rn(e4m3_value(sb), s_t);
+    float o[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = __fmul_rn(e2m1_value(p.x >> (4 * i)), eff);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[8 + i] = __fmul_rn(e2m1_value(p.y >> (4 * i)), eff);
+    if (kBF16Out) {
+      U32x8 w;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w.w[i] = pack_bf16x2(o[2 * i], o[2 * i + 1]);
+      st_v8(static_cast<uint16_t*>(y) + 16 * b, w);
+    } else {
+      store_f32x16(static_cast<float*>(y) + 16 * b, o);
+    }
+  }
+}
+
+// v = ((W - lr*G) + r), each step one fp32 operation.
+template <bool kG, bool kRes>
+__device__ __forceinline__ void qdq_update(const uint16_t* w, const float* g, float lr,
+                                           const float* residual, int64_t b, float v[16],
+                                           float r[16], bool stream_res) {
+  U32x8 wr = ld_v8(w + 16 * b);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    v[2 * i] = bf16_lo(wr.w[i]);
+    v[2 * i + 1] = bf16_hi(wr.w[i]);
+  }
+  if (kG) {
+    float gg[16];
+    load_f32x16_stream(g + 16 * b, gg);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __fsub_rn(v[i], __fmul_rn(lr, gg[i]));
+  }
+  if (kRes) {
+    if (stream_res)
+      load_f32x16_stream(residual + 16 * b, r);
+    else
+      load_f32x16(residual + 16 * b, r);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __fadd_rn(v[i], r[i]);
+  }
+}
+
+template <bool kG, bool kRes>
+__global__ void __launch_bounds__(kThreads)
+    qdq_amax_kernel(const uint16_t* __restrict__ w, const float* __restrict__ g, float lr,
+                    const float* __restrict__ residual, int64_t nblocks, float* __restrict__ amax_ws) {
+  float m = 0.0f;
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  for (int64_t b = (int64_t)blockIdx.x * kThreads + threadIdx.x; b < nblocks; b += stride) {
+    float v[16], r[16];
+    qdq_update<kG, kRes>(w, g, lr, residual, b, v, r, true);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
+  }
+  block_max_to(m, amax_ws);
+}
+
+template <bool kG, bool kRes, bool kSR, bool kPacked>
+__global__ void __launch_bounds__(kThreads)
+    qdq_kernel(uint16_t* __restrict__ w, const float* __restrict__ g, float lr,
+               float* __restrict__ residual, int64_t nblocks, uint64_t seed, uint64_t step,
+               int tscale_mode, float* __restrict__ tensor_scale, const float* __restrict__ amax_ws,
+               uint8_t* __restrict__ packed, uint8_t* __restrict__ scales) {
+  float s_t;
+  if (tscale_mode == FP4_TSCALE_GIVEN) {
+    s_t = sanitize_scale(*tensor_scale);
+  } else {
+    s_t = tensor_scale_from_amax(*amax_ws);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *tensor_scale = s_t;
+  }
+  const float den6 = __fmul_rn(6.0f, s_t);
+  const uint32_t key0 = (uint32_t)seed, key1 = (uint32_t)(seed >> 32);
+  const uint32_t st0 = (uint32_t)step, st1 = (uint32_t)(step >> 32);
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  for (int64_t b = (int64_t)blockIdx.x * kThreads + threadIdx.x; b < nblocks; b += stride) {
+    float v[16], r[16], q[16];
+    qdq_update<kG, kRes>(w, g, lr, residual, b, v, r, false);
+    uint2 out;
+    uint32_t sb = quantize_block<kSR, true>(v, s_t, den6, (uint64_t)(16 * b), key0, key1, st0, st1,
+                                            out, q);
+    if (kPacked) {
+      *reinterpret_cast<uint2*>(packed + 8 * b) = out;
+      scales[b] = (uint8_t)sb;
+    }
+    U32x8 wo;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) wo.w[i] = pack_bf16x2(q[2 * i], q[2 * i + 1]);
+    st_v8(w + 16 * b, wo);
+    if (kRes) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) r[i] = __fsub_rn(v[i], q[i]);
+      store_f32x16(residual + 16 * b, r);
+    }
+  }
+}
+
+fp4_status launch_amax(const void* x, int dtype, int64_t n, const float* residual, float* amax_ws,
+                       cudaStream_t s) {
+  if (cudaMemsetAsync(amax_ws, 0, sizeof(float), s) != cudaSuccess) return FP4_ERR_CUDA;
+  const int64_t nb = n / 16;
+  if (nb == 0) return FP4_OK;
+  if (dtype == FP4_BF16) {
+    if (residual) return launch<amax_kernel<true, true>>(nb, kThreads, 0, s, x, residual, nb, amax_ws);
+    return launch<amax_kernel<true, false>>(nb, kThreads, 0, s, x, residual, nb, amax_ws);
+  }
+  if (residual) return launch<amax_kernel<false, true>>(nb, kThreads, 0, s, x, residual, nb, amax_ws);
+  return launch<amax_kernel<false, false>>(nb, kThreads, 0, s, x, residual, nb, amax_ws);
+}
+
+template <bool kBF16, bool kSR, bool kRes>
+fp4_status launch_quantize_k(const void* x, int64_t nb, float* residual, uint64_t seed, uint64_t step,
+                             int mode, float* ts, const float* amax, uint8_t* packed, uint8_t* scales,
+                             cudaStream_t s) {
+  return launch<quantize_kernel<kBF16, kSR, kRes>>(nb, kThreads, 0, s, x, residual, nb, seed, step,
+                                                   mode, ts, amax, packed, scales);
+}
+
+template <bool kBF16>
+fp4_status launch_quantize_t(const void* x, int64_t nb, float* residual, int rounding, uint64_t seed,
+                             uint64_t step, int mode, float* ts, const float* amax, uint8_t* packed,
+                             uint8_t* scales, cudaStream_t s) {
+  if (rounding == FP4_SR) {
+    if (residual)
+      return launch_quantize_k<kBF16, true, true>(x, nb, residual, seed, step, mode, ts, amax, packed, scales, s);
+    return launch_quantize_k<kBF16, true, false>(x, nb, residual, seed, step, mode, ts, amax, packed, scales, s);
+  }
+  if (residual)
+    return launch_quantize_k<kBF16, false, true>(x, nb, residual, seed, step, mode, ts, amax, packed, scales, s);
+  return launch_quantize_k<kBF16, false, false>(x, nb, residual, seed, step, mode, ts, amax, packed, scales, s);
+}
+
+template <bool kG, bool kRes, bool kSR, bool kPacked>
+fp4_status launch_qdq_k(uint16_t* w, const float* g, float lr, float* r, int64_t nb, uint64_t seed,
+                        uint64_t step, int mode, float* ts, const float* amax, uint8_t* packed,
+                        uint8_t* scales, cudaStream_t s) {
+  return launch<qdq_kernel<kG, kRes, kSR, kPacked>>(nb, kThreads, 0, s, w, g, lr, r, nb, seed, step,
+                                                    mode, ts, amax, packed, scales);
+}
+
+template <bool kG, bool kRes>
+fp4_status launch_qdq_t(uint16_t* w, const float* g, float lr, float* r, int64_t nb, int rounding,
+                        uint64_t seed, uint64_t step, int mode, float* ts, const float* amax,
+                        uint8_t* packed, uint8_t* scales, cudaStream_t s) {
+  const bool pk = packed != nullptr;
+  if (rounding == FP4_SR) {
+    if (pk) return launch_qdq_k<kG, kRes, true, true>(w, g, lr, r, nb, seed, step, mode, ts, amax, packed, scales, s);
+    return launch_qdq_k<kG, kRes, true, false>(w, g, lr, r, nb, seed, step, mode, ts, amax, packed, scales, s);
+  }
+  if (pk) return launch_qdq_k<kG, kRes, false, true>(w, g, lr, r, nb, seed, step, mode, ts, amax, packed, scales, s);
+  return launch_qdq_k<kG, kRes, false, false>(w, g, lr, r, nb, seed, step, mode, ts, amax, packed, scales, s);
+}
+
+fp4_status launch_qdq_amax(const uint16_t* w, const float* g, float lr, const float* r, int64_t n,
+                           float* amax_ws, cudaStream_t s) {
+  if (cudaMemsetAsync(amax_ws, 0, sizeof(float), s) != cudaSuccess) return FP4_ERR_CUDA;
+  const int64_t nb = n / 16;
+  if (nb == 0) return FP4_OK;
+  if (g) {
+    if (r) return launch<qdq_amax_kernel<true, true>>(nb, kThreads, 0, s, w, g, lr, r, nb, amax_ws);
+    return launch<qdq_amax_kernel<true, false>>(nb, kThreads, 0, s, w, g, lr, r, nb, amax_ws);
+  }
+  if (r) return launch<qdq_amax_kernel<false, true>>(nb, kThreads, 0, s, w, g, lr, r, nb, amax_ws);
+  return launch<qdq_amax_kernel<false, false>>(nb, kThreads, 0, s, w, g, lr, r, nb, amax_ws);
+}
+
+bool mode_ok(int m) {
+  return m == FP4_TSCALE_GIVEN || m == FP4_TSCALE_COMPUTE || m == FP4_TSCALE_FROM_AMAX;
+}
+
+}  // namespace
+}  // namespace fp4
+
+using namespace fp4;
+
+extern "C" {
+
+fp4_status nvfp4_amax(const void* x, int dtype, int64_t n, const float* residual, float* amax_ws,
+                      void* stream) {
+  if (!dtype_ok(dtype)) return FP4_ERR_DTYPE;
+  if (n < 0 || n % 16 != 0) return FP4_ERR_SHAPE;
+  if (!amax_ws || (n > 0 && !x)) return FP4_ERR_NULL;
+  if (!aligned(x, 32) || !aligned(residual, 32) || !aligned(amax_ws, 4)) return FP4_ERR_ALIGN;
+  return launch_amax(x, dtype, n, residual, amax_ws, as_stream(stream));
+}
+
+fp4_status nvfp4_quantize(const void* x, int dtype, int64_t n, float* residual, int rounding,
+                          uint64_t seed, uint64_t step, int tscale_mode, float* tensor_scale,
+                          float* amax_ws, uint8_t* packed, uint8_t* scales, void* stream) {
+  if (!dtype_ok(dtype)) return FP4_ERR_DTYPE;
+  if (rounding != FP4_RTN && rounding != FP4_SR) return FP4_ERR_ARG;
+  if (!mode_ok(tscale_mode)) return FP4_ERR_ARG;
+  if (n < 0 || n % 16 != 0) return FP4_ERR_SHAPE;
+  if (!tensor_scale) return FP4_ERR_NULL;
+  if (tscale_mode != FP4_TSCALE_GIVEN && !amax_ws) return FP4_ERR_NULL;
+  if (n > 0 && (!x || !packed || !scales)) return FP4_ERR_NULL;
+  if (!aligned(x, 32) || !aligned(residual, 32) || !aligned(packed, 16) ||
+      !aligned(tensor_scale, 4) || !aligned(amax_ws, 4))
+    return FP4_ERR_ALIGN;
+  cudaStream_t s = as_stream(stream);
+  if (tscale_mode == FP4_TSCALE_COMPUTE) {
+    fp4_status st = launch_amax(x, dtype, n, residual, amax_ws, s);
+    if (st != FP4_OK) return st;
+  }
+  const int64_t nb = n / 16;
+  // An empty tensor still publishes its tensor scale (amax 0 -> 1): the
+  // kernel runs with one CTA and no blocks.
+  if (nb == 0 && tscale_mode == FP4_TSCALE_GIVEN) return FP4_OK;
+  if (dtype == FP4_BF16)
+    return launch_quantize_t<true>(x, nb, residual, rounding, seed, step, tscale_mode, tensor_scale,
+                                   amax_ws, packed, scales, s);
+  return launch_quantize_t<false>(x, nb, residual, rounding, seed, step, tscale_mode, tensor_scale,
+                                  amax_ws, packed, scales, s);
+}
+
+fp4_status nvfp4_dequantize(const uint8_t* packed, const uint8_t* scales, const float* tensor_scale,
+                            int64_t n, void* y, int out_dtype, void* stream) {
+  if (!dtype_ok(out_dtype)) return FP4_ERR_DTYPE;
+  if (n < 0 || n % 16 != 0) return FP4_ERR_SHAPE;
+  if (n > 0 && (!packed || !scales || !y)) return FP4_ERR_NULL;
+  if (!aligned(packed, 16) || !aligned(y, 32) || !aligned(tensor_scale, 4)) return FP4_ERR_ALIGN;
+  const int64_t nb = n / 16;
+  if (nb == 0) return FP4_OK;
+  cudaStream_t s = as_stream(stream);
+  if (out_dtype == FP4_BF16)
+    return launch<dequantize_kernel<true>>(nb, kThreads, 0, s, packed, scales, tensor_scale, nb, y);
+  return launch<dequantize_kernel<false>>(nb, kThreads, 0, s, packed, scales, tensor_scale, nb, y);
+}
+
+fp4_status nvfp4_qdq_amax(const uint16_t* w_bf16, const float* g, float lr, const float* residual,
+                          int64_t n, float* amax_ws, void* stream) {
+  if (n < 0 || n % 16 != 0) return FP4_ERR_SHAPE;
+  if (!amax_ws || (n > 0 && !w_bf16)) return FP4_ERR_NULL;
+  if (!aligned(w_bf16, 32) || !aligned(g, 32) || !aligned(residual, 32) || !aligned(amax_ws, 4))
+    return FP4_ERR_ALIGN;
+  return launch_qdq_amax(w_bf16, g, lr, residual, n, amax_ws, as_stream(stream));
+}
+
+fp4_status nvfp4_qdq(uint16_t* w_bf16, const float* g, float lr, int64_t n, float* residual,
+                     int rounding, uint64_t seed, uint64_t step, int tscale_mode,
+                     float* tensor_scale, float* amax_ws, uint8_t* packed, uint8_t* scales,
+                     void* stream) {
+  if (rounding != FP4_RTN && rounding != FP4_SR) return FP4_ERR_ARG;
+  if (!mode_ok(tscale_mode)) return FP4_ERR_ARG;
+  if (n < 0 || n % 16 != 0) return FP4_ERR_SHAPE;
+  if (!tensor_scale) return FP4_ERR_NULL;
+  if (tscale_mode != FP4_TSCALE_GIVEN && !amax_ws) return FP4_ERR_NULL;
+  if ((packed == nullptr) != (scales == nullptr)) return FP4_ERR_NULL;
+  if (n > 0 && !w_bf16) return FP4_ERR_NULL;
+  if (!aligned(w_bf16, 32) || !aligned(g, 32) || !aligned(residual, 32) || !aligned(packed, 16) ||
+      !aligned(tensor_scale, 4) || !aligned(amax_ws, 4))
+    return FP4_ERR_ALIGN;
+  cudaStream_t s = as_stream(stream);
+  if (tscale_mode == FP4_TSCALE_COMPUTE) {
+    fp4_status st = launch_qdq_amax(w_bf16, g, lr, residual, n, amax_ws, s);
+    if (st != FP4_OK) return st;
+  }
+  const int64_t nb = n / 16;
+  if (nb == 0 && tscale_mode == FP4_TSCALE_GIVEN) return FP4_OK;
+  if (g) {
+    if (residual)
+      return launch_qdq_t<true, true>(w_bf16, g, lr, residual, nb, rounding, seed, step, tscale_mode,
+                                      tensor_scale, amax_ws, packed, scales, s);
+    return launch_qdq_t<true, false>(w_bf16, g, lr, residual, nb, rounding, seed, step, tscale_mode,
+                                     tensor_scale, amax_ws, packed, scales, s);
+  }
+  if (residual)
+    return launch_qdq_t<false, true>(w_bf16, g, lr, residual, nb, rounding, seed, step, tscale_mode,
+                                     tensor_scale, amax_ws, packed, scales, s);
+  return launch_qdq_t<false, false>(w_bf16, g, lr, residual, nb, rounding, seed, step, tscale_mode,
+                                    tensor_scale, amax_ws, packed, scales, s);
+}
+
+}  // extern "C"

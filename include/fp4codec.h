@@ -1,0 +1,208 @@
+/*
+ * fp4codec.h -- C ABI of the block-scaled FP4 (E2M1) codec for GB300 (sm_103a).
+ *
+ * Sources (cited by short key below):
+ *   [FP4Quant]  cybernoise.de, "FP4Quant speeds up GPU communication, with a
+ *               measurable accuracy trade-off".
+ *   [fp4-train] huggingface.co/kernels/phanerozoic/fp4-train, model card.
+ *   [MoE-FP4]   paper-daily.com review (2026-03-05) of "Practical FP4 Training
+ *               for Large-Scale MoE Models on Hopper GPUs".
+ *   [WP2]       hiren.me, "Weight precision, part 2".
+ *
+ * Conventions, for every entry point:
+ *   - Array pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates, frees or synchronizes.  Work is enqueued on `stream`
+ *     (a cudaStream_t; NULL = the legacy default stream) and is asynchronous.
+ *   - Arguments are checked before anything is enqueued.  A failed check
+ *     returns its status and enqueues nothing.  A launch error is returned as
+ *     FP4_ERR_CUDA (the CUDA error is left for cudaGetLastError()).
+ *   - Sizes are element counts.  A size of 0 is legal and enqueues nothing.
+ *   - Packed E2M1 codes hold two codes per byte, element 2i in the low nibble;
+ *     code bits: [3] sign, [2:1] exponent, [0] mantissa ([WP2] "What FP4 can
+ *     hold"; [fp4-train] "How it works": the two-codes-per-byte layout).
+ *   - Inputs must be finite.  NaN or infinite inputs give deterministic but
+ *     unspecified codes.
+ *   - The library keeps no state between calls except a process-wide count of
+ *     kernel launches, so calls are thread-safe.
+ */
+#ifndef FP4CODEC_H
+#define FP4CODEC_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FP4CODEC_ABI_VERSION 1
+
+typedef enum {
+  FP4_OK = 0,
+  FP4_ERR_NULL = 1,      /* a required pointer is NULL */
+  FP4_ERR_ALIGN = 2,     /* a pointer breaks its stated alignment */
+  FP4_ERR_SHAPE = 3,     /* a size is negative or breaks its divisibility rule */
+  FP4_ERR_DTYPE = 4,     /* unknown dtype */
+  FP4_ERR_ARG = 5,       /* another argument out of range (mode, group, ...) */
+  FP4_ERR_CUDA = 6,      /* a kernel launch failed */
+  FP4_ERR_INTERNAL = 7
+} fp4_status;
+
+typedef enum { FP4_F32 = 0, FP4_BF16 = 1 } fp4_dtype;
+typedef enum { FP4_RTN = 0, FP4_SR = 1 } fp4_round;
+
+/* How the NVFP4 per-tensor fp32 scale s_t is obtained ([WP2] "Block scaling":
+ * one 32-bit scale for the whole matrix; the pages do not say how it is
+ * chosen):
+ *   GIVEN      read from *tensor_scale;
+ *   COMPUTE    s_t = amax / (6 * 448) from a tensor-amax pass run inside the
+ *              call (amax_ws is its workspace), written to *tensor_scale;
+ *   FROM_AMAX  like COMPUTE, but the amax is the one a previous nvfp4_amax /
+ *              nvfp4_qdq_amax call left in *amax_ws (no amax pass here).
+ * In every mode a scale that is not finite or not > 0 is used as 1 (and
+ * written as 1). */
+typedef enum { FP4_TSCALE_GIVEN = 0, FP4_TSCALE_COMPUTE = 1, FP4_TSCALE_FROM_AMAX = 2 } fp4_tscale;
+
+const char* fp4_status_string(int status);
+int fp4_abi_version(void);
+/* Number of kernels this library has launched in this process. */
+uint64_t fp4_kernel_launches(void);
+
+/* ------------------------------------------------------------------ NVFP4
+ * [fp4-train] "How it works": 16-element blocks, block scale block_absmax / 6
+ * encoded to e4m3, every element divided by the decoded scale (e4m3 block
+ * scale times s_t) and encoded to E2M1 by round-to-nearest-even or by
+ * stochastic rounding from a counter-based (seed, step, global index) RNG,
+ * optional per-element error-feedback residual.  "Requirements and limits":
+ * float32 or bfloat16 input, K a multiple of 16.
+ */
+
+/* *amax_ws = max |x[i] (+ residual[i])| over n elements (NaN ignored).
+ *   x         [n] fp32 or bf16, 32-byte aligned
+ *   residual  [n] fp32, 32-byte aligned, or NULL
+ *   amax_ws   1 fp32, 4-byte aligned; zeroed and then written by this call
+ *   n % 16 == 0 */
+fp4_status nvfp4_amax(const void* x, int dtype, int64_t n, const float* residual,
+                      float* amax_ws, void* stream);
+
+/* Quantize x (flat, n % 16 == 0) to NVFP4.
+ *   x            [n] fp32 or bf16 (dtype), 32-byte aligned
+ *   residual     [n] fp32 error-feedback residual, read and updated in place
+ *                (r <- (x + r) - dequant(code)), 32-byte aligned, or NULL
+ *   rounding     FP4_RTN or FP4_SR; SR draws Philox4x32-10 with key = seed and
+ *                counter = (g >> 2, step), g the flat element index, word g & 3
+ *   tscale_mode  fp4_tscale; tensor_scale: 1 fp32 on the device (read for
+ *                GIVEN, written otherwise); amax_ws: 1 fp32 workspace, needed
+ *                for COMPUTE and FROM_AMAX (may be NULL for GIVEN)
+ *   packed       [n/2] bytes out, 16-byte aligned
+ *   scales       [n/16] e4m3 bytes out, block b for elements 16b..16b+15,
+ *                linear order (not swizzled) */
+fp4_status nvfp4_quantize(const void* x, int dtype, int64_t n, float* residual,
+                          int rounding, uint64_t seed, uint64_t step, int tscale_mode,
+                          float* tensor_scale, float* amax_ws, uint8_t* packed,
+                          uint8_t* scales, void* stream);
+
+/* y[i] = value(code_i) * (e4m3(scales[i/16]) * s_t), one fp32 product,
+ * then rounded to bf16 (nearest-even) if out_dtype is FP4_BF16.
+ * ([WP2] "Block scaling", step 5: multiply back by the scale.)
+ *   tensor_scale  1 fp32 on the device, or NULL for s_t = 1
+ *   y             [n] out, 32-byte aligned; n % 16 == 0 */
+fp4_status nvfp4_dequantize(const uint8_t* packed, const uint8_t* scales,
+                            const float* tensor_scale, int64_t n, void* y, int out_dtype,
+                            void* stream);
+
+/* *amax_ws = max |(W - lr*G) + r| over n elements, for FROM_AMAX qdq. */
+fp4_status nvfp4_qdq_amax(const uint16_t* w_bf16, const float* g, float lr,
+                          const float* residual, int64_t n, float* amax_ws, void* stream);
+
+/* One training step on an NVFP4-stored bf16 weight ([fp4-train] "Usage":
+ * W = ef.qdq(key, W - lr * grad, step)):
+ *   v = ((W - lr*G) + r), quantize v as nvfp4_quantize does, q = dequant,
+ *   W <- bf16(q) in place, r <- v - q in place.
+ *   w_bf16    [n] bf16, 32-byte aligned, updated in place
+ *   g         [n] fp32 gradient, 32-byte aligned, or NULL (no update term)
+ *   residual  [n] fp32, 32-byte aligned, or NULL (no error feedback)
+ *   packed, scales  as nvfp4_quantize, or both NULL to skip writing them */
+fp4_status nvfp4_qdq(uint16_t* w_bf16, const float* g, float lr, int64_t n, float* residual,
+                     int rounding, uint64_t seed, uint64_t step, int tscale_mode,
+                     float* tensor_scale, float* amax_ws, uint8_t* packed, uint8_t* scales,
+                     void* stream);
+
+/* ------------------------------------------------------------------ MXFP4
+ * [MoE-FP4] "方法概述" / "核心技术贡献" 2 (BF16ToFP4Row): each row in
+ * 32-element blocks, one UE8M0 scale per block ([WP2] "Block scaling": a
+ * power of two): E = floor(log2(block amax)) - 2, clamped to [-127, 127]
+ * (E = -127 for an all-zero block), scale byte E + 127, codes
+ * RN_e2m1(x * 2^-E) with [6, 8) saturating to 6.
+ *   x       [rows, cols] fp32 or bf16 row-major, 32-byte aligned
+ *   packed  [rows, cols/2] out, 16-byte aligned
+ *   scales  [rows, cols/32] UE8M0 bytes out
+ *   cols % 32 == 0 */
+fp4_status mxfp4_quantize(const void* x, int dtype, int64_t rows, int64_t cols,
+                          uint8_t* packed, uint8_t* scales, void* stream);
+
+/* ------------------------------------------------------ MXFP4 -> FP8 E4M3
+ * [MoE-FP4] "核心技术贡献" 1: direct bit conversion, E_fp8 = E_fp4 - 1 + 7,
+ * the mantissa bit shifted into the E4M3 mantissa field; four MXFP4 blocks
+ * form one FP8 block of 128 whose scale S_t is the largest of the four UE8M0
+ * scales, and each element's exponent drops by S_t - S_sub.  Defined result:
+ * the E4M3 value nearest to value(code) * 2^-(S_t - S_sub) (exact unless it
+ * underflows, i.e. unless S_t - S_sub >= 9); fp32 scale 2^(S_t - 127).
+ */
+
+/* FP4RowToFP8Row.
+ *   packed      [rows, cols/2], 32-byte aligned; scales [rows, cols/32] UE8M0
+ *   fp8         [rows, cols] E4M3 out, 32-byte aligned
+ *   fp8_scales  [rows, cols/128] fp32 out, 16-byte aligned
+ *   cols % 128 == 0 */
+fp4_status fp4_to_fp8_row(const uint8_t* packed, const uint8_t* scales, int64_t rows,
+                          int64_t cols, uint8_t* fp8, float* fp8_scales, void* stream);
+
+/* FP4RowToFP8Col ([MoE-FP4] "核心技术贡献" 2 and 3): dequantize, transpose
+ * and requantize per expert segment, over ragged segments given by
+ * precomputed offsets.  Segment e holds source rows seg_row_off[e] ..
+ * seg_row_off[e+1]-1 (n_e rows, n_e >= 0, non-decreasing offsets,
+ * seg_row_off[0] = 0, seg_row_off[E] = total_rows) and becomes:
+ *   fp8_t + cols * seg_row_off[e]:          [cols, n_e] E4M3, row-major;
+ *   fp8_t_scales + cols * seg_scale_off[e]: [cols, ceil(n_e/128)] fp32,
+ * where seg_scale_off is the running sum of ceil(n_e/128) (fp4_seg_scale_offsets).
+ * Output row k, token block b: S_t = the largest source scale among the block's
+ * (<= 128) tokens for feature block k/32.
+ *   packed [total_rows, cols/2], scales [total_rows, cols/32] (as the row form)
+ *   seg_row_off, seg_scale_off  device int64 [num_segments + 1]
+ *   total_blocks  = seg_scale_off[num_segments] (host copy, sizes the grid)
+ *   cols % 128 == 0.  Offsets are trusted: the device reads them as given. */
+fp4_status fp4_to_fp8_col(const uint8_t* packed, const uint8_t* scales, int64_t cols,
+                          const int64_t* seg_row_off, const int64_t* seg_scale_off,
+                          int32_t num_segments, int64_t total_rows, int64_t total_blocks,
+                          uint8_t* fp8_t, float* fp8_t_scales, void* stream);
+
+/* Host helper: host_scale_off[0] = 0, host_scale_off[e+1] = host_scale_off[e]
+ * + ceil((host_row_off[e+1] - host_row_off[e]) / 128).  Returns FP4_ERR_SHAPE
+ * on a decreasing offset. */
+fp4_status fp4_seg_scale_offsets(const int64_t* host_row_off, int32_t num_segments,
+                                 int64_t* host_scale_off);
+
+/* --------------------------------------------------------------- FP4Quant
+ * [FP4Quant] "Why four bits need more than rounding": per contiguous group of
+ * G in {64, 128, 256} along each row: s1 = RMS of the group (balanced
+ * pairwise sum of squares), y = x * RN(1/s1), z = normalized Walsh-Hadamard
+ * transform of y (butterflies h = 1, 2, ..., G/2, then times RN(1/sqrt(G))),
+ * s2 = max|z| / 6, codes = RN_e2m1(z * RN(1/s2)); both scales are stored.
+ * "Making compression cheap enough to help": the decode unpacks,
+ * dequantizes (z' = value * s2), runs the inverse transform (the same
+ * normalized transform) and undoes the RMS scale (x' = y' * s1).
+ *   x / y   [rows, cols] fp32 or bf16, 32-byte aligned
+ *   packed  [rows, cols/2], 16-byte aligned
+ *   s1, s2  [rows, cols/G] fp32, 4-byte aligned
+ *   cols % G == 0 */
+fp4_status fp4quant_encode(const void* x, int dtype, int64_t rows, int64_t cols, int group,
+                           uint8_t* packed, float* s1, float* s2, void* stream);
+fp4_status fp4quant_decode(const uint8_t* packed, const float* s1, const float* s2,
+                           int64_t rows, int64_t cols, int group, void* y, int out_dtype,
+                           void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP4CODEC_H */

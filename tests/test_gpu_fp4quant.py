@@ -1,0 +1,76 @@
+"""GPU parity: FP4Quant encode / decode for G in {64, 128, 256} through the
+C ABI against the CPU oracle, bit for bit (codes, both scales, decoded
+values)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as ora
+from block_scaled_fp4_e2m1_gb300 import workloads
+from parity_util import assert_bits_equal, bf16_bits, dev, ensure_built, to_f32_np, u8
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+def fp4():
+    import block_scaled_fp4_e2m1_gb300 as m
+    return m
+
+
+def _check(x, G, out_dtype=torch.bfloat16):
+    m = fp4()
+    packed, s1, s2 = m.fp4quant_encode(x.to(dev()), G)
+    xn = to_f32_np(x)
+    wp, w1, w2 = ora.fp4quant_encode(xn, G)
+    assert_bits_equal(to_f32_np(s1), w1, "s1")
+    assert_bits_equal(to_f32_np(s2), w2, "s2")
+    assert_bits_equal(u8(packed), wp, "packed")
+    y = m.fp4quant_decode(packed, s1, s2, G, out_dtype)
+    wy = ora.fp4quant_decode(wp, w1, w2, G)
+    if out_dtype == torch.bfloat16:
+        assert_bits_equal(bf16_bits(y), ora.bf16_rn(wy), "decoded bf16")
+    else:
+        assert_bits_equal(to_f32_np(y), wy, "decoded f32")
+
+
+@pytest.mark.parametrize("G", [64, 128, 256])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("rows,cols", [(1, 256), (3, 512), (37, 4096), (1031, 768)])
+def test_encode_decode_matches_oracle(G, dtype, rows, cols):
+    x = workloads.fp4quant_acts(seed=rows, tokens=rows, hidden=cols, device="cpu").to(dtype)
+    _check(x, G, torch.bfloat16 if dtype == torch.bfloat16 else torch.float32)
+
+
+@pytest.mark.parametrize("G", [64, 128, 256])
+def test_degenerate_groups(G):
+    x = torch.zeros(4, 2 * G)
+    x[0, 5] = 37.0                       # a single spike
+    x[1, :] = 1.0                        # constant group
+    x[2, G:] = -0.0
+    x[3, :G] = torch.linspace(-1e-30, 1e-30, G)
+    _check(x, G, torch.float32)
+
+
+@pytest.mark.parametrize("G", [64, 128, 256])
+def test_activation_workload_full_size_sampled(G):
+    """bf16 [16384, 4096] Student-t(4) with 8 outlier channels x20: the whole
+    tensor through the CUDA path, sampled rows against the oracle."""
+    m = fp4()
+    x = workloads.fp4quant_acts(seed=0, device=dev())
+    packed, s1, s2 = m.fp4quant_encode(x, G)
+    y = m.fp4quant_decode(packed, s1, s2, G)
+    rng = np.random.default_rng(G)
+    rows = torch.from_numpy(np.concatenate([[0, x.shape[0] - 1],
+                                            rng.integers(0, x.shape[0], 40)])).to(dev())
+    xs = to_f32_np(x[rows])
+    wp, w1, w2 = ora.fp4quant_encode(xs, G)
+    assert_bits_equal(to_f32_np(s1[rows]), w1, "s1")
+    assert_bits_equal(to_f32_np(s2[rows]), w2, "s2")
+    assert_bits_equal(u8(packed[rows]), wp, "packed")
+    wy = ora.fp4quant_decode(wp, w1, w2, G)
+    assert_bits_equal(bf16_bits(y[rows]), ora.bf16_rn(wy), "decoded")

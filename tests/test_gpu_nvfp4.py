@@ -1,0 +1,278 @@
+"""GPU parity: NVFP4 amax / quantize / dequantize / qdq through the C ABI
+against the CPU oracle, bit for bit (codes, scales, tensor scale, residual,
+dequantized values, updated weights)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as ora
+from block_scaled_fp4_e2m1_gb300 import workloads
+from parity_util import assert_bits_equal, bf16_bits, dev, ensure_built, to_f32_np, u8
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+def fp4():
+    import block_scaled_fp4_e2m1_gb300 as m
+    return m
+
+
+# sizes in elements: tiny, one CTA pass, several passes with a ragged tail
+SIZES = [0, 16, 48, 4096, 16 * (256 * 7 + 37), 16 * 1216 * 256 * 2 + 16 * 5]
+
+
+def _input(n, dtype, seed):
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    x = torch.randn(n, generator=g) * 0.02
+    if n:
+        k = max(1, n // 1000)
+        idx = torch.randperm(n, generator=g)[:k]
+        x[idx] = torch.randn(k, generator=g)
+    return x.to(dtype).to(dev())
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("n", SIZES)
+@pytest.mark.parametrize("rounding", ["rtn", "sr"])
+def test_quantize_compute_matches_oracle(dtype, n, rounding):
+    if n > 100000 and rounding == "sr" and dtype == torch.float32:
+        pytest.skip("covered by the bf16 case")
+    m = fp4()
+    x = _input(n, dtype, seed=n + 1)
+    packed, scales, ts = m.nvfp4_quantize(x, rounding=rounding, seed=1234, step=7, tscale="compute")
+    xn = to_f32_np(x)
+    wp, ws, wt = ora.nvfp4_quantize(xn, rounding=ora.SR if rounding == "sr" else ora.RTN,
+                                    seed=1234, step=7, tscale_mode=ora.TSCALE_COMPUTE)
+    assert np.float32(ts.item()) == np.float32(wt)
+    assert_bits_equal(u8(packed), wp, "packed")
+    assert_bits_equal(u8(scales), ws, "scales")
+    # dequantize, both output dtypes
+    for od in (torch.float32, torch.bfloat16):
+        y = m.nvfp4_dequantize(packed, scales, ts, (n,), od)
+        wy = ora.nvfp4_dequantize(wp, ws, wt, n)
+        if od == torch.bfloat16:
+            assert_bits_equal(bf16_bits(y), ora.bf16_rn(wy), "dequant bf16")
+        else:
+            assert_bits_equal(to_f32_np(y), wy, "dequant f32")
+
+
+@pytest.mark.parametrize("tscale", ["given", "from_amax"])
+def test_quantize_tensor_scale_modes(tscale):
+    m = fp4()
+    n = 16 * 3000
+    x = _input(n, torch.bfloat16, seed=5)
+    xn = to_f32_np(x)
+    if tscale == "given":
+        ts_in = torch.full((1,), 0.00037, dtype=torch.float32, device=dev())
+        packed, scales, ts = m.nvfp4_quantize(x, tscale="given", tensor_scale=ts_in)
+        wp, ws, wt = ora.nvfp4_quantize(xn, tscale_mode=ora.TSCALE_GIVEN,
+                                        tensor_scale=float(np.float32(0.00037)))
+        assert ts.item() == np.float32(0.00037)  # GIVEN never writes
+    else:
+        amax = m.nvfp4_amax(x)
+        assert np.float32(amax.item()) == np.float32(ora.nvfp4_amax(xn))
+        packed, scales, ts = m.nvfp4_quantize(x, tscale="from_amax", amax_ws=amax)
+        wp, ws, wt = ora.nvfp4_quantize(xn, tscale_mode=ora.TSCALE_COMPUTE)
+        assert np.float32(ts.item()) == np.float32(wt)
+    assert_bits_equal(u8(packed), wp, "packed")
+    assert_bits_equal(u8(scales), ws, "scales")
+
+
+@pytest.mark.parametrize("given", [0.0, -1.0, float("inf"), float("nan")])
+def test_given_scale_fallback_is_one(given):
+    m = fp4()
+    x = _input(16 * 64, torch.float32, seed=3)
+    ts_in = torch.full((1,), given, dtype=torch.float32, device=dev())
+    packed, scales, _ = m.nvfp4_quantize(x, tscale="given", tensor_scale=ts_in)
+    wp, ws, _ = ora.nvfp4_quantize(to_f32_np(x), tscale_mode=ora.TSCALE_GIVEN, tensor_scale=1.0)
+    assert_bits_equal(u8(packed), wp, "packed")
+    assert_bits_equal(u8(scales), ws, "scales")
+
+
+@pytest.mark.parametrize("rounding", ["rtn", "sr"])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_error_feedback_residual_in_place(rounding, dtype):
+    m = fp4()
+    n = 16 * (256 * 3 + 11)
+    x = _input(n, dtype, seed=9)
+    g = torch.Generator(device="cpu").manual_seed(10)
+    r0 = (torch.randn(n, generator=g) * 1e-3).to(torch.float32)
+    r = r0.to(dev())
+    packed, scales, ts = m.nvfp4_quantize(x, residual=r, rounding=rounding, seed=77, step=3)
+    rn = r0.numpy().copy()
+    wp, ws, wt = ora.nvfp4_quantize(to_f32_np(x), residual=rn,
+                                    rounding=ora.SR if rounding == "sr" else ora.RTN,
+                                    seed=77, step=3)
+    assert np.float32(ts.item()) == np.float32(wt)
+    assert_bits_equal(u8(packed), wp, "packed")
+    assert_bits_equal(u8(scales), ws, "scales")
+    assert_bits_equal(to_f32_np(r), rn, "residual")
+
+
+def test_worked_example_on_gpu():
+    """hiren.me "Block scaling" worked block, through the CUDA path."""
+    m = fp4()
+    v = torch.zeros(16, dtype=torch.float32)
+    v[:4] = torch.tensor([0.0132, -0.0471, -0.0109, -0.0347])
+    ts = torch.ones(1, dtype=torch.float32, device=dev())
+    packed, scales, _ = m.nvfp4_quantize(v.to(dev()), tscale="given", tensor_scale=ts)
+    assert u8(packed)[:2].tolist() == [0xF3, 0xEB]
+    assert u8(scales)[0] == 0x04
+    y = m.nvfp4_dequantize(packed, scales, ts, (16,))
+    assert y[:4].cpu().tolist() == [0.01171875, -0.046875, -0.01171875, -0.03125]
+
+
+def test_degenerate_blocks():
+    """All-zero blocks, a single nonzero, fp32 subnormals, negative zeros,
+    values that saturate, and a huge dynamic range across blocks."""
+    m = fp4()
+    x = np.zeros(16 * 8, np.float32)
+    x[16 + 3] = 1.0
+    x[32:48] = np.float32(1e-40)                      # subnormals
+    x[48:64] = -0.0
+    x[64:80] = np.linspace(-3e38, 3e38, 16, dtype=np.float32)
+    x[80:96] = np.float32(1e-30) * np.arange(16)
+    x[96:112] = -np.float32(6.0)
+    x[112:128] = np.float32(2.0 ** -140)
+    xt = torch.from_numpy(x).to(dev())
+    for mode in ("compute", "given"):
+        ts = torch.ones(1, dtype=torch.float32, device=dev())
+        packed, scales, tso = m.nvfp4_quantize(xt, tscale=mode, tensor_scale=ts)
+        wp, ws, wt = ora.nvfp4_quantize(x, tscale_mode=ora.TSCALE_COMPUTE if mode == "compute"
+                                        else ora.TSCALE_GIVEN, tensor_scale=1.0)
+        assert np.float32(tso.item()) == np.float32(wt)
+        assert_bits_equal(u8(packed), wp, f"packed {mode}")
+        assert_bits_equal(u8(scales), ws, f"scales {mode}")
+        y = m.nvfp4_dequantize(packed, scales, tso, (x.size,))
+        assert_bits_equal(to_f32_np(y), ora.nvfp4_dequantize(wp, ws, wt, x.size), "dequant")
+
+
+def test_empty_tensor_publishes_unit_scale():
+    m = fp4()
+    x = torch.empty(0, dtype=torch.float32, device=dev())
+    ts = torch.full((1,), 5.0, device=dev())
+    m.nvfp4_quantize(x, tscale="compute", tensor_scale=ts)
+    assert ts.item() == 1.0
+
+
+def test_nvfp4_roundtrip_workload_full():
+    """The fp32 [1024, 1024] N(0, 0.02) + 0.1% N(0, 1) outlier workload, in
+    full: amax, quantize (RTN, computed tensor scale), dequantize."""
+    m = fp4()
+    x = workloads.nvfp4_roundtrip(seed=0, device="cpu")
+    xd = x.to(dev())
+    packed, scales, ts = m.nvfp4_quantize(xd.view(-1))
+    y = m.nvfp4_dequantize(packed, scales, ts, x.shape)
+    wp, ws, wt = ora.nvfp4_quantize(x.numpy().ravel())
+    assert np.float32(ts.item()) == np.float32(wt)
+    assert_bits_equal(u8(packed), wp, "packed")
+    assert_bits_equal(u8(scales), ws, "scales")
+    assert_bits_equal(to_f32_np(y).ravel(), ora.nvfp4_dequantize(wp, ws, wt, x.numel()), "y")
+
+
+@pytest.mark.parametrize("rounding", ["rtn", "sr"])
+@pytest.mark.parametrize("with_g,with_r", [(True, True), (True, False), (False, True)])
+def test_qdq_matches_oracle(rounding, with_g, with_r):
+    m = fp4()
+    n = 16 * (256 * 4 + 3)
+    w0 = workloads.nvfp4_train_weight(seed=1, shape=(n // 64, 64), device="cpu").view(-1)
+    g = workloads.nvfp4_train_grad(1, 0, shape=(n,), device="cpu") if with_g else None
+    r0 = (torch.randn(n, generator=torch.Generator().manual_seed(2)) * 1e-4) if with_r else None
+    w = w0.to(dev())
+    rd = r0.to(dev()) if with_r else None
+    gd = g.to(dev()) if with_g else None
+    lr = 1e-4
+    _, packed, scales, ts = m.nvfp4_qdq(w, gd, lr, rd, rounding=rounding, seed=5, step=11)
+    wb = bf16_bits(w0).copy()
+    rn = r0.numpy().copy() if with_r else None
+    wp, ws, wt = ora.nvfp4_qdq(wb, None if g is None else g.numpy(), lr, rn,
+                               rounding=ora.SR if rounding == "sr" else ora.RTN, seed=5, step=11)
+    assert np.float32(ts.item()) == np.float32(wt)
+    assert_bits_equal(u8(packed), wp, "packed")
+    assert_bits_equal(u8(scales), ws, "scales")
+    assert_bits_equal(bf16_bits(w), wb, "W")
+    if with_r:
+        assert_bits_equal(to_f32_np(rd), rn, "residual")
+
+
+def test_qdq_training_workload_steps():
+    """The bf16 [6144, 2048] N(0, 0.02) weight with G_t ~ N(0, 1), lr 1e-4,
+    SR + error feedback: 3 full-size steps bit-exact, with the amax pass and
+    the qdq pass as separate calls (FROM_AMAX) as the benchmark runs them."""
+    m = fp4()
+    shape = (6144, 2048)
+    w0 = workloads.nvfp4_train_weight(seed=0, shape=shape, device="cpu")
+    w = w0.to(dev()).view(-1)
+    r = torch.zeros(w.numel(), dtype=torch.float32, device=dev())
+    wb = bf16_bits(w0).ravel().copy()
+    rn = np.zeros(w.numel(), np.float32)
+    amax = torch.empty(1, dtype=torch.float32, device=dev())
+    ts = torch.empty(1, dtype=torch.float32, device=dev())
+    for t in range(3):
+        g = workloads.nvfp4_train_grad(0, t, shape=shape, device="cpu").view(-1)
+        gd = g.to(dev())
+        m.nvfp4_qdq_amax(w, gd, 1e-4, r, amax_ws=amax)
+        _, packed, scales, _ = m.nvfp4_qdq(w, gd, 1e-4, r, rounding="sr", seed=0, step=t,
+                                           tscale="from_amax", amax_ws=amax, tensor_scale=ts)
+        wp, ws, wt = ora.nvfp4_qdq(wb, g.numpy(), 1e-4, rn, rounding=ora.SR, seed=0, step=t)
+        assert np.float32(ts.item()) == np.float32(wt)
+        assert_bits_equal(bf16_bits(w), wb, f"W step {t}")
+        assert_bits_equal(to_f32_np(r), rn, f"r step {t}")
+        assert_bits_equal(u8(packed), wp, f"packed step {t}")
+        assert_bits_equal(u8(scales), ws, f"scales step {t}")
+
+
+def test_qdq_sub_ulp_accumulation_on_gpu():
+    """fp4-train "Correctness": a sub-ULP accumulation reaches 1.50 under EF
+    and SR and stays at 0.50 under RTN (the same run as the oracle pin)."""
+    m = fp4()
+    blocks = 64
+    w = torch.full((blocks, 16), 0.5)
+    w[:, 0] = 6.0
+    g = torch.full((blocks, 16), -(2.0 ** -7))
+    g[:, 0] = 0.0
+    ts = torch.ones(1, dtype=torch.float32, device=dev())
+    out = {}
+    for name, rounding, ef in (("rtn", "rtn", False), ("ef", "rtn", True), ("sr", "sr", False)):
+        wd = w.to(torch.bfloat16).to(dev()).view(-1)
+        gd = g.to(dev()).view(-1)
+        r = torch.zeros(wd.numel(), device=dev()) if ef else None
+        for t in range(128):
+            m.nvfp4_qdq(wd, gd, 1.0, r, rounding=rounding, seed=0, step=t, tscale="given",
+                        tensor_scale=ts, want_packed=False)
+        out[name] = wd.view(blocks, 16)[:, 1:].float().cpu()
+    assert torch.all(out["rtn"] == 0.5)
+    assert torch.all(out["ef"] == 1.5)
+    assert abs(out["sr"].mean().item() - 1.5) < 0.05
+
+
+def test_qwen_shaped_matrices_sampled():
+    """The Laplace weight set's matrix shapes at full size (one of each
+    shape): tensor amax exact, then sampled blocks against the oracle."""
+    m = fp4()
+    rng = np.random.default_rng(0)
+    for i, shape in enumerate([(1024, 4096), (4096, 12288)]):
+        w = workloads.laplace_weight(100 + i, shape, device=dev())
+        packed, scales, ts = m.nvfp4_quantize(w.view(-1))
+        wn = to_f32_np(w).ravel()
+        amax = ora.nvfp4_amax(wn)
+        wt = ora.nvfp4_tensor_scale(amax)
+        assert np.float32(ts.item()) == np.float32(wt)
+        nb = wn.size // 16
+        for b0 in list(rng.integers(0, nb - 64, 20)) + [0, nb - 64]:
+            b0 = int(b0)
+            wp, ws, _ = ora.nvfp4_blocks(wn[16 * b0:16 * (b0 + 64)], b0, wt)
+            assert_bits_equal(u8(packed[8 * b0:8 * (b0 + 64)]), wp, f"packed {shape} @{b0}")
+            assert_bits_equal(u8(scales[b0:b0 + 64]), ws, f"scales {shape} @{b0}")
+        y = m.nvfp4_dequantize(packed, scales, ts, shape, torch.bfloat16)
+        yb = bf16_bits(y).ravel()
+        for b0 in rng.integers(0, nb - 64, 10):
+            b0 = int(b0)
+            wy = ora.nvfp4_dequantize(u8(packed[8 * b0:8 * (b0 + 64)]), u8(scales[b0:b0 + 64]),
+                                      wt, 64 * 16)
+            assert_bits_equal(yb[16 * b0:16 * (b0 + 64)], ora.bf16_rn(wy), "dequant bf16")
