@@ -51,6 +51,9 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--small", action="store_true",
                    help="reduced shapes (a quick check, not a bench value)")
+    p.add_argument("--summarize-launches", metavar="CSV",
+                   help="print a per-kernel table of an ncu gpu__time_duration.sum launch list "
+                        "(this library's kernels, last --steps steps) and exit")
     return p.parse_args(argv)
 
 
@@ -484,8 +487,53 @@ def e2e_measure(groups, st, steps, warmup, device):
     return statistics.median(times), h2d, d2h
 
 
+def summarize_launches(path, steps, warmup):
+    """Per-kernel launches, total device time and share, from an ncu CSV
+    launch list (one gpu__time_duration.sum row per launch), restricted to
+    this library's kernels in the last `steps` bench steps."""
+    import csv
+    import re
+    rows = []
+    with open(path) as f:
+        lines = [ln for ln in f if ln.startswith('"')]
+    for r in csv.DictReader(lines):
+        if r.get("Metric Name") != "gpu__time_duration.sum":
+            continue
+        name = r["Kernel Name"]
+        if "fp4::" not in name:
+            continue
+        m = re.search(r"fp4::(?:<unnamed>|\(anonymous namespace\))::([A-Za-z0-9_]+(?:<[^()]*>)?)", name)
+        short = m.group(1) if m else name[:80]
+        unit = r.get("Metric Unit", "ns")
+        v = float(r["Metric Value"].replace(",", ""))
+        ns = v * {"ns": 1.0, "us": 1e3, "usecond": 1e3, "ms": 1e6, "msecond": 1e6}.get(unit, 1.0)
+        rows.append((short, ns, r["Grid Size"], r["Block Size"]))
+    # the run is: one setup launch (the MXFP4 quantize feeding the dispatch
+    # gather), max(3, warmup) warm-up steps, then the timed steps
+    total = len(rows)
+    nsteps = max(3, warmup) + steps
+    per_step = (total - 1) // nsteps
+    if per_step * nsteps + 1 != total:
+        raise ValueError(f"{total} launches do not split into {nsteps} steps + 1")
+    sel = rows[total - per_step * steps:]
+    agg = {}
+    for short, ns, grid, block in sel:
+        a = agg.setdefault(short, [0, 0.0, grid, block])
+        a[0] += 1
+        a[1] += ns
+    tot = sum(a[1] for a in agg.values())
+    out = ["| kernel | launches | total ms | share | grid | block |", "|---|---|---|---|---|---|"]
+    for k, (n, ns, grid, block) in sorted(agg.items(), key=lambda kv: -kv[1][1]):
+        out.append(f"| `{k}` | {n} | {ns / 1e6:.3f} | {ns / tot:.1%} | {grid} | {block} |")
+    out.append(f"| total | {sum(a[0] for a in agg.values())} | {tot / 1e6:.3f} | 100% | | |")
+    return "\n".join(out)
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.summarize_launches:
+        print(summarize_launches(args.summarize_launches, args.steps, args.warmup))
+        return 0
     if args.impl == "reference":
         return reference_arm(args)
 
@@ -514,7 +562,9 @@ def main(argv=None):
     steps = args.steps
     events = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in groups] for _ in range(steps)]
-    sampler = ClockSampler(local)
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    smi_id = vis.split(",")[local].strip() if vis else str(local)
+    sampler = ClockSampler(smi_id)
     sampler.start()
     time.sleep(0.3)
     if world > 1:
@@ -532,17 +582,13 @@ def main(argv=None):
         dist.barrier()
     launches = m.kernel_launches() - launches0
     clocks = sampler.stop()
-    total_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        tt = torch.tensor([total_ms], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), device if world > 1 else None)
     ms_per_step = total_ms / steps
 
     for gi, g in enumerate(groups):
         g.times_ms = [events[s][gi][0].elapsed_time(events[s][gi][1]) for s in range(steps)]
     bytes_step = sum(g.bytes_per_step for g in groups)
-    value = bytes_step * world / (ms_per_step * 1e-3) / 1e9
+    value = job_gbs(bytes_step, world, ms_per_step)
     peak, peak_kind = measured_peak()
 
     kernels = {}
@@ -599,6 +645,25 @@ def main(argv=None):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def max_over_ranks(ms, device=None):
+    """The slowest rank's time (every rank gets it); no-op without a process
+    group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(ms)
+    t = torch.tensor([float(ms)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_rank_step, world, ms_per_step):
+    """Whole-job GB/s: every rank processes its own copy of the workload
+    (weak scaling), timed by the slowest rank."""
+    return bytes_per_rank_step * world / (ms_per_step * 1e-3) / 1e9
 
 
 def load_traffic(kernel_name):
