@@ -7,10 +7,11 @@ not been built (there is no CPU fallback).
 """
 from .codec import (Segments, fp4_seg_scale_offsets, fp4_to_fp8_col, fp4_to_fp8_row,
                     fp4quant_decode, fp4quant_encode, kernel_launches, mxfp4_quantize,
-                    nvfp4_amax, nvfp4_dequantize, nvfp4_qdq, nvfp4_qdq_amax, nvfp4_quantize)
+                    nvfp4_amax, nvfp4_dequantize, nvfp4_qdq, nvfp4_qdq_amax, nvfp4_quantize,
+                    nvfp4_quantize_noalloc)
 
 __all__ = [
     "Segments", "fp4_seg_scale_offsets", "fp4_to_fp8_col", "fp4_to_fp8_row", "fp4quant_decode",
     "fp4quant_encode", "kernel_launches", "mxfp4_quantize", "nvfp4_amax", "nvfp4_dequantize",
-    "nvfp4_qdq", "nvfp4_qdq_amax", "nvfp4_quantize",
+    "nvfp4_qdq", "nvfp4_qdq_amax", "nvfp4_quantize", "nvfp4_quantize_noalloc",
 ]

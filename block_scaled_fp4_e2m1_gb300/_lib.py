@@ -29,6 +29,7 @@ SIGNATURES = {
     "nvfp4_dequantize": (INT, [P, P, P, I64, P, INT, P]),
     "nvfp4_qdq_amax": (INT, [P, P, F32, P, I64, P, P]),
     "nvfp4_qdq": (INT, [P, P, F32, I64, P, INT, U64, U64, INT, P, P, P, P, P]),
+    "nvfp4_quantize_noalloc": (INT, [P, INT, I64, P, INT, U64, U64, P, P, P, P]),
     "mxfp4_quantize": (INT, [P, INT, I64, I64, P, P, P]),
     "fp4_to_fp8_row": (INT, [P, P, I64, I64, P, P, P]),
     "fp4_to_fp8_col": (INT, [P, P, I64, P, P, I32, I64, I64, P, P, P]),

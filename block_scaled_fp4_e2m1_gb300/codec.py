@@ -134,6 +134,25 @@ def nvfp4_qdq(w: torch.Tensor, g: Optional[torch.Tensor] = None, lr: float = 0.0
     return w, packed, scales, tensor_scale
 
 
+def nvfp4_quantize_noalloc(x: torch.Tensor, residual: Optional[torch.Tensor] = None,
+                           rounding: str = "rtn", seed: int = 0, step: int = 0,
+                           tensor_scale: Optional[torch.Tensor] = None,
+                           packed: Optional[torch.Tensor] = None,
+                           scales: Optional[torch.Tensor] = None):
+    """nvfp4_quantize with a computed tensor scale whose amax workspace is
+    the library's own device array (for callers that cannot allocate device
+    memory).  Calls that overlap on the GPU must be serialized."""
+    _cuda(x, "x")
+    n = x.numel()
+    dev = x.device
+    tensor_scale = _scalar(dev) if tensor_scale is None else tensor_scale
+    packed = torch.empty(n // 2, dtype=torch.uint8, device=dev) if packed is None else packed
+    scales = torch.empty(n // 16, dtype=torch.uint8, device=dev) if scales is None else scales
+    call("nvfp4_quantize_noalloc", _ptr(x), _dtype(x, "x"), n, _ptr(residual), _ROUND[rounding],
+         seed, step, _ptr(tensor_scale), _ptr(packed), _ptr(scales), _stream(dev))
+    return packed, scales, tensor_scale
+
+
 # ------------------------------------------------------------------ MXFP4
 
 def mxfp4_quantize(x: torch.Tensor, packed: Optional[torch.Tensor] = None,

@@ -14,6 +14,8 @@
 // 256-bit load one full 32-byte sector.  HBM-bound; no shared memory.
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "host_common.h"
 
@@ -485,3 +487,77 @@ fp4_status nvfp4_qdq(uint16_t* w_bf16, const float* g, float lr, int64_t n, floa
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// No-allocation variant of nvfp4_quantize in COMPUTE mode.
+//
+// The tensor-amax pass needs one fp32 of device workspace that nvfp4_quantize
+// takes from its caller (amax_ws).  Some callers cannot hand one over: a
+// plugin that receives only the tensors it works on from a host framework or
+// inference engine that owns all device memory, or C code with no device
+// allocator of its own.  For them the workspace lives in a file-scope device
+// array below, which every GPU that loads this library holds until the
+// process exits.
+
+namespace fp4 {
+namespace {
+
+// 256 bytes; a call uses one fp32 slot, the tensor amax, whatever n is.
+constexpr size_t kNoAllocScratchBytes = 256;
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+float* g_noalloc_addr[kNoAllocMaxDevices];  // device address of the array, per device
+
+// The array's device address on the current device.  In host code the name
+// g_noalloc_scratch is only a host-side stand-in, so the address is looked up
+// with cudaGetSymbolAddress once per device, with that device current.
+fp4_status noalloc_scratch_address(float** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FP4_ERR_CUDA;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return FP4_ERR_ARG;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return FP4_ERR_CUDA;
+    g_noalloc_addr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_addr[dev];
+  return FP4_OK;
+}
+
+}  // namespace
+}  // namespace fp4
+
+extern "C" fp4_status nvfp4_quantize_noalloc(const void* x, int dtype, int64_t n, float* residual,
+                                             int rounding, uint64_t seed, uint64_t step,
+                                             float* tensor_scale, uint8_t* packed, uint8_t* scales,
+                                             void* stream) {
+  if (!dtype_ok(dtype)) return FP4_ERR_DTYPE;
+  if (rounding != FP4_RTN && rounding != FP4_SR) return FP4_ERR_ARG;
+  if (n < 0 || n % 16 != 0) return FP4_ERR_SHAPE;
+  if (!tensor_scale) return FP4_ERR_NULL;
+  if (n > 0 && (!x || !packed || !scales)) return FP4_ERR_NULL;
+  if (!aligned(x, 32) || !aligned(residual, 32) || !aligned(packed, 16) ||
+      !aligned(tensor_scale, 4))
+    return FP4_ERR_ALIGN;
+  // Scratch this call needs: the amax slot.  It does not grow with n, so no
+  // size passes the contract above and still fails here.
+  const size_t need = sizeof(float);
+  if (need > kNoAllocScratchBytes) return FP4_ERR_SHAPE;
+  float* amax_ws = nullptr;
+  fp4_status st = noalloc_scratch_address(&amax_ws);
+  if (st != FP4_OK) return st;
+  cudaStream_t s = as_stream(stream);
+  // launch_amax clears the slot (cudaMemsetAsync) before its max pass.
+  st = launch_amax(x, dtype, n, residual, amax_ws, s);
+  if (st != FP4_OK) return st;
+  const int64_t nb = n / 16;
+  if (dtype == FP4_BF16)
+    return launch_quantize_t<true>(x, nb, residual, rounding, seed, step, FP4_TSCALE_COMPUTE,
+                                   tensor_scale, amax_ws, packed, scales, s);
+  return launch_quantize_t<false>(x, nb, residual, rounding, seed, step, FP4_TSCALE_COMPUTE,
+                                  tensor_scale, amax_ws, packed, scales, s);
+}

@@ -23,7 +23,8 @@
  *   - Inputs must be finite.  NaN or infinite inputs give deterministic but
  *     unspecified codes.
  *   - The library keeps no state between calls except a process-wide count of
- *     kernel launches, so calls are thread-safe.
+ *     kernel launches and the workspace of nvfp4_quantize_noalloc, so calls
+ *     other than nvfp4_quantize_noalloc are thread-safe.
  */
 #ifndef FP4CODEC_H
 #define FP4CODEC_H
@@ -58,8 +59,8 @@ typedef enum { FP4_RTN = 0, FP4_SR = 1 } fp4_round;
  *              call (amax_ws is its workspace), written to *tensor_scale;
  *   FROM_AMAX  like COMPUTE, but the amax is the one a previous nvfp4_amax /
  *              nvfp4_qdq_amax call left in *amax_ws (no amax pass here).
- * In every mode a scale that is not finite or not > 0 is used as 1 (and
- * written as 1). */
+ * In every mode a scale that is not finite or not > 0 is used as 1; COMPUTE
+ * and FROM_AMAX write the scale they used, GIVEN never writes it. */
 typedef enum { FP4_TSCALE_GIVEN = 0, FP4_TSCALE_COMPUTE = 1, FP4_TSCALE_FROM_AMAX = 2 } fp4_tscale;
 
 const char* fp4_status_string(int status);
@@ -126,6 +127,31 @@ fp4_status nvfp4_qdq(uint16_t* w_bf16, const float* g, float lr, int64_t n, floa
                      int rounding, uint64_t seed, uint64_t step, int tscale_mode,
                      float* tensor_scale, float* amax_ws, uint8_t* packed, uint8_t* scales,
                      void* stream);
+
+/* nvfp4_quantize in COMPUTE mode without a caller-supplied workspace.  The
+ * pages have no counterpart to this entry point; it exists for callers that
+ * cannot allocate device memory: a plugin that is handed only the tensors it
+ * works on by a framework or inference engine that owns all device memory,
+ * or C code with no device allocator of its own.  Such callers cannot provide
+ * the one-fp32 amax workspace that COMPUTE mode needs, so here that
+ * workspace is a 256-byte array inside the library, in device memory that
+ * every GPU which loads the library holds until the process exits.
+ *   Arguments and results are those of nvfp4_quantize with
+ *   tscale_mode = FP4_TSCALE_COMPUTE (tensor_scale is written).
+ *   Scratch: one fp32 per call, whatever n is, out of a 256-byte array; a
+ *   call whose scratch need exceeded the array would fail with
+ *   FP4_ERR_SHAPE, which the one-fp32 need never does.
+ *   Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   The first call on each device looks the array's device address up with
+ *   cudaGetSymbolAddress (with that device current) and caches it; make that
+ *   first call before any stream capture on the device.
+ *   Every call on a device shares the one slot, which the call clears before
+ *   use; calls whose work overlaps on the GPU (other streams, or two host
+ *   threads) race on it and must be serialized by the caller. */
+fp4_status nvfp4_quantize_noalloc(const void* x, int dtype, int64_t n, float* residual,
+                                  int rounding, uint64_t seed, uint64_t step,
+                                  float* tensor_scale, uint8_t* packed, uint8_t* scales,
+                                  void* stream);
 
 /* ------------------------------------------------------------------ MXFP4
  * [MoE-FP4] "方法概述" / "核心技术贡献" 2 (BF16ToFP4Row): each row in
