@@ -51,6 +51,10 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--small", action="store_true",
                    help="reduced shapes (a quick check, not a bench value)")
+    p.add_argument("--kernel", metavar="NAME",
+                   help="time one kernel alone on a tensor of --size-mb input (a kernel "
+                        "study for profiling; prints its own JSON line)")
+    p.add_argument("--size-mb", type=float, default=1024.0)
     p.add_argument("--summarize-launches", metavar="CSV",
                    help="print a per-kernel table of an ncu gpu__time_duration.sum launch list "
                         "(this library's kernels, last --steps steps) and exit")
@@ -345,7 +349,7 @@ def cpu_oracle_rates(budget_s=12.0):
     rates["nvfp4_qdq_amax@nvfp4_train"] = timed(lambda: ora.nvfp4_qdq_amax(w, g, 1e-4, r),
                                                 10 * w.size)
     rates["nvfp4_qdq@nvfp4_train"] = timed(
-        lambda: ora.nvfp4_qdq(w, g, 1e-4, r, rounding=ora.SR), 26.5625 * w.size)
+        lambda: ora.nvfp4_qdq(w, g, 1e-4, r, rounding=ora.SR), 16.5625 * w.size)
     # MoE (16 tokens, then 128 dispatched rows)
     t = ora.bf16_to_f32(bits(W.moe_tokens(seed=0, tokens=16, hidden=7168)))
     mp, ms = ora.mxfp4_quantize(t)
@@ -425,7 +429,7 @@ def suite_shapes():
                Group(f"fp4quant_decode_g{G}", "fp4quant_acts", n2 * (2.5 + 8 / G), [None])]
     n3 = 6144 * 2048
     gs += [Group("nvfp4_qdq_amax", "nvfp4_train", 10 * n3, [None]),
-           Group("nvfp4_qdq", "nvfp4_train", 26.5625 * n3, [None])]
+           Group("nvfp4_qdq", "nvfp4_train", 16.5625 * n3, [None])]
     n4 = 32768 * 7168
     nd = 8 * n4
     gs += [Group("mxfp4_quantize", "moe_tokens", 2.53125 * n4, [None]),
@@ -529,8 +533,117 @@ def summarize_launches(path, steps, warmup):
     return "\n".join(out)
 
 
+KERNEL_STUDIES = ["nvfp4_amax", "nvfp4_quantize", "nvfp4_quantize_sr", "nvfp4_dequantize",
+                  "nvfp4_qdq", "mxfp4_quantize", "fp4_to_fp8_row", "fp4_to_fp8_col",
+                  "fp4quant_encode_g64", "fp4quant_encode_g128", "fp4quant_encode_g256",
+                  "fp4quant_decode_g64", "fp4quant_decode_g128", "fp4quant_decode_g256"]
+
+
+def kernel_study(name, size_mb, steps, warmup, device):
+    """One kernel on a bf16 input of ~size_mb MB (the shapes of its bench
+    workload, rows scaled), timed per launch with CUDA events.  Returns
+    (group, per-launch ms list)."""
+    import torch
+    import block_scaled_fp4_e2m1_gb300 as m
+    from block_scaled_fp4_e2m1_gb300 import workloads as W
+    f32, bf16, u8 = torch.float32, torch.bfloat16, torch.uint8
+    n = int(size_mb * 1e6 / 2) // 4096 * 4096
+    def z(shape, dt):
+        return torch.empty(shape, dtype=dt, device=device)
+    if name in ("nvfp4_amax", "nvfp4_quantize", "nvfp4_quantize_sr", "nvfp4_dequantize"):
+        w = W.laplace_weight(7, (n // 4096, 4096), device=device).view(-1)
+        a, t = z(1, f32), z(1, f32)
+        pk, sc, y = z(n // 2, u8), z(n // 16, u8), z(n, bf16)
+        m.nvfp4_amax(w, amax_ws=a)
+        m.nvfp4_quantize(w, tscale="from_amax", amax_ws=a, tensor_scale=t, packed=pk, scales=sc)
+        if name == "nvfp4_amax":
+            g = Group(name, "study", 2 * n, [lambda: m.nvfp4_amax(w, amax_ws=a)])
+        elif name == "nvfp4_dequantize":
+            g = Group(name, "study", 2.5625 * n,
+                      [lambda: m.nvfp4_dequantize(pk, sc, t, (n,), bf16, out=y)])
+        else:
+            rnd = "sr" if name.endswith("_sr") else "rtn"
+            g = Group(name, "study", 2.5625 * n,
+                      [lambda: m.nvfp4_quantize(w, rounding=rnd, tscale="from_amax", amax_ws=a,
+                                                tensor_scale=t, packed=pk, scales=sc)])
+    elif name == "nvfp4_qdq":
+        n3 = n // 4
+        w = W.nvfp4_train_weight(seed=0, shape=(n3 // 2048, 2048), device=device).view(-1)
+        gr = W.nvfp4_train_grad(0, 0, shape=(n3,), device=device)
+        r = torch.zeros(n3, dtype=f32, device=device)
+        a, t = z(1, f32), z(1, f32)
+        pk, sc = z(n3 // 2, u8), z(n3 // 16, u8)
+        m.nvfp4_qdq_amax(w, gr, 1e-4, r, amax_ws=a)
+        g = Group(name, "study", 16.5625 * n3,
+                  [lambda: m.nvfp4_qdq(w, gr, 1e-4, r, rounding="sr", tscale="from_amax",
+                                       amax_ws=a, tensor_scale=t, packed=pk, scales=sc)])
+    elif name == "mxfp4_quantize":
+        x = W.moe_tokens(seed=0, tokens=n // 7168, hidden=7168, device=device)
+        pk, sc = m.mxfp4_quantize(x)
+        g = Group(name, "study", 2.53125 * x.numel(), [lambda: m.mxfp4_quantize(x, pk, sc)])
+    elif name in ("fp4_to_fp8_row", "fp4_to_fp8_col"):
+        T = max(8, n // 7168 // 8)
+        x = W.moe_tokens(seed=0, tokens=T, hidden=7168, device=device)
+        row_token, row_off = W.moe_routing(seed=0, tokens=T, experts=256)
+        mp, ms = m.mxfp4_quantize(x)
+        idx = row_token.to(device)
+        dp, ds = mp.index_select(0, idx).contiguous(), ms.index_select(0, idx).contiguous()
+        del x, mp, ms
+        nd = dp.shape[0] * 7168
+        if name == "fp4_to_fp8_row":
+            f8, fs = m.fp4_to_fp8_row(dp, ds)
+            g = Group(name, "study", 1.5625 * nd, [lambda: m.fp4_to_fp8_row(dp, ds, f8, fs)])
+        else:
+            segs = m.Segments(row_off, device)
+            ft, fts = m.fp4_to_fp8_col(dp, ds, segs)
+            g = Group(name, "study", nd * (0.5 + 1 / 32 + 1) + 4 * 7168 * segs.total_blocks,
+                      [lambda: m.fp4_to_fp8_col(dp, ds, segs, ft, fts)])
+    elif name.startswith("fp4quant_"):
+        G = int(name.rsplit("_g", 1)[1])
+        x = W.fp4quant_acts(seed=0, tokens=n // 4096, hidden=4096, device=device)
+        pk, s1, s2 = m.fp4quant_encode(x, G)
+        y = torch.empty_like(x)
+        b = x.numel() * (2.5 + 8 / G)
+        if "encode" in name:
+            g = Group(name, "study", b, [lambda: m.fp4quant_encode(x, G, pk, s1, s2)])
+        else:
+            g = Group(name, "study", b, [lambda: m.fp4quant_decode(pk, s1, s2, G, bf16, out=y)])
+    else:
+        raise SystemExit(f"unknown kernel {name}; one of {KERNEL_STUDIES}")
+    torch.cuda.synchronize()
+    for _ in range(max(1, warmup)):
+        g.calls[0]()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    torch.cuda.synchronize()
+    for s in range(steps):
+        ev[s][0].record()
+        g.calls[0]()
+        ev[s][1].record()
+    torch.cuda.synchronize()
+    return g, [a.elapsed_time(b) for a, b in ev]
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.kernel:
+        import torch
+        import __graft_entry__
+        __graft_entry__.build()
+        dev = torch.device("cuda", 0)
+        names = KERNEL_STUDIES if args.kernel == "all" else args.kernel.split(",")
+        peak, kind = measured_peak()
+        for nm in names:
+            g, ts = kernel_study(nm, args.size_mb, args.steps, args.warmup, dev)
+            t = statistics.median(ts)
+            gbs = g.bytes_per_launch / (t * 1e-3) / 1e9
+            print(json.dumps({"kernel": nm, "size_mb": args.size_mb,
+                              "bytes_per_launch": int(g.bytes_per_launch),
+                              "ms_median": round(t, 4), "ms_min": round(min(ts), 4),
+                              "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                              "peak_kind": kind}), flush=True)
+            torch.cuda.empty_cache()
+        return 0
     if args.summarize_launches:
         print(summarize_launches(args.summarize_launches, args.steps, args.warmup))
         return 0

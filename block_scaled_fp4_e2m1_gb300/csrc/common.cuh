@@ -74,6 +74,40 @@ __device__ __forceinline__ uint32_t ld_stream_u8(const void* p) {
   return r;
 }
 
+// ---------------------------------------------------- asynchronous staging
+//
+// Streaming kernels keep several units of input per thread in flight by
+// copying them into shared memory with cp.async (16-byte copies that bypass
+// L1) a few units ahead of use.  Each thread only reads back what it copied
+// itself, so cp.async.wait_group is the only wait: no barrier, no spin loop.
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Ring of kStages slots of kPieces 16-byte pieces per thread in dynamic
+// shared memory; piece p of slot s of thread t is at
+// base[(s * kPieces + p) * kThreads + t], so each (slot, piece) is one
+// contiguous, conflict-free row of 16-byte words across the CTA.
+template <int kPieces, int kStages, int kThreads>
+struct StageRing {
+  static constexpr size_t kBytes = (size_t)kStages * kPieces * kThreads * 16;
+  uint4* base;
+  __device__ __forceinline__ uint4* at(int slot, int piece) const {
+    return base + (slot * kPieces + piece) * kThreads + threadIdx.x;
+  }
+};
+
 // ------------------------------------------------------------ bf16 <-> f32
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -97,6 +131,30 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
       : "=r"(r)
       : "f"(hi), "f"(lo));
   return r;
+}
+
+// Eight floats to eight E2M1 codes (round-to-nearest-even, saturating) in one
+// 32-bit word, a[i] in bits 4i+3..4i.
+__device__ __forceinline__ uint32_t cvt_e2m1x8(float a0, float a1, float a2, float a3, float a4,
+                                               float a5, float a6, float a7) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(a0), "f"(a1), "f"(a2), "f"(a3), "f"(a4), "f"(a5), "f"(a6), "f"(a7));
+  return r;
+}
+
+// Two floats to two E4M3 bytes (round-to-nearest-even, saturating): lo in
+// bits 7:0, hi in bits 15:8.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return (uint32_t)r;
 }
 
 // Exact value of the E2M1 code in bits 3:0 of c: sign to bit 31, the three

@@ -20,9 +20,10 @@
 // exact values value(j) * 2^-d.
 //
 // [MoE-FP4] "核心技术贡献" 2 and 3: FP4RowToFP8Col fuses dequantize,
-// transpose and requantize, with a padded shared-memory tile against bank
-// conflicts, over ragged per-expert row segments located by precomputed
-// offsets.
+// transpose and requantize in one pass (the page stages the transpose
+// through a padded shared-memory tile; here each warp transposes its block
+// in registers, see the column kernel), over ragged per-expert row segments
+// located by precomputed offsets.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -112,13 +113,20 @@ __global__ void __launch_bounds__(kRowThreads)
 }
 
 // ------------------------------------------------------------------- col
+//
+// Work unit: one warp converts one FP8 scale block, i.e. 128 tokens of one
+// segment x 32 features (one MXFP4 scale column).  Lane (g, c) = (lane & 7,
+// lane >> 3) owns tokens 16g .. 16g+15 and features 8c .. 8c+7 of the unit:
+// it loads one 32-bit word of 8 codes and one scale byte per token, the warp
+// reduces the block's target scale with three shuffles, each lane converts
+// its 16 words through the shift tables and transposes them into 8 feature
+// rows x 16 token bytes, and writes those rows to the (unaligned) segment
+// output with aligned 16-byte stores assembled from its own bytes and the
+// next lane's.  No shared-memory tile and no CTA barrier: the warps of a
+// CTA are independent, and consecutive warps take neighbouring feature
+// blocks of the same token block so their 16-byte row slices share sectors.
 
 constexpr int kColThreads = 256;
-constexpr int kInRowWords = 20;  // 64 B of codes + 16 B pad per token row
-
-// Physical word of logical word `w` in output-tile row `row` (XOR swizzle
-// that keeps both the transposed writes and the row reads conflict-free).
-__device__ __forceinline__ int out_word(int row, int w) { return w ^ (((row >> 3) & 15) << 1); }
 
 // Largest e in [0, nseg) with off[e] <= v, for off non-decreasing, off[0] = 0
 // <= v < off[nseg]: a 32-way search by one warp.
@@ -138,153 +146,152 @@ __device__ __forceinline__ int find_segment(const int64_t* __restrict__ off, int
   return lo;
 }
 
-struct ColTile {
-  int64_t row0;     // first source row of the segment
-  int64_t n_e;      // tokens in the segment
-  int64_t sofs;     // segment's first global token block
-  int64_t b;        // token block within the segment
-};
+// Bytes o .. o+15 (1 <= o <= 15) of the 32-byte sequence x[0..3] | y[0..3].
+__device__ __forceinline__ uint4 window16(uint4 x, uint4 y, int o) {
+  uint32_t w0 = x.x, w1 = x.y, w2 = x.z, w3 = x.w, w4 = y.x, w5 = y.y, w6 = y.z, w7 = y.w;
+  if (o & 8) {
+    w0 = w2; w1 = w3; w2 = w4; w3 = w5; w4 = w6; w5 = w7;
+  }
+  if (o & 4) {
+    w0 = w1; w1 = w2; w2 = w3; w3 = w4; w4 = w5;
+  }
+  const uint32_t sh = 8u * (uint32_t)(o & 3);
+  return make_uint4(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh),
+                    __funnelshift_r(w2, w3, sh), __funnelshift_r(w3, w4, sh));
+}
+
+// Store bytes lo .. hi-1 (0 <= lo < hi <= 16) of the 16-byte value v to the
+// 16-byte aligned p: one 128-bit store when the chunk is whole, otherwise
+// the whole 32-bit words inside [lo, hi) as word stores and the bytes of the
+// (at most two) edge words as byte stores, all predicated, no loop.
+__device__ __forceinline__ void store_chunk(uint8_t* p, uint4 v, int lo, int hi) {
+  if (lo <= 0 && hi >= 16) {
+    *reinterpret_cast<uint4*>(p) = v;
+    return;
+  }
+  const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int t = 0; t < 4; ++t)
+    if (lo <= 4 * t && 4 * t + 4 <= hi) reinterpret_cast<uint32_t*>(p)[t] = vw[t];
+  // edge words: the word holding byte lo (if lo is not word aligned) and the
+  // word holding byte hi - 1 (if hi is not word aligned)
+  const int wl = lo >> 2, wh = (hi - 1) >> 2;
+  const uint32_t xl = vw[0] * (wl == 0) + vw[1] * (wl == 1) + vw[2] * (wl == 2) + vw[3] * (wl == 3);
+  const uint32_t xh = vw[0] * (wh == 0) + vw[1] * (wh == 1) + vw[2] * (wh == 2) + vw[3] * (wh == 3);
+#pragma unroll
+  for (int q = 0; q < 3; ++q) {
+    if ((lo & 3) != 0 && q < 4 - (lo & 3) && lo + q < hi)
+      p[lo + q] = (uint8_t)(xl >> (8 * ((lo + q) & 3)));
+    const int bh = 4 * wh + q;      // bytes of the last word before hi
+    if ((hi & 3) != 0 && q < (hi & 3) && bh >= lo && (wl != wh || (lo & 3) == 0))
+      p[bh] = (uint8_t)(xh >> (8 * q));
+  }
+}
 
 __global__ void __launch_bounds__(kColThreads)
     fp4_to_fp8_col_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ scales,
                           int64_t cols, const int64_t* __restrict__ seg_row_off,
-                          const int64_t* __restrict__ seg_scale_off, int nseg, int64_t ntiles,
+                          const int64_t* __restrict__ seg_scale_off, int nseg, int64_t nunits,
                           uint8_t* __restrict__ fp8_t, float* __restrict__ fp8_t_scales) {
-  __shared__ __align__(16) uint32_t in_tile[128 * kInRowWords];
-  __shared__ __align__(16) uint32_t out_tile[128 * 32];
-  __shared__ uint32_t sc_tile[128];
-  __shared__ uint32_t warp_st[4];
   __shared__ __align__(8) uint8_t lut[128];
-  __shared__ ColTile tile;
-
   build_shift_tables(lut);
+  __syncthreads();
   const uint2* lut2 = reinterpret_cast<const uint2*>(lut);
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int64_t ftiles = cols / 128;
-  const int64_t row_bytes = cols / 2, row_scales = cols / 32;
+  const int lane = threadIdx.x & 31;
+  const int g = lane & 7;   // token group
+  const int c = lane >> 3;  // 8-feature slice of the 32-feature block
+  const int64_t kblocks = cols / 32;
+  const int64_t row_bytes = cols / 2;
+  const int64_t nwarps = (int64_t)gridDim.x * (kColThreads / 32);
+  for (int64_t unit = (int64_t)blockIdx.x * (kColThreads / 32) + (threadIdx.x >> 5); unit < nunits;
+       unit += nwarps) {
+    const int64_t fb = unit / kblocks;              // global token block
+    const int kb = (int)(unit - fb * kblocks);      // feature block
+    const int e = find_segment(seg_scale_off, nseg, fb);
+    const int64_t row0 = seg_row_off[e];
+    const int64_t n_e = seg_row_off[e + 1] - row0;
+    const int64_t sofs = seg_scale_off[e];
+    const int64_t b = fb - sofs;
+    const int64_t left = n_e - 128 * b;
+    const int nv = left < 128 ? (int)left : 128;    // tokens in this block
 
-  for (int64_t tid = blockIdx.x; tid < ntiles; tid += gridDim.x) {
-    const int64_t fb = tid / ftiles;  // global token block
-    const int64_t f = tid - fb * ftiles;  // feature tile (128 features)
-    if (warp == 0) {
-      const int e = find_segment(seg_scale_off, nseg, fb);
-      if (lane == 0) {
-        tile.row0 = seg_row_off[e];
-        tile.n_e = seg_row_off[e + 1] - tile.row0;
-        tile.sofs = seg_scale_off[e];
-        tile.b = fb - tile.sofs;
+    // Load: 16 tokens x (8 codes, 1 scale byte).
+    uint32_t w[16], s[16];
+    {
+      const int64_t r = row0 + 128 * b + 16 * g;
+      const uint8_t* pw = packed + r * row_bytes + 16 * kb + 4 * c;
+      const uint8_t* ps = scales + r * kblocks + kb;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const bool ok = 16 * g + i < nv;
+        w[i] = ok ? ld_stream_u32(pw + i * row_bytes) : 0u;
+        s[i] = ok ? ld_stream_u8(ps + i * kblocks) : 0u;
       }
     }
-    __syncthreads();  // tile (and, first time, lut) visible; previous tile's smem free
-    const int64_t row0 = tile.row0, n_e = tile.n_e, b = tile.b;
+    // Target scale: the block's largest source scale.
+    uint32_t st = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) st = max(st, s[i]);
+    st = max(st, __shfl_xor_sync(0xFFFFFFFFu, st, 1));
+    st = max(st, __shfl_xor_sync(0xFFFFFFFFu, st, 2));
+    st = max(st, __shfl_xor_sync(0xFFFFFFFFu, st, 4));
     const int64_t nb_e = (n_e + 127) / 128;
-    const int nv = (int)((n_e - 128 * b) < 128 ? (n_e - 128 * b) : 128);  // valid tokens
-    const int64_t src_row = row0 + 128 * b;
+    fp8_t_scales[cols * sofs + (32 * kb + lane) * nb_e + b] = ue8m0_to_f32(st);
 
-    // Stage the 128 x 64 B code tile (two threads per token row) and the
-    // 128 x 4 scale bytes; rows past the segment end read as zero.
-    {
-      const int r = t >> 1, h = t & 1;
-      U32x8 v;
-      if (r < nv) {
-        v = ld_stream_v8(packed + (src_row + r) * row_bytes + 64 * f + 32 * h);
+    // Convert and transpose: o[f][q] = 4 token bytes (16g + 4q ..) of feature 8c + f.
+    uint32_t o[8][4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t lo[4], hi[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint32_t d = st - s[4 * q + i];
+        d = d > 15u ? 15u : d;
+        convert8(w[4 * q + i], lut2[d], lo[i], hi[i]);
+      }
+      const uint32_t a0 = __byte_perm(lo[0], lo[1], 0x5140u), a1 = __byte_perm(lo[0], lo[1], 0x7362u);
+      const uint32_t a2 = __byte_perm(lo[2], lo[3], 0x5140u), a3 = __byte_perm(lo[2], lo[3], 0x7362u);
+      const uint32_t b0 = __byte_perm(hi[0], hi[1], 0x5140u), b1 = __byte_perm(hi[0], hi[1], 0x7362u);
+      const uint32_t b2 = __byte_perm(hi[2], hi[3], 0x5140u), b3 = __byte_perm(hi[2], hi[3], 0x7362u);
+      o[0][q] = __byte_perm(a0, a2, 0x5410u);
+      o[1][q] = __byte_perm(a0, a2, 0x7632u);
+      o[2][q] = __byte_perm(a1, a3, 0x5410u);
+      o[3][q] = __byte_perm(a1, a3, 0x7632u);
+      o[4][q] = __byte_perm(b0, b2, 0x5410u);
+      o[5][q] = __byte_perm(b0, b2, 0x7632u);
+      o[6][q] = __byte_perm(b1, b3, 0x5410u);
+      o[7][q] = __byte_perm(b1, b3, 0x7632u);
+    }
+
+    // Store: feature row k = 32kb + 8c + f holds the block's nv tokens at
+    // S = fp8_t + cols*row0 + k*n_e + 128b, a = S mod 16.  With a = 0 lane g
+    // writes bytes 16g .. 16g+15 as they are; otherwise it writes the
+    // aligned chunk starting at token 16g + 16 - a (its last a bytes and the
+    // next lane's first 16 - a bytes), and lane 0 also the head chunk.
+    uint8_t* const blk = fp8_t + cols * row0 + 128 * b;
+    const int own_end = nv - 16 * g;  // bytes of this lane's 16 that are valid (may be <= 0)
+#pragma unroll
+    for (int f = 0; f < 8; ++f) {
+      const uint4 mine = make_uint4(o[f][0], o[f][1], o[f][2], o[f][3]);
+      const uint4 next = make_uint4(__shfl_down_sync(0xFFFFFFFFu, mine.x, 1),
+                                    __shfl_down_sync(0xFFFFFFFFu, mine.y, 1),
+                                    __shfl_down_sync(0xFFFFFFFFu, mine.z, 1),
+                                    __shfl_down_sync(0xFFFFFFFFu, mine.w, 1));
+      uint8_t* const S = blk + (32 * (int64_t)kb + 8 * c + f) * n_e;
+      const int a = (int)(reinterpret_cast<uintptr_t>(S) & 15u);
+      if (own_end <= 0) continue;
+      if (a == 0) {
+        store_chunk(S + 16 * g, mine, 0, own_end);
       } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v.w[i] = 0u;
-      }
-      uint4* dst = reinterpret_cast<uint4*>(in_tile + r * kInRowWords + 8 * h);
-      dst[0] = make_uint4(v.w[0], v.w[1], v.w[2], v.w[3]);
-      dst[1] = make_uint4(v.w[4], v.w[5], v.w[6], v.w[7]);
-      if (t < 128) {
-        const uint32_t s = t < nv ? ld_stream_u32(scales + (src_row + t) * row_scales + 4 * f) : 0u;
-        sc_tile[t] = s;
-        // per-byte max over the block's tokens: S_t of the 4 feature blocks
-        uint32_t m = s;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = __vmaxu4(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-        if (lane == 0) warp_st[warp] = m;
+        const int o16 = 16 - a;
+        // main chunk: tokens 16g + o16 .. 16g + o16 + 15
+        const int valid = nv - (16 * g + o16);
+        if (valid > 0) store_chunk(S + 16 * g + o16, window16(mine, next, o16), 0, valid);
+        // head chunk (tokens 0 .. o16 - 1 at bytes a .. 15 of the chunk before S + o16)
+        if (g == 0) store_chunk(S - a, window16(make_uint4(0u, 0u, 0u, 0u), mine, o16), a,
+                                a + (nv < o16 ? nv : o16));
       }
     }
-    __syncthreads();
-    const uint32_t st4 = __vmaxu4(__vmaxu4(warp_st[0], warp_st[1]), __vmaxu4(warp_st[2], warp_st[3]));
-
-    // Output scales: feature k of this tile, token block b.
-    if (t < 128) {
-      const uint32_t st = (st4 >> (8 * (t >> 5))) & 0xFFu;
-      fp8_t_scales[cols * tile.sofs + (128 * f + t) * nb_e + b] = ue8m0_to_f32(st);
-    }
-
-    // Convert and transpose: lane owns word column c (features 8c..8c+7)
-    // for token quads tq and tq + 16.
-    {
-      const int c = lane & 15;
-      const int kb = c >> 2;
-      const uint32_t st = (st4 >> (8 * kb)) & 0xFFu;
-#pragma unroll
-      for (int rep = 0; rep < 2; ++rep) {
-        const int tq = 2 * warp + (lane >> 4) + 16 * rep;
-        uint32_t lo[4], hi[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int j = 4 * tq + i;
-          const uint32_t w = in_tile[j * kInRowWords + c];
-          uint32_t d = st - ((sc_tile[j] >> (8 * kb)) & 0xFFu);
-          d = d > 15u ? 15u : d;
-          convert8(w, lut2[d], lo[i], hi[i]);
-        }
-        // 4x4 byte transposes: token-major words -> feature-major words
-        const uint32_t a0 = __byte_perm(lo[0], lo[1], 0x5140u), a1 = __byte_perm(lo[0], lo[1], 0x7362u);
-        const uint32_t a2 = __byte_perm(lo[2], lo[3], 0x5140u), a3 = __byte_perm(lo[2], lo[3], 0x7362u);
-        const uint32_t b0 = __byte_perm(hi[0], hi[1], 0x5140u), b1 = __byte_perm(hi[0], hi[1], 0x7362u);
-        const uint32_t b2 = __byte_perm(hi[2], hi[3], 0x5140u), b3 = __byte_perm(hi[2], hi[3], 0x7362u);
-        uint32_t o[8];
-        o[0] = __byte_perm(a0, a2, 0x5410u);
-        o[1] = __byte_perm(a0, a2, 0x7632u);
-        o[2] = __byte_perm(a1, a3, 0x5410u);
-        o[3] = __byte_perm(a1, a3, 0x7632u);
-        o[4] = __byte_perm(b0, b2, 0x5410u);
-        o[5] = __byte_perm(b0, b2, 0x7632u);
-        o[6] = __byte_perm(b1, b3, 0x5410u);
-        o[7] = __byte_perm(b1, b3, 0x7632u);
-#pragma unroll
-        for (int fi = 0; fi < 8; ++fi) {
-          const int row = 8 * c + fi;
-          out_tile[row * 32 + out_word(row, tq)] = o[fi];
-        }
-      }
-    }
-    __syncthreads();
-
-    // Store: each warp writes 16 feature rows; a row is nv bytes at an
-    // arbitrary byte address, written as aligned 32-bit words (bytes at the
-    // two ragged ends).
-    for (int rr = 0; rr < 16; ++rr) {
-      const int row = 16 * warp + rr;
-      uint8_t* dst = fp8_t + cols * row0 + (128 * f + row) * n_e + 128 * b;
-      const int a = (int)(reinterpret_cast<uintptr_t>(dst) & 3u);
-      uint8_t* base = dst - a;
-      const int nwords = (a + nv + 3) >> 2;
-      for (int wi = lane; wi < nwords; wi += 32) {
-        const int t0 = 4 * wi - a;  // tile byte held by the word's first byte
-        uint32_t val;
-        if (a == 0) {
-          val = out_tile[row * 32 + out_word(row, wi)];
-        } else {
-          const uint32_t lo = wi >= 1 ? out_tile[row * 32 + out_word(row, wi - 1)] : 0u;
-          const uint32_t hi = wi < 32 ? out_tile[row * 32 + out_word(row, wi)] : 0u;
-          val = __funnelshift_r(lo, hi, 8 * (4 - a));
-        }
-        if (t0 >= 0 && t0 + 3 < nv) {
-          *reinterpret_cast<uint32_t*>(base + 4 * wi) = val;
-        } else {
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            if (t0 + q >= 0 && t0 + q < nv) base[4 * wi + q] = (uint8_t)(val >> (8 * q));
-        }
-      }
-    }
-    // the __syncthreads at the top of the next tile orders these reads
-    // before the next tile's shared-memory writes
   }
 }
 
@@ -321,13 +328,11 @@ fp4_status fp4_to_fp8_col(const uint8_t* packed, const uint8_t* scales, int64_t 
       !aligned(seg_row_off, 8) || !aligned(seg_scale_off, 8))
     return FP4_ERR_ALIGN;
   if (ntiles == 0 || num_segments == 0) return FP4_OK;
-  // one CTA per tile, grid-stride over tiles
-  static const int occ = occupancy(fp4_to_fp8_col_kernel, kColThreads, 0);
-  int64_t grid = (int64_t)sm_count() * occ;
-  if (grid > ntiles) grid = ntiles;
-  fp4_to_fp8_col_kernel<<<(unsigned)grid, kColThreads, 0, as_stream(stream)>>>(
-      packed, scales, cols, seg_row_off, seg_scale_off, num_segments, ntiles, fp8_t, fp8_t_scales);
-  return after_launch();
+  // one warp per (token block, 32-feature block), grid-stride over them
+  const int64_t nunits = total_blocks * (cols / 32);
+  return launch<fp4_to_fp8_col_kernel>(nunits * 32, kColThreads, 0, as_stream(stream), packed,
+                                       scales, cols, seg_row_off, seg_scale_off, num_segments,
+                                       nunits, fp8_t, fp8_t_scales);
 }
 
 }  // extern "C"

@@ -30,6 +30,17 @@ inline int occupancy(K kernel, int threads, size_t smem) {
   return n;
 }
 
+// Opt `Kernel` in to `smem` bytes of dynamic shared memory (once per
+// process; needed above 48 KB).
+template <auto Kernel>
+inline bool allow_dynamic_smem(size_t smem) {
+  static const bool ok =
+      smem <= 48 * 1024 ||
+      cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
+          cudaSuccess;
+  return ok;
+}
+
 // Grid for a grid-stride loop over `units` thread-level work units: one
 // thread per unit up to one full wave of resident CTAs on every SM.
 template <auto Kernel>

@@ -96,24 +96,73 @@ __device__ __forceinline__ void block_max_to(float m, float* out) {
   }
 }
 
+// Per-kernel constants of the block-scale division u = bmax / den6.
+struct ScaleDiv {
+  float den6;    // 6 * s_t
+  float r_lo;    // RN(RN(1/den6) * (1 - 2^-21)), 0 when den6 is outside [2^-125, 2^125]
+  float r_hi;    // RN(RN(1/den6) * (1 + 2^-21))
+};
+
+__device__ __forceinline__ ScaleDiv make_scale_div(float s_t) {
+  ScaleDiv d;
+  d.den6 = __fmul_rn(6.0f, s_t);
+  if (d.den6 >= 0x1p-125f && d.den6 <= 0x1p125f) {
+    const float r = __frcp_rn(d.den6);
+    d.r_lo = __fmul_rn(r, 0x1.fffffp-1f);
+    d.r_hi = __fmul_rn(r, 0x1.000008p+0f);
+  } else {
+    d.r_lo = d.r_hi = 0.0f;
+  }
+  return d;
+}
+
+// Certified rounding without a division.  For q = RN(x / y) and an encoder
+// E that is monotone in its argument (RN_e4m3, RN_e2m1: both keep the sign,
+// round to nearest and saturate), let r = RN(1/y) with y a normal float in
+// [2^-125, 2^125], L = RN(x * RN(r * (1 - 2^-21))) and
+// H = RN(x * RN(r * (1 + 2^-21))).  Each of the three roundings has relative
+// error <= 2^-24, so (1 - 2^-21)(1 + 2^-24)^3 < 1 - 2^-24 and
+// (1 + 2^-21)(1 - 2^-24)^3 > 1 + 2^-24 put q between L and H whenever x / y
+// is a normal float (below that all three are far under the smallest
+// nonzero E2M1 or E4M3 magnitude and encode to the same signed zero; above
+// it all saturate).  Hence E(L) == E(H) implies E(q) == E(L); otherwise the
+// caller divides exactly.
+
+// Exact fallbacks of the certified fast paths, kept out of line so that the
+// compiler cannot evaluate them speculatively on the common path.
+__device__ __noinline__ uint32_t exact_e4m3_quotient(float x, float y) {
+  return cvt_e4m3(__fdiv_rn(x, y));
+}
+
+__device__ __noinline__ uint32_t exact_e2m1_quotient(float x, float y) {
+  return cvt_e2m1x2(__fdiv_rn(x, y), 0.0f) & 0xFu;
+}
+
 // Quantize one block v[16] (residual already added) under tensor scale s_t.
 // Writes the 8 packed bytes as two words, returns the e4m3 scale byte, and
 // (kEF) leaves the dequantized values in q[16].
 template <bool kSR, bool kEF>
-__device__ __forceinline__ uint32_t quantize_block(const float v[16], float s_t, float den6,
+__device__ __forceinline__ uint32_t quantize_block(const float v[16], float s_t, const ScaleDiv& sd,
                                                    uint64_t g0, uint32_t key0, uint32_t key1,
                                                    uint32_t step0, uint32_t step1, uint2& out,
                                                    float q[16]) {
   float bmax = 0.0f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(v[i]));
-  uint32_t sb = cvt_e4m3(__fdiv_rn(bmax, den6));
-  float eff = __fmul_rn(e4m3_value(sb), s_t);
-  float a[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) a[i] = (eff == 0.0f) ? __fmul_rn(v[i], 0.0f) : __fdiv_rn(v[i], eff);
-  uint32_t codes[16];
+  // e4m3 block scale RN_e4m3(RN(bmax / den6)), through the certified bracket
+  uint32_t sb;
+  {
+    const uint32_t lh = cvt_e4m3x2(__fmul_rn(bmax, sd.r_lo), __fmul_rn(bmax, sd.r_hi));
+    sb = lh & 0xFFu;
+    if (sd.r_lo == 0.0f || sb != (lh >> 8)) sb = exact_e4m3_quotient(bmax, sd.den6);
+  }
+  const float eff = __fmul_rn(e4m3_value(sb), s_t);
+  uint32_t w0, w1;
   if (kSR) {
+    float a[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) a[i] = (eff == 0.0f) ? __fmul_rn(v[i], 0.0f) : __fdiv_rn(v[i], eff);
+    uint32_t codes[16];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       uint64_t quad = (g0 >> 2) + (uint64_t)k;
@@ -123,47 +172,171 @@ __device__ __forceinline__ uint32_t quantize_block(const float v[16], float s_t,
       codes[4 * k + 2] = e2m1_sr(a[4 * k + 2], r.z);
       codes[4 * k + 3] = e2m1_sr(a[4 * k + 3], r.w);
     }
-  } else {
+    w0 = w1 = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      uint32_t byte = cvt_e2m1x2(a[2 * i], a[2 * i + 1]);
-      codes[2 * i] = byte & 0xFu;
-      codes[2 * i + 1] = byte >> 4;
+    for (int i = 0; i < 8; ++i) w0 |= codes[i] << (4 * i);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w1 |= codes[8 + i] << (4 * i);
+  } else if (eff >= 0x1p-125f && eff <= 0x1p125f) {
+    // RTN codes of RN(v / eff) through the certified bracket, 8 at a time
+    const float inv = __frcp_rn(eff);
+    const float il = __fmul_rn(inv, 0x1.fffffp-1f);   // 1 - 2^-21
+    const float ih = __fmul_rn(inv, 0x1.000008p+0f);  // 1 + 2^-21
+    uint32_t lo[2], hi[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float* x = v + 8 * h;
+      lo[h] = cvt_e2m1x8(__fmul_rn(x[0], il), __fmul_rn(x[1], il), __fmul_rn(x[2], il),
+                         __fmul_rn(x[3], il), __fmul_rn(x[4], il), __fmul_rn(x[5], il),
+                         __fmul_rn(x[6], il), __fmul_rn(x[7], il));
+      hi[h] = cvt_e2m1x8(__fmul_rn(x[0], ih), __fmul_rn(x[1], ih), __fmul_rn(x[2], ih),
+                         __fmul_rn(x[3], ih), __fmul_rn(x[4], ih), __fmul_rn(x[5], ih),
+                         __fmul_rn(x[6], ih), __fmul_rn(x[7], ih));
     }
+    w0 = lo[0];
+    w1 = lo[1];
+    // Only the elements whose two bracket codes differ (a few per thousand,
+    // quotients on or next to an E2M1 rounding midpoint) are divided; each
+    // position is its own guarded call so a warp pays only for the positions
+    // some lane needs.
+    uint32_t p0 = lo[0] ^ hi[0], p1 = lo[1] ^ hi[1];  // nibbles still to settle
+    // The lanes of a warp settle their pending elements together, one per
+    // lane per round (usually a single round), sharing one division.
+    const unsigned active = __activemask();
+    while (__any_sync(active, (p0 | p1) != 0u)) {
+      if ((p0 | p1) != 0u) {
+        const bool first = p0 != 0u;
+        const uint32_t p = first ? p0 : p1;
+        const int i = (__ffs(p) - 1) >> 2;
+        const float* x = first ? v : v + 8;
+        float xi = x[0];
+#pragma unroll
+        for (int k = 1; k < 8; ++k) xi = (i == k) ? x[k] : xi;
+        const uint32_t c = exact_e2m1_quotient(xi, eff) << (4 * i);
+        const uint32_t m = 0xFu << (4 * i);
+        if (first) {
+          w0 = (w0 & ~m) | c;
+          p0 &= ~m;
+        } else {
+          w1 = (w1 & ~m) | c;
+          p1 &= ~m;
+        }
+      }
+    }
+  } else {
+    // zero, tiny or huge decoded scale: exact division throughout
+    float a[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) a[i] = (eff == 0.0f) ? __fmul_rn(v[i], 0.0f) : __fdiv_rn(v[i], eff);
+    w0 = cvt_e2m1x8(a[0], a[1], a[2], a[3], a[4], a[5], a[6], a[7]);
+    w1 = cvt_e2m1x8(a[8], a[9], a[10], a[11], a[12], a[13], a[14], a[15]);
   }
-  uint32_t w0 = 0, w1 = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) w0 |= codes[i] << (4 * i);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) w1 |= codes[8 + i] << (4 * i);
   out = make_uint2(w0, w1);
   if (kEF) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) q[i] = __fmul_rn(e2m1_value(codes[i]), eff);
+    for (int i = 0; i < 8; ++i) q[i] = __fmul_rn(e2m1_value(w0 >> (4 * i)), eff);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[8 + i] = __fmul_rn(e2m1_value(w1 >> (4 * i)), eff);
   }
   return sb;
 }
+
+// Blocks handled by one thread per pass of the amax loop: their loads are
+// all issued before any is used, which keeps 4 x 32 (bf16) or 4 x 64 (fp32)
+// bytes per thread in flight.
+constexpr int kAmaxUnroll = 4;
 
 template <bool kBF16, bool kRes>
 __global__ void __launch_bounds__(kThreads)
     amax_kernel(const void* __restrict__ x, const float* __restrict__ residual, int64_t nblocks,
                 float* __restrict__ amax_ws) {
+  constexpr int kWords = kBF16 ? 1 : 2;  // 256-bit loads per block of x
   float m = 0.0f;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
-  for (int64_t b = (int64_t)blockIdx.x * kThreads + threadIdx.x; b < nblocks; b += stride) {
-    float v[16];
-    load_block<kBF16>(x, b, v);
-    if (kRes) {
-      float r[16];
-      load_f32x16_stream(residual + 16 * b, r);
+  for (int64_t b0 = (int64_t)blockIdx.x * kThreads + threadIdx.x; b0 < nblocks;
+       b0 += kAmaxUnroll * stride) {
+    U32x8 raw[kAmaxUnroll][kWords];
+    U32x8 res[kRes ? kAmaxUnroll : 1][2];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = __fadd_rn(v[i], r[i]);
+    for (int u = 0; u < kAmaxUnroll; ++u) {
+      const int64_t b = b0 + u * stride;
+#pragma unroll
+      for (int k = 0; k < kWords; ++k) {
+        if (b < nblocks) {
+          raw[u][k] = ld_stream_v8(static_cast<const uint8_t*>(x) + (kBF16 ? 32 : 64) * b + 32 * k);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) raw[u][k].w[i] = 0u;
+        }
+      }
+      if (kRes) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          if (b < nblocks) {
+            res[u][k] = ld_stream_v8(residual + 16 * b + 8 * k);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) res[u][k].w[i] = 0u;
+          }
+        }
+      }
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
+    for (int u = 0; u < kAmaxUnroll; ++u) {
+      float v[16];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (kBF16) {
+          v[2 * i] = bf16_lo(raw[u][0].w[i]);
+          v[2 * i + 1] = bf16_hi(raw[u][0].w[i]);
+        } else {
+          v[i] = __uint_as_float(raw[u][0].w[i]);
+          v[8 + i] = __uint_as_float(raw[u][kWords - 1].w[i]);
+        }
+      }
+      if (kRes) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          v[i] = __fadd_rn(v[i], __uint_as_float(res[u][0].w[i]));
+          v[8 + i] = __fadd_rn(v[8 + i], __uint_as_float(res[u][1].w[i]));
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
+    }
   }
   block_max_to(m, amax_ws);
 }
+
+// Raw inputs of one block: x (one 256-bit word of bf16, two of fp32) and,
+// with error feedback, the residual (two words).
+template <bool kBF16, bool kRes>
+struct BlockIn {
+  U32x8 x[kBF16 ? 1 : 2];
+  U32x8 r[kRes ? 2 : 1];
+};
+
+template <bool kBF16, bool kRes>
+__device__ __forceinline__ void issue_block(const void* x, const float* residual, int64_t b,
+                                            int64_t nblocks, BlockIn<kBF16, kRes>& in) {
+  if (b < nblocks) {
+    const uint8_t* xb = static_cast<const uint8_t*>(x) + b * (kBF16 ? 32 : 64);
+    in.x[0] = ld_stream_v8(xb);
+    if (!kBF16) in.x[kBF16 ? 0 : 1] = ld_stream_v8(xb + 32);
+    if (kRes) {
+      in.r[0] = ld_v8(residual + 16 * b);
+      in.r[kRes ? 1 : 0] = ld_v8(residual + 16 * b + 8);
+    }
+  }
+}
+
+// Blocks a thread keeps in flight ahead of the one it computes: the loads of
+// the next kDepth blocks of its grid-stride sequence are issued before the
+// current block is quantized, so HBM latency hides behind the arithmetic.
+template <bool kBF16, bool kRes>
+struct QuantPipe {
+  static constexpr int kDepth = (kBF16 && !kRes) ? 2 : 1;
+};
 
 template <bool kBF16, bool kSR, bool kRes>
 __global__ void __launch_bounds__(kThreads)
@@ -171,6 +344,7 @@ __global__ void __launch_bounds__(kThreads)
                     uint64_t seed, uint64_t step, int tscale_mode, float* __restrict__ tensor_scale,
                     const float* __restrict__ amax_ws, uint8_t* __restrict__ packed,
                     uint8_t* __restrict__ scales) {
+  constexpr int kD = QuantPipe<kBF16, kRes>::kDepth;
   float s_t;
   if (tscale_mode == FP4_TSCALE_GIVEN) {
     s_t = sanitize_scale(*tensor_scale);
@@ -178,20 +352,40 @@ __global__ void __launch_bounds__(kThreads)
     s_t = tensor_scale_from_amax(*amax_ws);
     if (blockIdx.x == 0 && threadIdx.x == 0) *tensor_scale = s_t;
   }
-  const float den6 = __fmul_rn(6.0f, s_t);
+  const ScaleDiv sd = make_scale_div(s_t);
   const uint32_t key0 = (uint32_t)seed, key1 = (uint32_t)(seed >> 32);
   const uint32_t st0 = (uint32_t)step, st1 = (uint32_t)(step >> 32);
   const int64_t stride = (int64_t)gridDim.x * kThreads;
-  for (int64_t b = (int64_t)blockIdx.x * kThreads + threadIdx.x; b < nblocks; b += stride) {
+  int64_t b = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+
+  BlockIn<kBF16, kRes> buf[kD + 1];
+#pragma unroll
+  for (int d = 0; d < kD; ++d) issue_block<kBF16, kRes>(x, residual, b + d * stride, nblocks, buf[d]);
+  for (; b < nblocks; b += stride) {
+    issue_block<kBF16, kRes>(x, residual, b + kD * stride, nblocks, buf[kD]);
+    const BlockIn<kBF16, kRes>& in = buf[0];
     float v[16], r[16], q[16];
-    load_block<kBF16>(x, b, v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (kBF16) {
+        v[2 * i] = bf16_lo(in.x[0].w[i]);
+        v[2 * i + 1] = bf16_hi(in.x[0].w[i]);
+      } else {
+        v[i] = __uint_as_float(in.x[0].w[i]);
+        v[8 + i] = __uint_as_float(in.x[kBF16 ? 0 : 1].w[i]);
+      }
+    }
     if (kRes) {
-      load_f32x16(residual + 16 * b, r);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        r[i] = __uint_as_float(in.r[0].w[i]);
+        r[8 + i] = __uint_as_float(in.r[kRes ? 1 : 0].w[i]);
+      }
 #pragma unroll
       for (int i = 0; i < 16; ++i) v[i] = __fadd_rn(v[i], r[i]);
     }
     uint2 out;
-    uint32_t sb = quantize_block<kSR, kRes>(v, s_t, den6, (uint64_t)(16 * b), key0, key1, st0, st1,
+    uint32_t sb = quantize_block<kSR, kRes>(v, s_t, sd, (uint64_t)(16 * b), key0, key1, st0, st1,
                                             out, q);
     *reinterpret_cast<uint2*>(packed + 8 * b) = out;
     scales[b] = (uint8_t)sb;
@@ -200,32 +394,84 @@ __global__ void __launch_bounds__(kThreads)
       for (int i = 0; i < 16; ++i) r[i] = __fsub_rn(v[i], q[i]);
       store_f32x16(residual + 16 * b, r);
     }
+#pragma unroll
+    for (int d = 0; d < kD; ++d) buf[d] = buf[d + 1];
   }
 }
 
+// Decode the 8 codes of w (code i in bits 4i+3..4i) to exact floats via the
+// hardware e2m1x2 -> f16x2 conversion.
+__device__ __forceinline__ void e2m1x8_to_f32(uint32_t w, float o[8]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint32_t h2;
+    const uint16_t byte = (uint16_t)((w >> (8 * k)) & 0xFFu);
+    asm("{\n\t.reg .b8 b;\n\tcvt.u8.u16 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}"
+        : "=r"(h2)
+        : "h"(byte));
+    uint16_t lo = (uint16_t)(h2 & 0xFFFFu), hi = (uint16_t)(h2 >> 16);
+    asm("cvt.f32.f16 %0, %1;" : "=f"(o[2 * k]) : "h"(lo));
+    asm("cvt.f32.f16 %0, %1;" : "=f"(o[2 * k + 1]) : "h"(hi));
+  }
+}
+
+template <bool kBF16Out>
+__device__ __forceinline__ void dequantize_store(uint32_t w0, uint32_t w1, float eff, void* y,
+                                                 int64_t b) {
+  float o[16];
+  e2m1x8_to_f32(w0, o);
+  e2m1x8_to_f32(w1, o + 8);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) o[i] = __fmul_rn(o[i], eff);
+  if (kBF16Out) {
+    U32x8 w;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w.w[i] = pack_bf16x2(o[2 * i], o[2 * i + 1]);
+    st_v8(static_cast<uint16_t*>(y) + 16 * b, w);
+  } else {
+    store_f32x16(static_cast<float*>(y) + 16 * b, o);
+  }
+}
+
+// A thread decodes units of two blocks (16 B of codes, 2 scale bytes, one
+// 128-bit and one 16-bit load), two units per pass with all loads first.
+// An odd last block is decoded alone.
 template <bool kBF16Out>
 __global__ void __launch_bounds__(kThreads)
     dequantize_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ scales,
                       const float* __restrict__ tensor_scale, int64_t nblocks, void* __restrict__ y) {
   const float s_t = tensor_scale ? sanitize_scale(*tensor_scale) : 1.0f;
+  const int64_t npairs = nblocks >> 1;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
-  for (int64_t b = (int64_t)blockIdx.x * kThreads + threadIdx.x; b < nblocks; b += stride) {
-    uint2 p = ld_stream_v2(packed + 8 * b);
-    uint32_t sb = ld_stream_u8(scales + b);
-    float eff = __fmul_rn(e4m3_value(sb), s_t);
-    float o[16];
+  const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  for (int64_t p0 = tid; p0 < npairs; p0 += 2 * stride) {
+    uint4 pk[2];
+    uint32_t sc[2];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) o[i] = __fmul_rn(e2m1_value(p.x >> (4 * i)), eff);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) o[8 + i] = __fmul_rn(e2m1_value(p.y >> (4 * i)), eff);
-    if (kBF16Out) {
-      U32x8 w;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) w.w[i] = pack_bf16x2(o[2 * i], o[2 * i + 1]);
-      st_v8(static_cast<uint16_t*>(y) + 16 * b, w);
-    } else {
-      store_f32x16(static_cast<float*>(y) + 16 * b, o);
+    for (int u = 0; u < 2; ++u) {
+      const int64_t p = p0 + u * stride;
+      if (p < npairs) {
+        pk[u] = ld_stream_v4(packed + 16 * p);
+        uint16_t s2;
+        asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(s2) : "l"(scales + 2 * p));
+        sc[u] = s2;
+      }
     }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int64_t p = p0 + u * stride;
+      if (p < npairs) {
+        dequantize_store<kBF16Out>(pk[u].x, pk[u].y, __fmul_rn(e4m3_value(sc[u] & 0xFFu), s_t),
+                                   y, 2 * p);
+        dequantize_store<kBF16Out>(pk[u].z, pk[u].w, __fmul_rn(e4m3_value(sc[u] >> 8), s_t), y,
+                                   2 * p + 1);
+      }
+    }
+  }
+  if ((nblocks & 1) && tid == 0) {
+    const int64_t b = nblocks - 1;
+    const uint2 q = ld_stream_v2(packed + 8 * b);
+    dequantize_store<kBF16Out>(q.x, q.y, __fmul_rn(e4m3_value(ld_stream_u8(scales + b)), s_t), y, b);
   }
 }
 
@@ -284,7 +530,7 @@ __global__ void __launch_bounds__(kThreads)
     s_t = tensor_scale_from_amax(*amax_ws);
     if (blockIdx.x == 0 && threadIdx.x == 0) *tensor_scale = s_t;
   }
-  const float den6 = __fmul_rn(6.0f, s_t);
+  const ScaleDiv sd = make_scale_div(s_t);
   const uint32_t key0 = (uint32_t)seed, key1 = (uint32_t)(seed >> 32);
   const uint32_t st0 = (uint32_t)step, st1 = (uint32_t)(step >> 32);
   const int64_t stride = (int64_t)gridDim.x * kThreads;
@@ -292,7 +538,7 @@ __global__ void __launch_bounds__(kThreads)
     float v[16], r[16], q[16];
     qdq_update<kG, kRes>(w, g, lr, residual, b, v, r, false);
     uint2 out;
-    uint32_t sb = quantize_block<kSR, true>(v, s_t, den6, (uint64_t)(16 * b), key0, key1, st0, st1,
+    uint32_t sb = quantize_block<kSR, true>(v, s_t, sd, (uint64_t)(16 * b), key0, key1, st0, st1,
                                             out, q);
     if (kPacked) {
       *reinterpret_cast<uint2*>(packed + 8 * b) = out;
@@ -315,12 +561,13 @@ fp4_status launch_amax(const void* x, int dtype, int64_t n, const float* residua
   if (cudaMemsetAsync(amax_ws, 0, sizeof(float), s) != cudaSuccess) return FP4_ERR_CUDA;
   const int64_t nb = n / 16;
   if (nb == 0) return FP4_OK;
+  const int64_t units = (nb + kAmaxUnroll - 1) / kAmaxUnroll;
   if (dtype == FP4_BF16) {
-    if (residual) return launch<amax_kernel<true, true>>(nb, kThreads, 0, s, x, residual, nb, amax_ws);
-    return launch<amax_kernel<true, false>>(nb, kThreads, 0, s, x, residual, nb, amax_ws);
+    if (residual) return launch<amax_kernel<true, true>>(units, kThreads, 0, s, x, residual, nb, amax_ws);
+    return launch<amax_kernel<true, false>>(units, kThreads, 0, s, x, residual, nb, amax_ws);
   }
-  if (residual) return launch<amax_kernel<false, true>>(nb, kThreads, 0, s, x, residual, nb, amax_ws);
-  return launch<amax_kernel<false, false>>(nb, kThreads, 0, s, x, residual, nb, amax_ws);
+  if (residual) return launch<amax_kernel<false, true>>(units, kThreads, 0, s, x, residual, nb, amax_ws);
+  return launch<amax_kernel<false, false>>(units, kThreads, 0, s, x, residual, nb, amax_ws);
 }
 
 template <bool kBF16, bool kSR, bool kRes>
@@ -437,9 +684,10 @@ fp4_status nvfp4_dequantize(const uint8_t* packed, const uint8_t* scales, const 
   const int64_t nb = n / 16;
   if (nb == 0) return FP4_OK;
   cudaStream_t s = as_stream(stream);
+  const int64_t units = (nb / 2 + 1) / 2 + 1;
   if (out_dtype == FP4_BF16)
-    return launch<dequantize_kernel<true>>(nb, kThreads, 0, s, packed, scales, tensor_scale, nb, y);
-  return launch<dequantize_kernel<false>>(nb, kThreads, 0, s, packed, scales, tensor_scale, nb, y);
+    return launch<dequantize_kernel<true>>(units, kThreads, 0, s, packed, scales, tensor_scale, nb, y);
+  return launch<dequantize_kernel<false>>(units, kThreads, 0, s, packed, scales, tensor_scale, nb, y);
 }
 
 fp4_status nvfp4_qdq_amax(const uint16_t* w_bf16, const float* g, float lr, const float* residual,

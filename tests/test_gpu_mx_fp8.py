@@ -158,6 +158,8 @@ SEGMENT_SETS = [
     [129, 0, 1, 127, 128, 0],
     [0, 0, 0, 300],
     [1, 2, 3, 250, 513, 77, 131, 0, 64],
+    list(range(1, 50)),                   # every row start / end alignment
+    [17 * k + 3 for k in range(12)],
 ]
 
 

@@ -276,3 +276,44 @@ def test_qwen_shaped_matrices_sampled():
             wy = ora.nvfp4_dequantize(u8(packed[8 * b0:8 * (b0 + 64)]), u8(scales[b0:b0 + 64]),
                                       wt, 64 * 16)
             assert_bits_equal(yb[16 * b0:16 * (b0 + 64)], ora.bf16_rn(wy), "dequant bf16")
+
+
+def test_rtn_quotients_on_and_near_rounding_midpoints():
+    """Elements whose quotient v / scale lies exactly on, or within a few ulps
+    of, an E2M1 rounding midpoint (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5) and
+    the saturation point, under many non-power-of-two decoded scales: the
+    device's RTN codes must equal RN_e2m1(RN(v / scale)) (the oracle divides
+    each element; the kernel's fast path must fall back exactly here)."""
+    m = fp4()
+    rng = np.random.default_rng(11)
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0], np.float32)
+    blocks = []
+    s_t = np.float32(0.37)
+    for _ in range(1200):
+        bmax = np.float32(rng.uniform(0.05, 40.0))
+        den6 = np.float32(6.0) * s_t
+        sb = ora.e4m3_rn([np.float32(bmax / den6)])[0]
+        eff = np.float32(np.float32(ora.e4m3_value([sb])[0]) * s_t)
+        v = np.zeros(16, np.float32)
+        v[0] = bmax
+        for i in range(1, 16):
+            mid = mids[rng.integers(0, mids.size)] * (1 if rng.random() < 0.5 else -1)
+            base = np.float32(np.float32(mid) * eff)
+            k = int(rng.integers(-3, 4))
+            x = base
+            step = np.float32(np.inf if k > 0 else -np.inf)
+            for _ in range(abs(k)):
+                x = np.nextafter(x, step)
+            v[i] = x if abs(x) < bmax else base
+        blocks.append(v)
+    x = np.concatenate(blocks)
+    ts = torch.full((1,), float(s_t), dtype=torch.float32, device=dev())
+    packed, scales, _ = m.nvfp4_quantize(torch.from_numpy(x).to(dev()), tscale="given",
+                                         tensor_scale=ts)
+    wp, ws, _ = ora.nvfp4_quantize(x, tscale_mode=ora.TSCALE_GIVEN, tensor_scale=float(s_t))
+    assert_bits_equal(u8(scales), ws, "scales")
+    assert_bits_equal(u8(packed), wp, "packed")
+    # the construction really produces quotients on midpoints
+    eff_all = (ora.e4m3_value(ws).astype(np.float32) * s_t).astype(np.float32)
+    q = (x.reshape(-1, 16) / eff_all[:, None]).astype(np.float32)
+    assert np.isin(np.abs(q), mids[:-1]).sum() > 1000
