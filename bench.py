@@ -196,39 +196,29 @@ def build_suite(device, rank=0, small=False, host_inputs=False):
                         nd * (0.5 + 1 / 32 + 1) + 4 * H4 * segs.total_blocks,
                         [lambda: m.fp4_to_fp8_col(dp, ds, segs, ft, fts)]))
 
-    # qwen3_8b_weights: 252 Laplace bf16 matrices
+    # qwen3_8b_weights: 252 Laplace bf16 matrices, one batched launch per pass
     shapes = W.qwen3_8b_weight_shapes(layers=2 if small else 36)
-    mats, amax5, ts5, pk5, sc5, out5 = [], [], [], [], [], []
+    mats, pk5, sc5, out5 = [], [], [], []
     for i, (r, c) in enumerate(shapes):
         w = W.laplace_weight(seed + i, (r, c), device=device).view(-1)
         mats.append(w)
-        amax5.append(zeros(1, f32))
-        ts5.append(zeros(1, f32))
         pk5.append(zeros(r * c // 2, u8))
         sc5.append(zeros(r * c // 16, u8))
         out5.append(zeros(r * c, bf16))
-    st["inputs"] += mats
-    st["outputs"] += pk5 + sc5 + out5 + ts5
-    n5 = sum(w.numel() for w in mats)
     k5 = len(mats)
-
-    def mk_amax(i):
-        return lambda: m.nvfp4_amax(mats[i], amax_ws=amax5[i])
-
-    def mk_quant(i):
-        return lambda: m.nvfp4_quantize(mats[i], tscale="from_amax", amax_ws=amax5[i],
-                                        tensor_scale=ts5[i], packed=pk5[i], scales=sc5[i])
-
-    def mk_deq(i):
-        return lambda: m.nvfp4_dequantize(pk5[i], sc5[i], ts5[i], (mats[i].numel(),), bf16,
-                                          out=out5[i])
-
-    groups.append(Group("nvfp4_amax", "qwen3_8b_weights", 2 * n5 / k5,
-                        [mk_amax(i) for i in range(k5)]))
-    groups.append(Group("nvfp4_quantize", "qwen3_8b_weights", n5 * (2 + 0.5 + 1 / 16) / k5,
-                        [mk_quant(i) for i in range(k5)]))
-    groups.append(Group("nvfp4_dequantize", "qwen3_8b_weights", n5 * (0.5 + 1 / 16 + 2) / k5,
-                        [mk_deq(i) for i in range(k5)]))
+    amax5, ts5 = zeros(k5, f32), zeros(k5, f32)
+    qbatch = m.Batch(xs=mats, packed=pk5, scales=sc5)
+    dbatch = m.Batch(packed=pk5, scales=sc5, ys=out5, sizes=[w.numel() for w in mats])
+    st["inputs"] += mats
+    st["outputs"] += pk5 + sc5 + out5 + [ts5]
+    n5 = sum(w.numel() for w in mats)
+    groups.append(Group("nvfp4_amax", "qwen3_8b_weights", 2 * n5,
+                        [lambda: m.nvfp4_amax_batched(qbatch, bf16, amax=amax5)]))
+    groups.append(Group("nvfp4_quantize", "qwen3_8b_weights", n5 * (2 + 0.5 + 1 / 16),
+                        [lambda: m.nvfp4_quantize_batched(qbatch, bf16, tscale="from_amax",
+                                                          tensor_scale=ts5, amax=amax5)]))
+    groups.append(Group("nvfp4_dequantize", "qwen3_8b_weights", n5 * (0.5 + 1 / 16 + 2),
+                        [lambda: m.nvfp4_dequantize_batched(dbatch, ts5, bf16)]))
     st["elements"] = {"nvfp4_roundtrip": n1, "fp4quant_acts": n2, "nvfp4_train": n3,
                       "moe_tokens": n4, "moe_dispatched": nd, "qwen3_8b_weights": n5}
     return groups, st

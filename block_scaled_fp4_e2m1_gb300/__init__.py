@@ -5,12 +5,14 @@ include/fp4codec.h); this package is its Python binding.  Importing the
 package does not load the library; the first call does, and raises if it has
 not been built (there is no CPU fallback).
 """
-from .codec import (Segments, fp4_seg_scale_offsets, fp4_to_fp8_col, fp4_to_fp8_row,
+from .codec import (Batch, Segments, fp4_seg_scale_offsets, fp4_to_fp8_col, fp4_to_fp8_row,
                     fp4quant_decode, fp4quant_encode, kernel_launches, mxfp4_quantize,
                     nvfp4_amax, nvfp4_dequantize, nvfp4_qdq, nvfp4_qdq_amax, nvfp4_quantize,
-                    nvfp4_quantize_noalloc)
+                    nvfp4_quantize_noalloc, nvfp4_amax_batched,
+                    nvfp4_quantize_batched, nvfp4_dequantize_batched)
 
 __all__ = [
+    "Batch", "nvfp4_amax_batched", "nvfp4_quantize_batched", "nvfp4_dequantize_batched",
     "Segments", "fp4_seg_scale_offsets", "fp4_to_fp8_col", "fp4_to_fp8_row", "fp4quant_decode",
     "fp4quant_encode", "kernel_launches", "mxfp4_quantize", "nvfp4_amax", "nvfp4_dequantize",
     "nvfp4_qdq", "nvfp4_qdq_amax", "nvfp4_quantize", "nvfp4_quantize_noalloc",

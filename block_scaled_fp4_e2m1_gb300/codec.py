@@ -6,6 +6,7 @@ the computation runs in the library's CUDA kernels.
 """
 from __future__ import annotations
 
+import ctypes
 from typing import Optional, Sequence, Tuple
 
 import torch
@@ -151,6 +152,76 @@ def nvfp4_quantize_noalloc(x: torch.Tensor, residual: Optional[torch.Tensor] = N
     call("nvfp4_quantize_noalloc", _ptr(x), _dtype(x, "x"), n, _ptr(residual), _ROUND[rounding],
          seed, step, _ptr(tensor_scale), _ptr(packed), _ptr(scales), _stream(dev))
     return packed, scales, tensor_scale
+
+
+# --------------------------------------------------------- NVFP4, batched
+
+class Batch:
+    """A list of independent tensors for the batched NVFP4 calls: the
+    descriptor table of include/fp4codec.h (fp4_tensor_desc), checked and
+    numbered on the host by fp4_batch_plan and uploaded once to the device.
+    Holds references to the tensors it points at."""
+
+    DESC = None  # numpy dtype of fp4_tensor_desc, built on first use
+
+    def __init__(self, xs=None, packed=None, scales=None, ys=None, sizes=None, device=None):
+        import numpy as np
+        if Batch.DESC is None:
+            Batch.DESC = np.dtype([("x", "<u8"), ("packed", "<u8"), ("scales", "<u8"),
+                                   ("y", "<u8"), ("n", "<i8"), ("chunk_start", "<i8")])
+        lists = [lst for lst in (xs, packed, scales, ys) if lst is not None]
+        count = len(lists[0]) if lists else len(sizes)
+        if sizes is None:
+            src = xs if xs is not None else ys
+            sizes = [t.numel() for t in src]
+        self.count = count
+        self.sizes = [int(s) for s in sizes]
+        self._keep = [xs, packed, scales, ys]
+        host = np.zeros(count, Batch.DESC)
+        for name, lst in (("x", xs), ("packed", packed), ("scales", scales), ("y", ys)):
+            if lst is not None:
+                for i, t in enumerate(lst):
+                    _cuda(t, name)
+                    host[name][i] = t.data_ptr()
+        host["n"] = self.sizes
+        total = ctypes.c_int64(0)
+        call("fp4_batch_plan", host.ctypes.data, count, ctypes.addressof(total))
+        self.total_chunks = int(total.value)
+        self.host = host
+        dev = device if device is not None else (lists[0][0].device if lists and count else "cuda")
+        self.desc = torch.from_numpy(host.view(np.uint8).copy()).to(dev)
+        self.device = self.desc.device
+
+
+def nvfp4_amax_batched(batch: Batch, dtype: torch.dtype,
+                       amax: Optional[torch.Tensor] = None) -> torch.Tensor:
+    amax = torch.empty(batch.count, dtype=torch.float32, device=batch.device) if amax is None else amax
+    call("nvfp4_amax_batched", _ptr(batch.desc), batch.count, batch.total_chunks, _DT[dtype],
+         _ptr(amax), _stream(batch.device))
+    return amax
+
+
+def nvfp4_quantize_batched(batch: Batch, dtype: torch.dtype, rounding: str = "rtn",
+                           seed: int = 0, step: int = 0, tscale: str = "compute",
+                           tensor_scale: Optional[torch.Tensor] = None,
+                           amax: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Quantizes every tensor of the batch into its packed/scales buffers;
+    returns the per-tensor scales (fp32 [count])."""
+    dev = batch.device
+    if tensor_scale is None:
+        tensor_scale = torch.ones(batch.count, dtype=torch.float32, device=dev)
+    if amax is None and tscale != "given":
+        amax = torch.empty(batch.count, dtype=torch.float32, device=dev)
+    call("nvfp4_quantize_batched", _ptr(batch.desc), batch.count, batch.total_chunks, _DT[dtype],
+         _ROUND[rounding], seed, step, _TSCALE[tscale], _ptr(tensor_scale), _ptr(amax),
+         _stream(dev))
+    return tensor_scale
+
+
+def nvfp4_dequantize_batched(batch: Batch, tensor_scale: Optional[torch.Tensor],
+                             out_dtype: torch.dtype = torch.bfloat16) -> None:
+    call("nvfp4_dequantize_batched", _ptr(batch.desc), batch.count, batch.total_chunks,
+         _ptr(tensor_scale), _DT[out_dtype], _stream(batch.device))
 
 
 # ------------------------------------------------------------------ MXFP4

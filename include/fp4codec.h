@@ -105,6 +105,7 @@ fp4_status nvfp4_quantize(const void* x, int dtype, int64_t n, float* residual,
 /* y[i] = value(code_i) * (e4m3(scales[i/16]) * s_t), one fp32 product,
  * then rounded to bf16 (nearest-even) if out_dtype is FP4_BF16.
  * ([WP2] "Block scaling", step 5: multiply back by the scale.)
+ *   packed        [n/2], 16-byte aligned; scales [n/16], 2-byte aligned
  *   tensor_scale  1 fp32 on the device, or NULL for s_t = 1
  *   y             [n] out, 32-byte aligned; n % 16 == 0 */
 fp4_status nvfp4_dequantize(const uint8_t* packed, const uint8_t* scales,
@@ -152,6 +153,56 @@ fp4_status nvfp4_quantize_noalloc(const void* x, int dtype, int64_t n, float* re
                                   int rounding, uint64_t seed, uint64_t step,
                                   float* tensor_scale, uint8_t* packed, uint8_t* scales,
                                   void* stream);
+
+/* ------------------------------------------------------- NVFP4, batched
+ * The same NVFP4 operations on a list of independent tensors in one launch
+ * per pass (a whole model's weight matrices, say), each tensor with its own
+ * per-tensor scale.  The result for every tensor is bit-identical to the
+ * single-tensor call on it.  Each tensor is split into work chunks of
+ * FP4_BATCH_CHUNK_BLOCKS 16-element blocks; the chunks of all tensors form
+ * one flat index space that the kernels walk, so small tensors cost no
+ * launch of their own.
+ */
+#define FP4_BATCH_CHUNK_BLOCKS 256
+
+/* One tensor of a batch.  The array of these descriptors lives in device
+ * memory (the caller fills it, e.g. by copying a host array prepared with
+ * fp4_batch_plan).  Pointers are device pointers; fields an operation does
+ * not use may be NULL (x for dequantize, y for amax/quantize). */
+typedef struct {
+  const void* x;        /* [n] input, fp32 or bf16, 32-byte aligned */
+  uint8_t* packed;      /* [n/2] codes, 16-byte aligned */
+  uint8_t* scales;      /* [n/16] e4m3 block scales, 2-byte aligned */
+  void* y;              /* [n] dequantized output, 32-byte aligned */
+  int64_t n;            /* elements, n % 16 == 0 (0 allowed) */
+  int64_t chunk_start;  /* index of the tensor's first chunk (fp4_batch_plan) */
+} fp4_tensor_desc;
+
+/* Host helper: checks every descriptor of a host array (n % 16, alignment of
+ * the non-NULL pointers) and fills chunk_start; *total_chunks receives the
+ * number of chunks of the batch.  The batched calls trust a table that
+ * passed this check. */
+fp4_status fp4_batch_plan(fp4_tensor_desc* host_desc, int32_t count, int64_t* total_chunks);
+
+/* amax[t] = max |x_t[i]| for every tensor t (as nvfp4_amax); amax is a
+ * device array of count fp32 (4-byte aligned), zeroed and written. */
+fp4_status nvfp4_amax_batched(const fp4_tensor_desc* desc, int32_t count, int64_t total_chunks,
+                              int dtype, float* amax, void* stream);
+
+/* nvfp4_quantize on every tensor (no error feedback): tensor_scale and amax
+ * are device arrays of count fp32, read or written per tscale_mode exactly as
+ * the single-tensor call does with its scalars; COMPUTE runs the batched
+ * amax pass first.  Stochastic rounding draws with the element index inside
+ * each tensor, as the single-tensor call does. */
+fp4_status nvfp4_quantize_batched(const fp4_tensor_desc* desc, int32_t count, int64_t total_chunks,
+                                  int dtype, int rounding, uint64_t seed, uint64_t step,
+                                  int tscale_mode, float* tensor_scale, float* amax, void* stream);
+
+/* nvfp4_dequantize on every tensor; tensor_scale is a device array of count
+ * fp32, or NULL for scale 1. */
+fp4_status nvfp4_dequantize_batched(const fp4_tensor_desc* desc, int32_t count,
+                                    int64_t total_chunks, const float* tensor_scale, int out_dtype,
+                                    void* stream);
 
 /* ------------------------------------------------------------------ MXFP4
  * [MoE-FP4] "方法概述" / "核心技术贡献" 2 (BF16ToFP4Row): each row in

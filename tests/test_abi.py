@@ -131,3 +131,34 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         _lib.lib()
+
+
+def test_batch_plan_host_helper(L):
+    import numpy as np
+    desc = np.dtype([("x", "<u8"), ("packed", "<u8"), ("scales", "<u8"), ("y", "<u8"),
+                     ("n", "<i8"), ("chunk_start", "<i8")])
+    assert desc.itemsize == 48
+    h = np.zeros(4, desc)
+    h["x"] = A
+    h["packed"] = A
+    h["scales"] = A
+    h["n"] = [16 * 256 * 3 + 16, 0, 16, 16 * 256]
+    total = ctypes.c_int64(-1)
+    assert L.fp4_batch_plan(h.ctypes.data, 4, ctypes.addressof(total)) == 0
+    assert list(h["chunk_start"]) == [0, 4, 4, 5] and total.value == 6
+    h["n"][2] = 8
+    assert L.fp4_batch_plan(h.ctypes.data, 4, ctypes.addressof(total)) == 3
+    h["n"][2] = 16
+    h["scales"][1] = A + 1
+    assert L.fp4_batch_plan(h.ctypes.data, 4, ctypes.addressof(total)) == 2
+    assert L.fp4_batch_plan(None, 4, ctypes.addressof(total)) == 1
+    # batched entry points: checks before anything is enqueued
+    assert L.nvfp4_amax_batched(A, 2, 3, 7, A, None) == 4
+    assert L.nvfp4_amax_batched(A, 2, 3, 1, None, None) == 1
+    assert L.nvfp4_amax_batched(A + 4, 2, 3, 1, A, None) == 2
+    assert L.nvfp4_amax_batched(A, -1, 3, 1, A, None) == 3
+    assert L.nvfp4_quantize_batched(A, 2, 3, 1, 5, 0, 0, 1, A, A, None) == 5
+    assert L.nvfp4_quantize_batched(A, 2, 3, 1, 0, 0, 0, 1, A, None, None) == 1
+    assert L.nvfp4_quantize_batched(A, 2, 3, 1, 0, 0, 0, 0, None, None, None) == 1
+    assert L.nvfp4_dequantize_batched(A, 2, 3, A + 2, 0, None) == 2
+    assert L.nvfp4_dequantize_batched(A, 2, 3, None, 3, None) == 4
