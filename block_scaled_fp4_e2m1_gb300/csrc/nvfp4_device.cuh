@@ -134,6 +134,27 @@ __device__ __noinline__ uint32_t exact_e2m1_quotient(float x, float y) {
   return cvt_e2m1x2(__fdiv_rn(x, y), 0.0f) & 0xFu;
 }
 
+// Settling a bracket that straddles a rounding midpoint, without dividing.
+// The two bracket codes are the neighbours lo < hi around the midpoint M of
+// their values, and |x| / y lies within 2^-20 of M.  Then
+// r = RN(M * y - |x|) is exact (M * y and |x| are multiples of a common
+// quantum at most 2^7 apart), and q = RN(|x| / y) equals M exactly when |r|
+// is at most y times half an ulp of M on the side of q (half an ulp below a
+// power of two is half as large; at that bound the tie goes to M, whose
+// significand is even).  So the code is the even one of lo and hi when
+// q == M, lo when M * y > |x|, hi otherwise; no division, and exact.
+__device__ __forceinline__ uint32_t settle_midpoint(float ax, float y, float M, uint32_t lo,
+                                                    uint32_t hi) {
+  const float r = __fmaf_rn(M, y, -ax);
+  const uint32_t mb = __float_as_uint(M);
+  const uint32_t half_bits = ((mb >> 23) - 24u) << 23;      // 2^(exponent(M) - 24)
+  const bool pow2 = (mb & 0x7FFFFFu) == 0u;
+  float half = __fmul_rn(y, __uint_as_float(half_bits));
+  if (pow2 && r > 0.0f) half = __fmul_rn(half, 0.5f);
+  if (fabsf(r) <= half) return (lo & 1u) ? hi : lo;
+  return r > 0.0f ? lo : hi;
+}
+
 // Quantize one block v[16] (residual already added) under tensor scale s_t.
 // Writes the 8 packed bytes as two words, returns the e4m3 scale byte, and
 // (kEF) leaves the dequantized values in q[16].
@@ -150,7 +171,16 @@ __device__ __forceinline__ uint32_t quantize_block(const float v[16], float s_t,
   {
     const uint32_t lh = cvt_e4m3x2(__fmul_rn(bmax, sd.r_lo), __fmul_rn(bmax, sd.r_hi));
     sb = lh & 0xFFu;
-    if (sd.r_lo == 0.0f || sb != (lh >> 8)) sb = exact_e4m3_quotient(bmax, sd.den6);
+    if (sd.r_lo == 0.0f || sb != (lh >> 8)) {
+      // the bracket straddles the e4m3 midpoint between codes sb and sb + 1
+      const uint32_t hb = lh >> 8;
+      if (sd.r_lo != 0.0f && hb == sb + 1u && sd.den6 >= 0x1p-100f) {
+        const float M = __fmul_rn(__fadd_rn(e4m3_value(sb), e4m3_value(hb)), 0.5f);
+        sb = settle_midpoint(bmax, sd.den6, M, sb, hb);
+      } else {
+        sb = exact_e4m3_quotient(bmax, sd.den6);
+      }
+    }
   }
   const float eff = __fmul_rn(e4m3_value(sb), s_t);
   uint32_t w0, w1;
@@ -196,11 +226,11 @@ __device__ __forceinline__ uint32_t quantize_block(const float v[16], float s_t,
     // position is its own guarded call so a warp pays only for the positions
     // some lane needs.
     uint32_t p0 = lo[0] ^ hi[0], p1 = lo[1] ^ hi[1];  // nibbles still to settle
-    // The lanes of a warp settle their pending elements together, one per
-    // lane per round (usually a single round), sharing one division.
-    const unsigned active = __activemask();
-    while (__any_sync(active, (p0 | p1) != 0u)) {
-      if ((p0 | p1) != 0u) {
+    // Elements whose two bracket codes differ (a few per thousand: quotients
+    // on or next to an E2M1 rounding midpoint, many of them exact ties for
+    // bf16 weights) are settled one at a time.
+    while ((p0 | p1) != 0u) {
+      {
         const bool first = p0 != 0u;
         const uint32_t p = first ? p0 : p1;
         const int i = (__ffs(p) - 1) >> 2;
@@ -208,7 +238,19 @@ __device__ __forceinline__ uint32_t quantize_block(const float v[16], float s_t,
         float xi = x[0];
 #pragma unroll
         for (int k = 1; k < 8; ++k) xi = (i == k) ? x[k] : xi;
-        const uint32_t c = exact_e2m1_quotient(xi, eff) << (4 * i);
+        // the element's lo/hi codes straddle the E2M1 midpoint between
+        // magnitudes ml and ml + 1
+        const uint32_t cl = ((first ? w0 : w1) >> (4 * i)) & 0xFu;
+        const uint32_t ch = ((first ? hi[0] : hi[1]) >> (4 * i)) & 0xFu;
+        const uint32_t ml = cl & 7u;
+        uint32_t code;
+        if ((ch & 7u) == ml + 1u && (ch & 8u) == (cl & 8u) && eff >= 0x1p-100f) {
+          const float M = __fmul_rn(__fadd_rn(e2m1_value(ml), e2m1_value(ml + 1u)), 0.5f);
+          code = (cl & 8u) | settle_midpoint(fabsf(xi), eff, M, ml, ml + 1u);
+        } else {
+          code = exact_e2m1_quotient(xi, eff);
+        }
+        const uint32_t c = code << (4 * i);
         const uint32_t m = 0xFu << (4 * i);
         if (first) {
           w0 = (w0 & ~m) | c;

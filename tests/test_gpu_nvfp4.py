@@ -317,3 +317,23 @@ def test_rtn_quotients_on_and_near_rounding_midpoints():
     eff_all = (ora.e4m3_value(ws).astype(np.float32) * s_t).astype(np.float32)
     q = (x.reshape(-1, 16) / eff_all[:, None]).astype(np.float32)
     assert np.isin(np.abs(q), mids[:-1]).sum() > 1000
+
+
+def test_rtn_structural_ties_full_matrix():
+    """bf16 weights under the computed tensor scale amax / (6 * 448) put many
+    quotients v / scale exactly on E2M1 rounding midpoints (and some block
+    maxima exactly on E4M3 midpoints); a whole 4M-element matrix is compared
+    with the oracle, which divides every element."""
+    m = fp4()
+    w = workloads.laplace_weight(321, (1024, 4096), device=dev()).view(-1)
+    packed, scales, ts = m.nvfp4_quantize(w)
+    wn = to_f32_np(w)
+    wp, ws, wt = ora.nvfp4_quantize(wn)
+    assert np.float32(ts.item()) == np.float32(wt)
+    assert_bits_equal(u8(scales), ws, "scales")
+    assert_bits_equal(u8(packed), wp, "packed")
+    # the matrix really has exact ties (quotients equal to a midpoint)
+    eff = (ora.e4m3_value(ws).astype(np.float32) * np.float32(wt)).astype(np.float32)
+    q = (wn.reshape(-1, 16) / eff[:, None]).astype(np.float32)
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32)
+    assert np.isin(np.abs(q), mids).sum() > 1000
