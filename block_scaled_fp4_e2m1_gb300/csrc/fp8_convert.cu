@@ -114,19 +114,30 @@ __global__ void __launch_bounds__(kRowThreads)
 
 // ------------------------------------------------------------------- col
 //
-// Work unit: one warp converts one FP8 scale block, i.e. 128 tokens of one
-// segment x 32 features (one MXFP4 scale column).  Lane (g, c) = (lane & 7,
-// lane >> 3) owns tokens 16g .. 16g+15 and features 8c .. 8c+7 of the unit:
-// it loads one 32-bit word of 8 codes and one scale byte per token, the warp
-// reduces the block's target scale with three shuffles, each lane converts
-// its 16 words through the shift tables and transposes them into 8 feature
-// rows x 16 token bytes, and writes those rows to the (unaligned) segment
-// output with aligned 16-byte stores assembled from its own bytes and the
-// next lane's.  No shared-memory tile and no CTA barrier: the warps of a
-// CTA are independent, and consecutive warps take neighbouring feature
-// blocks of the same token block so their 16-byte row slices share sectors.
+// Work unit: one warp converts one 32-feature block (one MXFP4 scale column)
+// over a run of up to kColRun consecutive 128-token blocks of the global
+// block order (a run may cross segment boundaries).  Per token block:
+//   - lane (g, c) = (lane >> 1, lane & 1) loads the 16 codes of features
+//     16c .. 16c+15 (8 bytes) and the scale byte of tokens 8g .. 8g+7;
+//   - the block's target scale S_t is one warp max reduction;
+//   - each lane converts its 8 tokens x 16 features through the shift
+//     tables and transposes them (4 x 4 byte transposes) into 16 feature
+//     rows x 8 token bytes, written to the warp's tile in shared memory
+//     (32 feature rows of 128 token bytes);
+//   - the warp then writes the 32 rows one at a time, lane l storing the
+//     l-th aligned 32-bit word of the row's output span.  A row's output
+//     start is byte-aligned only, so each word is two tile words funnel-
+//     shifted, and the last (start mod 4) bytes of the row are carried in a
+//     slot before the row to the next block of the same segment.  Inside a
+//     run every word is whole; only the first and last block of a run of
+//     one segment write partial words, byte by byte.
+// No CTA barrier in the loop: the warps of a CTA are independent, and
+// consecutive warps take neighbouring feature blocks of the same run, so
+// their 16-byte row slices of the input share sectors in L2.
 
 constexpr int kColThreads = 256;
+constexpr int kColRun = 16;      // token blocks per unit
+constexpr int kTileRow = 34;     // tile words per feature row: pad, carry, 32 data words
 
 // Largest e in [0, nseg) with off[e] <= v, for off non-decreasing, off[0] = 0
 // <= v < off[nseg]: a 32-way search by one warp.
@@ -146,151 +157,202 @@ __device__ __forceinline__ int find_segment(const int64_t* __restrict__ off, int
   return lo;
 }
 
-// Bytes o .. o+15 (1 <= o <= 15) of the 32-byte sequence x[0..3] | y[0..3].
-__device__ __forceinline__ uint4 window16(uint4 x, uint4 y, int o) {
-  uint32_t w0 = x.x, w1 = x.y, w2 = x.z, w3 = x.w, w4 = y.x, w5 = y.y, w6 = y.z, w7 = y.w;
-  if (o & 8) {
-    w0 = w2; w1 = w3; w2 = w4; w3 = w5; w4 = w6; w5 = w7;
-  }
-  if (o & 4) {
-    w0 = w1; w1 = w2; w2 = w3; w3 = w4; w4 = w5;
-  }
-  const uint32_t sh = 8u * (uint32_t)(o & 3);
-  return make_uint4(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh),
-                    __funnelshift_r(w2, w3, sh), __funnelshift_r(w3, w4, sh));
+// 4 x 4 byte transpose: x[i] holds bytes (i, 0..3); y[j] receives (0..3, j).
+__device__ __forceinline__ void transpose4(const uint32_t x[4], uint32_t y[4]) {
+  const uint32_t a0 = __byte_perm(x[0], x[1], 0x5140u), a1 = __byte_perm(x[0], x[1], 0x7362u);
+  const uint32_t a2 = __byte_perm(x[2], x[3], 0x5140u), a3 = __byte_perm(x[2], x[3], 0x7362u);
+  y[0] = __byte_perm(a0, a2, 0x5410u);
+  y[1] = __byte_perm(a0, a2, 0x7632u);
+  y[2] = __byte_perm(a1, a3, 0x5410u);
+  y[3] = __byte_perm(a1, a3, 0x7632u);
 }
 
-// Store bytes lo .. hi-1 (0 <= lo < hi <= 16) of the 16-byte value v to the
-// 16-byte aligned p: one 128-bit store when the chunk is whole, otherwise
-// the whole 32-bit words inside [lo, hi) as word stores and the bytes of the
-// (at most two) edge words as byte stores, all predicated, no loop.
-__device__ __forceinline__ void store_chunk(uint8_t* p, uint4 v, int lo, int hi) {
-  if (lo <= 0 && hi >= 16) {
-    *reinterpret_cast<uint4*>(p) = v;
+// Bytes [lo, hi) (0 <= lo < hi <= 4) of the 4-byte value v to p[lo .. hi).
+__device__ __forceinline__ void store_bytes(uint8_t* p, uint32_t v, int lo, int hi) {
+  if (lo == 0 && hi == 4) {
+    *reinterpret_cast<uint32_t*>(p) = v;
     return;
   }
-  const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int t = 0; t < 4; ++t)
-    if (lo <= 4 * t && 4 * t + 4 <= hi) reinterpret_cast<uint32_t*>(p)[t] = vw[t];
-  // edge words: the word holding byte lo (if lo is not word aligned) and the
-  // word holding byte hi - 1 (if hi is not word aligned)
-  const int wl = lo >> 2, wh = (hi - 1) >> 2;
-  const uint32_t xl = vw[0] * (wl == 0) + vw[1] * (wl == 1) + vw[2] * (wl == 2) + vw[3] * (wl == 3);
-  const uint32_t xh = vw[0] * (wh == 0) + vw[1] * (wh == 1) + vw[2] * (wh == 2) + vw[3] * (wh == 3);
+  for (int j = 0; j < 4; ++j)
+    if (j >= lo && j < hi) p[j] = (uint8_t)(v >> (8 * j));
+}
+
+// The segment holding a token block, walked forward block by block.
+struct SegPos {
+  int e;
+  int64_t sofs, send;  // its blocks: [sofs, send)
+  int64_t row0, n_e;   // its rows
+};
+
+__device__ __forceinline__ void seg_load(SegPos& p, const int64_t* __restrict__ row_off,
+                                         const int64_t* __restrict__ scale_off) {
+  p.sofs = scale_off[p.e];
+  p.send = scale_off[p.e + 1];
+  p.row0 = row_off[p.e];
+  p.n_e = row_off[p.e + 1] - p.row0;
+}
+
+// Moves p forward to the segment holding block fb (warp-uniform); false if
+// the offsets end before fb.
+__device__ __forceinline__ bool seg_advance(SegPos& p, int64_t fb, int nseg,
+                                            const int64_t* __restrict__ row_off,
+                                            const int64_t* __restrict__ scale_off) {
+  while (fb >= p.send && p.e + 1 < nseg) {
+    ++p.e;
+    seg_load(p, row_off, scale_off);
+  }
+  return fb < p.send;
+}
+
+// Codes (16 features) and scale bytes of a lane's 8 tokens of one block.
+struct ColIn {
+  uint2 w[8];
+  uint32_t s[8];
+};
+
+__device__ __forceinline__ void col_issue(ColIn& in, const uint8_t* __restrict__ packed,
+                                          const uint8_t* __restrict__ scales, const SegPos& p,
+                                          int64_t fb, int64_t row_bytes, int64_t kblocks, int kb,
+                                          int g, int c) {
+  const int64_t t0 = 128 * (fb - p.sofs);
+  const int64_t left = p.n_e - t0 - 8 * g;  // tokens of this lane's 8 that exist
+  const int64_t r = p.row0 + t0 + 8 * g;
+  const uint8_t* pw = packed + r * row_bytes + 16 * kb + 8 * c;
+  const uint8_t* ps = scales + r * kblocks + kb;
 #pragma unroll
-  for (int q = 0; q < 3; ++q) {
-    if ((lo & 3) != 0 && q < 4 - (lo & 3) && lo + q < hi)
-      p[lo + q] = (uint8_t)(xl >> (8 * ((lo + q) & 3)));
-    const int bh = 4 * wh + q;      // bytes of the last word before hi
-    if ((hi & 3) != 0 && q < (hi & 3) && bh >= lo && (wl != wh || (lo & 3) == 0))
-      p[bh] = (uint8_t)(xh >> (8 * q));
+  for (int i = 0; i < 8; ++i) {
+    const bool ok = i < left;
+    in.w[i] = ok ? ld_stream_v2(pw + i * row_bytes) : make_uint2(0u, 0u);
+    in.s[i] = ok ? ld_stream_u8(ps + i * kblocks) : 0u;
   }
 }
 
+// Converts and writes one token block of one 32-feature block (see above).
+__device__ __forceinline__ void col_block(const ColIn& in, const SegPos& p, int64_t fb, bool carry,
+                                          bool run_end, int64_t cols, int kb, int lane, int g,
+                                          int c, const uint2* lut2, uint32_t* tile,
+                                          uint8_t* __restrict__ fp8_t,
+                                          float* __restrict__ fp8_t_scales) {
+  const int64_t b = fb - p.sofs;  // block inside the segment
+  const int64_t t0 = 128 * b;
+  const int nv = p.n_e - t0 < 128 ? (int)(p.n_e - t0) : 128;  // tokens in this block
+  uint32_t st = in.s[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) st = max(st, in.s[i]);
+  st = __reduce_max_sync(0xFFFFFFFFu, st);
+  fp8_t_scales[cols * p.sofs + (32 * kb + lane) * (p.send - p.sofs) + b] = ue8m0_to_f32(st);
+
+  // Convert and transpose into the tile: row 16c + f, token bytes 8g .. 8g+7.
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t x[4][4];  // x[i][k]: token 4h+i, features 4k .. 4k+3
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t d = st - in.s[4 * h + i];
+      d = d > 15u ? 15u : d;
+      const uint2 l = lut2[d];
+      convert8(in.w[4 * h + i].x, l, x[i][0], x[i][1]);
+      convert8(in.w[4 * h + i].y, l, x[i][2], x[i][3]);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t xi[4] = {x[0][k], x[1][k], x[2][k], x[3][k]};
+      uint32_t y[4];
+      transpose4(xi, y);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) tile[(16 * c + 4 * k + j) * kTileRow + 2 + 2 * g + h] = y[j];
+    }
+  }
+  __syncwarp();
+
+  // Store the 32 rows: row r of this block covers output bytes
+  // [D, D + nv), D = fp8_t + cols*row0 + (32kb + r)*n_e + t0.
+  uint8_t* D = fp8_t + cols * p.row0 + 32 * kb * p.n_e + t0;
+  if (carry && !run_end) {  // every word of every row is whole
+#pragma unroll 8
+    for (int r = 0; r < 32; ++r, D += p.n_e) {
+      const uint32_t a = (uint32_t)reinterpret_cast<uintptr_t>(D) & 3u;
+      const uint32_t* row = tile + r * kTileRow + 1;  // row[0] is the carry slot
+      reinterpret_cast<uint32_t*>(D - a)[lane] =
+          __funnelshift_rc(row[lane], row[lane + 1], 8u * (4u - a));
+    }
+  } else {
+    for (int r = 0; r < 32; ++r, D += p.n_e) {
+      const uint32_t a = (uint32_t)reinterpret_cast<uintptr_t>(D) & 3u;
+      uint8_t* const W = D - a;  // word l covers row bytes [4l - a, 4l - a + 4)
+      const uint32_t* row = tile + r * kTileRow + 1;
+      const uint32_t v = __funnelshift_rc(row[lane], row[lane + 1], 8u * (4u - a));
+      // valid row bytes: [lo, hi) relative to t0
+      const int lo = carry ? -(int)a : 0;
+      const int hi = run_end ? nv : 128 - (int)a;
+      const int p0 = 4 * lane - (int)a;
+      const int blo = lo - p0 > 0 ? lo - p0 : 0;
+      const int bhi = hi - p0 < 4 ? hi - p0 : 4;
+      if (blo < bhi) store_bytes(W + 4 * lane, v, blo, bhi);
+      if (lane == 0 && hi > 128 - (int)a) {  // word 32: the row's last a bytes
+        const uint32_t v32 = __funnelshift_rc(row[32], 0u, 8u * (4u - a));
+        store_bytes(W + 128, v32, 0, hi - (128 - (int)a));
+      }
+    }
+  }
+  __syncwarp();
+  if (!run_end) tile[lane * kTileRow + 1] = tile[lane * kTileRow + 1 + 32];
+  __syncwarp();
+}
+
+// The loads of the next token block are issued before the current one is
+// converted and written (two register buffers, swapped by unrolling).
 __global__ void __launch_bounds__(kColThreads)
     fp4_to_fp8_col_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ scales,
                           int64_t cols, const int64_t* __restrict__ seg_row_off,
-                          const int64_t* __restrict__ seg_scale_off, int nseg, int64_t nunits,
-                          uint8_t* __restrict__ fp8_t, float* __restrict__ fp8_t_scales) {
+                          const int64_t* __restrict__ seg_scale_off, int nseg, int64_t total_blocks,
+                          int64_t nunits, uint8_t* __restrict__ fp8_t,
+                          float* __restrict__ fp8_t_scales) {
   __shared__ __align__(8) uint8_t lut[128];
+  __shared__ __align__(16) uint32_t tiles[kColThreads / 32][32 * kTileRow];
   build_shift_tables(lut);
   __syncthreads();
   const uint2* lut2 = reinterpret_cast<const uint2*>(lut);
+  uint32_t* const tile = tiles[threadIdx.x >> 5];
   const int lane = threadIdx.x & 31;
-  const int g = lane & 7;   // token group
-  const int c = lane >> 3;  // 8-feature slice of the 32-feature block
+  const int g = lane >> 1;  // tokens 8g .. 8g+7 of a block
+  const int c = lane & 1;   // features 16c .. 16c+15 of the feature block
   const int64_t kblocks = cols / 32;
   const int64_t row_bytes = cols / 2;
   const int64_t nwarps = (int64_t)gridDim.x * (kColThreads / 32);
   for (int64_t unit = (int64_t)blockIdx.x * (kColThreads / 32) + (threadIdx.x >> 5); unit < nunits;
        unit += nwarps) {
-    const int64_t fb = unit / kblocks;              // global token block
-    const int kb = (int)(unit - fb * kblocks);      // feature block
-    const int e = find_segment(seg_scale_off, nseg, fb);
-    const int64_t row0 = seg_row_off[e];
-    const int64_t n_e = seg_row_off[e + 1] - row0;
-    const int64_t sofs = seg_scale_off[e];
-    const int64_t b = fb - sofs;
-    const int64_t left = n_e - 128 * b;
-    const int nv = left < 128 ? (int)left : 128;    // tokens in this block
-
-    // Load: 16 tokens x (8 codes, 1 scale byte).
-    uint32_t w[16], s[16];
-    {
-      const int64_t r = row0 + 128 * b + 16 * g;
-      const uint8_t* pw = packed + r * row_bytes + 16 * kb + 4 * c;
-      const uint8_t* ps = scales + r * kblocks + kb;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const bool ok = 16 * g + i < nv;
-        w[i] = ok ? ld_stream_u32(pw + i * row_bytes) : 0u;
-        s[i] = ok ? ld_stream_u8(ps + i * kblocks) : 0u;
-      }
-    }
-    // Target scale: the block's largest source scale.
-    uint32_t st = 0;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) st = max(st, s[i]);
-    st = max(st, __shfl_xor_sync(0xFFFFFFFFu, st, 1));
-    st = max(st, __shfl_xor_sync(0xFFFFFFFFu, st, 2));
-    st = max(st, __shfl_xor_sync(0xFFFFFFFFu, st, 4));
-    const int64_t nb_e = (n_e + 127) / 128;
-    fp8_t_scales[cols * sofs + (32 * kb + lane) * nb_e + b] = ue8m0_to_f32(st);
-
-    // Convert and transpose: o[f][q] = 4 token bytes (16g + 4q ..) of feature 8c + f.
-    uint32_t o[8][4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint32_t lo[4], hi[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t d = st - s[4 * q + i];
-        d = d > 15u ? 15u : d;
-        convert8(w[4 * q + i], lut2[d], lo[i], hi[i]);
-      }
-      const uint32_t a0 = __byte_perm(lo[0], lo[1], 0x5140u), a1 = __byte_perm(lo[0], lo[1], 0x7362u);
-      const uint32_t a2 = __byte_perm(lo[2], lo[3], 0x5140u), a3 = __byte_perm(lo[2], lo[3], 0x7362u);
-      const uint32_t b0 = __byte_perm(hi[0], hi[1], 0x5140u), b1 = __byte_perm(hi[0], hi[1], 0x7362u);
-      const uint32_t b2 = __byte_perm(hi[2], hi[3], 0x5140u), b3 = __byte_perm(hi[2], hi[3], 0x7362u);
-      o[0][q] = __byte_perm(a0, a2, 0x5410u);
-      o[1][q] = __byte_perm(a0, a2, 0x7632u);
-      o[2][q] = __byte_perm(a1, a3, 0x5410u);
-      o[3][q] = __byte_perm(a1, a3, 0x7632u);
-      o[4][q] = __byte_perm(b0, b2, 0x5410u);
-      o[5][q] = __byte_perm(b0, b2, 0x7632u);
-      o[6][q] = __byte_perm(b1, b3, 0x5410u);
-      o[7][q] = __byte_perm(b1, b3, 0x7632u);
-    }
-
-    // Store: feature row k = 32kb + 8c + f holds the block's nv tokens at
-    // S = fp8_t + cols*row0 + k*n_e + 128b, a = S mod 16.  With a = 0 lane g
-    // writes bytes 16g .. 16g+15 as they are; otherwise it writes the
-    // aligned chunk starting at token 16g + 16 - a (its last a bytes and the
-    // next lane's first 16 - a bytes), and lane 0 also the head chunk.
-    uint8_t* const blk = fp8_t + cols * row0 + 128 * b;
-    const int own_end = nv - 16 * g;  // bytes of this lane's 16 that are valid (may be <= 0)
-#pragma unroll
-    for (int f = 0; f < 8; ++f) {
-      const uint4 mine = make_uint4(o[f][0], o[f][1], o[f][2], o[f][3]);
-      const uint4 next = make_uint4(__shfl_down_sync(0xFFFFFFFFu, mine.x, 1),
-                                    __shfl_down_sync(0xFFFFFFFFu, mine.y, 1),
-                                    __shfl_down_sync(0xFFFFFFFFu, mine.z, 1),
-                                    __shfl_down_sync(0xFFFFFFFFu, mine.w, 1));
-      uint8_t* const S = blk + (32 * (int64_t)kb + 8 * c + f) * n_e;
-      const int a = (int)(reinterpret_cast<uintptr_t>(S) & 15u);
-      if (own_end <= 0) continue;
-      if (a == 0) {
-        store_chunk(S + 16 * g, mine, 0, own_end);
-      } else {
-        const int o16 = 16 - a;
-        // main chunk: tokens 16g + o16 .. 16g + o16 + 15
-        const int valid = nv - (16 * g + o16);
-        if (valid > 0) store_chunk(S + 16 * g + o16, window16(mine, next, o16), 0, valid);
-        // head chunk (tokens 0 .. o16 - 1 at bytes a .. 15 of the chunk before S + o16)
-        if (g == 0) store_chunk(S - a, window16(make_uint4(0u, 0u, 0u, 0u), mine, o16), a,
-                                a + (nv < o16 ? nv : o16));
-      }
+    const int64_t run = unit / kblocks;
+    const int kb = (int)(unit - run * kblocks);
+    const int64_t fb0 = run * kColRun;
+    const int64_t fb1 = fb0 + kColRun < total_blocks ? fb0 + kColRun : total_blocks;
+    SegPos pa;
+    pa.e = find_segment(seg_scale_off, nseg, fb0);
+    seg_load(pa, seg_row_off, seg_scale_off);
+    if (!seg_advance(pa, fb0, nseg, seg_row_off, seg_scale_off)) continue;
+    ColIn A, B;
+    col_issue(A, packed, scales, pa, fb0, row_bytes, kblocks, kb, g, c);
+    SegPos pb = pa;
+    for (int64_t fb = fb0;;) {
+      // A holds block fb (segment pa); fetch fb + 1 into B
+      bool next = fb + 1 < fb1;
+      pb = pa;
+      if (next) next = seg_advance(pb, fb + 1, nseg, seg_row_off, seg_scale_off);
+      if (next) col_issue(B, packed, scales, pb, fb + 1, row_bytes, kblocks, kb, g, c);
+      col_block(A, pa, fb, fb != fb0 && fb != pa.sofs, !next || fb + 1 == pa.send, cols, kb, lane,
+                g, c, lut2, tile, fp8_t, fp8_t_scales);
+      if (!next) break;
+      ++fb;
+      // B holds block fb (segment pb); fetch fb + 1 into A
+      next = fb + 1 < fb1;
+      pa = pb;
+      if (next) next = seg_advance(pa, fb + 1, nseg, seg_row_off, seg_scale_off);
+      if (next) col_issue(A, packed, scales, pa, fb + 1, row_bytes, kblocks, kb, g, c);
+      col_block(B, pb, fb, fb != fb0 && fb != pb.sofs, !next || fb + 1 == pb.send, cols, kb, lane,
+                g, c, lut2, tile, fp8_t, fp8_t_scales);
+      if (!next) break;
+      ++fb;
     }
   }
 }
@@ -328,11 +390,11 @@ fp4_status fp4_to_fp8_col(const uint8_t* packed, const uint8_t* scales, int64_t 
       !aligned(seg_row_off, 8) || !aligned(seg_scale_off, 8))
     return FP4_ERR_ALIGN;
   if (ntiles == 0 || num_segments == 0) return FP4_OK;
-  // one warp per (token block, 32-feature block), grid-stride over them
-  const int64_t nunits = total_blocks * (cols / 32);
+  // one warp per (run of kColRun token blocks, 32-feature block)
+  const int64_t nunits = (total_blocks + kColRun - 1) / kColRun * (cols / 32);
   return launch<fp4_to_fp8_col_kernel>(nunits * 32, kColThreads, 0, as_stream(stream), packed,
                                        scales, cols, seg_row_off, seg_scale_off, num_segments,
-                                       nunits, fp8_t, fp8_t_scales);
+                                       total_blocks, nunits, fp8_t, fp8_t_scales);
 }
 
 }  // extern "C"

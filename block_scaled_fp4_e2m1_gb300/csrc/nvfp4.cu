@@ -98,8 +98,20 @@ struct QuantPipe {
   static constexpr int kDepth = (kBF16 && !kRes) ? 2 : 1;
 };
 
+// CTAs of kThreads per SM that the register allocation must allow: 4 is 64
+// registers a thread, 3 is 80, 2 is 128.
 template <bool kBF16, bool kSR, bool kRes>
-__global__ void __launch_bounds__(kThreads)
+constexpr int quantize_min_ctas() {
+  return kRes ? 2 : ((kSR || !kBF16) ? 3 : 4);
+}
+
+// A thread quantizes one block per grid-stride step; the loads of the next
+// kD blocks are in flight meanwhile.  The ring of kD + 1 buffers is walked
+// by a fully unrolled inner loop, so every buffer index is a constant and no
+// registers are copied.  bf16 round-to-nearest without error feedback takes
+// quantize_block_bf16_rtn, everything else quantize_block.
+template <bool kBF16, bool kSR, bool kRes>
+__global__ void __launch_bounds__(kThreads, quantize_min_ctas<kBF16, kSR, kRes>())
     quantize_kernel(const void* __restrict__ x, float* __restrict__ residual, int64_t nblocks,
                     uint64_t seed, uint64_t step, int tscale_mode, float* __restrict__ tensor_scale,
                     const float* __restrict__ amax_ws, uint8_t* __restrict__ packed,
@@ -121,41 +133,29 @@ __global__ void __launch_bounds__(kThreads)
   BlockIn<kBF16, kRes> buf[kD + 1];
 #pragma unroll
   for (int d = 0; d < kD; ++d) issue_block<kBF16, kRes>(x, residual, b + d * stride, nblocks, buf[d]);
-  for (; b < nblocks; b += stride) {
-    issue_block<kBF16, kRes>(x, residual, b + kD * stride, nblocks, buf[kD]);
-    const BlockIn<kBF16, kRes>& in = buf[0];
-    float v[16], r[16], q[16];
+  for (;;) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if (kBF16) {
-        v[2 * i] = bf16_lo(in.x[0].w[i]);
-        v[2 * i + 1] = bf16_hi(in.x[0].w[i]);
-      } else {
-        v[i] = __uint_as_float(in.x[0].w[i]);
-        v[8 + i] = __uint_as_float(in.x[kBF16 ? 0 : 1].w[i]);
+    for (int s = 0; s <= kD; ++s) {
+      if (b >= nblocks) return;
+      issue_block<kBF16, kRes>(x, residual, b + kD * stride, nblocks, buf[(s + kD) % (kD + 1)]);
+      float v[16], r[16], q[16];
+      unpack_block<kBF16, kRes>(buf[s], v, r);
+      uint2 out;
+      uint32_t sb;
+      if (kBF16 && !kSR && !kRes)
+        sb = quantize_block_bf16_rtn(v, s_t, sd, out);
+      else
+        sb = quantize_block<kSR, kRes>(v, s_t, sd, (uint64_t)(16 * b), key0, key1, st0, st1, out,
+                                       q);
+      *reinterpret_cast<uint2*>(packed + 8 * b) = out;
+      scales[b] = (uint8_t)sb;
+      if (kRes) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) r[i] = __fsub_rn(v[i], q[i]);
+        store_f32x16(residual + 16 * b, r);
       }
+      b += stride;
     }
-    if (kRes) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        r[i] = __uint_as_float(in.r[0].w[i]);
-        r[8 + i] = __uint_as_float(in.r[kRes ? 1 : 0].w[i]);
-      }
-#pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = __fadd_rn(v[i], r[i]);
-    }
-    uint2 out;
-    uint32_t sb = quantize_block<kSR, kRes>(v, s_t, sd, (uint64_t)(16 * b), key0, key1, st0, st1,
-                                            out, q);
-    *reinterpret_cast<uint2*>(packed + 8 * b) = out;
-    scales[b] = (uint8_t)sb;
-    if (kRes) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) r[i] = __fsub_rn(v[i], q[i]);
-      store_f32x16(residual + 16 * b, r);
-    }
-#pragma unroll
-    for (int d = 0; d < kD; ++d) buf[d] = buf[d + 1];
   }
 }
 

@@ -71,23 +71,29 @@ __device__ __forceinline__ Chunk locate(const fp4_tensor_desc* __restrict__ desc
   return k;
 }
 
+// A lane keeps kAmaxInFlight of its chunk's blocks in flight at a time (all
+// eight for bf16), and the next chunk is located while they are loading.
 template <bool kBF16>
 __global__ void __launch_bounds__(kBThreads)
     amax_batched_kernel(const fp4_tensor_desc* __restrict__ desc, int count, int64_t total_chunks,
                         float* __restrict__ amax) {
   constexpr int kWords = kBF16 ? 1 : 2;
+  constexpr int kAmaxInFlight = kBF16 ? kLaneBlocks : kLaneBlocks / 2;
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = (int64_t)gridDim.x * (kBThreads / 32);
-  for (int64_t c = (int64_t)blockIdx.x * (kBThreads / 32) + (threadIdx.x >> 5); c < total_chunks;
-       c += nwarps) {
-    const Chunk k = locate(desc, count, c);
+  int64_t c = (int64_t)blockIdx.x * (kBThreads / 32) + (threadIdx.x >> 5);
+  if (c >= total_chunks) return;
+  Chunk k = locate(desc, count, c);
+  while (c < total_chunks) {
     const uint8_t* x = static_cast<const uint8_t*>(ldg_ptr(&desc[k.t].x));
+    const int64_t cn = c + nwarps;
+    Chunk kn = k;
     float m = 0.0f;
 #pragma unroll
-    for (int h = 0; h < kLaneBlocks; h += 4) {
-      U32x8 raw[4][kWords];
+    for (int h = 0; h < kLaneBlocks; h += kAmaxInFlight) {
+      U32x8 raw[kAmaxInFlight][kWords];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kAmaxInFlight; ++u) {
         const int64_t b = k.b0 + lane + 32 * (h + u);
 #pragma unroll
         for (int w = 0; w < kWords; ++w) {
@@ -99,8 +105,9 @@ __global__ void __launch_bounds__(kBThreads)
           }
         }
       }
+      if (h == 0 && cn < total_chunks) kn = locate(desc, count, cn);
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+      for (int u = 0; u < kAmaxInFlight; ++u)
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           if (kBF16) {
@@ -114,15 +121,17 @@ __global__ void __launch_bounds__(kBThreads)
     }
     const uint32_t wm = warp_max_u32(__float_as_uint(m));
     if (lane == 0 && wm != 0u) atomicMax(reinterpret_cast<unsigned int*>(amax + k.t), wm);
+    c = cn;
+    k = kn;
   }
 }
 
 template <bool kBF16, bool kSR>
-__global__ void __launch_bounds__(kBThreads)
+__global__ void __launch_bounds__(kBThreads, kSR ? 1 : (kBF16 ? 3 : 2))
     quantize_batched_kernel(const fp4_tensor_desc* __restrict__ desc, int count,
                             int64_t total_chunks, uint64_t seed, uint64_t step, int tscale_mode,
                             float* __restrict__ tensor_scale, const float* __restrict__ amax) {
-  constexpr int kD = 2;  // blocks in flight ahead of the one being quantized
+  constexpr int kD = kBF16 ? 2 : 1;  // blocks in flight ahead of the one being quantized
   const int lane = threadIdx.x & 31;
   const uint32_t key0 = (uint32_t)seed, key1 = (uint32_t)(seed >> 32);
   const uint32_t st0 = (uint32_t)step, st1 = (uint32_t)(step >> 32);
@@ -147,29 +156,24 @@ __global__ void __launch_bounds__(kBThreads)
 #pragma unroll
     for (int d = 0; d < kD; ++d)
       issue_block<kBF16, false>(x, nullptr, k.b0 + lane + 32 * d, k.nb, buf[d]);
+#pragma unroll
     for (int u = 0; u < kLaneBlocks; ++u) {
       const int64_t b = k.b0 + lane + 32 * u;
-      issue_block<kBF16, false>(x, nullptr, b + 32 * kD, u + kD < kLaneBlocks ? k.nb : 0, buf[kD]);
+      issue_block<kBF16, false>(x, nullptr, b + 32 * kD, u + kD < kLaneBlocks ? k.nb : 0,
+                                buf[(u + kD) % (kD + 1)]);
       if (b < k.nb) {
-        float v[16], q[16];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (kBF16) {
-            v[2 * i] = bf16_lo(buf[0].x[0].w[i]);
-            v[2 * i + 1] = bf16_hi(buf[0].x[0].w[i]);
-          } else {
-            v[i] = __uint_as_float(buf[0].x[0].w[i]);
-            v[8 + i] = __uint_as_float(buf[0].x[kBF16 ? 0 : 1].w[i]);
-          }
-        }
+        float v[16], r[16], q[16];
+        unpack_block<kBF16, false>(buf[u % (kD + 1)], v, r);
         uint2 out;
-        const uint32_t sb = quantize_block<kSR, false>(v, s_t, sd, (uint64_t)(16 * b), key0, key1,
-                                                       st0, st1, out, q);
+        uint32_t sb;
+        if (kBF16 && !kSR)
+          sb = quantize_block_bf16_rtn(v, s_t, sd, out);
+        else
+          sb = quantize_block<kSR, false>(v, s_t, sd, (uint64_t)(16 * b), key0, key1, st0, st1,
+                                          out, q);
         *reinterpret_cast<uint2*>(packed + 8 * b) = out;
         scales[b] = (uint8_t)sb;
       }
-#pragma unroll
-      for (int d = 0; d < kD; ++d) buf[d] = buf[d + 1];
     }
   }
 }
@@ -223,7 +227,7 @@ __global__ void __launch_bounds__(kBThreads)
 }
 
 fp4_status check_desc(const fp4_tensor_desc* desc, int32_t count, int64_t total_chunks) {
-  if (count < 0 || total_chunks < 0) return FP4_ERR_SHAPE;
+  if (count < 0 || count >= (1 << 24) || total_chunks < 0) return FP4_ERR_SHAPE;
   if (count > 0 && desc == nullptr) return FP4_ERR_NULL;
   if (!aligned(desc, 8)) return FP4_ERR_ALIGN;
   return FP4_OK;
@@ -250,10 +254,10 @@ extern "C" {
 
 fp4_status fp4_batch_plan(fp4_tensor_desc* host_desc, int32_t count, int64_t* total_chunks) {
   if (!total_chunks || (count > 0 && !host_desc)) return FP4_ERR_NULL;
-  if (count < 0) return FP4_ERR_SHAPE;
+  if (count < 0 || count >= (1 << 24)) return FP4_ERR_SHAPE;
   for (int32_t t = 0; t < count; ++t) {
     const fp4_tensor_desc& d = host_desc[t];
-    if (d.n < 0 || d.n % 16 != 0) return FP4_ERR_SHAPE;
+    if (d.n < 0 || d.n % 16 != 0 || d.n >= (int64_t(16) << 40)) return FP4_ERR_SHAPE;
     if (!aligned(d.x, 32) || !aligned(d.packed, 16) || !aligned(d.scales, 2) || !aligned(d.y, 32))
       return FP4_ERR_ALIGN;
   }

@@ -12,6 +12,8 @@
 
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace fp4 {
@@ -92,11 +94,27 @@ __device__ __forceinline__ void block_max_to(float m, float* out) {
   }
 }
 
+// Exact ties of bf16 quotients.  Let the dividend have at most 8
+// significant bits (a bf16 value) and the divisor y = m * 2^k, m odd, have
+// m < 2^14 (the low 10 bits of its significand are zero: "short").  Every
+// rounding midpoint M of E2M1 or E4M3 is j * 2^s with j odd, j < 32.  If
+// x / y != M, then |x - M*y| is a nonzero multiple of the coarser of the two
+// quanta of x and M*y, which puts x / y at a relative distance of at least
+// min(1 / (j*m), 2^-8) > 2^-19 from M.  The bracket (below) spans less than
+// 2^-20 relative, so when its two codes differ, x / y == M exactly:
+// RN(x / y) is the midpoint itself, and the code is the even one of the two.
+// Divisors of this kind are common: the tensor scale amax / (6 * 448)
+// carries the factors 3 and 7, which bf16 maxima often cancel.
+__device__ __forceinline__ bool short_divisor(float y) {
+  return (__float_as_uint(y) & 0x3FFu) == 0u;
+}
+
 // Per-kernel constants of the block-scale division u = bmax / den6.
 struct ScaleDiv {
   float den6;    // 6 * s_t
   float r_lo;    // RN(RN(1/den6) * (1 - 2^-21)), 0 when den6 is outside [2^-125, 2^125]
   float r_hi;    // RN(RN(1/den6) * (1 + 2^-21))
+  bool short6;   // den6 certified and short (see short_divisor)
 };
 
 __device__ __forceinline__ ScaleDiv make_scale_div(float s_t) {
@@ -109,6 +127,7 @@ __device__ __forceinline__ ScaleDiv make_scale_div(float s_t) {
   } else {
     d.r_lo = d.r_hi = 0.0f;
   }
+  d.short6 = d.r_lo != 0.0f && short_divisor(d.den6);
   return d;
 }
 
@@ -155,6 +174,67 @@ __device__ __forceinline__ uint32_t settle_midpoint(float ax, float y, float M, 
   return r > 0.0f ? lo : hi;
 }
 
+// e4m3 block scale code RN_e4m3(RN(bmax / den6)) through the certified
+// bracket, settled exactly when the bracket straddles an e4m3 midpoint.
+__device__ __forceinline__ uint32_t block_scale_code(float bmax, const ScaleDiv& sd) {
+  const uint32_t lh = cvt_e4m3x2(__fmul_rn(bmax, sd.r_lo), __fmul_rn(bmax, sd.r_hi));
+  uint32_t sb = lh & 0xFFu;
+  if (sd.r_lo == 0.0f || sb != (lh >> 8)) {
+    const uint32_t hb = lh >> 8;
+    if (sd.r_lo != 0.0f && hb == sb + 1u && sd.den6 >= 0x1p-100f) {
+      const float M = __fmul_rn(__fadd_rn(e4m3_value(sb), e4m3_value(hb)), 0.5f);
+      sb = settle_midpoint(bmax, sd.den6, M, sb, hb);
+    } else {
+      sb = exact_e4m3_quotient(bmax, sd.den6);
+    }
+  }
+  return sb;
+}
+
+// The multipliers of the E2M1 bracket for a decoded block scale eff:
+// RN(RN(1/eff) * (1 -+ 2^-21)), both 0 when eff is 0 (the codes are then
+// those of x * 0).  Certified only for eff in [2^-125, 2^125].
+struct Bracket {
+  float il, ih;
+};
+
+__device__ __forceinline__ Bracket make_bracket(float eff) {
+  const float inv = __frcp_rn(eff);
+  const bool zero = eff == 0.0f;
+  return Bracket{zero ? 0.0f : __fmul_rn(inv, 0x1.fffffp-1f),    // 1 - 2^-21
+                 zero ? 0.0f : __fmul_rn(inv, 0x1.000008p+0f)};  // 1 + 2^-21
+}
+
+__device__ __forceinline__ bool bracket_certified(float eff) {
+  return eff == 0.0f || (eff >= 0x1p-125f && eff <= 0x1p125f);
+}
+
+// The E2M1 code of RN(x / eff) for eff in [2^-125, 2^125] when the bracket
+// codes cl and ch of x differ.
+__device__ __forceinline__ uint32_t settle_e2m1(float x, float eff, uint32_t cl, uint32_t ch) {
+  const uint32_t ml = cl & 7u;
+  if ((ch & 7u) == ml + 1u && (ch & 8u) == (cl & 8u) && eff >= 0x1p-100f) {
+    const float M = __fmul_rn(__fadd_rn(e2m1_value(ml), e2m1_value(ml + 1u)), 0.5f);
+    return (cl & 8u) | settle_midpoint(fabsf(x), eff, M, ml, ml + 1u);
+  }
+  return exact_e2m1_quotient(x, eff);
+}
+
+// One element under round-to-nearest: the code the fast path stores for it
+// (the lower bracket code) and its exact code.
+__device__ __forceinline__ void rtn_element(float x, float eff, uint32_t& stored, uint32_t& code) {
+  const Bracket k = make_bracket(eff);
+  const uint32_t c2 = cvt_e2m1x2(__fmul_rn(x, k.il), __fmul_rn(x, k.ih));
+  stored = c2 & 0xFu;
+  const uint32_t ch = c2 >> 4;
+  if (!bracket_certified(eff))  // the two bracket codes prove nothing here
+    code = exact_e2m1_quotient(x, eff);
+  else if (eff == 0.0f || stored == ch)
+    code = stored;
+  else
+    code = settle_e2m1(x, eff, stored, ch);
+}
+
 // Quantize one block v[16] (residual already added) under tensor scale s_t.
 // Writes the 8 packed bytes as two words, returns the e4m3 scale byte, and
 // (kEF) leaves the dequantized values in q[16].
@@ -166,22 +246,7 @@ __device__ __forceinline__ uint32_t quantize_block(const float v[16], float s_t,
   float bmax = 0.0f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(v[i]));
-  // e4m3 block scale RN_e4m3(RN(bmax / den6)), through the certified bracket
-  uint32_t sb;
-  {
-    const uint32_t lh = cvt_e4m3x2(__fmul_rn(bmax, sd.r_lo), __fmul_rn(bmax, sd.r_hi));
-    sb = lh & 0xFFu;
-    if (sd.r_lo == 0.0f || sb != (lh >> 8)) {
-      // the bracket straddles the e4m3 midpoint between codes sb and sb + 1
-      const uint32_t hb = lh >> 8;
-      if (sd.r_lo != 0.0f && hb == sb + 1u && sd.den6 >= 0x1p-100f) {
-        const float M = __fmul_rn(__fadd_rn(e4m3_value(sb), e4m3_value(hb)), 0.5f);
-        sb = settle_midpoint(bmax, sd.den6, M, sb, hb);
-      } else {
-        sb = exact_e4m3_quotient(bmax, sd.den6);
-      }
-    }
-  }
+  const uint32_t sb = block_scale_code(bmax, sd);
   const float eff = __fmul_rn(e4m3_value(sb), s_t);
   uint32_t w0, w1;
   if (kSR) {
@@ -221,14 +286,10 @@ __device__ __forceinline__ uint32_t quantize_block(const float v[16], float s_t,
     }
     w0 = lo[0];
     w1 = lo[1];
-    // Only the elements whose two bracket codes differ (a few per thousand,
-    // quotients on or next to an E2M1 rounding midpoint) are divided; each
-    // position is its own guarded call so a warp pays only for the positions
-    // some lane needs.
-    uint32_t p0 = lo[0] ^ hi[0], p1 = lo[1] ^ hi[1];  // nibbles still to settle
     // Elements whose two bracket codes differ (a few per thousand: quotients
     // on or next to an E2M1 rounding midpoint, many of them exact ties for
     // bf16 weights) are settled one at a time.
+    uint32_t p0 = lo[0] ^ hi[0], p1 = lo[1] ^ hi[1];  // nibbles still to settle
     while ((p0 | p1) != 0u) {
       {
         const bool first = p0 != 0u;
@@ -238,18 +299,9 @@ __device__ __forceinline__ uint32_t quantize_block(const float v[16], float s_t,
         float xi = x[0];
 #pragma unroll
         for (int k = 1; k < 8; ++k) xi = (i == k) ? x[k] : xi;
-        // the element's lo/hi codes straddle the E2M1 midpoint between
-        // magnitudes ml and ml + 1
         const uint32_t cl = ((first ? w0 : w1) >> (4 * i)) & 0xFu;
         const uint32_t ch = ((first ? hi[0] : hi[1]) >> (4 * i)) & 0xFu;
-        const uint32_t ml = cl & 7u;
-        uint32_t code;
-        if ((ch & 7u) == ml + 1u && (ch & 8u) == (cl & 8u) && eff >= 0x1p-100f) {
-          const float M = __fmul_rn(__fadd_rn(e2m1_value(ml), e2m1_value(ml + 1u)), 0.5f);
-          code = (cl & 8u) | settle_midpoint(fabsf(xi), eff, M, ml, ml + 1u);
-        } else {
-          code = exact_e2m1_quotient(xi, eff);
-        }
+        const uint32_t code = settle_e2m1(xi, eff, cl, ch);
         const uint32_t c = code << (4 * i);
         const uint32_t m = 0xFu << (4 * i);
         if (first) {
@@ -276,6 +328,78 @@ __device__ __forceinline__ uint32_t quantize_block(const float v[16], float s_t,
 #pragma unroll
     for (int i = 0; i < 8; ++i) q[8 + i] = __fmul_rn(e2m1_value(w1 >> (4 * i)), eff);
   }
+  return sb;
+}
+
+// Round-to-nearest quantization of one block of bf16 values (v[16], no
+// residual): the result of quantize_block<false, false>, faster.  Bracket
+// disagreements under a short divisor are exact ties and take the even code
+// branch-free (short_divisor); the rest (near ties under a full-precision
+// decoded scale, a block or two per hundred, or a scale outside the
+// certified range) are settled one element at a time.
+__device__ __forceinline__ uint32_t quantize_block_bf16_rtn(const float v[16], float s_t,
+                                                            const ScaleDiv& sd, uint2& out) {
+  float bmax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(v[i]));
+  uint32_t sb;
+  if (sd.short6) {
+    const uint32_t lh = cvt_e4m3x2(__fmul_rn(bmax, sd.r_lo), __fmul_rn(bmax, sd.r_hi));
+    sb = lh & 0xFFu;
+    sb += (sb ^ (lh >> 8)) & sb & 1u;  // a tie: the even code
+  } else {
+    sb = block_scale_code(bmax, sd);
+  }
+  const float eff = __fmul_rn(e4m3_value(sb), s_t);
+  const Bracket k = make_bracket(eff);
+  uint32_t lo[2], hi[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const float* x = v + 8 * h;
+    lo[h] = cvt_e2m1x8(__fmul_rn(x[0], k.il), __fmul_rn(x[1], k.il), __fmul_rn(x[2], k.il),
+                       __fmul_rn(x[3], k.il), __fmul_rn(x[4], k.il), __fmul_rn(x[5], k.il),
+                       __fmul_rn(x[6], k.il), __fmul_rn(x[7], k.il));
+    hi[h] = cvt_e2m1x8(__fmul_rn(x[0], k.ih), __fmul_rn(x[1], k.ih), __fmul_rn(x[2], k.ih),
+                       __fmul_rn(x[3], k.ih), __fmul_rn(x[4], k.ih), __fmul_rn(x[5], k.ih),
+                       __fmul_rn(x[6], k.ih), __fmul_rn(x[7], k.ih));
+  }
+  const bool cert = bracket_certified(eff);
+  uint32_t w[2], p[2];
+  if (cert && short_divisor(eff)) {
+    // ties: a differing nibble is lo's magnitude + 1, and the even code is
+    // lo + 1 exactly when lo's magnitude is odd (it is at most 5)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      w[h] = lo[h] + ((lo[h] ^ hi[h]) & lo[h] & 0x11111111u);
+      p[h] = 0u;
+    }
+  } else {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      w[h] = lo[h];
+      p[h] = cert ? lo[h] ^ hi[h] : 0xFFFFFFFFu;
+    }
+  }
+  while ((p[0] | p[1]) != 0u) {
+    const bool first = p[0] != 0u;
+    const uint32_t ph = first ? p[0] : p[1];
+    const int i = (__ffs(ph) - 1) >> 2;
+    const float* x = first ? v : v + 8;
+    float xi = x[0];
+#pragma unroll
+    for (int j = 1; j < 8; ++j) xi = (i == j) ? x[j] : xi;
+    uint32_t stored, code;
+    rtn_element(xi, eff, stored, code);
+    const uint32_t m = 0xFu << (4 * i);
+    if (first) {
+      w[0] = (w[0] & ~m) | (code << (4 * i));
+      p[0] &= ~m;
+    } else {
+      w[1] = (w[1] & ~m) | (code << (4 * i));
+      p[1] &= ~m;
+    }
+  }
+  out = make_uint2(w[0], w[1]);
   return sb;
 }
 
@@ -333,6 +457,32 @@ __device__ __forceinline__ void issue_block(const void* x, const float* residual
       in.r[0] = ld_v8(residual + 16 * b);
       in.r[kRes ? 1 : 0] = ld_v8(residual + 16 * b + 8);
     }
+  }
+}
+
+// The 16 values of a block (bf16 or fp32 x, plus the residual with error
+// feedback, one fp32 addition each) from its raw words.
+template <bool kBF16, bool kRes>
+__device__ __forceinline__ void unpack_block(const BlockIn<kBF16, kRes>& in, float v[16],
+                                             float r[16]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (kBF16) {
+      v[2 * i] = bf16_lo(in.x[0].w[i]);
+      v[2 * i + 1] = bf16_hi(in.x[0].w[i]);
+    } else {
+      v[i] = __uint_as_float(in.x[0].w[i]);
+      v[8 + i] = __uint_as_float(in.x[kBF16 ? 0 : 1].w[i]);
+    }
+  }
+  if (kRes) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      r[i] = __uint_as_float(in.r[0].w[i]);
+      r[8 + i] = __uint_as_float(in.r[kRes ? 1 : 0].w[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __fadd_rn(v[i], r[i]);
   }
 }
 

@@ -174,14 +174,15 @@ typedef struct {
   uint8_t* packed;      /* [n/2] codes, 16-byte aligned */
   uint8_t* scales;      /* [n/16] e4m3 block scales, 2-byte aligned */
   void* y;              /* [n] dequantized output, 32-byte aligned */
-  int64_t n;            /* elements, n % 16 == 0 (0 allowed) */
+  int64_t n;            /* elements, n % 16 == 0 (0 allowed), n < 2^44 */
   int64_t chunk_start;  /* index of the tensor's first chunk (fp4_batch_plan) */
 } fp4_tensor_desc;
 
-/* Host helper: checks every descriptor of a host array (n % 16, alignment of
- * the non-NULL pointers) and fills chunk_start; *total_chunks receives the
- * number of chunks of the batch.  The batched calls trust a table that
- * passed this check. */
+/* Host helper: checks every descriptor of a host array (n % 16, n < 2^44,
+ * alignment of the non-NULL pointers) and count < 2^24 (FP4_ERR_SHAPE
+ * otherwise), then fills chunk_start; *total_chunks receives the number of
+ * chunks of the batch.  The batched calls trust a table that passed this
+ * check. */
 fp4_status fp4_batch_plan(fp4_tensor_desc* host_desc, int32_t count, int64_t* total_chunks);
 
 /* amax[t] = max |x_t[i]| for every tensor t (as nvfp4_amax); amax is a

@@ -337,3 +337,63 @@ def test_rtn_structural_ties_full_matrix():
     q = (wn.reshape(-1, 16) / eff[:, None]).astype(np.float32)
     mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32)
     assert np.isin(np.abs(q), mids).sum() > 1000
+
+
+@pytest.mark.parametrize("s_t", [2.0 ** -131, 2.0 ** 121])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_rtn_decoded_scale_outside_bracket_range(s_t, dtype):
+    """A given tensor scale so small or so large that the decoded block
+    scales fall outside [2^-125, 2^125], where the kernel cannot use its
+    reciprocal bracket and every element of the block takes the exact
+    division (all 16 elements of every lane go through the warp's pending
+    list at once, many list flushes per pass)."""
+    m = fp4()
+    n = 16 * (256 * 5 + 7)
+    g = torch.Generator(device="cpu").manual_seed(23)
+    mag = torch.exp2(torch.randint(-6, 9, (n,), generator=g).float())
+    # finite inputs only (NaN and Inf are outside the contract)
+    x = (torch.randn(n, generator=g) * mag * float(s_t)).clamp(-3e38, 3e38).to(dtype)
+    ts = torch.full((1,), s_t, dtype=torch.float32, device=dev())
+    packed, scales, _ = m.nvfp4_quantize(x.to(dev()), tscale="given", tensor_scale=ts)
+    wp, ws, _ = ora.nvfp4_quantize(to_f32_np(x), tscale_mode=ora.TSCALE_GIVEN,
+                                   tensor_scale=float(np.float32(s_t)))
+    assert_bits_equal(u8(scales), ws, "scales")
+    assert_bits_equal(u8(packed), wp, "packed")
+    eff = ora.e4m3_value(ws).astype(np.float64) * np.float32(s_t)
+    out = (eff != 0) & ((eff < 2.0 ** -125) | (eff > 2.0 ** 125))
+    assert out.mean() > 0.5
+
+
+def test_rtn_error_feedback_on_structural_ties():
+    """Round-to-nearest with error feedback on bf16 Laplace weights, whose
+    quotients often sit exactly on E2M1 midpoints: blocks the kernel defers
+    are redone from the untouched residual; codes, scales and residual are
+    compared bit for bit."""
+    m = fp4()
+    w = workloads.laplace_weight(77, (512, 4096), device=dev()).view(-1)
+    n = w.numel()
+    r0 = (torch.randn(n, generator=torch.Generator().manual_seed(4)) * 1e-3).to(torch.float32)
+    r = r0.to(dev())
+    packed, scales, ts = m.nvfp4_quantize(w, residual=r, rounding="rtn")
+    rn = r0.numpy().copy()
+    wp, ws, wt = ora.nvfp4_quantize(to_f32_np(w), residual=rn, rounding=ora.RTN)
+    assert np.float32(ts.item()) == np.float32(wt)
+    assert_bits_equal(u8(scales), ws, "scales")
+    assert_bits_equal(u8(packed), wp, "packed")
+    assert_bits_equal(to_f32_np(r), rn, "residual")
+
+
+def test_rtn_qdq_on_structural_ties():
+    """The in-place qdq step under round-to-nearest on bf16 Laplace weights
+    (no gradient, no residual: v = W exactly, so quotients hit midpoints):
+    deferred blocks are redone from the not yet updated W."""
+    m = fp4()
+    w0 = workloads.laplace_weight(78, (512, 4096), device="cpu").view(-1)
+    w = w0.to(dev())
+    _, packed, scales, ts = m.nvfp4_qdq(w, None, 0.0, None, rounding="rtn")
+    wb = bf16_bits(w0).copy()
+    wp, ws, wt = ora.nvfp4_qdq(wb, None, 0.0, None, rounding=ora.RTN)
+    assert np.float32(ts.item()) == np.float32(wt)
+    assert_bits_equal(u8(packed), wp, "packed")
+    assert_bits_equal(u8(scales), ws, "scales")
+    assert_bits_equal(bf16_bits(w), wb, "W")

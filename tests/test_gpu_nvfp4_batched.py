@@ -136,3 +136,34 @@ def test_batched_weight_set_layer_sampled():
             wp, wsc, _ = ora.nvfp4_blocks(wn[16 * b0:16 * (b0 + 64)], b0, wt)
             assert_bits_equal(u8(pk[i][8 * b0:8 * (b0 + 64)]), wp, f"packed {i} @{b0}")
             assert_bits_equal(u8(sc[i][b0:b0 + 64]), wsc, f"scales {i} @{b0}")
+
+
+def test_batched_rtn_ties_and_extreme_scales_full():
+    """A batch mixing tie-heavy bf16 Laplace matrices (computed scales) with
+    tensors whose given scale puts the decoded block scales outside the
+    kernel's bracket range: the per-warp list of pending elements then holds
+    entries of several tensors at once.  Every tensor is compared in full
+    with the oracle."""
+    m = fp4()
+    xs, given = [], []
+    for i, s_t in enumerate([None, 2.0 ** -131, None, 2.0 ** 121, 0.37, None]):
+        if s_t is None:
+            x = workloads.laplace_weight(400 + i, (256, 1024 + 16 * i), device="cpu").view(-1)
+            s = ora.nvfp4_tensor_scale(ora.nvfp4_amax(to_f32_np(x)))
+        else:
+            g = torch.Generator().manual_seed(500 + i)
+            n = 16 * (256 * 3 + 5 * i)
+            mag = torch.exp2(torch.randint(-6, 9, (n,), generator=g).float())
+            x = (torch.randn(n, generator=g) * mag * s_t).clamp(-3e38, 3e38).to(torch.bfloat16)
+            s = s_t
+        xs.append(x.to(dev()))
+        given.append(float(np.float32(s)))
+    pk, sc = _buffers(xs)
+    batch = m.Batch(xs=xs, packed=pk, scales=sc)
+    ts = torch.tensor(given, dtype=torch.float32, device=dev())
+    m.nvfp4_quantize_batched(batch, torch.bfloat16, tscale="given", tensor_scale=ts)
+    for i, x in enumerate(xs):
+        wp, ws, _ = ora.nvfp4_quantize(to_f32_np(x), tscale_mode=ora.TSCALE_GIVEN,
+                                       tensor_scale=given[i])
+        assert_bits_equal(u8(sc[i]), ws, f"scales {i}")
+        assert_bits_equal(u8(pk[i]), wp, f"packed {i}")
