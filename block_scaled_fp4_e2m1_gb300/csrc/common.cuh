@@ -74,6 +74,20 @@ __device__ __forceinline__ uint32_t ld_stream_u8(const void* p) {
   return r;
 }
 
+// Read-only loads cached in L1, for data that neighbouring warps of the CTA
+// read too (a line is fetched from L2 once per CTA instead of once per warp).
+__device__ __forceinline__ uint2 ld_shared_v2(const void* p) {
+  uint2 r;
+  asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t ld_shared_u8(const void* p) {
+  uint32_t r;
+  asm volatile("ld.global.nc.u8 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+
 // ---------------------------------------------------- asynchronous staging
 //
 // Streaming kernels keep several units of input per thread in flight by
@@ -107,6 +121,56 @@ struct StageRing {
     return base + (slot * kPieces + piece) * kThreads + threadIdx.x;
   }
 };
+
+// ------------------------------------------------------ packed fp32 pairs
+//
+// Two fp32 values in one 64-bit register pair, operated on by the packed
+// add / sub / mul / fma.rn.f32x2 instructions: each lane is one correctly
+// rounded fp32 operation, identical to the scalar .rn form, at one issue
+// slot for both.  Unlike the scalar .rn forms, a packed multiply whose
+// result feeds a packed addition can be fused into one fma by the compiler
+// (measured on sm_103a), so callers form such products with scalar
+// multiplies.
+
+struct F2 {
+  float x, y;
+};
+
+__device__ __forceinline__ F2 add2(F2 a, F2 b) {
+  F2 r;
+  asm("{.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
+__device__ __forceinline__ F2 sub2(F2 a, F2 b) {
+  F2 r;
+  asm("{.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "sub.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
+__device__ __forceinline__ F2 mul2(F2 a, F2 b) {
+  F2 r;
+  asm("{.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
+__device__ __forceinline__ F2 fma2(F2 a, F2 b, F2 c) {
+  F2 r;
+  asm("{.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "mov.b64 c, {%6, %7};\n\tfma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return r;
+}
 
 // ------------------------------------------------------------ bf16 <-> f32
 

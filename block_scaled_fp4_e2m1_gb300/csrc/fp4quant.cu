@@ -36,32 +36,52 @@ __device__ __forceinline__ float wht_norm() {
   return G == 64 ? 0.125f : (G == 256 ? 0.0625f : __uint_as_float(0x3DB504F3u));
 }
 
+// A thread's 16 elements as 8 packed pairs P[i] = (y[i], y[i + 8]), so that
+// the butterfly stages h = 1, 2, 4, the cross-lane stages and the final
+// scalings run two elements per instruction; stage h = 8 pairs the two
+// halves of each P[i].  A product that feeds an addition is always formed
+// by a scalar multiply: the compiler may fuse a packed multiply into the
+// packed addition that consumes it (one rounding instead of two), which
+// would break the exact operation order.
+struct Row16 {
+  F2 p[8];
+  __device__ __forceinline__ float& at(int i) { return i < 8 ? p[i].x : p[i - 8].y; }
+};
+
+__device__ __forceinline__ F2 splat(float v) { return F2{v, v}; }
+
 // Normalized Walsh-Hadamard transform of the group whose elements
-// 16*(lane % (G/16)) .. +15 this thread holds in y[].
+// 16*(lane % (G/16)) .. +15 this thread holds.
 template <int G>
-__device__ __forceinline__ void wht_group(float y[16], int lane) {
+__device__ __forceinline__ void wht_group(Row16& y, int lane) {
 #pragma unroll
-  for (int h = 1; h < 16; h <<= 1) {
+  for (int h = 1; h < 8; h <<= 1) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < 8; ++i) {
       if (i & h) continue;
-      const float a = y[i], b = y[i + h];
-      y[i] = __fadd_rn(a, b);
-      y[i + h] = __fsub_rn(a, b);
+      const F2 a = y.p[i], b = y.p[i + h];
+      y.p[i] = add2(a, b);
+      y.p[i + h] = sub2(a, b);
     }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {  // h = 8
+    const float a = y.p[i].x, b = y.p[i].y;
+    y.p[i] = F2{__fadd_rn(a, b), __fsub_rn(a, b)};
   }
 #pragma unroll
   for (int m = 1; m < G / 16; m <<= 1) {
-    const float sgn = (lane & m) ? -1.0f : 1.0f;  // upper partner: partner - own
+    const F2 sgn = splat((lane & m) ? -1.0f : 1.0f);  // upper partner: partner - own
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float p = __shfl_xor_sync(0xFFFFFFFFu, y[i], m);
-      y[i] = __fmaf_rn(sgn, y[i], p);
+    for (int i = 0; i < 8; ++i) {
+      const F2 q{__shfl_xor_sync(0xFFFFFFFFu, y.p[i].x, m),
+                 __shfl_xor_sync(0xFFFFFFFFu, y.p[i].y, m)};
+      y.p[i] = fma2(sgn, y.p[i], q);
     }
   }
-  const float c = wht_norm<G>();
+  const F2 c = splat(wht_norm<G>());
 #pragma unroll
-  for (int i = 0; i < 16; ++i) y[i] = __fmul_rn(y[i], c);
+  for (int i = 0; i < 8; ++i) y.p[i] = mul2(y.p[i], c);
 }
 
 template <int G>
@@ -79,21 +99,21 @@ __device__ __forceinline__ float group_max(float v) {
 }
 
 template <bool kBF16>
-__device__ __forceinline__ void load16(const void* x, int64_t u, float v[16]) {
+__device__ __forceinline__ void load16(const void* x, int64_t u, Row16& y) {
   if (kBF16) {
     U32x8 r = ld_stream_v8(static_cast<const uint16_t*>(x) + 16 * u);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      v[2 * i] = bf16_lo(r.w[i]);
-      v[2 * i + 1] = bf16_hi(r.w[i]);
+      y.at(2 * i) = bf16_lo(r.w[i]);
+      y.at(2 * i + 1) = bf16_hi(r.w[i]);
     }
   } else {
     const float* p = static_cast<const float*>(x) + 16 * u;
     U32x8 a = ld_stream_v8(p), b = ld_stream_v8(p + 8);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      v[i] = __uint_as_float(a.w[i]);
-      v[8 + i] = __uint_as_float(b.w[i]);
+      y.p[i].x = __uint_as_float(a.w[i]);
+      y.p[i].y = __uint_as_float(b.w[i]);
     }
   }
 }
@@ -112,42 +132,44 @@ __global__ void __launch_bounds__(kThreads)
   for (int64_t u0 = (int64_t)blockIdx.x * kThreads + (threadIdx.x & ~31); u0 < nchunks; u0 += stride) {
     const int64_t u = u0 + lane;
     const bool valid = u < nchunks;
-    float y[16];
+    Row16 y;
     if (valid) {
       load16<kBF16>(x, u, y);
     } else {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) y[i] = 0.0f;
+      for (int i = 0; i < 8; ++i) y.p[i] = splat(0.0f);
     }
-    // RMS scale
-    float sq[16];
+    // RMS scale: the pairwise tree over adjacent squares, levels 1-3 two
+    // sums per instruction ((0..7 | 8..15) halves side by side)
+    F2 sq[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) sq[i] = __fmul_rn(y[i], y[i]);
+    for (int i = 0; i < 8; ++i)
+      sq[i] = F2{__fmul_rn(y.p[i].x, y.p[i].x), __fmul_rn(y.p[i].y, y.p[i].y)};
 #pragma unroll
-    for (int w = 16; w > 1; w >>= 1) {
+    for (int w = 8; w > 1; w >>= 1) {
 #pragma unroll
-      for (int i = 0; i < w / 2; ++i) sq[i] = __fadd_rn(sq[2 * i], sq[2 * i + 1]);
+      for (int i = 0; i < w / 2; ++i) sq[i] = add2(sq[2 * i], sq[2 * i + 1]);
     }
-    const float ss = group_sum<G>(sq[0]);
+    const float ss = group_sum<G>(__fadd_rn(sq[0].x, sq[0].y));
     const float rms = __fsqrt_rn(__fmul_rn(ss, 1.0f / (float)G));
     const float inv1 = rms == 0.0f ? 0.0f : __frcp_rn(rms);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) y[i] = __fmul_rn(y[i], inv1);
+    for (int i = 0; i < 8; ++i) y.p[i] = F2{__fmul_rn(y.p[i].x, inv1), __fmul_rn(y.p[i].y, inv1)};
     // transform
     wht_group<G>(y, lane);
     // absmax scale into [-6, 6]
     float zmax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) zmax = fmaxf(zmax, fabsf(y[i]));
+    for (int i = 0; i < 8; ++i) zmax = fmaxf(zmax, fmaxf(fabsf(y.p[i].x), fabsf(y.p[i].y)));
     zmax = group_max<G>(zmax);
     const float sc2 = __fdiv_rn(zmax, 6.0f);
-    const float inv2 = sc2 == 0.0f ? 0.0f : __frcp_rn(sc2);
-    uint32_t w0 = 0, w1 = 0;
+    const F2 inv2 = splat(sc2 == 0.0f ? 0.0f : __frcp_rn(sc2));
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      w0 |= cvt_e2m1x2(__fmul_rn(y[2 * i], inv2), __fmul_rn(y[2 * i + 1], inv2)) << (8 * i);
-      w1 |= cvt_e2m1x2(__fmul_rn(y[8 + 2 * i], inv2), __fmul_rn(y[8 + 2 * i + 1], inv2)) << (8 * i);
-    }
+    for (int i = 0; i < 8; ++i) y.p[i] = mul2(y.p[i], inv2);
+    const uint32_t w0 = cvt_e2m1x8(y.at(0), y.at(1), y.at(2), y.at(3), y.at(4), y.at(5), y.at(6),
+                                   y.at(7));
+    const uint32_t w1 = cvt_e2m1x8(y.at(8), y.at(9), y.at(10), y.at(11), y.at(12), y.at(13),
+                                   y.at(14), y.at(15));
     if (valid) {
       *reinterpret_cast<uint2*>(packed + 8 * u) = make_uint2(w0, w1);
       if ((lane & (LPG - 1)) == 0) {
@@ -155,6 +177,22 @@ __global__ void __launch_bounds__(kThreads)
         s2_out[u / LPG] = sc2;
       }
     }
+  }
+}
+
+// The 8 codes of w (code i in bits 4i+3..4i) as exact floats, through the
+// hardware e2m1x2 -> f16x2 conversion.
+__device__ __forceinline__ void e2m1x8_values(uint32_t w, float o[8]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint32_t h2;
+    const uint16_t byte = (uint16_t)((w >> (8 * k)) & 0xFFu);
+    asm("{\n\t.reg .b8 b;\n\tcvt.u8.u16 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}"
+        : "=r"(h2)
+        : "h"(byte));
+    const uint16_t lo = (uint16_t)(h2 & 0xFFFFu), hi = (uint16_t)(h2 >> 16);
+    asm("cvt.f32.f16 %0, %1;" : "=f"(o[2 * k]) : "h"(lo));
+    asm("cvt.f32.f16 %0, %1;" : "=f"(o[2 * k + 1]) : "h"(hi));
   }
 }
 
@@ -175,31 +213,32 @@ __global__ void __launch_bounds__(kThreads)
       sc1 = s1_in[u / LPG];
       sc2 = s2_in[u / LPG];
     }
-    float z[16];
+    float a[8], b[8];
+    e2m1x8_values(p.x, a);
+    e2m1x8_values(p.y, b);
+    Row16 z;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      z[i] = __fmul_rn(e2m1_value(p.x >> (4 * i)), sc2);
-      z[8 + i] = __fmul_rn(e2m1_value(p.y >> (4 * i)), sc2);
-    }
+    for (int i = 0; i < 8; ++i) z.p[i] = F2{__fmul_rn(a[i], sc2), __fmul_rn(b[i], sc2)};
     wht_group<G>(z, lane);
+    const F2 m1 = splat(sc1);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) z[i] = __fmul_rn(z[i], sc1);
+    for (int i = 0; i < 8; ++i) z.p[i] = mul2(z.p[i], m1);
     if (valid) {
       if (kBF16Out) {
         U32x8 w;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) w.w[i] = pack_bf16x2(z[2 * i], z[2 * i + 1]);
+        for (int i = 0; i < 8; ++i) w.w[i] = pack_bf16x2(z.at(2 * i), z.at(2 * i + 1));
         st_v8(static_cast<uint16_t*>(out) + 16 * u, w);
       } else {
         float* o = static_cast<float*>(out) + 16 * u;
-        U32x8 a, b;
+        U32x8 lo, hi;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          a.w[i] = __float_as_uint(z[i]);
-          b.w[i] = __float_as_uint(z[8 + i]);
+          lo.w[i] = __float_as_uint(z.p[i].x);
+          hi.w[i] = __float_as_uint(z.p[i].y);
         }
-        st_v8(o, a);
-        st_v8(o + 8, b);
+        st_v8(o, lo);
+        st_v8(o + 8, hi);
       }
     }
   }

@@ -131,9 +131,11 @@ __global__ void __launch_bounds__(kRowThreads)
 //     slot before the row to the next block of the same segment.  Inside a
 //     run every word is whole; only the first and last block of a run of
 //     one segment write partial words, byte by byte.
-// No CTA barrier in the loop: the warps of a CTA are independent, and
-// consecutive warps take neighbouring feature blocks of the same run, so
-// their 16-byte row slices of the input share sectors in L2.
+// No CTA barrier in the loop: the warps of a CTA are independent.  The 8
+// warps of a CTA take neighbouring feature blocks of the same run, so their
+// 16-byte row slices of the codes share one 128-byte line and their scale
+// bytes one sector: those loads are cached in L1, so a line leaves L2 once
+// per CTA rather than once per warp.
 
 constexpr int kColThreads = 256;
 constexpr int kColRun = 16;      // token blocks per unit
@@ -223,8 +225,8 @@ __device__ __forceinline__ void col_issue(ColIn& in, const uint8_t* __restrict__
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const bool ok = i < left;
-    in.w[i] = ok ? ld_stream_v2(pw + i * row_bytes) : make_uint2(0u, 0u);
-    in.s[i] = ok ? ld_stream_u8(ps + i * kblocks) : 0u;
+    in.w[i] = ok ? ld_shared_v2(pw + i * row_bytes) : make_uint2(0u, 0u);
+    in.s[i] = ok ? ld_shared_u8(ps + i * kblocks) : 0u;
   }
 }
 

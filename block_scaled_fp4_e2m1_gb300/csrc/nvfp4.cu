@@ -260,12 +260,22 @@ __global__ void __launch_bounds__(kThreads)
   const uint32_t key0 = (uint32_t)seed, key1 = (uint32_t)(seed >> 32);
   const uint32_t st0 = (uint32_t)step, st1 = (uint32_t)(step >> 32);
   const int64_t stride = (int64_t)gridDim.x * kThreads;
-  for (int64_t b = (int64_t)blockIdx.x * kThreads + threadIdx.x; b < nblocks; b += stride) {
+  const int lane = threadIdx.x & 31;
+  // warp-uniform trip count (lanes past the end compute on zeros and store
+  // nothing): measured faster than a per-thread bound for this kernel
+  for (int64_t b = (int64_t)blockIdx.x * kThreads + threadIdx.x; b - lane < nblocks; b += stride) {
+    const bool valid = b < nblocks;
     float v[16], r[16], q[16];
-    qdq_update<kG, kRes>(w, g, lr, residual, b, v, r, false);
+    if (valid) {
+      qdq_update<kG, kRes>(w, g, lr, residual, b, v, r, false);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = r[i] = 0.0f;
+    }
     uint2 out;
     uint32_t sb = quantize_block<kSR, true>(v, s_t, sd, (uint64_t)(16 * b), key0, key1, st0, st1,
                                             out, q);
+    if (!valid) continue;
     if (kPacked) {
       *reinterpret_cast<uint2*>(packed + 8 * b) = out;
       scales[b] = (uint8_t)sb;

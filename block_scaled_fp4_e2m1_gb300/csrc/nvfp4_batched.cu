@@ -3,13 +3,20 @@
 //
 // Each tensor is cut into chunks of FP4_BATCH_CHUNK_BLOCKS (256) blocks of
 // 16 elements; the chunks of all tensors form one flat index space
-// (fp4_tensor_desc::chunk_start, filled on the host by fp4_batch_plan).  A
-// warp takes chunks in grid-stride order, finds the chunk's tensor by a
-// 32-way search over the descriptors, and processes the chunk with all 32
-// lanes (lane l owns blocks l, l + 32, ...), so every lane of a warp works on
-// the same tensor and the per-tensor scale is warp-uniform.  The arithmetic
-// per block is the single-tensor kernels' (nvfp4_device.cuh), so each
-// tensor's result is bit-identical to the single-tensor call.
+// (fp4_tensor_desc::chunk_start, filled on the host by fp4_batch_plan), in
+// which tensor t owns blocks [256 * chunk_start[t], + n_t / 16) (the rest of
+// its last chunk is a hole).
+//   - amax and quantize: warp w takes one contiguous range of that space,
+//     ~1/nwarps of it, and walks it tensor by tensor; inside a tensor its
+//     lanes stream through the blocks exactly as the single-tensor kernels
+//     do (lane l: blocks l, l + 32, ...), with their loads in flight ahead.
+//     A warp meets a tensor boundary once or twice, so the per-tensor set-up
+//     (locating it, its scale) costs nothing on the way.
+//   - dequantize: warps take whole chunks in grid-stride order and locate
+//     each chunk's tensor by a 32-way search over the descriptors.
+// Either way every lane of a warp works on the same tensor, and the
+// arithmetic per block is the single-tensor kernels' (nvfp4_device.cuh), so
+// each tensor's result is bit-identical to the single-tensor call.
 //
 // This removes the per-launch ramp and tail of many small launches: a model
 // of a few hundred weight matrices is one amax, one quantize and one
@@ -71,33 +78,59 @@ __device__ __forceinline__ Chunk locate(const fp4_tensor_desc* __restrict__ desc
   return k;
 }
 
-// A lane keeps kAmaxInFlight of its chunk's blocks in flight at a time (all
-// eight for bf16), and the next chunk is located while they are loading.
+// This warp's range [r0, r1) of the flat block space, whole warps of 32.
+struct WarpRange {
+  int64_t r0, r1;
+};
+
+__device__ __forceinline__ WarpRange warp_range(int64_t total_chunks) {
+  const int64_t nwarps = (int64_t)gridDim.x * (kBThreads / 32);
+  const int64_t w = (int64_t)blockIdx.x * (kBThreads / 32) + (threadIdx.x >> 5);
+  const int64_t total = total_chunks * kChunk;
+  const int64_t len = ((total + nwarps - 1) / nwarps + 31) & ~int64_t(31);
+  const int64_t r0 = w * len;
+  return WarpRange{r0 < total ? r0 : total, r0 + len < total ? r0 + len : total};
+}
+
+// Walks this warp's range tensor by tensor (warp-uniform): seg(t, s0, s1)
+// gets the blocks [s0, s1) of tensor t that fall into the range.
+template <typename Seg>
+__device__ __forceinline__ void for_each_segment(const fp4_tensor_desc* __restrict__ desc,
+                                                 int count, int64_t total_chunks, Seg seg) {
+  const WarpRange wr = warp_range(total_chunks);
+  if (wr.r0 >= wr.r1) return;
+  int64_t r0 = wr.r0;
+  for (int t = find_tensor(desc, count, r0 / kChunk); t < count && r0 < wr.r1; ++t) {
+    const int64_t tb0 = ldg_i64(&desc[t].chunk_start) * kChunk;
+    const int64_t nb = ldg_i64(&desc[t].n) / 16;
+    const int64_t s0 = (r0 > tb0 ? r0 : tb0) - tb0;
+    const int64_t s1 = wr.r1 - tb0 < nb ? wr.r1 - tb0 : nb;
+    if (s0 < s1) seg(t, s0, s1);
+    if (t + 1 < count) {
+      const int64_t next = ldg_i64(&desc[t + 1].chunk_start) * kChunk;
+      if (next > r0) r0 = next;
+    }
+  }
+}
+
 template <bool kBF16>
 __global__ void __launch_bounds__(kBThreads)
     amax_batched_kernel(const fp4_tensor_desc* __restrict__ desc, int count, int64_t total_chunks,
                         float* __restrict__ amax) {
   constexpr int kWords = kBF16 ? 1 : 2;
-  constexpr int kAmaxInFlight = kBF16 ? kLaneBlocks : kLaneBlocks / 2;
+  constexpr int kU = 4;  // blocks a lane has in flight
   const int lane = threadIdx.x & 31;
-  const int64_t nwarps = (int64_t)gridDim.x * (kBThreads / 32);
-  int64_t c = (int64_t)blockIdx.x * (kBThreads / 32) + (threadIdx.x >> 5);
-  if (c >= total_chunks) return;
-  Chunk k = locate(desc, count, c);
-  while (c < total_chunks) {
-    const uint8_t* x = static_cast<const uint8_t*>(ldg_ptr(&desc[k.t].x));
-    const int64_t cn = c + nwarps;
-    Chunk kn = k;
+  for_each_segment(desc, count, total_chunks, [&](int t, int64_t s0, int64_t s1) {
+    const uint8_t* x = static_cast<const uint8_t*>(ldg_ptr(&desc[t].x));
     float m = 0.0f;
+    for (int64_t b0 = s0 + lane; b0 < s1; b0 += 32 * kU) {
+      U32x8 raw[kU][kWords];
 #pragma unroll
-    for (int h = 0; h < kLaneBlocks; h += kAmaxInFlight) {
-      U32x8 raw[kAmaxInFlight][kWords];
-#pragma unroll
-      for (int u = 0; u < kAmaxInFlight; ++u) {
-        const int64_t b = k.b0 + lane + 32 * (h + u);
+      for (int u = 0; u < kU; ++u) {
+        const int64_t b = b0 + 32 * u;
 #pragma unroll
         for (int w = 0; w < kWords; ++w) {
-          if (b < k.nb) {
+          if (b < s1) {
             raw[u][w] = ld_stream_v8(x + b * (32 * kWords) + 32 * w);
           } else {
 #pragma unroll
@@ -105,9 +138,8 @@ __global__ void __launch_bounds__(kBThreads)
           }
         }
       }
-      if (h == 0 && cn < total_chunks) kn = locate(desc, count, cn);
 #pragma unroll
-      for (int u = 0; u < kAmaxInFlight; ++u)
+      for (int u = 0; u < kU; ++u)
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           if (kBF16) {
@@ -120,12 +152,12 @@ __global__ void __launch_bounds__(kBThreads)
         }
     }
     const uint32_t wm = warp_max_u32(__float_as_uint(m));
-    if (lane == 0 && wm != 0u) atomicMax(reinterpret_cast<unsigned int*>(amax + k.t), wm);
-    c = cn;
-    k = kn;
-  }
+    if (lane == 0 && wm != 0u) atomicMax(reinterpret_cast<unsigned int*>(amax + t), wm);
+  });
 }
 
+// Inside a tensor a lane quantizes blocks s0 + lane, + 32, ... with the
+// loads of its next kD blocks in flight (the single-tensor kernel's ring).
 template <bool kBF16, bool kSR>
 __global__ void __launch_bounds__(kBThreads, kSR ? 1 : (kBF16 ? 3 : 2))
     quantize_batched_kernel(const fp4_tensor_desc* __restrict__ desc, int count,
@@ -135,35 +167,25 @@ __global__ void __launch_bounds__(kBThreads, kSR ? 1 : (kBF16 ? 3 : 2))
   const int lane = threadIdx.x & 31;
   const uint32_t key0 = (uint32_t)seed, key1 = (uint32_t)(seed >> 32);
   const uint32_t st0 = (uint32_t)step, st1 = (uint32_t)(step >> 32);
-  const int64_t nwarps = (int64_t)gridDim.x * (kBThreads / 32);
-  int cur_t = -1;
-  float s_t = 1.0f;
-  ScaleDiv sd = make_scale_div(1.0f);
-  for (int64_t c = (int64_t)blockIdx.x * (kBThreads / 32) + (threadIdx.x >> 5); c < total_chunks;
-       c += nwarps) {
-    const Chunk k = locate(desc, count, c);
-    if (k.t != cur_t) {  // warp-uniform
-      cur_t = k.t;
-      s_t = tscale_mode == FP4_TSCALE_GIVEN ? sanitize_scale(tensor_scale[k.t])
-                                            : tensor_scale_from_amax(amax[k.t]);
-      sd = make_scale_div(s_t);
-    }
-    if (tscale_mode != FP4_TSCALE_GIVEN && k.j == 0 && lane == 0) tensor_scale[k.t] = s_t;
-    const void* x = ldg_ptr(&desc[k.t].x);
-    uint8_t* packed = ldg_ptr(&desc[k.t].packed);
-    uint8_t* scales = ldg_ptr(&desc[k.t].scales);
+  for_each_segment(desc, count, total_chunks, [&](int t, int64_t s0, int64_t s1) {
+    const float s_t = tscale_mode == FP4_TSCALE_GIVEN ? sanitize_scale(tensor_scale[t])
+                                                      : tensor_scale_from_amax(amax[t]);
+    if (tscale_mode != FP4_TSCALE_GIVEN && s0 == 0 && lane == 0) tensor_scale[t] = s_t;
+    const ScaleDiv sd = make_scale_div(s_t);
+    const void* x = ldg_ptr(&desc[t].x);
+    uint8_t* const packed = ldg_ptr(&desc[t].packed);
+    uint8_t* const scales = ldg_ptr(&desc[t].scales);
+    int64_t b = s0 + lane;
     BlockIn<kBF16, false> buf[kD + 1];
 #pragma unroll
-    for (int d = 0; d < kD; ++d)
-      issue_block<kBF16, false>(x, nullptr, k.b0 + lane + 32 * d, k.nb, buf[d]);
+    for (int d = 0; d < kD; ++d) issue_block<kBF16, false>(x, nullptr, b + 32 * d, s1, buf[d]);
+    for (;;) {
 #pragma unroll
-    for (int u = 0; u < kLaneBlocks; ++u) {
-      const int64_t b = k.b0 + lane + 32 * u;
-      issue_block<kBF16, false>(x, nullptr, b + 32 * kD, u + kD < kLaneBlocks ? k.nb : 0,
-                                buf[(u + kD) % (kD + 1)]);
-      if (b < k.nb) {
-        float v[16], r[16], q[16];
-        unpack_block<kBF16, false>(buf[u % (kD + 1)], v, r);
+      for (int r = 0; r <= kD; ++r) {
+        if (b >= s1) goto segment_done;
+        issue_block<kBF16, false>(x, nullptr, b + 32 * kD, s1, buf[(r + kD) % (kD + 1)]);
+        float v[16], rr[16], q[16];
+        unpack_block<kBF16, false>(buf[r], v, rr);
         uint2 out;
         uint32_t sb;
         if (kBF16 && !kSR)
@@ -173,9 +195,11 @@ __global__ void __launch_bounds__(kBThreads, kSR ? 1 : (kBF16 ? 3 : 2))
                                           out, q);
         *reinterpret_cast<uint2*>(packed + 8 * b) = out;
         scales[b] = (uint8_t)sb;
+        b += 32;
       }
     }
-  }
+  segment_done:;
+  });
 }
 
 template <bool kBF16Out>
@@ -239,9 +263,9 @@ fp4_status launch_amax_batched(const fp4_tensor_desc* desc, int32_t count, int64
     return FP4_ERR_CUDA;
   if (total_chunks == 0) return FP4_OK;
   if (dtype == FP4_BF16)
-    return launch<amax_batched_kernel<true>>(total_chunks * 32, kBThreads, 0, s, desc, count,
+    return launch<amax_batched_kernel<true>>(total_chunks * kChunk, kBThreads, 0, s, desc, count,
                                              total_chunks, amax);
-  return launch<amax_batched_kernel<false>>(total_chunks * 32, kBThreads, 0, s, desc, count,
+  return launch<amax_batched_kernel<false>>(total_chunks * kChunk, kBThreads, 0, s, desc, count,
                                             total_chunks, amax);
 }
 
@@ -297,7 +321,7 @@ fp4_status nvfp4_quantize_batched(const fp4_tensor_desc* desc, int32_t count, in
     if (st != FP4_OK) return st;
   }
   if (total_chunks == 0) return FP4_OK;
-  const int64_t units = total_chunks * 32;
+  const int64_t units = total_chunks * kChunk;  // one thread per block of the flat space
   if (dtype == FP4_BF16) {
     if (rounding == FP4_SR)
       return launch<quantize_batched_kernel<true, true>>(units, kBThreads, 0, s, desc, count,
