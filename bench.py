@@ -55,6 +55,8 @@ def parse_args(argv=None):
                    help="time one kernel alone on a tensor of --size-mb input (a kernel "
                         "study for profiling; prints its own JSON line)")
     p.add_argument("--size-mb", type=float, default=1024.0)
+    p.add_argument("--source-hash", metavar="GROUP",
+                   help="print the source hash a traffic figure of GROUP must carry")
     p.add_argument("--summarize-launches", metavar="CSV",
                    help="print a per-kernel table of an ncu gpu__time_duration.sum launch list "
                         "(this library's kernels, last --steps steps) and exit")
@@ -526,7 +528,8 @@ def summarize_launches(path, steps, warmup):
 KERNEL_STUDIES = ["nvfp4_amax", "nvfp4_quantize", "nvfp4_quantize_sr", "nvfp4_dequantize",
                   "nvfp4_qdq", "mxfp4_quantize", "fp4_to_fp8_row", "fp4_to_fp8_col",
                   "fp4quant_encode_g64", "fp4quant_encode_g128", "fp4quant_encode_g256",
-                  "fp4quant_decode_g64", "fp4quant_decode_g128", "fp4quant_decode_g256"]
+                  "fp4quant_decode_g64", "fp4quant_decode_g128", "fp4quant_decode_g256",
+                  "nvfp4_amax_batched", "nvfp4_quantize_batched", "nvfp4_dequantize_batched"]
 
 
 def kernel_study(name, size_mb, steps, warmup, device):
@@ -598,6 +601,28 @@ def kernel_study(name, size_mb, steps, warmup, device):
             g = Group(name, "study", b, [lambda: m.fp4quant_encode(x, G, pk, s1, s2)])
         else:
             g = Group(name, "study", b, [lambda: m.fp4quant_decode(pk, s1, s2, G, bf16, out=y)])
+    elif name.endswith("_batched"):
+        # whole layers of the Qwen3-8B-shaped set (~386 MB of bf16 per layer)
+        layers = max(1, int(round(size_mb / 386.0)))
+        mats = [W.laplace_weight(100 + i, s, device=device).view(-1)
+                for i, s in enumerate(W.qwen3_8b_weight_shapes(layers=layers))]
+        nq = sum(w.numel() for w in mats)
+        pks = [z(w.numel() // 2, u8) for w in mats]
+        scs = [z(w.numel() // 16, u8) for w in mats]
+        ys = [z(w.numel(), bf16) for w in mats]
+        qb = m.Batch(xs=mats, packed=pks, scales=scs)
+        db = m.Batch(packed=pks, scales=scs, ys=ys, sizes=[w.numel() for w in mats])
+        am, ts = z(len(mats), f32), z(len(mats), f32)
+        m.nvfp4_amax_batched(qb, bf16, amax=am)
+        m.nvfp4_quantize_batched(qb, bf16, tscale="from_amax", tensor_scale=ts, amax=am)
+        if name.startswith("nvfp4_amax"):
+            g = Group(name, "study", 2 * nq, [lambda: m.nvfp4_amax_batched(qb, bf16, amax=am)])
+        elif name.startswith("nvfp4_quantize"):
+            g = Group(name, "study", 2.5625 * nq,
+                      [lambda: m.nvfp4_quantize_batched(qb, bf16, tscale="from_amax",
+                                                        tensor_scale=ts, amax=am)])
+        else:
+            g = Group(name, "study", 2.5625 * nq, [lambda: m.nvfp4_dequantize_batched(db, ts, bf16)])
     else:
         raise SystemExit(f"unknown kernel {name}; one of {KERNEL_STUDIES}")
     torch.cuda.synchronize()
@@ -633,6 +658,9 @@ def main(argv=None):
                               "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
                               "peak_kind": kind}), flush=True)
             torch.cuda.empty_cache()
+        return 0
+    if args.source_hash:
+        print(kernel_source_hash(args.source_hash))
         return 0
     if args.summarize_launches:
         print(summarize_launches(args.summarize_launches, args.steps, args.warmup))
@@ -769,14 +797,40 @@ def job_gbs(bytes_per_rank_step, world, ms_per_step):
     return bytes_per_rank_step * world / (ms_per_step * 1e-3) / 1e9
 
 
+# Sources whose build a traffic figure belongs to, per bench kernel group.
+TRAFFIC_SOURCES = {
+    "nvfp4_amax@qwen3_8b_weights": ["nvfp4_batched.cu", "nvfp4_device.cuh", "common.cuh"],
+    "nvfp4_quantize@qwen3_8b_weights": ["nvfp4_batched.cu", "nvfp4_device.cuh", "common.cuh"],
+    "nvfp4_dequantize@qwen3_8b_weights": ["nvfp4_batched.cu", "nvfp4_device.cuh", "common.cuh"],
+    "fp4_to_fp8_col@moe_tokens": ["fp8_convert.cu", "common.cuh"],
+}
+
+
+def kernel_source_hash(kernel_name):
+    """sha256 (first 16 hex digits) of the CUDA sources a kernel group is built
+    from, or None if the group is not listed."""
+    import hashlib
+    files = TRAFFIC_SOURCES.get(kernel_name)
+    if not files:
+        return None
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "block_scaled_fp4_e2m1_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def load_traffic(kernel_name):
-    """DRAM bytes per launch of `kernel_name` from the committed ncu summary,
-    if one exists for the current kernel build."""
+    """DRAM bytes (read + write) per launch of `kernel_name` from
+    profiles/traffic.json, or None when there is no figure or the kernel's
+    sources changed since it was captured."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            d = json.load(f)
-        return d.get(kernel_name)
+            d = json.load(f).get(kernel_name)
+        if not d or d.get("source_hash") != kernel_source_hash(kernel_name):
+            return None
+        return d.get("bytes_per_launch")
     except Exception:
         return None
 

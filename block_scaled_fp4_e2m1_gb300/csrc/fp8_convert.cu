@@ -124,13 +124,14 @@ __global__ void __launch_bounds__(kRowThreads)
 //     tables and transposes them (4 x 4 byte transposes) into 16 feature
 //     rows x 8 token bytes, written to the warp's tile in shared memory
 //     (32 feature rows of 128 token bytes);
-//   - the warp then writes the 32 rows one at a time, lane l storing the
-//     l-th aligned 32-bit word of the row's output span.  A row's output
-//     start is byte-aligned only, so each word is two tile words funnel-
-//     shifted, and the last (start mod 4) bytes of the row are carried in a
-//     slot before the row to the next block of the same segment.  Inside a
-//     run every word is whole; only the first and last block of a run of
-//     one segment write partial words, byte by byte.
+//   - the warp then writes the 32 rows, four at a time, eight lanes per row
+//     each storing one aligned 16-byte chunk of the row's output span.  A
+//     row's output start D is byte-aligned only, so each chunk is a window
+//     of two aligned tile pieces, and the row's last (D mod 16) bytes are
+//     carried, in a 16-byte slot before the row, to the next block of the
+//     same segment.  Inside a run every chunk is whole; only the first and
+//     last block of a run of one segment write partial chunks, as 32-bit
+//     words and bytes.
 // No CTA barrier in the loop: the warps of a CTA are independent.  The 8
 // warps of a CTA take neighbouring feature blocks of the same run, so their
 // 16-byte row slices of the codes share one 128-byte line and their scale
@@ -138,8 +139,8 @@ __global__ void __launch_bounds__(kRowThreads)
 // per CTA rather than once per warp.
 
 constexpr int kColThreads = 256;
-constexpr int kColRun = 16;      // token blocks per unit
-constexpr int kTileRow = 34;     // tile words per feature row: pad, carry, 32 data words
+constexpr int kColRun = 32;      // token blocks per unit
+constexpr int kTileRow = 36;     // tile words per feature row: 4 carry words, 32 data words
 
 // Largest e in [0, nseg) with off[e] <= v, for off non-decreasing, off[0] = 0
 // <= v < off[nseg]: a 32-way search by one warp.
@@ -159,6 +160,21 @@ __device__ __forceinline__ int find_segment(const int64_t* __restrict__ off, int
   return lo;
 }
 
+// Bytes o .. o+15 (1 <= o <= 16) of the 32-byte sequence x[0..3] | y[0..3].
+__device__ __forceinline__ uint4 window16(uint4 x, uint4 y, uint32_t o) {
+  uint32_t w0 = x.x, w1 = x.y, w2 = x.z, w3 = x.w, w4 = y.x, w5 = y.y, w6 = y.z, w7 = y.w;
+  if (o & 16u) return y;
+  if (o & 8u) {
+    w0 = w2; w1 = w3; w2 = w4; w3 = w5; w4 = w6; w5 = w7;
+  }
+  if (o & 4u) {
+    w0 = w1; w1 = w2; w2 = w3; w3 = w4; w4 = w5;
+  }
+  const uint32_t sh = 8u * (o & 3u);
+  return make_uint4(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh),
+                    __funnelshift_r(w2, w3, sh), __funnelshift_r(w3, w4, sh));
+}
+
 // 4 x 4 byte transpose: x[i] holds bytes (i, 0..3); y[j] receives (0..3, j).
 __device__ __forceinline__ void transpose4(const uint32_t x[4], uint32_t y[4]) {
   const uint32_t a0 = __byte_perm(x[0], x[1], 0x5140u), a1 = __byte_perm(x[0], x[1], 0x7362u);
@@ -169,15 +185,27 @@ __device__ __forceinline__ void transpose4(const uint32_t x[4], uint32_t y[4]) {
   y[3] = __byte_perm(a1, a3, 0x7632u);
 }
 
-// Bytes [lo, hi) (0 <= lo < hi <= 4) of the 4-byte value v to p[lo .. hi).
-__device__ __forceinline__ void store_bytes(uint8_t* p, uint32_t v, int lo, int hi) {
-  if (lo == 0 && hi == 4) {
-    *reinterpret_cast<uint32_t*>(p) = v;
+// Bytes lo .. hi-1 (0 <= lo < hi <= 16) of the 16-byte value v to the
+// 16-byte aligned p: one 128-bit store when the chunk is whole, otherwise
+// the whole 32-bit words inside [lo, hi) as word stores and the bytes of
+// the (at most two) edge words as byte stores.
+__device__ __forceinline__ void store_chunk(uint8_t* p, uint4 v, int lo, int hi) {
+  if (lo == 0 && hi == 16) {
+    *reinterpret_cast<uint4*>(p) = v;
     return;
   }
+  const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
-    if (j >= lo && j < hi) p[j] = (uint8_t)(v >> (8 * j));
+  for (int t = 0; t < 4; ++t) {
+    const int b0 = 4 * t;
+    if (lo <= b0 && b0 + 4 <= hi) {
+      reinterpret_cast<uint32_t*>(p)[t] = vw[t];
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (b0 + q >= lo && b0 + q < hi) p[b0 + q] = (uint8_t)(vw[t] >> (8 * q));
+    }
+  }
 }
 
 // The segment holding a token block, walked forward block by block.
@@ -263,43 +291,58 @@ __device__ __forceinline__ void col_block(const ColIn& in, const SegPos& p, int6
       uint32_t y[4];
       transpose4(xi, y);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) tile[(16 * c + 4 * k + j) * kTileRow + 2 + 2 * g + h] = y[j];
+      for (int j = 0; j < 4; ++j) tile[(16 * c + 4 * k + j) * kTileRow + 4 + 2 * g + h] = y[j];
     }
   }
   __syncwarp();
 
   // Store the 32 rows: row r of this block covers output bytes
-  // [D, D + nv), D = fp8_t + cols*row0 + (32kb + r)*n_e + t0.
-  uint8_t* D = fp8_t + cols * p.row0 + 32 * kb * p.n_e + t0;
-  if (carry && !run_end) {  // every word of every row is whole
-#pragma unroll 8
-    for (int r = 0; r < 32; ++r, D += p.n_e) {
-      const uint32_t a = (uint32_t)reinterpret_cast<uintptr_t>(D) & 3u;
-      const uint32_t* row = tile + r * kTileRow + 1;  // row[0] is the carry slot
-      reinterpret_cast<uint32_t*>(D - a)[lane] =
-          __funnelshift_rc(row[lane], row[lane + 1], 8u * (4u - a));
+  // [D, D + nv), D = fp8_t + cols*row0 + (32kb + r)*n_e + t0.  A tile row
+  // holds 16 carry bytes (bytes 112..127 of the previous block of the
+  // segment) and then the block's 128 bytes.
+  uint8_t* const D0 = fp8_t + cols * p.row0 + 32 * kb * p.n_e + t0;
+  if (carry && !run_end) {
+    // every chunk whole: row r writes the aligned 16-byte chunks j = 0..7
+    // of [D - a, D - a + 128), a = D mod 16, lanes 8q + j of step i take
+    // row 4i + q
+    const int q = lane >> 3, j = lane & 7;
+#pragma unroll 4
+    for (int i = 0; i < 8; ++i) {
+      const int r = 4 * i + q;
+      uint8_t* const D = D0 + (int64_t)r * p.n_e;
+      const uint32_t a = (uint32_t)reinterpret_cast<uintptr_t>(D) & 15u;
+      const uint4* row = reinterpret_cast<const uint4*>(tile + r * kTileRow);  // row[0]: carry
+      reinterpret_cast<uint4*>(D - a)[j] = window16(row[j], row[j + 1], 16u - a);
     }
   } else {
-    for (int r = 0; r < 32; ++r, D += p.n_e) {
-      const uint32_t a = (uint32_t)reinterpret_cast<uintptr_t>(D) & 3u;
-      uint8_t* const W = D - a;  // word l covers row bytes [4l - a, 4l - a + 4)
-      const uint32_t* row = tile + r * kTileRow + 1;
-      const uint32_t v = __funnelshift_rc(row[lane], row[lane + 1], 8u * (4u - a));
-      // valid row bytes: [lo, hi) relative to t0
-      const int lo = carry ? -(int)a : 0;
-      const int hi = run_end ? nv : 128 - (int)a;
-      const int p0 = 4 * lane - (int)a;
-      const int blo = lo - p0 > 0 ? lo - p0 : 0;
-      const int bhi = hi - p0 < 4 ? hi - p0 : 4;
-      if (blo < bhi) store_bytes(W + 4 * lane, v, blo, bhi);
-      if (lane == 0 && hi > 128 - (int)a) {  // word 32: the row's last a bytes
-        const uint32_t v32 = __funnelshift_rc(row[32], 0u, 8u * (4u - a));
-        store_bytes(W + 128, v32, 0, hi - (128 - (int)a));
+    // first or last block of a run: the same chunks (nine when the span
+    // ends past chunk 7), each clipped to the row bytes [lo, hi) this block
+    // writes
+    const int q = lane >> 3, j = lane & 7;
+    for (int i = 0; i < 8; ++i) {
+      const int r = 4 * i + q;
+      uint8_t* const D = D0 + (int64_t)r * p.n_e;
+      const int a = (int)(reinterpret_cast<uintptr_t>(D) & 15u);
+      const int lo = carry ? -a : 0;  // without carry the bytes before t0 are not ours
+      const int hi = run_end ? nv : 128 - a;
+      const uint4* row = reinterpret_cast<const uint4*>(tile + r * kTileRow);
+#pragma unroll
+      for (int k = j; k < 9; k += 8) {  // chunk k: row bytes [16k - a, 16k - a + 16)
+        const int c0 = 16 * k - a;
+        const int blo = lo - c0 > 0 ? lo - c0 : 0;
+        const int bhi = hi - c0 < 16 ? hi - c0 : 16;
+        if (blo < bhi) {
+          const uint4 nxt = k + 1 < 9 ? row[k + 1] : make_uint4(0u, 0u, 0u, 0u);
+          store_chunk(D - a + 16 * k, window16(row[k], nxt, 16u - (uint32_t)a), blo, bhi);
+        }
       }
     }
   }
   __syncwarp();
-  if (!run_end) tile[lane * kTileRow + 1] = tile[lane * kTileRow + 1 + 32];
+  if (!run_end) {  // carry: lane r copies row r's last 16 bytes
+    uint4* row = reinterpret_cast<uint4*>(tile + lane * kTileRow);
+    row[0] = row[8];
+  }
   __syncwarp();
 }
 
