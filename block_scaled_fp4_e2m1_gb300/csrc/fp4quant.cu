@@ -8,16 +8,18 @@
 // shuffles, codes are paired and packed two per byte in registers, and the
 // receiver unpacks, dequantizes and runs the inverse transform.
 //
-// Layout: a thread owns 16 consecutive elements of a group (one 256-bit
-// load of bf16), so a group of G spans G/16 consecutive lanes (4, 8 or 16)
+// Layout: a thread owns 32 consecutive elements of a group (two 256-bit
+// loads of bf16), so a group of G spans G/32 consecutive lanes (2, 4 or 8)
 // and never leaves its warp: no shared memory and no CTA barrier.
 //   - sum of squares: a balanced pairwise tree over adjacent elements, first
-//     inside the thread (16 -> 1), then across lanes by xor-shuffle 1, 2, ...;
-//   - transform: butterfly stages h = 1, 2, 4, 8 inside the thread, stages
-//     h = 16, 32, ... across lanes (lane xor h/16), in the natural
+//     inside the thread (32 -> 1), then across lanes by xor-shuffle 1, 2, ...;
+//   - transform: butterfly stages h = 1 .. 16 inside the thread, stages
+//     h = 32, 64, ... across lanes (lane xor h/32), in the natural
 //     (Sylvester) order; the lower partner keeps a + b, the upper a - b,
-//     computed as one correctly rounded fma(+-1, own, partner);
-//   - each thread packs its 16 codes into 8 bytes and stores them directly.
+//     computed as one correctly rounded fma(+-1, own, partner).  Holding 32
+//     elements keeps one more stage inside the thread than 16 would: the
+//     shuffles, which bound these kernels, drop by a quarter to a half;
+//   - each thread packs its 32 codes into 16 bytes and stores them directly.
 // The arithmetic order (reciprocal scales, the tree, the stage order) is the
 // one the CPU oracle follows, so codes and scales are bit-exact.
 #include <cuda_runtime.h>
@@ -36,28 +38,30 @@ __device__ __forceinline__ float wht_norm() {
   return G == 64 ? 0.125f : (G == 256 ? 0.0625f : __uint_as_float(0x3DB504F3u));
 }
 
-// A thread's 16 elements as 8 packed pairs P[i] = (y[i], y[i + 8]), so that
-// the butterfly stages h = 1, 2, 4, the cross-lane stages and the final
-// scalings run two elements per instruction; stage h = 8 pairs the two
+// A thread's 32 elements as 16 packed pairs P[i] = (y[i], y[i + 16]), so
+// that the butterfly stages h = 1 .. 8, the cross-lane stages and the final
+// scalings run two elements per instruction; stage h = 16 pairs the two
 // halves of each P[i].  A product that feeds an addition is always formed
 // by a scalar multiply: the compiler may fuse a packed multiply into the
 // packed addition that consumes it (one rounding instead of two), which
 // would break the exact operation order.
-struct Row16 {
-  F2 p[8];
-  __device__ __forceinline__ float& at(int i) { return i < 8 ? p[i].x : p[i - 8].y; }
+constexpr int kE = 32;  // elements per thread
+
+struct Row32 {
+  F2 p[16];
+  __device__ __forceinline__ float& at(int i) { return i < 16 ? p[i].x : p[i - 16].y; }
 };
 
 __device__ __forceinline__ F2 splat(float v) { return F2{v, v}; }
 
 // Normalized Walsh-Hadamard transform of the group whose elements
-// 16*(lane % (G/16)) .. +15 this thread holds.
+// 32*(lane % (G/32)) .. +31 this thread holds.
 template <int G>
-__device__ __forceinline__ void wht_group(Row16& y, int lane) {
+__device__ __forceinline__ void wht_group(Row32& y, int lane) {
 #pragma unroll
-  for (int h = 1; h < 8; h <<= 1) {
+  for (int h = 1; h < 16; h <<= 1) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 16; ++i) {
       if (i & h) continue;
       const F2 a = y.p[i], b = y.p[i + h];
       y.p[i] = add2(a, b);
@@ -65,15 +69,15 @@ __device__ __forceinline__ void wht_group(Row16& y, int lane) {
     }
   }
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {  // h = 8
+  for (int i = 0; i < 16; ++i) {  // h = 16
     const float a = y.p[i].x, b = y.p[i].y;
     y.p[i] = F2{__fadd_rn(a, b), __fsub_rn(a, b)};
   }
 #pragma unroll
-  for (int m = 1; m < G / 16; m <<= 1) {
+  for (int m = 1; m < G / kE; m <<= 1) {
     const F2 sgn = splat((lane & m) ? -1.0f : 1.0f);  // upper partner: partner - own
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 16; ++i) {
       const F2 q{__shfl_xor_sync(0xFFFFFFFFu, y.p[i].x, m),
                  __shfl_xor_sync(0xFFFFFFFFu, y.p[i].y, m)};
       y.p[i] = fma2(sgn, y.p[i], q);
@@ -81,72 +85,78 @@ __device__ __forceinline__ void wht_group(Row16& y, int lane) {
   }
   const F2 c = splat(wht_norm<G>());
 #pragma unroll
-  for (int i = 0; i < 8; ++i) y.p[i] = mul2(y.p[i], c);
+  for (int i = 0; i < 16; ++i) y.p[i] = mul2(y.p[i], c);
 }
 
 template <int G>
 __device__ __forceinline__ float group_sum(float v) {
 #pragma unroll
-  for (int m = 1; m < G / 16; m <<= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, m));
+  for (int m = 1; m < G / kE; m <<= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, m));
   return v;
 }
 
 template <int G>
 __device__ __forceinline__ float group_max(float v) {
 #pragma unroll
-  for (int m = 1; m < G / 16; m <<= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, m));
+  for (int m = 1; m < G / kE; m <<= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, m));
   return v;
 }
 
 template <bool kBF16>
-__device__ __forceinline__ void load16(const void* x, int64_t u, Row16& y) {
+__device__ __forceinline__ void load32(const void* x, int64_t u, Row32& y) {
   if (kBF16) {
-    U32x8 r = ld_stream_v8(static_cast<const uint16_t*>(x) + 16 * u);
+    const uint16_t* p = static_cast<const uint16_t*>(x) + kE * u;
+    const U32x8 a = ld_stream_v8(p), b = ld_stream_v8(p + 16);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      y.at(2 * i) = bf16_lo(r.w[i]);
-      y.at(2 * i + 1) = bf16_hi(r.w[i]);
+      y.p[2 * i].x = bf16_lo(a.w[i]);
+      y.p[2 * i + 1].x = bf16_hi(a.w[i]);
+      y.p[2 * i].y = bf16_lo(b.w[i]);
+      y.p[2 * i + 1].y = bf16_hi(b.w[i]);
     }
   } else {
-    const float* p = static_cast<const float*>(x) + 16 * u;
-    U32x8 a = ld_stream_v8(p), b = ld_stream_v8(p + 8);
+    const float* p = static_cast<const float*>(x) + kE * u;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      y.p[i].x = __uint_as_float(a.w[i]);
-      y.p[i].y = __uint_as_float(b.w[i]);
+    for (int k = 0; k < 2; ++k) {
+      const U32x8 a = ld_stream_v8(p + 8 * k), b = ld_stream_v8(p + 16 + 8 * k);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        y.p[8 * k + i].x = __uint_as_float(a.w[i]);
+        y.p[8 * k + i].y = __uint_as_float(b.w[i]);
+      }
     }
   }
 }
 
-// Units are 16-element chunks; the loop is warp-uniform so that every lane
+// Units are 32-element chunks; the loop is warp-uniform so that every lane
 // takes part in the shuffles, and lanes past the end compute on zeros
-// without storing (the chunk count is a multiple of G/16, so a group is
+// without storing (the chunk count is a multiple of G/32, so a group is
 // either entirely inside or entirely past the end).
 template <int G, bool kBF16>
 __global__ void __launch_bounds__(kThreads)
     encode_kernel(const void* __restrict__ x, int64_t nchunks, uint8_t* __restrict__ packed,
                   float* __restrict__ s1_out, float* __restrict__ s2_out) {
-  constexpr int LPG = G / 16;
+  constexpr int LPG = G / kE;
   const int lane = threadIdx.x & 31;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   for (int64_t u0 = (int64_t)blockIdx.x * kThreads + (threadIdx.x & ~31); u0 < nchunks; u0 += stride) {
     const int64_t u = u0 + lane;
     const bool valid = u < nchunks;
-    Row16 y;
+    Row32 y;
     if (valid) {
-      load16<kBF16>(x, u, y);
+      load32<kBF16>(x, u, y);
     } else {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) y.p[i] = splat(0.0f);
+      for (int i = 0; i < 16; ++i) y.p[i] = splat(0.0f);
     }
-    // RMS scale: the pairwise tree over adjacent squares, levels 1-3 two
-    // sums per instruction ((0..7 | 8..15) halves side by side)
-    F2 sq[8];
+    // RMS scale: the pairwise tree over adjacent squares, levels 1-4 two
+    // sums per instruction ((0..15 | 16..31) halves side by side)
+    F2 sq[16];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < 16; ++i)
       sq[i] = F2{__fmul_rn(y.p[i].x, y.p[i].x), __fmul_rn(y.p[i].y, y.p[i].y)};
 #pragma unroll
-    for (int w = 8; w > 1; w >>= 1) {
+    for (int w = 16; w > 1; w >>= 1) {
 #pragma unroll
       for (int i = 0; i < w / 2; ++i) sq[i] = add2(sq[2 * i], sq[2 * i + 1]);
     }
@@ -154,24 +164,25 @@ __global__ void __launch_bounds__(kThreads)
     const float rms = __fsqrt_rn(__fmul_rn(ss, 1.0f / (float)G));
     const float inv1 = rms == 0.0f ? 0.0f : __frcp_rn(rms);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) y.p[i] = F2{__fmul_rn(y.p[i].x, inv1), __fmul_rn(y.p[i].y, inv1)};
+    for (int i = 0; i < 16; ++i) y.p[i] = F2{__fmul_rn(y.p[i].x, inv1), __fmul_rn(y.p[i].y, inv1)};
     // transform
     wht_group<G>(y, lane);
     // absmax scale into [-6, 6]
     float zmax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) zmax = fmaxf(zmax, fmaxf(fabsf(y.p[i].x), fabsf(y.p[i].y)));
+    for (int i = 0; i < 16; ++i) zmax = fmaxf(zmax, fmaxf(fabsf(y.p[i].x), fabsf(y.p[i].y)));
     zmax = group_max<G>(zmax);
     const float sc2 = __fdiv_rn(zmax, 6.0f);
     const F2 inv2 = splat(sc2 == 0.0f ? 0.0f : __frcp_rn(sc2));
 #pragma unroll
-    for (int i = 0; i < 8; ++i) y.p[i] = mul2(y.p[i], inv2);
-    const uint32_t w0 = cvt_e2m1x8(y.at(0), y.at(1), y.at(2), y.at(3), y.at(4), y.at(5), y.at(6),
-                                   y.at(7));
-    const uint32_t w1 = cvt_e2m1x8(y.at(8), y.at(9), y.at(10), y.at(11), y.at(12), y.at(13),
-                                   y.at(14), y.at(15));
+    for (int i = 0; i < 16; ++i) y.p[i] = mul2(y.p[i], inv2);
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      w[k] = cvt_e2m1x8(y.at(8 * k), y.at(8 * k + 1), y.at(8 * k + 2), y.at(8 * k + 3),
+                        y.at(8 * k + 4), y.at(8 * k + 5), y.at(8 * k + 6), y.at(8 * k + 7));
     if (valid) {
-      *reinterpret_cast<uint2*>(packed + 8 * u) = make_uint2(w0, w1);
+      *reinterpret_cast<uint4*>(packed + 16 * u) = make_uint4(w[0], w[1], w[2], w[3]);
       if ((lane & (LPG - 1)) == 0) {
         s1_out[u / LPG] = rms;
         s2_out[u / LPG] = sc2;
@@ -200,45 +211,50 @@ template <int G, bool kBF16Out>
 __global__ void __launch_bounds__(kThreads)
     decode_kernel(const uint8_t* __restrict__ packed, const float* __restrict__ s1_in,
                   const float* __restrict__ s2_in, int64_t nchunks, void* __restrict__ out) {
-  constexpr int LPG = G / 16;
+  constexpr int LPG = G / kE;
   const int lane = threadIdx.x & 31;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   for (int64_t u0 = (int64_t)blockIdx.x * kThreads + (threadIdx.x & ~31); u0 < nchunks; u0 += stride) {
     const int64_t u = u0 + lane;
     const bool valid = u < nchunks;
-    uint2 p = make_uint2(0u, 0u);
+    uint4 p = make_uint4(0u, 0u, 0u, 0u);
     float sc1 = 0.0f, sc2 = 0.0f;
     if (valid) {
-      p = ld_stream_v2(packed + 8 * u);
+      p = ld_stream_v4(packed + 16 * u);
       sc1 = s1_in[u / LPG];
       sc2 = s2_in[u / LPG];
     }
-    float a[8], b[8];
-    e2m1x8_values(p.x, a);
-    e2m1x8_values(p.y, b);
-    Row16 z;
+    float v[32];
+    e2m1x8_values(p.x, v);
+    e2m1x8_values(p.y, v + 8);
+    e2m1x8_values(p.z, v + 16);
+    e2m1x8_values(p.w, v + 24);
+    Row32 z;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) z.p[i] = F2{__fmul_rn(a[i], sc2), __fmul_rn(b[i], sc2)};
+    for (int i = 0; i < 16; ++i) z.p[i] = F2{__fmul_rn(v[i], sc2), __fmul_rn(v[i + 16], sc2)};
     wht_group<G>(z, lane);
     const F2 m1 = splat(sc1);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) z.p[i] = mul2(z.p[i], m1);
+    for (int i = 0; i < 16; ++i) z.p[i] = mul2(z.p[i], m1);
     if (valid) {
       if (kBF16Out) {
-        U32x8 w;
+        uint16_t* o = static_cast<uint16_t*>(out) + kE * u;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) w.w[i] = pack_bf16x2(z.at(2 * i), z.at(2 * i + 1));
-        st_v8(static_cast<uint16_t*>(out) + 16 * u, w);
-      } else {
-        float* o = static_cast<float*>(out) + 16 * u;
-        U32x8 lo, hi;
+        for (int k = 0; k < 2; ++k) {
+          U32x8 w;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          lo.w[i] = __float_as_uint(z.p[i].x);
-          hi.w[i] = __float_as_uint(z.p[i].y);
+          for (int i = 0; i < 8; ++i) w.w[i] = pack_bf16x2(z.at(16 * k + 2 * i), z.at(16 * k + 2 * i + 1));
+          st_v8(o + 16 * k, w);
         }
-        st_v8(o, lo);
-        st_v8(o + 8, hi);
+      } else {
+        float* o = static_cast<float*>(out) + kE * u;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          U32x8 w;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) w.w[i] = __float_as_uint(z.at(8 * k + i));
+          st_v8(o + 8 * k, w);
+        }
       }
     }
   }
@@ -274,7 +290,7 @@ fp4_status fp4quant_encode(const void* x, int dtype, int64_t rows, int64_t cols,
   if (!dtype_ok(dtype)) return FP4_ERR_DTYPE;
   if (!group_ok(group)) return FP4_ERR_ARG;
   if (rows < 0 || cols < 0 || cols % group != 0) return FP4_ERR_SHAPE;
-  const int64_t nchunks = rows * cols / 16;
+  const int64_t nchunks = rows * cols / kE;
   if (nchunks > 0 && (!x || !packed || !s1 || !s2)) return FP4_ERR_NULL;
   if (!aligned(x, 32) || !aligned(packed, 16) || !aligned(s1, 4) || !aligned(s2, 4))
     return FP4_ERR_ALIGN;
@@ -290,7 +306,7 @@ fp4_status fp4quant_decode(const uint8_t* packed, const float* s1, const float* 
   if (!dtype_ok(out_dtype)) return FP4_ERR_DTYPE;
   if (!group_ok(group)) return FP4_ERR_ARG;
   if (rows < 0 || cols < 0 || cols % group != 0) return FP4_ERR_SHAPE;
-  const int64_t nchunks = rows * cols / 16;
+  const int64_t nchunks = rows * cols / kE;
   if (nchunks > 0 && (!y || !packed || !s1 || !s2)) return FP4_ERR_NULL;
   if (!aligned(y, 32) || !aligned(packed, 16) || !aligned(s1, 4) || !aligned(s2, 4))
     return FP4_ERR_ALIGN;
