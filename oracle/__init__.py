@@ -74,6 +74,8 @@ _SIGS = {
     "ora_nvfp4_blocks": (None, [_P, _I64, _I64, _F, ctypes.c_int, _U64, _U64, _P, _P, _P]),
     "ora_mxfp4_quantize": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
     "ora_fp4_to_fp8_rows": (ctypes.c_int, [_P, _P, _I64, _I64, _P, _P]),
+    "ora_fp8_to_fp4_rows": (ctypes.c_int, [_P, _P, _I64, _I64, _P, _P]),
+    "ora_mxfp4_dequantize": (ctypes.c_int, [_P, _P, _I64, _I64, _P]),
     "ora_fp4_to_fp8_col": (ctypes.c_int, [_P, _P, _I64, _P, _I32, _P, _P]),
     "ora_fp4_to_fp8_col_segment": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P, _P]),
     "ora_wht_norm": (_F, [ctypes.c_int]),
@@ -290,6 +292,30 @@ def fp4_to_fp8_row(packed, scales):
     _check(lib().ora_fp4_to_fp8_rows(_ptr(p), _ptr(s), rows, cols, _ptr(fp8), _ptr(fsc)),
            "fp4_to_fp8_row")
     return fp8, fsc
+
+
+def fp8_to_fp4_row(fp8, fp8_scales):
+    """Backward-path FP4: E4M3 [rows, cols] with fp32 scales [rows, cols/128]
+    -> MXFP4 (packed [rows, cols/2], UE8M0 [rows, cols/32])."""
+    f = _c(fp8, np.uint8)
+    s = _c(fp8_scales, np.float32)
+    rows, cols = f.shape
+    packed = np.empty((rows, cols // 2), np.uint8)
+    scales = np.empty((rows, cols // 32), np.uint8)
+    _check(lib().ora_fp8_to_fp4_rows(_ptr(f), _ptr(s), rows, cols, _ptr(packed), _ptr(scales)),
+           "fp8_to_fp4_row")
+    return packed, scales
+
+
+def mxfp4_dequantize(packed, scales):
+    """MXFP4 -> fp32 [rows, cols]."""
+    p = _c(packed, np.uint8)
+    s = _c(scales, np.uint8)
+    rows, half = p.shape
+    y = np.empty((rows, 2 * half), np.float32)
+    _check(lib().ora_mxfp4_dequantize(_ptr(p), _ptr(s), rows, 2 * half, _ptr(y)),
+           "mxfp4_dequantize")
+    return y
 
 
 def seg_scale_offsets(row_off) -> np.ndarray:

@@ -58,6 +58,26 @@ int ora_fp4_to_fp8_rows(const uint8_t* packed, const uint8_t* scales, int64_t ro
   return 0;
 }
 
+int ora_fp8_to_fp4_rows(const uint8_t* fp8, const float* fp8_scales, int64_t rows,
+                        int64_t cols, uint8_t* packed, uint8_t* scales) {
+  for (int64_t r = 0; r < rows; ++r) {
+    int rc = ora_fp8_to_fp4_row(fp8 + r * cols, fp8_scales + r * (cols / 128), cols,
+                                packed + r * (cols / 2), scales + r * (cols / 32));
+    if (rc) return rc;
+  }
+  return 0;
+}
+
+int ora_mxfp4_dequantize(const uint8_t* packed, const uint8_t* scales, int64_t rows,
+                         int64_t cols, float* y) {
+  for (int64_t r = 0; r < rows; ++r) {
+    int rc = ora_mxfp4_dequantize_row(packed + r * (cols / 2), scales + r * (cols / 32), cols,
+                                      y + r * cols);
+    if (rc) return rc;
+  }
+  return 0;
+}
+
 /* All segments: segment e covers rows off[e] .. off[e+1]-1; its output starts
  * at byte cols * off[e] and its scales at float cols * scale_off[e], where
  * scale_off is the running sum of ceil(n_e / 128). */

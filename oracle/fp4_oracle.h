@@ -144,6 +144,17 @@ int ora_mxfp4_quantize_row(const float* x, int64_t cols, uint8_t* packed,
  * and each element becomes RN_e4m3(value(code) * 2^-(S_t - S_sub)).
  * [MoE-FP4] "核心技术贡献" 1 (direct FP4-to-FP8 bit conversion, hierarchical
  * scale alignment). */
+/* Backward-path FP4: E4M3 values times their per-128 fp32 scale, rounded
+ * to fp32, quantized to MXFP4 ([MoE-FP4] "局限与未来方向"). */
+int ora_fp8_to_fp4_row(const uint8_t* fp8, const float* fp8_scales, int64_t cols,
+                       uint8_t* packed, uint8_t* scales);
+int ora_fp8_to_fp4_rows(const uint8_t* fp8, const float* fp8_scales, int64_t rows,
+                        int64_t cols, uint8_t* packed, uint8_t* scales);
+int ora_mxfp4_dequantize(const uint8_t* packed, const uint8_t* scales, int64_t rows,
+                         int64_t cols, float* y);
+/* MXFP4 -> fp32: value(code) * 2^(S - 127). */
+int ora_mxfp4_dequantize_row(const uint8_t* packed, const uint8_t* scales, int64_t cols,
+                             float* y);
 int ora_fp4_to_fp8_row(const uint8_t* packed, const uint8_t* scales,
                        int64_t cols, uint8_t* fp8, float* fp8_scales);
 

@@ -97,3 +97,31 @@ int ora_fp4_to_fp8_col_segment(const uint8_t* packed, const uint8_t* scales,
   }
   return 0;
 }
+
+/* Backward-path FP4, which [MoE-FP4] "局限与未来方向" names as future work:
+ * FP8 gradients ("方法概述": E4M3 with one scale per 128 elements) become
+ * MXFP4 for communication.  Each element's value is the E4M3 value times its
+ * block's fp32 scale, rounded once to fp32; the MXFP4 rule above then
+ * quantizes those values. */
+int ora_fp8_to_fp4_row(const uint8_t* fp8, const float* fp8_scales, int64_t cols,
+                       uint8_t* packed, uint8_t* scales) {
+  if (cols < 0 || cols % 128 != 0) return -1;
+  float v[32];
+  for (int64_t b = 0; b < cols / 32; ++b) {
+    const double s = (double)fp8_scales[(32 * b) / 128];
+    for (int i = 0; i < 32; ++i) v[i] = (float)(ora_e4m3_value(fp8[32 * b + i]) * s);
+    if (ora_mxfp4_quantize_row(v, 32, packed + 16 * b, scales + b) != 0) return -1;
+  }
+  return 0;
+}
+
+/* MXFP4 dequantize: value(code) * 2^(S - 127) for the element's UE8M0 scale
+ * S (the product of a 2-bit E2M1 value and a power of two, exact in fp32
+ * unless it leaves the fp32 range). */
+int ora_mxfp4_dequantize_row(const uint8_t* packed, const uint8_t* scales, int64_t cols,
+                             float* y) {
+  if (cols < 0 || cols % 32 != 0) return -1;
+  for (int64_t k = 0; k < cols; ++k)
+    y[k] = (float)(ora_e2m1_value(code_at(packed, k)) * ora_ue8m0_value(scales[k / 32]));
+  return 0;
+}
