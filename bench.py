@@ -529,7 +529,8 @@ KERNEL_STUDIES = ["nvfp4_amax", "nvfp4_quantize", "nvfp4_quantize_sr", "nvfp4_de
                   "nvfp4_qdq", "mxfp4_quantize", "fp4_to_fp8_row", "fp4_to_fp8_col",
                   "fp4quant_encode_g64", "fp4quant_encode_g128", "fp4quant_encode_g256",
                   "fp4quant_decode_g64", "fp4quant_decode_g128", "fp4quant_decode_g256",
-                  "nvfp4_amax_batched", "nvfp4_quantize_batched", "nvfp4_dequantize_batched"]
+                  "nvfp4_amax_batched", "nvfp4_quantize_batched", "nvfp4_dequantize_batched",
+                  "fp8_to_fp4_row", "mxfp4_dequantize"]
 
 
 def kernel_study(name, size_mb, steps, warmup, device):
@@ -601,6 +602,19 @@ def kernel_study(name, size_mb, steps, warmup, device):
             g = Group(name, "study", b, [lambda: m.fp4quant_encode(x, G, pk, s1, s2)])
         else:
             g = Group(name, "study", b, [lambda: m.fp4quant_decode(pk, s1, s2, G, bf16, out=y)])
+    elif name in ("fp8_to_fp4_row", "mxfp4_dequantize"):
+        # the backward-path exchange on MoE-shaped gradients: FP8 -> MXFP4 -> bf16
+        x = W.moe_tokens(seed=1, tokens=max(8, n // 7168), hidden=7168, device=device)
+        pk, sc = m.mxfp4_quantize(x)
+        f8, fs = m.fp4_to_fp8_row(pk, sc)
+        nd = x.numel()
+        if name == "fp8_to_fp4_row":
+            g = Group(name, "study", nd * (1 + 4 / 128 + 0.5 + 1 / 32),
+                      [lambda: m.fp8_to_fp4_row(f8, fs, pk, sc)])
+        else:
+            y = torch.empty_like(x)
+            g = Group(name, "study", nd * (0.5 + 1 / 32 + 2),
+                      [lambda: m.mxfp4_dequantize(pk, sc, bf16, out=y)])
     elif name.endswith("_batched"):
         # whole layers of the Qwen3-8B-shaped set (~386 MB of bf16 per layer)
         layers = max(1, int(round(size_mb / 386.0)))

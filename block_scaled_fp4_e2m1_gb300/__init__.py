@@ -6,14 +6,15 @@ package does not load the library; the first call does, and raises if it has
 not been built (there is no CPU fallback).
 """
 from .codec import (Batch, Segments, fp4_seg_scale_offsets, fp4_to_fp8_col, fp4_to_fp8_row,
-                    fp4quant_decode, fp4quant_encode, kernel_launches, mxfp4_quantize,
-                    nvfp4_amax, nvfp4_dequantize, nvfp4_qdq, nvfp4_qdq_amax, nvfp4_quantize,
-                    nvfp4_quantize_noalloc, nvfp4_amax_batched,
-                    nvfp4_quantize_batched, nvfp4_dequantize_batched)
+                    fp4quant_decode, fp4quant_encode, fp8_to_fp4_row, kernel_launches,
+                    mxfp4_dequantize, mxfp4_quantize, nvfp4_amax, nvfp4_amax_batched,
+                    nvfp4_dequantize, nvfp4_dequantize_batched, nvfp4_qdq, nvfp4_qdq_amax,
+                    nvfp4_quantize, nvfp4_quantize_batched, nvfp4_quantize_noalloc)
 
 __all__ = [
-    "Batch", "nvfp4_amax_batched", "nvfp4_quantize_batched", "nvfp4_dequantize_batched",
-    "Segments", "fp4_seg_scale_offsets", "fp4_to_fp8_col", "fp4_to_fp8_row", "fp4quant_decode",
-    "fp4quant_encode", "kernel_launches", "mxfp4_quantize", "nvfp4_amax", "nvfp4_dequantize",
-    "nvfp4_qdq", "nvfp4_qdq_amax", "nvfp4_quantize", "nvfp4_quantize_noalloc",
+    "Batch", "Segments", "fp4_seg_scale_offsets", "fp4_to_fp8_col", "fp4_to_fp8_row",
+    "fp4quant_decode", "fp4quant_encode", "fp8_to_fp4_row", "kernel_launches",
+    "mxfp4_dequantize", "mxfp4_quantize", "nvfp4_amax", "nvfp4_amax_batched",
+    "nvfp4_dequantize", "nvfp4_dequantize_batched", "nvfp4_qdq", "nvfp4_qdq_amax",
+    "nvfp4_quantize", "nvfp4_quantize_batched", "nvfp4_quantize_noalloc",
 ]

@@ -239,6 +239,36 @@ def mxfp4_quantize(x: torch.Tensor, packed: Optional[torch.Tensor] = None,
     return packed, scales
 
 
+def fp8_to_fp4_row(fp8: torch.Tensor, fp8_scales: torch.Tensor,
+                   packed: Optional[torch.Tensor] = None,
+                   scales: Optional[torch.Tensor] = None):
+    """(E4M3 bytes uint8[rows, cols], fp32 scales [rows, cols/128]) ->
+    (packed uint8[rows, cols/2], UE8M0 scales uint8[rows, cols/32])."""
+    _cuda(fp8, "fp8")
+    rows, cols = fp8.shape
+    dev = fp8.device
+    packed = torch.empty(rows, cols // 2, dtype=torch.uint8, device=dev) if packed is None else packed
+    scales = torch.empty(rows, cols // 32, dtype=torch.uint8, device=dev) if scales is None else scales
+    call("fp8_to_fp4_row", _ptr(fp8), _ptr(fp8_scales), rows, cols, _ptr(packed), _ptr(scales),
+         _stream(dev))
+    return packed, scales
+
+
+def mxfp4_dequantize(packed: torch.Tensor, scales: torch.Tensor,
+                     out_dtype: torch.dtype = torch.bfloat16,
+                     out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """(packed [rows, cols/2], UE8M0 scales [rows, cols/32]) -> [rows, cols]
+    fp32 or bf16."""
+    _cuda(packed, "packed")
+    rows, half = packed.shape
+    cols = 2 * half
+    dev = packed.device
+    out = torch.empty(rows, cols, dtype=out_dtype, device=dev) if out is None else out
+    call("mxfp4_dequantize", _ptr(packed), _ptr(scales), rows, cols, _ptr(out),
+         _dtype(out, "out"), _stream(dev))
+    return out
+
+
 def fp4_to_fp8_row(packed: torch.Tensor, scales: torch.Tensor,
                    fp8: Optional[torch.Tensor] = None,
                    fp8_scales: Optional[torch.Tensor] = None):

@@ -218,6 +218,36 @@ fp4_status nvfp4_dequantize_batched(const fp4_tensor_desc* desc, int32_t count,
 fp4_status mxfp4_quantize(const void* x, int dtype, int64_t rows, int64_t cols,
                           uint8_t* packed, uint8_t* scales, void* stream);
 
+/* ------------------------------------------------ backward-path FP4
+ * [MoE-FP4] "方法概述": gradients travel and are stored in FP8 (E4M3 with one
+ * scale per 128 elements), because on Hopper the FP4 dequantize cost more
+ * than the exchange saved; "局限与未来方向" names FP4 for the backward pass
+ * as future work.  These two calls complete that path with
+ * fp4_to_fp8_row (below): FP8 -> MXFP4 for the exchange, MXFP4 -> FP8 or
+ * floats on the receiving side.
+ */
+
+/* FP8 -> MXFP4.  Each value is RN_fp32(e4m3(byte) * fp8_scales[k / 128]);
+ * the values are then quantized by the mxfp4_quantize rule.
+ *   fp8         [rows, cols] E4M3 bytes, 32-byte aligned (NaN bytes are
+ *               outside the contract)
+ *   fp8_scales  [rows, cols/128] fp32, 4-byte aligned
+ *   packed      [rows, cols/2] out, 16-byte aligned
+ *   scales      [rows, cols/32] UE8M0 bytes out
+ *   cols % 128 == 0 */
+fp4_status fp8_to_fp4_row(const uint8_t* fp8, const float* fp8_scales, int64_t rows,
+                          int64_t cols, uint8_t* packed, uint8_t* scales, void* stream);
+
+/* MXFP4 -> floats: y = value(code) * 2^(S - 127), S = 0 giving 2^-127;
+ * S = 255 is the format's NaN and makes every value of its block the quiet
+ * NaN 0x7FC00000 (bf16 0x7FC0).  Exact for fp32 output; bf16 output holds
+ * every such value as well.
+ *   packed  [rows, cols/2], 16-byte aligned; scales [rows, cols/32] UE8M0
+ *   y       [rows, cols] fp32 or bf16 (out_dtype) out, 32-byte aligned
+ *   cols % 32 == 0 */
+fp4_status mxfp4_dequantize(const uint8_t* packed, const uint8_t* scales, int64_t rows,
+                            int64_t cols, void* y, int out_dtype, void* stream);
+
 /* ------------------------------------------------------ MXFP4 -> FP8 E4M3
  * [MoE-FP4] "核心技术贡献" 1: direct bit conversion, E_fp8 = E_fp4 - 1 + 7,
  * the mantissa bit shifted into the E4M3 mantissa field; four MXFP4 blocks

@@ -110,6 +110,13 @@ def test_mx_fp8_fp4quant_argument_checks(L):
     assert L.fp4_to_fp8_row(A, A, 4, 96, A, A, None) == 3        # cols % 128
     assert L.fp4_to_fp8_row(A, A + 1, 4, 128, A, A, None) == 2
     assert L.fp4_to_fp8_row(None, A, 4, 128, A, A, None) == 1
+    assert L.fp8_to_fp4_row(A, A, 4, 96, A, A, None) == 3       # cols % 128
+    assert L.fp8_to_fp4_row(MIS, A, 4, 128, A, A, None) == 2     # fp8 needs 32 B
+    assert L.fp8_to_fp4_row(A, None, 4, 128, A, A, None) == 1
+    assert L.mxfp4_dequantize(A, A, 4, 48, A, 1, None) == 3      # cols % 32
+    assert L.mxfp4_dequantize(A, A, 4, 64, A, 7, None) == 4
+    assert L.mxfp4_dequantize(A, A, 4, 64, MIS, 1, None) == 2
+    assert L.mxfp4_dequantize(A, A, 4, 64, None, 1, None) == 1
     col = L.fp4_to_fp8_col
     assert col(A, A, 96, A, A, 2, 10, 2, A, A, None) == 3
     assert col(A, A, 128, None, A, 2, 10, 2, A, A, None) == 1
