@@ -76,6 +76,8 @@ _SIGS = {
     "ora_fp4_to_fp8_rows": (ctypes.c_int, [_P, _P, _I64, _I64, _P, _P]),
     "ora_fp8_to_fp4_rows": (ctypes.c_int, [_P, _P, _I64, _I64, _P, _P]),
     "ora_mxfp4_dequantize": (ctypes.c_int, [_P, _P, _I64, _I64, _P]),
+    "ora_fp4_scaled_quantize": (ctypes.c_int, [_P, _I64, ctypes.c_float, _P]),
+    "ora_fp4_scaled_dequantize": (ctypes.c_int, [_P, _I64, ctypes.c_float, _P]),
     "ora_fp4_to_fp8_col": (ctypes.c_int, [_P, _P, _I64, _P, _I32, _P, _P]),
     "ora_fp4_to_fp8_col_segment": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P, _P]),
     "ora_wht_norm": (_F, [ctypes.c_int]),
@@ -315,6 +317,23 @@ def mxfp4_dequantize(packed, scales):
     y = np.empty((rows, 2 * half), np.float32)
     _check(lib().ora_mxfp4_dequantize(_ptr(p), _ptr(s), rows, 2 * half, _ptr(y)),
            "mxfp4_dequantize")
+    return y
+
+
+def fp4_scaled_quantize(x, scale: float):
+    """One fp32 scale for the whole (flat) tensor: packed codes RN_e2m1(RN(x/s))."""
+    x = _c(np.asarray(x, np.float32).reshape(-1), np.float32)
+    packed = np.empty(x.size // 2, np.uint8)
+    _check(lib().ora_fp4_scaled_quantize(_ptr(x), x.size, float(np.float32(scale)), _ptr(packed)),
+           "fp4_scaled_quantize")
+    return packed
+
+
+def fp4_scaled_dequantize(packed, n: int, scale: float):
+    p = _c(np.asarray(packed, np.uint8).reshape(-1), np.uint8)
+    y = np.empty(n, np.float32)
+    _check(lib().ora_fp4_scaled_dequantize(_ptr(p), n, float(np.float32(scale)), _ptr(y)),
+           "fp4_scaled_dequantize")
     return y
 
 

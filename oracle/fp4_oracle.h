@@ -134,6 +134,11 @@ float ora_nvfp4_qdq_amax(const uint16_t* w, const float* g, float lr,
  * block) and codes RN_e2m1(x * 2^-E).  [MoE-FP4] "方法概述" (MXFP4: E2M1,
  * 32-element blocks, UE8M0 scale); [WP2] "Block scaling" (power-of-two
  * scale). */
+/* One fp32 scale per tensor ([WP2] "Block scaling", "Sixteen values aren't
+ * enough"): codes RN_e2m1(RN(x / s)); s = 1 rounds straight to FP4. */
+int ora_fp4_scaled_quantize(const float* x, int64_t n, float s, uint8_t* packed);
+int ora_fp4_scaled_dequantize(const uint8_t* packed, int64_t n, float s, float* y);
+
 int ora_mxfp4_quantize_row(const float* x, int64_t cols, uint8_t* packed,
                            uint8_t* scales);
 

@@ -148,3 +148,27 @@ int ora_nvfp4_qdq(uint16_t* w, const float* g, float lr, int64_t n,
   }
   return 0;
 }
+
+/* [WP2] "Block scaling" ("Why not one scale for the whole matrix?") and
+ * "Sixteen values aren't enough" (rounding straight to FP4): one fp32 scale
+ * s for the whole tensor, each code RN_e2m1(RN(x / s)), the division being
+ * one correctly rounded fp32 operation as in the block rule; s = 1 is
+ * rounding straight to FP4.  The quality comparison of that page's table
+ * uses both. */
+int ora_fp4_scaled_quantize(const float* x, int64_t n, float s, uint8_t* packed) {
+  if (n < 0 || n % 2 != 0 || !(s > 0.0f) || isinf(s)) return -1;
+  for (int64_t i = 0; i < n; i += 2) {
+    const float a = x[i] / s, b = x[i + 1] / s;
+    packed[i / 2] = (uint8_t)(ora_e2m1_rn(a) | (ora_e2m1_rn(b) << 4));
+  }
+  return 0;
+}
+
+int ora_fp4_scaled_dequantize(const uint8_t* packed, int64_t n, float s, float* y) {
+  if (n < 0 || n % 2 != 0) return -1;
+  for (int64_t i = 0; i < n; ++i) {
+    const uint8_t c = (i & 1) ? (uint8_t)(packed[i / 2] >> 4) : (uint8_t)(packed[i / 2] & 0xF);
+    y[i] = (float)ora_e2m1_value(c) * s;
+  }
+  return 0;
+}

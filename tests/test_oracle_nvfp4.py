@@ -212,3 +212,35 @@ def test_qdq_matches_quantize_then_dequantize():
         assert np.array_equal(r, r2)
         assert np.array_equal(r, (v - q).astype(np.float32))
         assert ts == ora.nvfp4_tensor_scale(float(np.abs(v).max()))
+
+
+def test_scaled_quantize_reproduces_the_page_counterexamples():
+    """[WP2] "Block scaling": one scale for the matrix (1.21 / 6) rounds all
+    four example weights to 0; "Sixteen values aren't enough": rounding
+    straight to FP4 does too.  The matrix maximum itself lands on 6."""
+    w = load("worked_block.txt")
+    weights = np.array([float(x) for x in w["weights"]], np.float32)
+    mmax = np.float32(float(w["matrix_max"][0]))
+    s = np.float32(mmax / np.float32(6.0))
+    x = np.concatenate([weights, [mmax, -mmax]]).astype(np.float32)
+    q = ora.fp4_scaled_dequantize(ora.fp4_scaled_quantize(x, s), x.size, s)
+    assert np.all(q[:4] == 0.0) and [float(v) for v in w["matrix_rounded"]] == [0, 0, 0, 0]
+    assert q[4] == np.float32(np.float32(6.0) * s) and q[5] == -q[4]
+    q1 = ora.fp4_scaled_dequantize(ora.fp4_scaled_quantize(weights, 1.0), 4, 1.0)
+    assert np.all(q1 == 0.0) and [float(v) for v in w["straight_to_fp4"]] == [0, 0, 0, 0]
+
+
+def test_scaled_quantize_under_unit_scale_is_the_encoder():
+    """s = 1 reduces to the pinned E2M1 encoder on every bf16 pattern, and a
+    power-of-two scale to the encoder of the exactly scaled values."""
+    allbf = ora.bf16_to_f32(np.arange(1 << 16, dtype=np.uint16))
+    allbf = allbf[np.isfinite(allbf)]
+    allbf = allbf[: allbf.size // 2 * 2]
+    p = ora.fp4_scaled_quantize(allbf, 1.0)
+    codes = np.stack([p & 0xF, p >> 4], -1).reshape(-1)
+    assert np.array_equal(codes, ora.e2m1_rn(allbf))
+    p8 = ora.fp4_scaled_quantize(allbf, 8.0)
+    codes8 = np.stack([p8 & 0xF, p8 >> 4], -1).reshape(-1)
+    assert np.array_equal(codes8, ora.e2m1_rn((allbf / np.float32(8)).astype(np.float32)))
+    y = ora.fp4_scaled_dequantize(p8, allbf.size, 8.0)
+    assert np.array_equal(y, (ora.e2m1_value(codes8) * 8.0).astype(np.float32))
