@@ -55,6 +55,9 @@ def parse_args(argv=None):
                    help="time one kernel alone on a tensor of --size-mb input (a kernel "
                         "study for profiling; prints its own JSON line)")
     p.add_argument("--size-mb", type=float, default=1024.0)
+    p.add_argument("--quality", action="store_true",
+                   help="print the FP4 quality table (zero share, average error) of the four "
+                        "methods on layer-18-shaped synthetic weights, one JSON line per matrix")
     p.add_argument("--source-hash", metavar="GROUP",
                    help="print the source hash a traffic figure of GROUP must carry")
     p.add_argument("--summarize-launches", metavar="CSV",
@@ -672,6 +675,18 @@ def main(argv=None):
                               "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
                               "peak_kind": kind}), flush=True)
             torch.cuda.empty_cache()
+        return 0
+    if args.quality:
+        import torch
+        import __graft_entry__
+        __graft_entry__.build()
+        import block_scaled_fp4_e2m1_gb300 as m
+        from block_scaled_fp4_e2m1_gb300 import workloads as W
+        names = ["q_proj", "k_proj", "v_proj", "o_proj", "gate_proj", "up_proj", "down_proj"]
+        for i, (nm, shp) in enumerate(zip(names, W.qwen3_8b_weight_shapes(layers=1))):
+            w = W.laplace_weight(1800 + i, shp, device=torch.device("cuda", 0))
+            print(json.dumps({"matrix": nm, "shape": list(shp), "quality": m.fp4_quality(w)}),
+                  flush=True)
         return 0
     if args.source_hash:
         print(kernel_source_hash(args.source_hash))

@@ -38,6 +38,8 @@ SIGNATURES = {
     "fp4_to_fp8_row": (INT, [P, P, I64, I64, P, P, P]),
     "fp8_to_fp4_row": (INT, [P, P, I64, I64, P, P, P]),
     "mxfp4_dequantize": (INT, [P, P, I64, I64, P, INT, P]),
+    "fp4_scaled_quantize": (INT, [P, INT, I64, ctypes.c_float, P, P]),
+    "fp4_scaled_dequantize": (INT, [P, I64, ctypes.c_float, P, INT, P]),
     "fp4_to_fp8_col": (INT, [P, P, I64, P, P, I32, I64, I64, P, P, P]),
     "fp4_seg_scale_offsets": (INT, [P, I32, P]),
     "fp4quant_encode": (INT, [P, INT, I64, I64, INT, P, P, P, P]),

@@ -239,6 +239,29 @@ def mxfp4_quantize(x: torch.Tensor, packed: Optional[torch.Tensor] = None,
     return packed, scales
 
 
+def fp4_scaled_quantize(x: torch.Tensor, scale: float,
+                        packed: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """One fp32 scale for the whole tensor: codes RN_e2m1(RN(x / scale)),
+    packed two per byte (n/2 bytes)."""
+    _cuda(x, "x")
+    n = x.numel()
+    packed = torch.empty(n // 2, dtype=torch.uint8, device=x.device) if packed is None else packed
+    call("fp4_scaled_quantize", _ptr(x), _dtype(x, "x"), n, float(scale), _ptr(packed),
+         _stream(x.device))
+    return packed
+
+
+def fp4_scaled_dequantize(packed: torch.Tensor, n: int, scale: float,
+                          out_dtype: torch.dtype = torch.float32,
+                          out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """value(code) * scale for the n codes of packed."""
+    _cuda(packed, "packed")
+    out = torch.empty(n, dtype=out_dtype, device=packed.device) if out is None else out
+    call("fp4_scaled_dequantize", _ptr(packed), n, float(scale), _ptr(out), _dtype(out, "out"),
+         _stream(packed.device))
+    return out
+
+
 def fp8_to_fp4_row(fp8: torch.Tensor, fp8_scales: torch.Tensor,
                    packed: Optional[torch.Tensor] = None,
                    scales: Optional[torch.Tensor] = None):

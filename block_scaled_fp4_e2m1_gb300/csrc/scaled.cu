@@ -1,0 +1,135 @@
+// scaled.cu -- E2M1 with one fp32 scale for a whole tensor.
+//
+// [WP2] "Block scaling" ("Why not one scale for the whole matrix?") and
+// "Sixteen values aren't enough": the comparison points of block scaling.
+// Codes are RN_e2m1(RN(x / s)) with one correctly rounded division per
+// element; s = 1 rounds straight to FP4.  Dequantize: value(code) * s.
+//
+// One thread per 16 elements: one 256-bit load of bf16 (two of fp32), an
+// 8-byte store of codes; the inverse reads 8 bytes and writes 32 (bf16) or
+// 64 (fp32).
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "host_common.h"
+
+namespace fp4 {
+namespace {
+
+constexpr int kThreads = 256;
+
+template <bool kBF16>
+__global__ void __launch_bounds__(kThreads)
+    scaled_quantize_kernel(const void* __restrict__ x, int64_t nunits, float s,
+                           uint8_t* __restrict__ packed) {
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  for (int64_t u = (int64_t)blockIdx.x * kThreads + threadIdx.x; u < nunits; u += stride) {
+    float v[16];
+    if (kBF16) {
+      const U32x8 r = ld_stream_v8(static_cast<const uint16_t*>(x) + 16 * u);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        v[2 * i] = bf16_lo(r.w[i]);
+        v[2 * i + 1] = bf16_hi(r.w[i]);
+      }
+    } else {
+      const float* p = static_cast<const float*>(x) + 16 * u;
+      const U32x8 a = ld_stream_v8(p), b = ld_stream_v8(p + 8);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        v[i] = __uint_as_float(a.w[i]);
+        v[8 + i] = __uint_as_float(b.w[i]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __fdiv_rn(v[i], s);
+    const uint32_t w0 = cvt_e2m1x8(v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]);
+    const uint32_t w1 = cvt_e2m1x8(v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15]);
+    *reinterpret_cast<uint2*>(packed + 8 * u) = make_uint2(w0, w1);
+  }
+}
+
+template <bool kBF16Out>
+__global__ void __launch_bounds__(kThreads)
+    scaled_dequantize_kernel(const uint8_t* __restrict__ packed, int64_t nunits, float s,
+                             void* __restrict__ y) {
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  for (int64_t u = (int64_t)blockIdx.x * kThreads + threadIdx.x; u < nunits; u += stride) {
+    const uint2 p = ld_stream_v2(packed + 8 * u);
+    const uint32_t words[2] = {p.x, p.y};
+    float o[16];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t h2;
+        const uint16_t byte = (uint16_t)((words[h] >> (8 * k)) & 0xFFu);
+        asm("{\n\t.reg .b8 c;\n\tcvt.u8.u16 c, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, c;\n\t}"
+            : "=r"(h2)
+            : "h"(byte));
+        float lo, hi;
+        asm("cvt.f32.f16 %0, %1;" : "=f"(lo) : "h"((uint16_t)(h2 & 0xFFFFu)));
+        asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"((uint16_t)(h2 >> 16)));
+        o[8 * h + 2 * k] = __fmul_rn(lo, s);
+        o[8 * h + 2 * k + 1] = __fmul_rn(hi, s);
+      }
+    }
+    if (kBF16Out) {
+      U32x8 w;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w.w[i] = pack_bf16x2(o[2 * i], o[2 * i + 1]);
+      st_v8(static_cast<uint16_t*>(y) + 16 * u, w);
+    } else {
+      float* out = static_cast<float*>(y) + 16 * u;
+      U32x8 a, b;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        a.w[i] = __float_as_uint(o[i]);
+        b.w[i] = __float_as_uint(o[8 + i]);
+      }
+      st_v8(out, a);
+      st_v8(out + 8, b);
+    }
+  }
+}
+
+bool scale_ok(float s) { return s > 0.0f && s <= 3.40282347e38f; }
+
+}  // namespace
+}  // namespace fp4
+
+using namespace fp4;
+
+extern "C" {
+
+fp4_status fp4_scaled_quantize(const void* x, int dtype, int64_t n, float scale, uint8_t* packed,
+                               void* stream) {
+  if (!dtype_ok(dtype)) return FP4_ERR_DTYPE;
+  if (n < 0 || n % 16 != 0) return FP4_ERR_SHAPE;
+  if (!scale_ok(scale)) return FP4_ERR_ARG;
+  if (n > 0 && (!x || !packed)) return FP4_ERR_NULL;
+  if (!aligned(x, 32) || !aligned(packed, 8)) return FP4_ERR_ALIGN;
+  if (n == 0) return FP4_OK;
+  const int64_t nu = n / 16;
+  cudaStream_t s = as_stream(stream);
+  if (dtype == FP4_BF16)
+    return launch<scaled_quantize_kernel<true>>(nu, kThreads, 0, s, x, nu, scale, packed);
+  return launch<scaled_quantize_kernel<false>>(nu, kThreads, 0, s, x, nu, scale, packed);
+}
+
+fp4_status fp4_scaled_dequantize(const uint8_t* packed, int64_t n, float scale, void* y,
+                                 int out_dtype, void* stream) {
+  if (!dtype_ok(out_dtype)) return FP4_ERR_DTYPE;
+  if (n < 0 || n % 16 != 0) return FP4_ERR_SHAPE;
+  if (!scale_ok(scale)) return FP4_ERR_ARG;
+  if (n > 0 && (!packed || !y)) return FP4_ERR_NULL;
+  if (!aligned(packed, 8) || !aligned(y, 32)) return FP4_ERR_ALIGN;
+  if (n == 0) return FP4_OK;
+  const int64_t nu = n / 16;
+  cudaStream_t s = as_stream(stream);
+  if (out_dtype == FP4_BF16)
+    return launch<scaled_dequantize_kernel<true>>(nu, kThreads, 0, s, packed, nu, scale, y);
+  return launch<scaled_dequantize_kernel<false>>(nu, kThreads, 0, s, packed, nu, scale, y);
+}
+
+}  // extern "C"

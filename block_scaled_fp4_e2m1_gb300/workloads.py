@@ -114,7 +114,8 @@ def laplace_weight(seed: int, shape, median_abs: float = 0.017, outliers: int = 
     g = _gen(seed, device)
     n = shape[0] * shape[1]
     b = median_abs / math.log(2.0)
-    u = torch.rand(n, generator=g, device=device, dtype=torch.float32) - 0.5
+    # rand() can return exactly 0; keep |u| < 1/2 so that every weight is finite
+    u = torch.rand(n, generator=g, device=device, dtype=torch.float32).clamp_(min=2.0 ** -25) - 0.5
     w = -b * torch.sign(u) * torch.log1p(-2.0 * u.abs())
     pos = torch.randperm(n, generator=g, device=device)[:outliers]
     mag = 0.3 + (max_abs - 0.3) * torch.rand(outliers, generator=g, device=device)

@@ -205,6 +205,20 @@ fp4_status nvfp4_dequantize_batched(const fp4_tensor_desc* desc, int32_t count,
                                     int64_t total_chunks, const float* tensor_scale, int out_dtype,
                                     void* stream);
 
+/* ---------------------------------------------------- one scale per tensor
+ * [WP2] "Block scaling" ("Why not one scale for the whole matrix?") and
+ * "Sixteen values aren't enough": the comparison points of block scaling.
+ * Codes RN_e2m1(RN(x / scale)), one correctly rounded division per
+ * element; scale = 1 rounds straight to FP4; dequantize value(code) *
+ * scale.  scale must be finite and > 0 (FP4_ERR_ARG).
+ *   x       [n] fp32 or bf16, 32-byte aligned; n % 16 == 0
+ *   packed  [n/2] codes, 8-byte aligned
+ *   y       [n] fp32 or bf16 (out_dtype), 32-byte aligned */
+fp4_status fp4_scaled_quantize(const void* x, int dtype, int64_t n, float scale,
+                               uint8_t* packed, void* stream);
+fp4_status fp4_scaled_dequantize(const uint8_t* packed, int64_t n, float scale, void* y,
+                                 int out_dtype, void* stream);
+
 /* ------------------------------------------------------------------ MXFP4
  * [MoE-FP4] "方法概述" / "核心技术贡献" 2 (BF16ToFP4Row): each row in
  * 32-element blocks, one UE8M0 scale per block ([WP2] "Block scaling": a

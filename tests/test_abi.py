@@ -117,6 +117,12 @@ def test_mx_fp8_fp4quant_argument_checks(L):
     assert L.mxfp4_dequantize(A, A, 4, 64, A, 7, None) == 4
     assert L.mxfp4_dequantize(A, A, 4, 64, MIS, 1, None) == 2
     assert L.mxfp4_dequantize(A, A, 4, 64, None, 1, None) == 1
+    assert L.fp4_scaled_quantize(A, 1, 24, 1.0, A, None) == 3      # n % 16
+    assert L.fp4_scaled_quantize(A, 1, 32, 0.0, A, None) == 5      # scale > 0
+    assert L.fp4_scaled_quantize(A, 1, 32, float("inf"), A, None) == 5
+    assert L.fp4_scaled_quantize(MIS, 1, 32, 1.0, A, None) == 2
+    assert L.fp4_scaled_dequantize(A, 32, 1.0, None, 1, None) == 1
+    assert L.fp4_scaled_dequantize(A, 32, 1.0, A, 9, None) == 4
     col = L.fp4_to_fp8_col
     assert col(A, A, 96, A, A, 2, 10, 2, A, A, None) == 3
     assert col(A, A, 128, None, A, 2, 10, 2, A, A, None) == 1
