@@ -21,7 +21,7 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
-_SOURCES = ["formats.c", "philox.c", "nvfp4.c", "mxfp4.c", "fp4quant.c", "arrays.c"]
+_SOURCES = ["formats.c", "philox.c", "nvfp4.c", "mxfp4.c", "fp4quant.c", "layout.c", "arrays.c"]
 CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
           "-Wall", "-Wextra"]
 
@@ -80,6 +80,9 @@ _SIGS = {
     "ora_fp4_scaled_dequantize": (ctypes.c_int, [_P, _I64, ctypes.c_float, _P]),
     "ora_fp4_to_fp8_col": (ctypes.c_int, [_P, _P, _I64, _P, _I32, _P, _P]),
     "ora_fp4_to_fp8_col_segment": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P, _P]),
+    "ora_blocked_scales_size": (_I64, [_I64, _I64]),
+    "ora_scales_to_blocked": (ctypes.c_int, [_P, _I64, _I64, _P]),
+    "ora_scales_from_blocked": (ctypes.c_int, [_P, _I64, _I64, _P]),
     "ora_wht_norm": (_F, [ctypes.c_int]),
     "ora_wht": (None, [_P, ctypes.c_int]),
     "ora_fp4quant_encode": (ctypes.c_int, [_P, _I64, _I64, ctypes.c_int, _P, _P, _P]),
@@ -335,6 +338,28 @@ def fp4_scaled_dequantize(packed, n: int, scale: float):
     _check(lib().ora_fp4_scaled_dequantize(_ptr(p), n, float(np.float32(scale)), _ptr(y)),
            "fp4_scaled_dequantize")
     return y
+
+
+def blocked_scales_size(rows: int, cols: int) -> int:
+    return int(lib().ora_blocked_scales_size(rows, cols))
+
+
+def scales_to_blocked(scales, rows: int, cols: int) -> np.ndarray:
+    """[rows, cols] uint8 scales -> the blocked (swizzled) uint8 buffer."""
+    s = _c(scales, np.uint8).reshape(-1)
+    assert s.size == rows * cols
+    out = np.full(blocked_scales_size(rows, cols), 0xA5, dtype=np.uint8)
+    _check(lib().ora_scales_to_blocked(_ptr(s), rows, cols, _ptr(out)), "scales_to_blocked")
+    return out
+
+
+def scales_from_blocked(blocked, rows: int, cols: int) -> np.ndarray:
+    """The inverse of scales_to_blocked: [rows, cols] uint8."""
+    b = _c(blocked, np.uint8).reshape(-1)
+    assert b.size == blocked_scales_size(rows, cols)
+    out = np.empty(rows * cols, dtype=np.uint8)
+    _check(lib().ora_scales_from_blocked(_ptr(b), rows, cols, _ptr(out)), "scales_from_blocked")
+    return out.reshape(rows, cols)
 
 
 def seg_scale_offsets(row_off) -> np.ndarray:

@@ -173,6 +173,25 @@ int ora_fp4_to_fp8_col_segment(const uint8_t* packed, const uint8_t* scales,
                                int64_t cols, int64_t row0, int64_t n_e,
                                uint8_t* out, float* out_scales);
 
+/* ------------------------------------------------------ blocked scale layout */
+
+/* Bytes of the blocked form of a [rows, cols] one-byte scale matrix:
+ * 128 * ceil(rows / 128) * 4 * ceil(cols / 4); -1 for negative sizes. */
+int64_t ora_blocked_scales_size(int64_t rows, int64_t cols);
+
+/* [rows, cols] row-major scales -> the blocked layout that block-scaled
+ * tensor-core matmuls read: zero padding to whole 128 x 4 tiles, tiles in
+ * row-major order, the scale of tile row r, column c at byte
+ * 16 * (r % 32) + 4 * (r / 32) + c of its 512-byte tile.  [fp4-train]
+ * "Scope" (scales swizzled for torch._scaled_mm); the layout itself follows
+ * the public description of the tensor cores' block-scale layout. */
+int ora_scales_to_blocked(const uint8_t* scales, int64_t rows, int64_t cols,
+                          uint8_t* blocked);
+
+/* The inverse: the [rows, cols] scales read back out of the blocked form. */
+int ora_scales_from_blocked(const uint8_t* blocked, int64_t rows, int64_t cols,
+                            uint8_t* scales);
+
 /* ------------------------------------------------------------------ FP4Quant */
 
 /* The normalization constant RN(1/sqrt(G)) for G in {64, 128, 256}. */
