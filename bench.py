@@ -533,7 +533,8 @@ KERNEL_STUDIES = ["nvfp4_amax", "nvfp4_quantize", "nvfp4_quantize_sr", "nvfp4_de
                   "fp4quant_encode_g64", "fp4quant_encode_g128", "fp4quant_encode_g256",
                   "fp4quant_decode_g64", "fp4quant_decode_g128", "fp4quant_decode_g256",
                   "nvfp4_amax_batched", "nvfp4_quantize_batched", "nvfp4_dequantize_batched",
-                  "fp8_to_fp4_row", "mxfp4_dequantize"]
+                  "fp8_to_fp4_row", "mxfp4_dequantize", "nvfp4_quantize_blocked",
+                  "fp4_scales_to_blocked", "fp4_scales_from_blocked"]
 
 
 def kernel_study(name, size_mb, steps, warmup, device):
@@ -618,6 +619,29 @@ def kernel_study(name, size_mb, steps, warmup, device):
             y = torch.empty_like(x)
             g = Group(name, "study", nd * (0.5 + 1 / 32 + 2),
                       [lambda: m.mxfp4_dequantize(pk, sc, bf16, out=y)])
+    elif name == "nvfp4_quantize_blocked":
+        # a [rows, 4096] bf16 weight matrix, block scales straight into the
+        # blocked layout of block-scaled matmuls
+        w = W.laplace_weight(7, (n // 4096, 4096), device=device)
+        a, t = z(1, f32), z(1, f32)
+        pk = z((n // 4096, 2048), u8)
+        blk = z(m.fp4_blocked_scales_size(n // 4096, 256), u8)
+        m.nvfp4_amax(w.view(-1), amax_ws=a)
+        g = Group(name, "study", 2.5 * n + blk.numel(),
+                  [lambda: m.nvfp4_quantize_blocked(w, tscale="from_amax", amax_ws=a,
+                                                    tensor_scale=t, packed=pk,
+                                                    blocked_scales=blk)])
+    elif name in ("fp4_scales_to_blocked", "fp4_scales_from_blocked"):
+        # the e4m3 scales of a [rows, 4096] weight: [rows, 256] bytes of size_mb MB
+        rows = max(128, int(size_mb * 1e6 / 256) // 128 * 128)
+        sc = torch.randint(0, 127, (rows, 256), dtype=u8, device=device)
+        blk = m.fp4_scales_to_blocked(sc)
+        if name == "fp4_scales_to_blocked":
+            g = Group(name, "study", sc.numel() + blk.numel(),
+                      [lambda: m.fp4_scales_to_blocked(sc, out=blk)])
+        else:
+            g = Group(name, "study", sc.numel() + blk.numel(),
+                      [lambda: m.fp4_scales_from_blocked(blk, rows, 256, out=sc)])
     elif name.endswith("_batched"):
         # whole layers of the Qwen3-8B-shaped set (~386 MB of bf16 per layer)
         layers = max(1, int(round(size_mb / 386.0)))

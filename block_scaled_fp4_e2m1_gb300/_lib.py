@@ -30,6 +30,10 @@ SIGNATURES = {
     "nvfp4_qdq_amax": (INT, [P, P, F32, P, I64, P, P]),
     "nvfp4_qdq": (INT, [P, P, F32, I64, P, INT, U64, U64, INT, P, P, P, P, P]),
     "nvfp4_quantize_noalloc": (INT, [P, INT, I64, P, INT, U64, U64, P, P, P, P]),
+    "fp4_blocked_scales_size": (I64, [I64, I64]),
+    "fp4_scales_to_blocked": (INT, [P, I64, I64, P, P]),
+    "fp4_scales_from_blocked": (INT, [P, I64, I64, P, P]),
+    "nvfp4_quantize_blocked": (INT, [P, INT, I64, I64, P, INT, U64, U64, INT, P, P, P, P, P]),
     "fp4_batch_plan": (INT, [P, I32, P]),
     "nvfp4_amax_batched": (INT, [P, I32, I64, INT, P, P]),
     "nvfp4_quantize_batched": (INT, [P, I32, I64, INT, INT, U64, U64, INT, P, P, P]),

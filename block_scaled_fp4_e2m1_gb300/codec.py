@@ -81,6 +81,72 @@ def nvfp4_quantize(x: torch.Tensor, residual: Optional[torch.Tensor] = None,
     return packed, scales, tensor_scale
 
 
+def fp4_blocked_scales_size(rows: int, cols: int) -> int:
+    """Bytes of the blocked (swizzled) form of a [rows, cols] scale matrix."""
+    size = int(_lib.lib().fp4_blocked_scales_size(rows, cols))
+    if size < 0:
+        raise ValueError(f"scale matrix [{rows}, {cols}] out of range")
+    return size
+
+
+def fp4_scales_to_blocked(scales: torch.Tensor, out: Optional[torch.Tensor] = None
+                          ) -> torch.Tensor:
+    """[rows, cols] uint8 scales -> the blocked layout block-scaled matmuls
+    read (uint8, fp4_blocked_scales_size(rows, cols) bytes)."""
+    _cuda(scales, "scales")
+    if scales.dim() != 2 or scales.dtype != torch.uint8:
+        raise ValueError("scales must be a 2-D uint8 tensor")
+    rows, cols = scales.shape
+    dev = scales.device
+    if out is None:
+        out = torch.empty(fp4_blocked_scales_size(rows, cols), dtype=torch.uint8, device=dev)
+    call("fp4_scales_to_blocked", _ptr(scales), rows, cols, _ptr(out), _stream(dev))
+    return out
+
+
+def fp4_scales_from_blocked(blocked: torch.Tensor, rows: int, cols: int,
+                            out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """The inverse of fp4_scales_to_blocked: uint8 [rows, cols]."""
+    _cuda(blocked, "blocked")
+    if blocked.numel() != fp4_blocked_scales_size(rows, cols):
+        raise ValueError("blocked has the wrong size for this scale matrix")
+    dev = blocked.device
+    out = torch.empty((rows, cols), dtype=torch.uint8, device=dev) if out is None else out
+    call("fp4_scales_from_blocked", _ptr(blocked), rows, cols, _ptr(out), _stream(dev))
+    return out
+
+
+def nvfp4_quantize_blocked(x: torch.Tensor, residual: Optional[torch.Tensor] = None,
+                           rounding: str = "rtn", seed: int = 0, step: int = 0,
+                           tscale: str = "compute",
+                           tensor_scale: Optional[torch.Tensor] = None,
+                           amax_ws: Optional[torch.Tensor] = None,
+                           packed: Optional[torch.Tensor] = None,
+                           blocked_scales: Optional[torch.Tensor] = None
+                           ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """nvfp4_quantize of the [rows, k] matrix x with its block scales written
+    in the blocked layout.  Returns (packed uint8[rows, k/2], blocked uint8
+    [fp4_blocked_scales_size(rows, k/16)], tensor_scale fp32[1])."""
+    _cuda(x, "x")
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D [rows, k]")
+    rows, k = x.shape
+    dev = x.device
+    if tensor_scale is None:
+        tensor_scale = _scalar(dev, 1.0)
+    if amax_ws is None and tscale != "given":
+        amax_ws = _scalar(dev)
+    if packed is None:
+        packed = torch.empty((rows, k // 2), dtype=torch.uint8, device=dev)
+    if blocked_scales is None:
+        blocked_scales = torch.empty(fp4_blocked_scales_size(rows, k // 16),
+                                     dtype=torch.uint8, device=dev)
+    call("nvfp4_quantize_blocked", _ptr(x), _dtype(x, "x"), rows, k, _ptr(residual),
+         _ROUND[rounding], seed, step, _TSCALE[tscale], _ptr(tensor_scale), _ptr(amax_ws),
+         _ptr(packed), _ptr(blocked_scales), _stream(dev))
+    return packed, blocked_scales, tensor_scale
+
+
 def nvfp4_dequantize(packed: torch.Tensor, scales: torch.Tensor,
                      tensor_scale: Optional[torch.Tensor], shape: Sequence[int],
                      out_dtype: torch.dtype = torch.float32,

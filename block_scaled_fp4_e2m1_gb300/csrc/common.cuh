@@ -296,6 +296,42 @@ __device__ __forceinline__ uint32_t e2m1_sr(float a, uint32_t rw) {
   return sign | (c + (uint32_t)(u < frac));
 }
 
+// ---------------------------------------------------- blocked scale layout
+// The layout of block scales that Blackwell block-scaled tensor-core matmuls
+// read: a [rows, cols] matrix of one-byte scales, zero-padded to whole tiles
+// of 128 rows x 4 columns, tiles stored in row-major order, 512 bytes each;
+// scale (r, c) of a tile at byte 16 (r mod 32) + 4 floor(r / 32) + c.
+
+// Byte offset of scale (r, c) of the padded matrix; col_tiles = ceil(cols/4).
+__device__ __forceinline__ int64_t blocked_offset(int64_t r, int64_t c, int64_t col_tiles) {
+  return ((((r >> 7) * col_tiles) + (c >> 2)) << 9) + ((r & 31) << 4) + (((r >> 5) & 3) << 2) +
+         (c & 3);
+}
+
+// Zero the padding bytes of a blocked buffer: columns cols .. 4 col_tiles - 1
+// of every row, then every column of rows rows .. 128 ceil(rows/128) - 1.
+// Threads t = 0, stride, 2 stride, ... share the work.
+__device__ __forceinline__ void blocked_zero_padding(uint8_t* out, int64_t rows, int64_t cols,
+                                                     int64_t col_tiles, int64_t t,
+                                                     int64_t stride) {
+  const int64_t pc = 4 * col_tiles - cols;               // padded columns, 0..3
+  const int64_t pw = 4 * col_tiles;                      // padded row width
+  const int64_t n1 = rows * pc;
+  const int64_t n2 = (((rows + 127) >> 7) * 128 - rows) * pw;
+  for (int64_t i = t; i < n1 + n2; i += stride) {
+    int64_t r, c;
+    if (i < n1) {
+      r = i / pc;
+      c = cols + (i - r * pc);
+    } else {
+      const int64_t j = i - n1, q = j / pw;
+      r = rows + q;
+      c = j - q * pw;
+    }
+    out[blocked_offset(r, c, col_tiles)] = 0;
+  }
+}
+
 // ------------------------------------------------------------- reductions
 
 __device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {

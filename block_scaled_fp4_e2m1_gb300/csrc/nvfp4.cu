@@ -105,17 +105,31 @@ constexpr int quantize_min_ctas() {
   return kRes ? 2 : ((kSR || !kBF16) ? 3 : 4);
 }
 
+// Geometry of a [rows, 16 * cols] matrix whose block scales go out in the
+// blocked layout (common.cuh): cols block scales per row, col_tiles =
+// ceil(cols / 4).  Unused (all zero) for the linear layout.
+struct BlockedMap {
+  int64_t rows;
+  int64_t cols;
+  int64_t col_tiles;
+};
+
 // A thread quantizes one block per grid-stride step; the loads of the next
 // kD blocks are in flight meanwhile.  The ring of kD + 1 buffers is walked
 // by a fully unrolled inner loop, so every buffer index is a constant and no
 // registers are copied.  bf16 round-to-nearest without error feedback takes
 // quantize_block_bf16_rtn, everything else quantize_block.
-template <bool kBF16, bool kSR, bool kRes>
+//
+// kBlk writes block b's scale at its place in the blocked layout instead of
+// at byte b: the thread keeps the (row, column) of its block and steps it by
+// the grid stride, so no division is left in the loop; the padding bytes
+// are zeroed first.
+template <bool kBF16, bool kSR, bool kRes, bool kBlk>
 __global__ void __launch_bounds__(kThreads, quantize_min_ctas<kBF16, kSR, kRes>())
     quantize_kernel(const void* __restrict__ x, float* __restrict__ residual, int64_t nblocks,
                     uint64_t seed, uint64_t step, int tscale_mode, float* __restrict__ tensor_scale,
                     const float* __restrict__ amax_ws, uint8_t* __restrict__ packed,
-                    uint8_t* __restrict__ scales) {
+                    uint8_t* __restrict__ scales, BlockedMap bm) {
   constexpr int kD = QuantPipe<kBF16, kRes>::kDepth;
   float s_t;
   if (tscale_mode == FP4_TSCALE_GIVEN) {
@@ -129,6 +143,16 @@ __global__ void __launch_bounds__(kThreads, quantize_min_ctas<kBF16, kSR, kRes>(
   const uint32_t st0 = (uint32_t)step, st1 = (uint32_t)(step >> 32);
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   int64_t b = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  int64_t br = 0, bc = 0, step_r = 0, step_c = 0;
+  if (kBlk) {
+    blocked_zero_padding(scales, bm.rows, bm.cols, bm.col_tiles, b, stride);
+    if (bm.cols > 0) {
+      br = b / bm.cols;
+      bc = b - br * bm.cols;
+      step_r = stride / bm.cols;
+      step_c = stride - step_r * bm.cols;
+    }
+  }
 
   BlockIn<kBF16, kRes> buf[kD + 1];
 #pragma unroll
@@ -148,7 +172,17 @@ __global__ void __launch_bounds__(kThreads, quantize_min_ctas<kBF16, kSR, kRes>(
         sb = quantize_block<kSR, kRes>(v, s_t, sd, (uint64_t)(16 * b), key0, key1, st0, st1, out,
                                        q);
       *reinterpret_cast<uint2*>(packed + 8 * b) = out;
-      scales[b] = (uint8_t)sb;
+      if (kBlk) {
+        scales[blocked_offset(br, bc, bm.col_tiles)] = (uint8_t)sb;
+        bc += step_c;
+        br += step_r;
+        if (bc >= bm.cols) {
+          bc -= bm.cols;
+          ++br;
+        }
+      } else {
+        scales[b] = (uint8_t)sb;
+      }
       if (kRes) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) r[i] = __fsub_rn(v[i], q[i]);
@@ -306,26 +340,53 @@ fp4_status launch_amax(const void* x, int dtype, int64_t n, const float* residua
   return launch<amax_kernel<false, false>>(units, kThreads, 0, s, x, residual, nb, amax_ws);
 }
 
-template <bool kBF16, bool kSR, bool kRes>
+template <bool kBF16, bool kSR, bool kRes, bool kBlk>
 fp4_status launch_quantize_k(const void* x, int64_t nb, float* residual, uint64_t seed, uint64_t step,
                              int mode, float* ts, const float* amax, uint8_t* packed, uint8_t* scales,
-                             cudaStream_t s) {
-  return launch<quantize_kernel<kBF16, kSR, kRes>>(nb, kThreads, 0, s, x, residual, nb, seed, step,
-                                                   mode, ts, amax, packed, scales);
+                             const BlockedMap& bm, cudaStream_t s) {
+  return launch<quantize_kernel<kBF16, kSR, kRes, kBlk>>(nb, kThreads, 0, s, x, residual, nb, seed,
+                                                         step, mode, ts, amax, packed, scales, bm);
 }
 
-template <bool kBF16>
+template <bool kBF16, bool kBlk>
 fp4_status launch_quantize_t(const void* x, int64_t nb, float* residual, int rounding, uint64_t seed,
                              uint64_t step, int mode, float* ts, const float* amax, uint8_t* packed,
-                             uint8_t* scales, cudaStream_t s) {
+                             uint8_t* scales, const BlockedMap& bm, cudaStream_t s) {
   if (rounding == FP4_SR) {
     if (residual)
-      return launch_quantize_k<kBF16, true, true>(x, nb, residual, seed, step, mode, ts, amax, packed, scales, s);
-    return launch_quantize_k<kBF16, true, false>(x, nb, residual, seed, step, mode, ts, amax, packed, scales, s);
+      return launch_quantize_k<kBF16, true, true, kBlk>(x, nb, residual, seed, step, mode, ts, amax,
+                                                        packed, scales, bm, s);
+    return launch_quantize_k<kBF16, true, false, kBlk>(x, nb, residual, seed, step, mode, ts, amax,
+                                                       packed, scales, bm, s);
   }
   if (residual)
-    return launch_quantize_k<kBF16, false, true>(x, nb, residual, seed, step, mode, ts, amax, packed, scales, s);
-  return launch_quantize_k<kBF16, false, false>(x, nb, residual, seed, step, mode, ts, amax, packed, scales, s);
+    return launch_quantize_k<kBF16, false, true, kBlk>(x, nb, residual, seed, step, mode, ts, amax,
+                                                       packed, scales, bm, s);
+  return launch_quantize_k<kBF16, false, false, kBlk>(x, nb, residual, seed, step, mode, ts, amax,
+                                                      packed, scales, bm, s);
+}
+
+// The shared part of nvfp4_quantize and nvfp4_quantize_blocked after the
+// argument checks: the amax pass in COMPUTE mode, then the quantize launch.
+template <bool kBlk>
+fp4_status quantize_common(const void* x, int dtype, int64_t n, float* residual, int rounding,
+                           uint64_t seed, uint64_t step, int tscale_mode, float* tensor_scale,
+                           float* amax_ws, uint8_t* packed, uint8_t* scales, const BlockedMap& bm,
+                           cudaStream_t s) {
+  if (tscale_mode == FP4_TSCALE_COMPUTE) {
+    fp4_status st = launch_amax(x, dtype, n, residual, amax_ws, s);
+    if (st != FP4_OK) return st;
+  }
+  const int64_t nb = n / 16;
+  // An empty tensor still publishes its tensor scale (amax 0 -> 1): the
+  // kernel runs with one CTA and no blocks.  (An empty matrix has no scale
+  // bytes, blocked or not, so nothing is left to pad.)
+  if (nb == 0 && tscale_mode == FP4_TSCALE_GIVEN) return FP4_OK;
+  if (dtype == FP4_BF16)
+    return launch_quantize_t<true, kBlk>(x, nb, residual, rounding, seed, step, tscale_mode,
+                                         tensor_scale, amax_ws, packed, scales, bm, s);
+  return launch_quantize_t<false, kBlk>(x, nb, residual, rounding, seed, step, tscale_mode,
+                                        tensor_scale, amax_ws, packed, scales, bm, s);
 }
 
 template <bool kG, bool kRes, bool kSR, bool kPacked>
@@ -395,20 +456,31 @@ fp4_status nvfp4_quantize(const void* x, int dtype, int64_t n, float* residual, 
   if (!aligned(x, 32) || !aligned(residual, 32) || !aligned(packed, 16) ||
       !aligned(tensor_scale, 4) || !aligned(amax_ws, 4))
     return FP4_ERR_ALIGN;
-  cudaStream_t s = as_stream(stream);
-  if (tscale_mode == FP4_TSCALE_COMPUTE) {
-    fp4_status st = launch_amax(x, dtype, n, residual, amax_ws, s);
-    if (st != FP4_OK) return st;
-  }
-  const int64_t nb = n / 16;
-  // An empty tensor still publishes its tensor scale (amax 0 -> 1): the
-  // kernel runs with one CTA and no blocks.
-  if (nb == 0 && tscale_mode == FP4_TSCALE_GIVEN) return FP4_OK;
-  if (dtype == FP4_BF16)
-    return launch_quantize_t<true>(x, nb, residual, rounding, seed, step, tscale_mode, tensor_scale,
-                                   amax_ws, packed, scales, s);
-  return launch_quantize_t<false>(x, nb, residual, rounding, seed, step, tscale_mode, tensor_scale,
-                                  amax_ws, packed, scales, s);
+  return quantize_common<false>(x, dtype, n, residual, rounding, seed, step, tscale_mode,
+                                tensor_scale, amax_ws, packed, scales, BlockedMap{0, 0, 0},
+                                as_stream(stream));
+}
+
+fp4_status nvfp4_quantize_blocked(const void* x, int dtype, int64_t rows, int64_t k,
+                                  float* residual, int rounding, uint64_t seed, uint64_t step,
+                                  int tscale_mode, float* tensor_scale, float* amax_ws,
+                                  uint8_t* packed, uint8_t* blocked_scales, void* stream) {
+  if (!dtype_ok(dtype)) return FP4_ERR_DTYPE;
+  if (rounding != FP4_RTN && rounding != FP4_SR) return FP4_ERR_ARG;
+  if (!mode_ok(tscale_mode)) return FP4_ERR_ARG;
+  if (rows < 0 || k < 0 || k % 16 != 0) return FP4_ERR_SHAPE;
+  if (k > 0 && rows > (INT64_C(1) << 44) / k) return FP4_ERR_SHAPE;
+  const int64_t n = rows * k;
+  if (!tensor_scale) return FP4_ERR_NULL;
+  if (tscale_mode != FP4_TSCALE_GIVEN && !amax_ws) return FP4_ERR_NULL;
+  if (n > 0 && (!x || !packed || !blocked_scales)) return FP4_ERR_NULL;
+  if (!aligned(x, 32) || !aligned(residual, 32) || !aligned(packed, 16) ||
+      !aligned(tensor_scale, 4) || !aligned(amax_ws, 4))
+    return FP4_ERR_ALIGN;
+  const BlockedMap bm{rows, k / 16, (k / 16 + 3) / 4};
+  return quantize_common<true>(x, dtype, n, residual, rounding, seed, step, tscale_mode,
+                               tensor_scale, amax_ws, packed, blocked_scales, bm,
+                               as_stream(stream));
 }
 
 fp4_status nvfp4_dequantize(const uint8_t* packed, const uint8_t* scales, const float* tensor_scale,
@@ -540,9 +612,11 @@ extern "C" fp4_status nvfp4_quantize_noalloc(const void* x, int dtype, int64_t n
   st = launch_amax(x, dtype, n, residual, amax_ws, s);
   if (st != FP4_OK) return st;
   const int64_t nb = n / 16;
+  const BlockedMap linear{0, 0, 0};
   if (dtype == FP4_BF16)
-    return launch_quantize_t<true>(x, nb, residual, rounding, seed, step, FP4_TSCALE_COMPUTE,
-                                   tensor_scale, amax_ws, packed, scales, s);
-  return launch_quantize_t<false>(x, nb, residual, rounding, seed, step, FP4_TSCALE_COMPUTE,
-                                  tensor_scale, amax_ws, packed, scales, s);
+    return launch_quantize_t<true, false>(x, nb, residual, rounding, seed, step,
+                                          FP4_TSCALE_COMPUTE, tensor_scale, amax_ws, packed,
+                                          scales, linear, s);
+  return launch_quantize_t<false, false>(x, nb, residual, rounding, seed, step, FP4_TSCALE_COMPUTE,
+                                         tensor_scale, amax_ws, packed, scales, linear, s);
 }

@@ -154,6 +154,47 @@ fp4_status nvfp4_quantize_noalloc(const void* x, int dtype, int64_t n, float* re
                                   float* tensor_scale, uint8_t* packed, uint8_t* scales,
                                   void* stream);
 
+/* ------------------------------------------------- blocked scale layout
+ * [fp4-train] "Scope": the NVFP4 tensor-core matmul hands its e4m3 block
+ * scales to the hardware after swizzling them into the layout
+ * torch._scaled_mm consumes.  That layout ("blocked"): the [rows, cols]
+ * one-byte scale matrix of a [rows, K] operand (cols = K/16 for NVFP4, K/32
+ * for MXFP4) is zero-padded to [128 * ceil(rows/128), 4 * ceil(cols/4)], cut
+ * into tiles of 128 rows x 4 columns stored in row-major tile order, 512
+ * bytes each, and scale (r, c) of a tile sits at byte
+ * 16 * (r % 32) + 4 * (r / 32) + c of its tile.
+ */
+
+/* Bytes of the blocked form of a [rows, cols] scale matrix, or -1 when
+ * rows or cols is negative, either is >= 2^40, or the matrix has more than
+ * 2^44 padded scales.  Host only; no device work. */
+int64_t fp4_blocked_scales_size(int64_t rows, int64_t cols);
+
+/* scales [rows, cols] row-major bytes (any alignment) -> blocked
+ * [fp4_blocked_scales_size(rows, cols)] bytes, 16-byte aligned; every byte
+ * of blocked is written, padding with 0.  Nothing to do for an empty
+ * matrix.  The bytes are moved, not interpreted. */
+fp4_status fp4_scales_to_blocked(const uint8_t* scales, int64_t rows, int64_t cols,
+                                 uint8_t* blocked, void* stream);
+
+/* The inverse: blocked (16-byte aligned) -> scales [rows, cols]; padding
+ * bytes are ignored. */
+fp4_status fp4_scales_from_blocked(const uint8_t* blocked, int64_t rows, int64_t cols,
+                                   uint8_t* scales, void* stream);
+
+/* nvfp4_quantize of a [rows, k] row-major matrix (k % 16 == 0, rows * k <
+ * 2^44) whose block scales are written straight into the blocked layout of
+ * the [rows, k/16] scale matrix, padding included (no second pass).  Codes,
+ * tensor scale, residual update and stochastic-rounding draws are those of
+ * nvfp4_quantize on the flat n = rows * k elements, and blocked_scales equals
+ * fp4_scales_to_blocked of nvfp4_quantize's scales.
+ *   blocked_scales  [fp4_blocked_scales_size(rows, k/16)] bytes out, any
+ *                   alignment; all other arguments as nvfp4_quantize. */
+fp4_status nvfp4_quantize_blocked(const void* x, int dtype, int64_t rows, int64_t k,
+                                  float* residual, int rounding, uint64_t seed, uint64_t step,
+                                  int tscale_mode, float* tensor_scale, float* amax_ws,
+                                  uint8_t* packed, uint8_t* blocked_scales, void* stream);
+
 /* ------------------------------------------------------- NVFP4, batched
  * The same NVFP4 operations on a list of independent tensors in one launch
  * per pass (a whole model's weight matrices, say), each tensor with its own

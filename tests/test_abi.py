@@ -32,7 +32,9 @@ def test_header_declares_the_boundary():
     for want in ["nvfp4_amax", "nvfp4_quantize", "nvfp4_dequantize", "nvfp4_qdq_amax",
                  "nvfp4_qdq", "mxfp4_quantize", "fp4_to_fp8_row", "fp4_to_fp8_col",
                  "fp4_seg_scale_offsets", "fp4quant_encode", "fp4quant_decode",
-                 "fp4_status_string", "fp4_abi_version", "fp4_kernel_launches"]:
+                 "fp4_status_string", "fp4_abi_version", "fp4_kernel_launches",
+                 "fp4_blocked_scales_size", "fp4_scales_to_blocked", "fp4_scales_from_blocked",
+                 "nvfp4_quantize_blocked"]:
         assert want in names, want
 
 
@@ -175,3 +177,39 @@ def test_batch_plan_host_helper(L):
     assert L.nvfp4_quantize_batched(A, 2, 3, 1, 0, 0, 0, 0, None, None, None) == 1
     assert L.nvfp4_dequantize_batched(A, 2, 3, A + 2, 0, None) == 2
     assert L.nvfp4_dequantize_batched(A, 2, 3, None, 3, None) == 4
+
+
+def test_blocked_scale_layout_host_checks(L):
+    size = L.fp4_blocked_scales_size
+    assert size(0, 0) == 0
+    assert size(1, 1) == 512
+    assert size(129, 5) == 256 * 8
+    assert size(4096, 256) == 4096 * 256
+    assert size(-1, 4) == -1 and size(4, -1) == -1
+    assert size(1 << 40, 1) == -1
+    assert size(1 << 30, 1 << 20) == -1                        # > 2^44 padded scales
+    to, frm = L.fp4_scales_to_blocked, L.fp4_scales_from_blocked
+    assert to(A, -1, 4, A, None) == 3
+    assert to(None, 4, 4, A, None) == 1
+    assert to(A, 4, 4, A + 4, None) == 2                         # blocked needs 16 B
+    assert frm(A, 4, 4, None, None) == 1
+    assert frm(MIS, 4, 4, A, None) == 2
+    assert to(None, 0, 7, None, None) == 0                       # empty: nothing to do
+    qb = L.nvfp4_quantize_blocked
+    ok = dict(x=A, dtype=1, rows=4, k=64, res=None, rnd=0, seed=0, step=0, mode=0, ts=A, ws=A,
+              pk=A, sc=A)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return qb(a["x"], a["dtype"], a["rows"], a["k"], a["res"], a["rnd"], a["seed"], a["step"],
+                  a["mode"], a["ts"], a["ws"], a["pk"], a["sc"], None)
+
+    assert call(k=24) == 3            # k % 16
+    assert call(rows=-1) == 3
+    assert call(rows=1 << 30, k=1 << 16) == 3
+    assert call(dtype=3) == 4
+    assert call(rnd=9) == 5
+    assert call(sc=None) == 1
+    assert call(mode=2, ws=None) == 1
+    assert call(x=MIS) == 2
+    assert call(pk=A + 8) == 2
