@@ -99,38 +99,85 @@ struct QuantPipe {
 };
 
 // CTAs of kThreads per SM that the register allocation must allow: 4 is 64
-// registers a thread, 3 is 80, 2 is 128.
-template <bool kBF16, bool kSR, bool kRes>
+// registers a thread, 3 is 80, 2 is 128.  The blocked-scale cursor needs a
+// few more registers than 64.
+template <bool kBF16, bool kSR, bool kRes, bool kBlk>
 constexpr int quantize_min_ctas() {
-  return kRes ? 2 : ((kSR || !kBF16) ? 3 : 4);
+  return kRes ? 2 : ((kSR || !kBF16 || kBlk) ? 3 : 4);
 }
 
-// Geometry of a [rows, 16 * cols] matrix whose block scales go out in the
-// blocked layout (common.cuh): cols block scales per row, col_tiles =
-// ceil(cols / 4).  Unused (all zero) for the linear layout.
+// Where the block scales of a [rows, 16 * cols] matrix go in the blocked
+// layout (common.cuh).  A thread keeps its block's place as the byte offset
+// of its row tile, the row inside the tile and the scale column, and steps
+// it by the grid stride with adds and compares only: no division and no
+// 64-bit multiply per block.  cols < 2^24 keeps every offset inside a row
+// tile below 2^31.
 struct BlockedMap {
-  int64_t rows;
-  int64_t cols;
-  int64_t col_tiles;
+  int64_t rows, cols, col_tiles;
 };
+
+struct BlockedCursor {
+  int64_t base;  // (row / 128) * col_tiles * 512
+  uint32_t rr;   // row % 128
+  uint32_t c;    // scale column
+};
+
+struct BlockedStep {
+  int64_t base;            // (stride rows / 128) * col_tiles * 512
+  int64_t tile_row_bytes;  // col_tiles * 512
+  uint32_t rr, c, cols;    // stride rows % 128, stride columns, cols
+};
+
+__device__ __forceinline__ BlockedCursor blocked_cursor(int64_t b, const BlockedMap& bm) {
+  const int64_t row = b / bm.cols;
+  return BlockedCursor{(row >> 7) * bm.col_tiles * 512, (uint32_t)(row & 127),
+                       (uint32_t)(b - row * bm.cols)};
+}
+
+__device__ __forceinline__ BlockedStep blocked_step(int64_t stride, const BlockedMap& bm) {
+  const int64_t rows = stride / bm.cols;
+  return BlockedStep{(rows >> 7) * bm.col_tiles * 512, bm.col_tiles * 512,
+                     (uint32_t)(rows & 127), (uint32_t)(stride - rows * bm.cols),
+                     (uint32_t)bm.cols};
+}
+
+// Byte offset of the cursor's scale: its row tile, then inside the tile the
+// column tile, the row group (row / 32), the row within it and the column
+// within the 4-byte word, which occupy disjoint bits.
+__device__ __forceinline__ int64_t blocked_at(const BlockedCursor& q) {
+  return q.base + (int64_t)(((q.c & ~3u) << 7) | ((q.rr & 31u) << 4) | ((q.rr >> 5) << 2) |
+                            (q.c & 3u));
+}
+
+__device__ __forceinline__ void blocked_advance(BlockedCursor& q, const BlockedStep& st) {
+  q.c += st.c;
+  const bool wrap = q.c >= st.cols;
+  q.c = wrap ? q.c - st.cols : q.c;
+  q.rr += st.rr + (wrap ? 1u : 0u);
+  const bool tile = q.rr >= 128u;
+  q.rr = tile ? q.rr - 128u : q.rr;
+  q.base += st.base + (tile ? st.tile_row_bytes : 0);
+}
 
 // A thread quantizes one block per grid-stride step; the loads of the next
 // kD blocks are in flight meanwhile.  The ring of kD + 1 buffers is walked
 // by a fully unrolled inner loop, so every buffer index is a constant and no
 // registers are copied.  bf16 round-to-nearest without error feedback takes
-// quantize_block_bf16_rtn, everything else quantize_block.
+// quantize_block_bf16_rtn with its warp's table of E2M1 constants,
+// everything else quantize_block.
 //
 // kBlk writes block b's scale at its place in the blocked layout instead of
-// at byte b: the thread keeps the (row, column) of its block and steps it by
-// the grid stride, so no division is left in the loop; the padding bytes
-// are zeroed first.
+// at byte b (a BlockedCursor per thread); the padding bytes are zeroed
+// first.
 template <bool kBF16, bool kSR, bool kRes, bool kBlk>
-__global__ void __launch_bounds__(kThreads, quantize_min_ctas<kBF16, kSR, kRes>())
+__global__ void __launch_bounds__(kThreads, quantize_min_ctas<kBF16, kSR, kRes, kBlk>())
     quantize_kernel(const void* __restrict__ x, float* __restrict__ residual, int64_t nblocks,
                     uint64_t seed, uint64_t step, int tscale_mode, float* __restrict__ tensor_scale,
                     const float* __restrict__ amax_ws, uint8_t* __restrict__ packed,
                     uint8_t* __restrict__ scales, BlockedMap bm) {
   constexpr int kD = QuantPipe<kBF16, kRes>::kDepth;
+  constexpr bool kFast = kBF16 && !kSR && !kRes;
+  __shared__ EffEntry eff_tabs[kFast ? (kThreads / 32) * kEffEntries : 1];
   float s_t;
   if (tscale_mode == FP4_TSCALE_GIVEN) {
     s_t = sanitize_scale(*tensor_scale);
@@ -139,18 +186,19 @@ __global__ void __launch_bounds__(kThreads, quantize_min_ctas<kBF16, kSR, kRes>(
     if (blockIdx.x == 0 && threadIdx.x == 0) *tensor_scale = s_t;
   }
   const ScaleDiv sd = make_scale_div(s_t);
+  EffEntry* const tab = eff_tabs + (kFast ? (threadIdx.x >> 5) * kEffEntries : 0);
+  if (kFast) build_eff_table(tab, s_t);
   const uint32_t key0 = (uint32_t)seed, key1 = (uint32_t)(seed >> 32);
   const uint32_t st0 = (uint32_t)step, st1 = (uint32_t)(step >> 32);
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   int64_t b = (int64_t)blockIdx.x * kThreads + threadIdx.x;
-  int64_t br = 0, bc = 0, step_r = 0, step_c = 0;
+  BlockedCursor cur{0, 0u, 0u};
+  BlockedStep cstep{0, 0, 0u, 0u, 1u};
   if (kBlk) {
     blocked_zero_padding(scales, bm.rows, bm.cols, bm.col_tiles, b, stride);
     if (bm.cols > 0) {
-      br = b / bm.cols;
-      bc = b - br * bm.cols;
-      step_r = stride / bm.cols;
-      step_c = stride - step_r * bm.cols;
+      cur = blocked_cursor(b, bm);
+      cstep = blocked_step(stride, bm);
     }
   }
 
@@ -162,32 +210,29 @@ __global__ void __launch_bounds__(kThreads, quantize_min_ctas<kBF16, kSR, kRes>(
     for (int s = 0; s <= kD; ++s) {
       if (b >= nblocks) return;
       issue_block<kBF16, kRes>(x, residual, b + kD * stride, nblocks, buf[(s + kD) % (kD + 1)]);
-      float v[16], r[16], q[16];
-      unpack_block<kBF16, kRes>(buf[s], v, r);
       uint2 out;
       uint32_t sb;
-      if (kBF16 && !kSR && !kRes)
-        sb = quantize_block_bf16_rtn(v, s_t, sd, out);
-      else
+      float r[16], q[16];
+      if (kFast) {
+        sb = quantize_block_bf16_rtn(buf[s].x[0], sd, tab, out);
+      } else {
+        float v[16];
+        unpack_block<kBF16, kRes>(buf[s], v, r);
         sb = quantize_block<kSR, kRes>(v, s_t, sd, (uint64_t)(16 * b), key0, key1, st0, st1, out,
                                        q);
+        if (kRes) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) r[i] = __fsub_rn(v[i], q[i]);
+        }
+      }
       *reinterpret_cast<uint2*>(packed + 8 * b) = out;
       if (kBlk) {
-        scales[blocked_offset(br, bc, bm.col_tiles)] = (uint8_t)sb;
-        bc += step_c;
-        br += step_r;
-        if (bc >= bm.cols) {
-          bc -= bm.cols;
-          ++br;
-        }
+        scales[blocked_at(cur)] = (uint8_t)sb;
+        blocked_advance(cur, cstep);
       } else {
         scales[b] = (uint8_t)sb;
       }
-      if (kRes) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) r[i] = __fsub_rn(v[i], q[i]);
-        store_f32x16(residual + 16 * b, r);
-      }
+      if (kRes) store_f32x16(residual + 16 * b, r);
       b += stride;
     }
   }
@@ -468,7 +513,7 @@ fp4_status nvfp4_quantize_blocked(const void* x, int dtype, int64_t rows, int64_
   if (!dtype_ok(dtype)) return FP4_ERR_DTYPE;
   if (rounding != FP4_RTN && rounding != FP4_SR) return FP4_ERR_ARG;
   if (!mode_ok(tscale_mode)) return FP4_ERR_ARG;
-  if (rows < 0 || k < 0 || k % 16 != 0) return FP4_ERR_SHAPE;
+  if (rows < 0 || k < 0 || k % 16 != 0 || k / 16 >= (INT64_C(1) << 24)) return FP4_ERR_SHAPE;
   if (k > 0 && rows > (INT64_C(1) << 44) / k) return FP4_ERR_SHAPE;
   const int64_t n = rows * k;
   if (!tensor_scale) return FP4_ERR_NULL;

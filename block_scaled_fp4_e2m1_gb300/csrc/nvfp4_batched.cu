@@ -158,12 +158,17 @@ __global__ void __launch_bounds__(kBThreads)
 
 // Inside a tensor a lane quantizes blocks s0 + lane, + 32, ... with the
 // loads of its next kD blocks in flight (the single-tensor kernel's ring).
+// bf16 round-to-nearest refills the warp's table of E2M1 constants for each
+// tensor it enters.
 template <bool kBF16, bool kSR>
 __global__ void __launch_bounds__(kBThreads, kSR ? 1 : (kBF16 ? 3 : 2))
     quantize_batched_kernel(const fp4_tensor_desc* __restrict__ desc, int count,
                             int64_t total_chunks, uint64_t seed, uint64_t step, int tscale_mode,
                             float* __restrict__ tensor_scale, const float* __restrict__ amax) {
   constexpr int kD = kBF16 ? 2 : 1;  // blocks in flight ahead of the one being quantized
+  constexpr bool kFast = kBF16 && !kSR;
+  __shared__ EffEntry eff_tabs[kFast ? (kBThreads / 32) * kEffEntries : 1];
+  EffEntry* const tab = eff_tabs + (kFast ? (threadIdx.x >> 5) * kEffEntries : 0);
   const int lane = threadIdx.x & 31;
   const uint32_t key0 = (uint32_t)seed, key1 = (uint32_t)(seed >> 32);
   const uint32_t st0 = (uint32_t)step, st1 = (uint32_t)(step >> 32);
@@ -172,6 +177,7 @@ __global__ void __launch_bounds__(kBThreads, kSR ? 1 : (kBF16 ? 3 : 2))
                                                       : tensor_scale_from_amax(amax[t]);
     if (tscale_mode != FP4_TSCALE_GIVEN && s0 == 0 && lane == 0) tensor_scale[t] = s_t;
     const ScaleDiv sd = make_scale_div(s_t);
+    if (kFast) build_eff_table(tab, s_t);
     const void* x = ldg_ptr(&desc[t].x);
     uint8_t* const packed = ldg_ptr(&desc[t].packed);
     uint8_t* const scales = ldg_ptr(&desc[t].scales);
@@ -184,15 +190,16 @@ __global__ void __launch_bounds__(kBThreads, kSR ? 1 : (kBF16 ? 3 : 2))
       for (int r = 0; r <= kD; ++r) {
         if (b >= s1) goto segment_done;
         issue_block<kBF16, false>(x, nullptr, b + 32 * kD, s1, buf[(r + kD) % (kD + 1)]);
-        float v[16], rr[16], q[16];
-        unpack_block<kBF16, false>(buf[r], v, rr);
         uint2 out;
         uint32_t sb;
-        if (kBF16 && !kSR)
-          sb = quantize_block_bf16_rtn(v, s_t, sd, out);
-        else
+        if (kFast) {
+          sb = quantize_block_bf16_rtn(buf[r].x[0], sd, tab, out);
+        } else {
+          float v[16], rr[16], q[16];
+          unpack_block<kBF16, false>(buf[r], v, rr);
           sb = quantize_block<kSR, false>(v, s_t, sd, (uint64_t)(16 * b), key0, key1, st0, st1,
                                           out, q);
+        }
         *reinterpret_cast<uint2*>(packed + 8 * b) = out;
         scales[b] = (uint8_t)sb;
         b += 32;

@@ -331,17 +331,61 @@ __device__ __forceinline__ uint32_t quantize_block(const float v[16], float s_t,
   return sb;
 }
 
-// Round-to-nearest quantization of one block of bf16 values (v[16], no
-// residual): the result of quantize_block<false, false>, faster.  Bracket
-// disagreements under a short divisor are exact ties and take the even code
-// branch-free (short_divisor); the rest (near ties under a full-precision
-// decoded scale, a block or two per hundred, or a scale outside the
-// certified range) are settled one element at a time.
-__device__ __forceinline__ uint32_t quantize_block_bf16_rtn(const float v[16], float s_t,
-                                                            const ScaleDiv& sd, uint2& out) {
-  float bmax = 0.0f;
+// Per-tensor constants of the E2M1 step for every e4m3 block-scale byte sb:
+// the bracket multipliers of the decoded scale eff = RN(e4m3(sb) * s_t),
+// eff itself, and flags: bit 0 the bracket is certified for eff, bit 1 eff
+// is short (short_divisor).  One table of kEffEntries serves a warp for a
+// whole tensor, so a block's E2M1 constants cost one shared-memory load
+// instead of a decode, a multiply and a correctly rounded reciprocal.
+struct alignas(16) EffEntry {
+  float il, ih, eff;
+  uint32_t flags;
+};
+constexpr int kEffEntries = 128;  // every byte with the sign bit clear
+
+// The calling warp fills tab[0 .. kEffEntries) for tensor scale s_t.  The
+// leading __syncwarp lets the table be refilled for another tensor after
+// the warp's last reads of the old one.
+__device__ __forceinline__ void build_eff_table(EffEntry* tab, float s_t) {
+  const uint32_t lane = threadIdx.x & 31u;
+  __syncwarp();
 #pragma unroll
-  for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(v[i]));
+  for (int k = 0; k < kEffEntries / 32; ++k) {
+    const uint32_t sb = lane + 32u * k;
+    const float eff = __fmul_rn(e4m3_value(sb), s_t);
+    const Bracket br = make_bracket(eff);
+    EffEntry e;
+    e.il = br.il;
+    e.ih = br.ih;
+    e.eff = eff;
+    e.flags = (bracket_certified(eff) ? 1u : 0u) | (short_divisor(eff) ? 2u : 0u);
+    tab[sb] = e;
+  }
+  __syncwarp();
+}
+
+// max(|a|, |b|) of each bf16 half; the sign bits of the result are junk.
+__device__ __forceinline__ uint32_t max_abs_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Round-to-nearest quantization of one block of 16 bf16 values (raw: the
+// block's 8 words, element 2i in the low half of word i; no residual): the
+// result of quantize_block<false, false>, faster.  The block maximum is
+// taken on the bf16 pairs, the 32 bracket products are packed pairs, and
+// the E2M1 constants come from the warp's table.  Bracket disagreements
+// under a short divisor are exact ties and take the even code branch-free
+// (short_divisor); the rest (near ties under a full-precision decoded scale,
+// about one element in a thousand, or a scale outside the certified range)
+// are settled one element at a time from the bracket codes already at hand.
+__device__ __forceinline__ uint32_t quantize_block_bf16_rtn(const U32x8& raw, const ScaleDiv& sd,
+                                                            const EffEntry* tab, uint2& out) {
+  const uint32_t m = max_abs_bf16x2(
+      max_abs_bf16x2(max_abs_bf16x2(raw.w[0], raw.w[1]), max_abs_bf16x2(raw.w[2], raw.w[3])),
+      max_abs_bf16x2(max_abs_bf16x2(raw.w[4], raw.w[5]), max_abs_bf16x2(raw.w[6], raw.w[7])));
+  const float bmax = fmaxf(bf16_lo(m & 0x7FFFu), bf16_hi(m & 0x7FFF0000u));
   uint32_t sb;
   if (sd.short6) {
     const uint32_t lh = cvt_e4m3x2(__fmul_rn(bmax, sd.r_lo), __fmul_rn(bmax, sd.r_hi));
@@ -350,22 +394,26 @@ __device__ __forceinline__ uint32_t quantize_block_bf16_rtn(const float v[16], f
   } else {
     sb = block_scale_code(bmax, sd);
   }
-  const float eff = __fmul_rn(e4m3_value(sb), s_t);
-  const Bracket k = make_bracket(eff);
+  const EffEntry e = tab[sb & (kEffEntries - 1)];
+  const F2 kl{e.il, e.il}, kh{e.ih, e.ih};
+  F2 pl[8], ph[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const F2 x{bf16_lo(raw.w[i]), bf16_hi(raw.w[i])};
+    pl[i] = mul2(x, kl);
+    ph[i] = mul2(x, kh);
+  }
   uint32_t lo[2], hi[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    const float* x = v + 8 * h;
-    lo[h] = cvt_e2m1x8(__fmul_rn(x[0], k.il), __fmul_rn(x[1], k.il), __fmul_rn(x[2], k.il),
-                       __fmul_rn(x[3], k.il), __fmul_rn(x[4], k.il), __fmul_rn(x[5], k.il),
-                       __fmul_rn(x[6], k.il), __fmul_rn(x[7], k.il));
-    hi[h] = cvt_e2m1x8(__fmul_rn(x[0], k.ih), __fmul_rn(x[1], k.ih), __fmul_rn(x[2], k.ih),
-                       __fmul_rn(x[3], k.ih), __fmul_rn(x[4], k.ih), __fmul_rn(x[5], k.ih),
-                       __fmul_rn(x[6], k.ih), __fmul_rn(x[7], k.ih));
+    const F2* a = pl + 4 * h;
+    const F2* b = ph + 4 * h;
+    lo[h] = cvt_e2m1x8(a[0].x, a[0].y, a[1].x, a[1].y, a[2].x, a[2].y, a[3].x, a[3].y);
+    hi[h] = cvt_e2m1x8(b[0].x, b[0].y, b[1].x, b[1].y, b[2].x, b[2].y, b[3].x, b[3].y);
   }
-  const bool cert = bracket_certified(eff);
+  const bool cert = (e.flags & 1u) != 0u;
   uint32_t w[2], p[2];
-  if (cert && short_divisor(eff)) {
+  if (e.flags == 3u) {
     // ties: a differing nibble is lo's magnitude + 1, and the even code is
     // lo + 1 exactly when lo's magnitude is odd (it is at most 5)
 #pragma unroll
@@ -382,21 +430,29 @@ __device__ __forceinline__ uint32_t quantize_block_bf16_rtn(const float v[16], f
   }
   while ((p[0] | p[1]) != 0u) {
     const bool first = p[0] != 0u;
-    const uint32_t ph = first ? p[0] : p[1];
-    const int i = (__ffs(ph) - 1) >> 2;
-    const float* x = first ? v : v + 8;
-    float xi = x[0];
-#pragma unroll
-    for (int j = 1; j < 8; ++j) xi = (i == j) ? x[j] : xi;
-    uint32_t stored, code;
-    rtn_element(xi, eff, stored, code);
-    const uint32_t m = 0xFu << (4 * i);
+    const uint32_t pend = first ? p[0] : p[1];
+    const int sh = (__ffs(pend) - 1) & ~3;  // the nibble of the element
+    const int i = sh >> 2;                  // element i of the half
+    // word (first ? 0 : 4) + i / 2 of the block, by a tree of selects
+    const bool b0 = (i & 2) != 0, b1 = (i & 4) != 0;
+    const uint32_t q0 = b0 ? raw.w[1] : raw.w[0], q1 = b0 ? raw.w[3] : raw.w[2];
+    const uint32_t q2 = b0 ? raw.w[5] : raw.w[4], q3 = b0 ? raw.w[7] : raw.w[6];
+    const uint32_t h0 = b1 ? q1 : q0, h1 = b1 ? q3 : q2;
+    const uint32_t word = first ? h0 : h1;
+    const float xi = (i & 1) ? bf16_hi(word) : bf16_lo(word);
+    uint32_t code;
+    if (cert)
+      code = settle_e2m1(xi, e.eff, ((first ? lo[0] : lo[1]) >> sh) & 0xFu,
+                         ((first ? hi[0] : hi[1]) >> sh) & 0xFu);
+    else
+      code = exact_e2m1_quotient(xi, e.eff);
+    const uint32_t mk = 0xFu << sh;
     if (first) {
-      w[0] = (w[0] & ~m) | (code << (4 * i));
-      p[0] &= ~m;
+      w[0] = (w[0] & ~mk) | (code << sh);
+      p[0] &= ~mk;
     } else {
-      w[1] = (w[1] & ~m) | (code << (4 * i));
-      p[1] &= ~m;
+      w[1] = (w[1] & ~mk) | (code << sh);
+      p[1] &= ~mk;
     }
   }
   out = make_uint2(w[0], w[1]);

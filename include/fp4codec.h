@@ -182,8 +182,8 @@ fp4_status fp4_scales_to_blocked(const uint8_t* scales, int64_t rows, int64_t co
 fp4_status fp4_scales_from_blocked(const uint8_t* blocked, int64_t rows, int64_t cols,
                                    uint8_t* scales, void* stream);
 
-/* nvfp4_quantize of a [rows, k] row-major matrix (k % 16 == 0, rows * k <
- * 2^44) whose block scales are written straight into the blocked layout of
+/* nvfp4_quantize of a [rows, k] row-major matrix (k % 16 == 0, k < 2^28,
+ * rows * k < 2^44) whose block scales are written straight into the blocked layout of
  * the [rows, k/16] scale matrix, padding included (no second pass).  Codes,
  * tensor scale, residual update and stochastic-rounding draws are those of
  * nvfp4_quantize on the flat n = rows * k elements, and blocked_scales equals
