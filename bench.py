@@ -141,10 +141,12 @@ def build_suite(device, rank=0, small=False, host_inputs=False):
     x2 = W.fp4quant_acts(seed=seed, tokens=T2, hidden=H2, device=device)
     st["inputs"] += [x2]
     n2 = x2.numel()
+    fq_out = []
     for G in (64, 128, 256):
         pk, q1, q2 = zeros((T2, H2 // 2), u8), zeros((T2, H2 // G), f32), zeros((T2, H2 // G), f32)
         yy = zeros((T2, H2), bf16)
         st["outputs"] += [pk, q1, q2, yy]
+        fq_out += [pk, q1, q2, yy]
         b = n2 * (2 + 0.5 + 8 / G)
         groups.append(Group(f"fp4quant_encode_g{G}", "fp4quant_acts", b,
                             [lambda G=G, pk=pk, q1=q1, q2=q2: m.fp4quant_encode(x2, G, pk, q1, q2)]))
@@ -226,6 +228,32 @@ def build_suite(device, rank=0, small=False, host_inputs=False):
                         [lambda: m.nvfp4_dequantize_batched(dbatch, ts5, bf16)]))
     st["elements"] = {"nvfp4_roundtrip": n1, "fp4quant_acts": n2, "nvfp4_train": n3,
                       "moe_tokens": n4, "moe_dispatched": nd, "qwen3_8b_weights": n5}
+
+    # The same work cut into stages for the end-to-end pipeline: each stage
+    # has its inputs, its calls and its outputs.  The weight set goes in
+    # chunks of whole layers (each chunk one batched launch per pass), so
+    # that one chunk's upload, another's kernels and a third's download can
+    # overlap.
+    stages = [([x1], [g.calls[0] for g in groups[0:3]], [p1, s1, y1, t1])]
+    stages.append(([x2], [g.calls[0] for g in groups[3:9]], fq_out))
+    stages.append(([w3, g3, r3], [qdq_amax, qdq], [w3, r3, p3, s3, t3]))
+    stages.append(([x4, dp, ds], [g.calls[0] for g in groups[11:14]], [mp, ms, f8, f8s, ft, fts]))
+    per_layer = 7
+    layers = k5 // per_layer
+    chunk_layers = max(1, min(4, layers))
+    for l0 in range(0, layers, chunk_layers):
+        i0, i1 = l0 * per_layer, min(k5, (l0 + chunk_layers) * per_layer)
+        qb = m.Batch(xs=mats[i0:i1], packed=pk5[i0:i1], scales=sc5[i0:i1])
+        db = m.Batch(packed=pk5[i0:i1], scales=sc5[i0:i1], ys=out5[i0:i1],
+                     sizes=[w.numel() for w in mats[i0:i1]])
+        am, ts = amax5[i0:i1], ts5[i0:i1]
+        stages.append((mats[i0:i1],
+                       [lambda qb=qb, am=am: m.nvfp4_amax_batched(qb, bf16, amax=am),
+                        lambda qb=qb, am=am, ts=ts: m.nvfp4_quantize_batched(
+                            qb, bf16, tscale="from_amax", tensor_scale=ts, amax=am),
+                        lambda db=db, ts=ts: m.nvfp4_dequantize_batched(db, ts, bf16)],
+                       pk5[i0:i1] + sc5[i0:i1] + out5[i0:i1] + [ts]))
+    st["stages"] = stages
     return groups, st
 
 
@@ -453,35 +481,62 @@ def host_mem_available():
 def e2e_measure(groups, st, steps, warmup, device):
     """Whole step through the public API with host buffers: every step copies
     all inputs host -> device from pinned memory, runs the kernels and copies
-    all outputs back."""
+    all outputs back.  The step is a three-stream pipeline over its stages
+    (build_suite): uploads on one copy stream, the kernels on the compute
+    stream, downloads on a second copy stream.  Events order each stage's
+    upload -> kernels -> download, so the two copy directions and the
+    kernels of different stages overlap.  The timed region ends when every
+    download has landed in host memory."""
     import torch
-    ins, outs = st["inputs"], st["outputs"]
+    stages = st["stages"]
     seen = set()
-    ins_u = [t for t in ins if not (t.data_ptr() in seen or seen.add(t.data_ptr()))]
-    seen_o = set()
-    outs_u = [t for t in outs if not (t.data_ptr() in seen_o or seen_o.add(t.data_ptr()))]
-    h2d = sum(t.numel() * t.element_size() for t in ins_u)
-    d2h = sum(t.numel() * t.element_size() for t in outs_u)
-    need = h2d + d2h
-    if host_mem_available() < 1.5 * need:
+    uniq = lambda ts: [t for t in ts if not (t.data_ptr() in seen or seen.add(t.data_ptr()))]
+    ins = [uniq(s_in) for s_in, _, _ in stages]
+    seen = set()
+    outs = [uniq(s_out) for _, _, s_out in stages]
+    h2d = sum(t.numel() * t.element_size() for ts in ins for t in ts)
+    d2h = sum(t.numel() * t.element_size() for ts in outs for t in ts)
+    if host_mem_available() < 1.5 * (h2d + d2h):
         return None, h2d, d2h
-    h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ins_u]
-    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs_u]
-    for h, t in zip(h_in, ins_u):
-        h.copy_(t)
+    h_in = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ts] for ts in ins]
+    h_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ts] for ts in outs]
+    for hs, ts in zip(h_in, ins):
+        for h, t in zip(hs, ts):
+            h.copy_(t)
+    up, down = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    comp = torch.cuda.current_stream(device)
     torch.cuda.synchronize()
     times = []
     for i in range(warmup + steps):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for h, t in zip(h_in, ins_u):
-            t.copy_(h, non_blocking=True)
-        run_step(groups, None)
-        for h, t in zip(h_out, outs_u):
-            h.copy_(t, non_blocking=True)
+        ready = []
+        with torch.cuda.stream(up):
+            for hs, ts in zip(h_in, ins):
+                for h, t in zip(hs, ts):
+                    t.copy_(h, non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(up)
+                ready.append(ev)
+        for k, (_, calls, _) in enumerate(stages):
+            comp.wait_event(ready[k])
+            for c in calls:
+                c()
+            done = torch.cuda.Event()
+            done.record(comp)
+            down.wait_event(done)
+            with torch.cuda.stream(down):
+                for h, t in zip(h_out[k], outs[k]):
+                    h.copy_(t, non_blocking=True)
         torch.cuda.synchronize()
         if i >= warmup:
             times.append(time.perf_counter() - t0)
+    # the downloads waited for their kernels: the host copies of the small
+    # stages and of the last chunk's tensor scales equal the device tensors
+    for k in list(range(min(4, len(stages)))) + [len(stages) - 1]:
+        for h, t in zip(h_out[k], outs[k]):
+            if t.numel() * t.element_size() <= (256 << 20) and not torch.equal(h.to(device), t):
+                raise RuntimeError(f"e2e stage {k}: a downloaded output differs from the device")
     del h_in, h_out
     return statistics.median(times), h2d, d2h
 

@@ -397,3 +397,57 @@ def test_rtn_qdq_on_structural_ties():
     assert_bits_equal(u8(packed), wp, "packed")
     assert_bits_equal(u8(scales), ws, "scales")
     assert_bits_equal(bf16_bits(w), wb, "W")
+
+
+def _nan_aware_equal(got_bits, want_f32, what):
+    """bf16 bits against the oracle's fp32 values rounded to bf16: equal bit
+    for bit, except that a NaN only has to be a NaN."""
+    want = ora.bf16_rn(want_f32)
+    got_nan = (got_bits & 0x7FFF) > 0x7F80
+    want_nan = np.isnan(want_f32)
+    assert np.array_equal(got_nan, want_nan), what
+    assert_bits_equal(got_bits[~want_nan], want[~want_nan], what)
+
+
+@pytest.mark.parametrize("s_t", [1.0, 0.000447591, 3.0e-41, 1.0e36])
+def test_dequantize_every_code_and_scale_byte(s_t):
+    """All 16 codes under all 256 scale bytes: the sign-set bytes (a negative
+    decoded scale), 0x00 and 0x80 (zero), 0x7F and 0xFF (NaN).  A tensor
+    scale of 1e36 overflows 448 * s_t; one of 3e-41 is subnormal.  bf16 and
+    fp32 outputs, single-tensor and batched calls."""
+    m = fp4()
+    nb = 256 * 8 + 3  # every byte, eight times, and a ragged tail
+    sc = np.concatenate([np.tile(np.arange(256, dtype=np.uint8), 8),
+                         np.array([0x7E, 0x01, 0x80], np.uint8)])
+    rng = np.random.default_rng(11)
+    codes = rng.integers(0, 256, nb * 8, dtype=np.uint8)
+    codes[: 8 * 256] = np.tile(np.array([0x10, 0x32, 0x54, 0x76, 0x98, 0xBA, 0xDC, 0xFE],
+                                        np.uint8), 256)  # all 16 codes in every block
+    pk = torch.from_numpy(codes).to(dev())
+    sct = torch.from_numpy(sc).to(dev())
+    ts = torch.tensor([s_t], dtype=torch.float32, device=dev())
+    want = ora.nvfp4_dequantize(codes, sc, float(np.float32(s_t)), 16 * nb)
+    yb = m.nvfp4_dequantize(pk, sct, ts, (16 * nb,), torch.bfloat16)
+    _nan_aware_equal(bf16_bits(yb), want, "single bf16")
+    yf = m.nvfp4_dequantize(pk, sct, ts, (16 * nb,), torch.float32)
+    wn = np.isnan(want)
+    assert np.array_equal(np.isnan(to_f32_np(yf)), wn)
+    assert_bits_equal(to_f32_np(yf)[~wn], want[~wn], "single f32")
+    # batched: the same blocks as three tensors (odd block counts)
+    cuts = [0, 501, 1733, nb]
+    pks = [pk[8 * a:8 * b].clone() for a, b in zip(cuts, cuts[1:])]
+    scs = [sct[a:b].clone() for a, b in zip(cuts, cuts[1:])]
+    for od in (torch.bfloat16, torch.float32):
+        ys = [torch.full((16 * (b - a),), 7.0, dtype=od, device=dev())
+              for a, b in zip(cuts, cuts[1:])]
+        batch = m.Batch(packed=pks, scales=scs, ys=ys, sizes=[16 * (b - a) for a, b in
+                                                               zip(cuts, cuts[1:])])
+        m.nvfp4_dequantize_batched(batch, ts.repeat(3), od)
+        for i, (a, b) in enumerate(zip(cuts, cuts[1:])):
+            w = want[16 * a:16 * b]
+            if od == torch.bfloat16:
+                _nan_aware_equal(bf16_bits(ys[i]), w, f"batched bf16 {i}")
+            else:
+                g = to_f32_np(ys[i])
+                assert np.array_equal(np.isnan(g), np.isnan(w))
+                assert_bits_equal(g[~np.isnan(w)], w[~np.isnan(w)], f"batched f32 {i}")
