@@ -260,13 +260,20 @@ struct Philox4 {
   uint32_t x, y, z, w;
 };
 
+// The 64-bit product of two 32-bit words as one wide multiply.
+__device__ __forceinline__ void mul_wide(uint32_t a, uint32_t b, uint32_t& hi, uint32_t& lo) {
+  asm("{\n\t.reg .b64 p;\n\tmul.wide.u32 p, %2, %3;\n\tmov.b64 {%1, %0}, p;\n\t}"
+      : "=r"(hi), "=r"(lo)
+      : "r"(a), "r"(b));
+}
+
 __device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2,
                                                   uint32_t c3, uint32_t k0, uint32_t k1) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    const uint32_t m0 = 0xD2511F53u, m1 = 0xCD9E8D57u;
-    uint32_t hi0 = __umulhi(m0, c0), lo0 = m0 * c0;
-    uint32_t hi1 = __umulhi(m1, c2), lo1 = m1 * c2;
+    uint32_t hi0, lo0, hi1, lo1;
+    mul_wide(0xD2511F53u, c0, hi0, lo0);
+    mul_wide(0xCD9E8D57u, c2, hi1, lo1);
     uint32_t n0 = hi1 ^ c1 ^ k0;
     uint32_t n2 = hi0 ^ c3 ^ k1;
     c0 = n0;

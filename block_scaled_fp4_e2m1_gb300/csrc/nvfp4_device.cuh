@@ -153,6 +153,46 @@ __device__ __noinline__ uint32_t exact_e2m1_quotient(float x, float y) {
   return cvt_e2m1x2(__fdiv_rn(x, y), 0.0f) & 0xFu;
 }
 
+// The stochastic-rounding code of RN(x / y) by the rule of e2m1_sr, with an
+// exact division (the fallback of sr_code_certified).
+__device__ __noinline__ uint32_t exact_e2m1_sr_quotient(float x, float y, uint32_t rw) {
+  return e2m1_sr(y == 0.0f ? __fmul_rn(x, 0.0f) : __fdiv_rn(x, y), rw);
+}
+
+// Stochastic rounding without a division.  For m = |a| < 6 the code of
+// e2m1_sr is c + [u < frac], c the grid interval of m and frac its position
+// in it; with the position s = c + frac that is ceil(s - u) (u < 1), and
+// s(m) is piecewise linear: 2m below 2, m + 2 on [2, 4), m/2 + 4 on [4, 6),
+// and 7 from 6 on (code 7), which is min(2m, m + 2, m/2 + 4, 7).  Here a = RN(x / eff) is replaced by
+// q = RN(x * inv), inv = RN(1/eff) with eff in [2^-125, 2^125]:
+// |q - a| <= 1.5 * 2^-23 |x / eff|, so with slopes <= 2 the position moves
+// by at most 1.5 * 2^-21, and the two fp32 roundings of s and s - u add at
+// most 2^-21.  Hence when t = s(q) - u lies more than 2^-19 from every
+// integer, ceil(t) is the code of a; returns false otherwise (and for NaN),
+// which is about one element in 10^5.  Subnormal quotients have absolute
+// errors far below the margin.
+//
+// Two equal ways to form s: kMin takes the least of the pieces (s is
+// concave, and RN is monotone, so the least rounded piece is the rounded
+// least piece), the other selects the piece by comparing m.  Measured on
+// GB300, the least-of form is faster in the plain stochastic quantizer and
+// the selecting form in the error-feedback kernels.
+template <bool kMin>
+__device__ __forceinline__ bool sr_code_certified(float x, float inv, uint32_t rw,
+                                                  uint32_t& code) {
+  const float m = fabsf(__fmul_rn(x, inv));
+  const float s = kMin ? fminf(fminf(__fmul_rn(m, 2.0f), __fadd_rn(m, 2.0f)),
+                               fminf(__fmaf_rn(m, 0.5f, 4.0f), 7.0f))
+                       : (m < 2.0f   ? __fmul_rn(m, 2.0f)
+                          : m < 4.0f ? __fadd_rn(m, 2.0f)
+                          : m < 6.0f ? __fmaf_rn(m, 0.5f, 4.0f)
+                                     : 7.0f);
+  const float t = __fsub_rn(s, __fmul_rn((float)(rw >> 8), 0x1p-24f));
+  const float r = __fsub_rn(t, rintf(t));
+  code = ((__float_as_uint(x) >> 28) & 8u) | (uint32_t)(int)ceilf(t);
+  return fabsf(r) > 0x1p-19f && m == m;
+}
+
 // Settling a bracket that straddles a rounding midpoint, without dividing.
 // The two bracket codes are the neighbours lo < hi around the midpoint M of
 // their values, and |x| / y lies within 2^-20 of M.  Then
@@ -250,24 +290,55 @@ __device__ __forceinline__ uint32_t quantize_block(const float v[16], float s_t,
   const float eff = __fmul_rn(e4m3_value(sb), s_t);
   uint32_t w0, w1;
   if (kSR) {
-    float a[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) a[i] = (eff == 0.0f) ? __fmul_rn(v[i], 0.0f) : __fdiv_rn(v[i], eff);
-    uint32_t codes[16];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      uint64_t quad = (g0 >> 2) + (uint64_t)k;
-      Philox4 r = philox4x32_10((uint32_t)quad, (uint32_t)(quad >> 32), step0, step1, key0, key1);
-      codes[4 * k + 0] = e2m1_sr(a[4 * k + 0], r.x);
-      codes[4 * k + 1] = e2m1_sr(a[4 * k + 1], r.y);
-      codes[4 * k + 2] = e2m1_sr(a[4 * k + 2], r.z);
-      codes[4 * k + 3] = e2m1_sr(a[4 * k + 3], r.w);
-    }
+    // codes by sr_code_certified; the few uncertified elements (and every
+    // element when eff is outside the certified range) take the exact
+    // division afterwards, their random word drawn again
+    const bool fast = eff >= 0x1p-125f && eff <= 0x1p125f;
+    const float inv = fast ? __frcp_rn(eff) : 0.0f;
+    uint32_t pend = 0u;  // bit i: element i still to settle
     w0 = w1 = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) w0 |= codes[i] << (4 * i);
+    for (int k = 0; k < 4; ++k) {
+      const uint64_t quad = (g0 >> 2) + (uint64_t)k;
+      const Philox4 r = philox4x32_10((uint32_t)quad, (uint32_t)(quad >> 32), step0, step1, key0,
+                                      key1);
+      const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) w1 |= codes[8 + i] << (4 * i);
+      for (int j = 0; j < 4; ++j) {
+        const int i = 4 * k + j;
+        uint32_t code;
+        const bool ok = sr_code_certified<!kEF>(v[i], inv, rw[j], code) && fast;
+        if (i < 8)
+          w0 |= (ok ? code : 0u) << (4 * i);
+        else
+          w1 |= (ok ? code : 0u) << (4 * (i - 8));
+        pend |= (ok ? 0u : 1u) << i;
+      }
+    }
+    while (pend != 0u) {
+      const int i = __ffs(pend) - 1;
+      pend &= pend - 1u;
+      // element i by a tree of selects on its index bits
+      const bool b0 = i & 1, b1 = i & 2, b2 = i & 4, b3 = i & 8;
+      float e[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) e[t] = b0 ? v[2 * t + 1] : v[2 * t];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) e[t] = b1 ? e[2 * t + 1] : e[2 * t];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) e[t] = b2 ? e[2 * t + 1] : e[2 * t];
+      const float xi = b3 ? e[1] : e[0];
+      const uint64_t quad = (g0 >> 2) + (uint64_t)(i >> 2);
+      const Philox4 r = philox4x32_10((uint32_t)quad, (uint32_t)(quad >> 32), step0, step1, key0,
+                                      key1);
+      const int j = i & 3;
+      const uint32_t rwi = j == 0 ? r.x : j == 1 ? r.y : j == 2 ? r.z : r.w;
+      const uint32_t code = exact_e2m1_sr_quotient(xi, eff, rwi);
+      if (i < 8)
+        w0 |= code << (4 * i);
+      else
+        w1 |= code << (4 * (i - 8));
+    }
   } else if (eff >= 0x1p-125f && eff <= 0x1p125f) {
     // RTN codes of RN(v / eff) through the certified bracket, 8 at a time
     const float inv = __frcp_rn(eff);

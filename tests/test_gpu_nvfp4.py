@@ -451,3 +451,42 @@ def test_dequantize_every_code_and_scale_byte(s_t):
                 g = to_f32_np(ys[i])
                 assert np.array_equal(np.isnan(g), np.isnan(w))
                 assert_bits_equal(g[~np.isnan(w)], w[~np.isnan(w)], f"batched f32 {i}")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_sr_on_and_near_the_rounding_thresholds(dtype):
+    """Stochastic rounding where the quotient sits on, or one ulp from, the
+    threshold lo + u * step that the element's own random word u defines
+    (and on grid points, with zeros and saturating values): the kernel's
+    division-free rule cannot decide these and must take the exact path.
+    Each block holds a 6.0, so with a tensor scale of 1 its decoded scale is
+    exactly 1 and the quotient is the element itself."""
+    m = fp4()
+    nb = 4096
+    seed, step = 77, 5
+    g = np.arange(16 * nb, dtype=np.uint64)
+    u = (ora.rng_words(seed, step, g) >> 8).astype(np.float64) * 2.0 ** -24
+    rng = np.random.default_rng(3)
+    lo_tab = np.array([0, 0.5, 1, 1.5, 2, 3, 4], np.float64)
+    step_tab = np.array([0.5, 0.5, 0.5, 0.5, 1, 1, 2], np.float64)
+    c = rng.integers(0, 7, 16 * nb)
+    a = lo_tab[c] + u * step_tab[c]                  # exactly on the threshold
+    x = a.astype(np.float32)
+    kind = rng.integers(0, 6, 16 * nb)
+    x = np.where(kind == 1, np.nextafter(x, np.float32(np.inf)), x)
+    x = np.where(kind == 2, np.nextafter(x, np.float32(0)), x)
+    x = np.where(kind == 3, lo_tab[c].astype(np.float32), x)          # grid points
+    x = np.where(kind == 4, np.float32(0.0), x)
+    x = np.where(kind == 5, np.float32(5.99999), x)
+    x = np.where(rng.integers(0, 2, 16 * nb) == 1, -x, x).astype(np.float32)
+    x[::16] = 6.0
+    xt = torch.from_numpy(x)
+    if dtype == torch.bfloat16:
+        xt = xt.to(torch.bfloat16)   # the thresholds move; still near-threshold cases
+    one = torch.ones(1, device=dev())
+    pk, sc, _ = m.nvfp4_quantize(xt.to(dev()), rounding="sr", seed=seed, step=step,
+                                 tscale="given", tensor_scale=one)
+    wp, ws, _ = ora.nvfp4_quantize(to_f32_np(xt), rounding=ora.SR, seed=seed, step=step,
+                                   tscale_mode=ora.TSCALE_GIVEN, tensor_scale=1.0)
+    assert_bits_equal(u8(sc), ws, "scales")
+    assert_bits_equal(u8(pk), wp, "packed")
