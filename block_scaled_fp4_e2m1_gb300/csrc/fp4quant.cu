@@ -128,65 +128,122 @@ __device__ __forceinline__ void load32(const void* x, int64_t u, Row32& y) {
   }
 }
 
+// The raw words of a chunk, fetched one grid-stride step ahead of their use
+// so that a thread's next loads are in flight while it transforms the
+// current chunk (bf16 input: two 256-bit words; fp32 input is loaded when
+// used, four words would cost too many registers).
+struct RawBF16 {
+  U32x8 a, b;
+};
+
+__device__ __forceinline__ void fetch_bf16(const void* x, int64_t u, bool ok, RawBF16& r) {
+  if (ok) {
+    const uint16_t* p = static_cast<const uint16_t*>(x) + kE * u;
+    r.a = ld_stream_v8(p);
+    r.b = ld_stream_v8(p + 16);
+  }
+}
+
+__device__ __forceinline__ void unpack_bf16(const RawBF16& r, bool ok, Row32& y) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    y.p[2 * i].x = ok ? bf16_lo(r.a.w[i]) : 0.0f;
+    y.p[2 * i + 1].x = ok ? bf16_hi(r.a.w[i]) : 0.0f;
+    y.p[2 * i].y = ok ? bf16_lo(r.b.w[i]) : 0.0f;
+    y.p[2 * i + 1].y = ok ? bf16_hi(r.b.w[i]) : 0.0f;
+  }
+}
+
 // Units are 32-element chunks; the loop is warp-uniform so that every lane
 // takes part in the shuffles, and lanes past the end compute on zeros
 // without storing (the chunk count is a multiple of G/32, so a group is
 // either entirely inside or entirely past the end).
+// Encodes the chunk u (32 elements in y) and stores its codes and, from the
+// group's first lane, its two scales.
+template <int G>
+__device__ __forceinline__ void encode_chunk(Row32& y, int64_t u, bool valid, int lane,
+                                             uint8_t* __restrict__ packed,
+                                             float* __restrict__ s1_out,
+                                             float* __restrict__ s2_out) {
+  constexpr int LPG = G / kE;
+  // RMS scale: the pairwise tree over adjacent squares, levels 1-4 two
+  // sums per instruction ((0..15 | 16..31) halves side by side)
+  F2 sq[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    sq[i] = F2{__fmul_rn(y.p[i].x, y.p[i].x), __fmul_rn(y.p[i].y, y.p[i].y)};
+#pragma unroll
+  for (int w = 16; w > 1; w >>= 1) {
+#pragma unroll
+    for (int i = 0; i < w / 2; ++i) sq[i] = add2(sq[2 * i], sq[2 * i + 1]);
+  }
+  const float ss = group_sum<G>(__fadd_rn(sq[0].x, sq[0].y));
+  const float rms = __fsqrt_rn(__fmul_rn(ss, 1.0f / (float)G));
+  const float inv1 = rms == 0.0f ? 0.0f : __frcp_rn(rms);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) y.p[i] = F2{__fmul_rn(y.p[i].x, inv1), __fmul_rn(y.p[i].y, inv1)};
+  // transform
+  wht_group<G>(y, lane);
+  // absmax scale into [-6, 6]
+  float zmax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) zmax = fmaxf(zmax, fmaxf(fabsf(y.p[i].x), fabsf(y.p[i].y)));
+  zmax = group_max<G>(zmax);
+  const float sc2 = __fdiv_rn(zmax, 6.0f);
+  const F2 inv2 = splat(sc2 == 0.0f ? 0.0f : __frcp_rn(sc2));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) y.p[i] = mul2(y.p[i], inv2);
+  uint32_t w[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    w[k] = cvt_e2m1x8(y.at(8 * k), y.at(8 * k + 1), y.at(8 * k + 2), y.at(8 * k + 3),
+                      y.at(8 * k + 4), y.at(8 * k + 5), y.at(8 * k + 6), y.at(8 * k + 7));
+  if (valid) {
+    *reinterpret_cast<uint4*>(packed + 16 * u) = make_uint4(w[0], w[1], w[2], w[3]);
+    if ((lane & (LPG - 1)) == 0) {
+      s1_out[u / LPG] = rms;
+      s2_out[u / LPG] = sc2;
+    }
+  }
+}
+
+// bf16 input keeps the next chunk's loads in flight (a two-buffer ring
+// walked by an unrolled loop, so no registers are copied); fp32 input loads
+// each chunk when it is used.
 template <int G, bool kBF16>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kBF16 ? 2 : 3)
     encode_kernel(const void* __restrict__ x, int64_t nchunks, uint8_t* __restrict__ packed,
                   float* __restrict__ s1_out, float* __restrict__ s2_out) {
-  constexpr int LPG = G / kE;
   const int lane = threadIdx.x & 31;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
-  for (int64_t u0 = (int64_t)blockIdx.x * kThreads + (threadIdx.x & ~31); u0 < nchunks; u0 += stride) {
-    const int64_t u = u0 + lane;
-    const bool valid = u < nchunks;
-    Row32 y;
-    if (valid) {
-      load32<kBF16>(x, u, y);
-    } else {
+  int64_t u0 = (int64_t)blockIdx.x * kThreads + (threadIdx.x & ~31);
+  if (kBF16) {
+    RawBF16 ring[2];
+    fetch_bf16(x, u0 + lane, u0 + lane < nchunks, ring[0]);
+    for (;;) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) y.p[i] = splat(0.0f);
-    }
-    // RMS scale: the pairwise tree over adjacent squares, levels 1-4 two
-    // sums per instruction ((0..15 | 16..31) halves side by side)
-    F2 sq[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      sq[i] = F2{__fmul_rn(y.p[i].x, y.p[i].x), __fmul_rn(y.p[i].y, y.p[i].y)};
-#pragma unroll
-    for (int w = 16; w > 1; w >>= 1) {
-#pragma unroll
-      for (int i = 0; i < w / 2; ++i) sq[i] = add2(sq[2 * i], sq[2 * i + 1]);
-    }
-    const float ss = group_sum<G>(__fadd_rn(sq[0].x, sq[0].y));
-    const float rms = __fsqrt_rn(__fmul_rn(ss, 1.0f / (float)G));
-    const float inv1 = rms == 0.0f ? 0.0f : __frcp_rn(rms);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) y.p[i] = F2{__fmul_rn(y.p[i].x, inv1), __fmul_rn(y.p[i].y, inv1)};
-    // transform
-    wht_group<G>(y, lane);
-    // absmax scale into [-6, 6]
-    float zmax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) zmax = fmaxf(zmax, fmaxf(fabsf(y.p[i].x), fabsf(y.p[i].y)));
-    zmax = group_max<G>(zmax);
-    const float sc2 = __fdiv_rn(zmax, 6.0f);
-    const F2 inv2 = splat(sc2 == 0.0f ? 0.0f : __frcp_rn(sc2));
-#pragma unroll
-    for (int i = 0; i < 16; ++i) y.p[i] = mul2(y.p[i], inv2);
-    uint32_t w[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      w[k] = cvt_e2m1x8(y.at(8 * k), y.at(8 * k + 1), y.at(8 * k + 2), y.at(8 * k + 3),
-                        y.at(8 * k + 4), y.at(8 * k + 5), y.at(8 * k + 6), y.at(8 * k + 7));
-    if (valid) {
-      *reinterpret_cast<uint4*>(packed + 16 * u) = make_uint4(w[0], w[1], w[2], w[3]);
-      if ((lane & (LPG - 1)) == 0) {
-        s1_out[u / LPG] = rms;
-        s2_out[u / LPG] = sc2;
+      for (int s = 0; s < 2; ++s) {
+        if (u0 >= nchunks) return;
+        const int64_t u = u0 + lane;
+        fetch_bf16(x, u + stride, u + stride < nchunks, ring[s ^ 1]);
+        Row32 y;
+        unpack_bf16(ring[s], u < nchunks, y);
+        encode_chunk<G>(y, u, u < nchunks, lane, packed, s1_out, s2_out);
+        u0 += stride;
       }
+    }
+  } else {
+    for (; u0 < nchunks; u0 += stride) {
+      const int64_t u = u0 + lane;
+      const bool valid = u < nchunks;
+      Row32 y;
+      if (valid) {
+        load32<false>(x, u, y);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) y.p[i] = splat(0.0f);
+      }
+      encode_chunk<G>(y, u, valid, lane, packed, s1_out, s2_out);
     }
   }
 }
@@ -207,55 +264,82 @@ __device__ __forceinline__ void e2m1x8_values(uint32_t w, float o[8]) {
   }
 }
 
+// A chunk's codes and its group's two scales.
+struct DecIn {
+  uint4 p;
+  float sc1, sc2;
+};
+
+template <int G>
+__device__ __forceinline__ void fetch_dec(const uint8_t* __restrict__ packed,
+                                          const float* __restrict__ s1_in,
+                                          const float* __restrict__ s2_in, int64_t u, bool ok,
+                                          DecIn& d) {
+  constexpr int LPG = G / kE;
+  if (ok) {
+    d.p = ld_stream_v4(packed + 16 * u);
+    d.sc1 = s1_in[u / LPG];
+    d.sc2 = s2_in[u / LPG];
+  } else {
+    d.p = make_uint4(0u, 0u, 0u, 0u);
+    d.sc1 = d.sc2 = 0.0f;
+  }
+}
+
+// The next chunk's codes and scales are in flight while the current one is
+// decoded (a two-buffer ring walked by an unrolled loop).
 template <int G, bool kBF16Out>
 __global__ void __launch_bounds__(kThreads)
     decode_kernel(const uint8_t* __restrict__ packed, const float* __restrict__ s1_in,
                   const float* __restrict__ s2_in, int64_t nchunks, void* __restrict__ out) {
-  constexpr int LPG = G / kE;
   const int lane = threadIdx.x & 31;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
-  for (int64_t u0 = (int64_t)blockIdx.x * kThreads + (threadIdx.x & ~31); u0 < nchunks; u0 += stride) {
-    const int64_t u = u0 + lane;
-    const bool valid = u < nchunks;
-    uint4 p = make_uint4(0u, 0u, 0u, 0u);
-    float sc1 = 0.0f, sc2 = 0.0f;
-    if (valid) {
-      p = ld_stream_v4(packed + 16 * u);
-      sc1 = s1_in[u / LPG];
-      sc2 = s2_in[u / LPG];
-    }
-    float v[32];
-    e2m1x8_values(p.x, v);
-    e2m1x8_values(p.y, v + 8);
-    e2m1x8_values(p.z, v + 16);
-    e2m1x8_values(p.w, v + 24);
-    Row32 z;
+  int64_t u0 = (int64_t)blockIdx.x * kThreads + (threadIdx.x & ~31);
+  DecIn ring[2];
+  fetch_dec<G>(packed, s1_in, s2_in, u0 + lane, u0 + lane < nchunks, ring[0]);
+  for (;;) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) z.p[i] = F2{__fmul_rn(v[i], sc2), __fmul_rn(v[i + 16], sc2)};
-    wht_group<G>(z, lane);
-    const F2 m1 = splat(sc1);
+    for (int s = 0; s < 2; ++s) {
+      if (u0 >= nchunks) return;
+      const int64_t u = u0 + lane;
+      const bool valid = u < nchunks;
+      fetch_dec<G>(packed, s1_in, s2_in, u + stride, u + stride < nchunks, ring[s ^ 1]);
+      const DecIn& d = ring[s];
+      float v[32];
+      e2m1x8_values(d.p.x, v);
+      e2m1x8_values(d.p.y, v + 8);
+      e2m1x8_values(d.p.z, v + 16);
+      e2m1x8_values(d.p.w, v + 24);
+      Row32 z;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) z.p[i] = mul2(z.p[i], m1);
-    if (valid) {
-      if (kBF16Out) {
-        uint16_t* o = static_cast<uint16_t*>(out) + kE * u;
+      for (int i = 0; i < 16; ++i) z.p[i] = F2{__fmul_rn(v[i], d.sc2), __fmul_rn(v[i + 16], d.sc2)};
+      wht_group<G>(z, lane);
+      const F2 m1 = splat(d.sc1);
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          U32x8 w;
+      for (int i = 0; i < 16; ++i) z.p[i] = mul2(z.p[i], m1);
+      if (valid) {
+        if (kBF16Out) {
+          uint16_t* o = static_cast<uint16_t*>(out) + kE * u;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) w.w[i] = pack_bf16x2(z.at(16 * k + 2 * i), z.at(16 * k + 2 * i + 1));
-          st_v8(o + 16 * k, w);
-        }
-      } else {
-        float* o = static_cast<float*>(out) + kE * u;
+          for (int k = 0; k < 2; ++k) {
+            U32x8 w;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          U32x8 w;
+            for (int i = 0; i < 8; ++i)
+              w.w[i] = pack_bf16x2(z.at(16 * k + 2 * i), z.at(16 * k + 2 * i + 1));
+            st_v8(o + 16 * k, w);
+          }
+        } else {
+          float* o = static_cast<float*>(out) + kE * u;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) w.w[i] = __float_as_uint(z.at(8 * k + i));
-          st_v8(o + 8 * k, w);
+          for (int k = 0; k < 4; ++k) {
+            U32x8 w;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) w.w[i] = __float_as_uint(z.at(8 * k + i));
+            st_v8(o + 8 * k, w);
+          }
         }
       }
+      u0 += stride;
     }
   }
 }
