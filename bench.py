@@ -55,6 +55,9 @@ def parse_args(argv=None):
                    help="time one kernel alone on a tensor of --size-mb input (a kernel "
                         "study for profiling; prints its own JSON line)")
     p.add_argument("--size-mb", type=float, default=1024.0)
+    p.add_argument("--sweep", action="store_true",
+                   help="NVFP4 amax / quantize / dequantize over the 1 MiB - 4 GiB size sweep "
+                        "of the weight-set workload, one JSON line per kernel and size")
     p.add_argument("--quality", action="store_true",
                    help="print the FP4 quality table (zero share, average error) of the four "
                         "methods on layer-18-shaped synthetic weights, one JSON line per matrix")
@@ -735,6 +738,53 @@ def kernel_study(name, size_mb, steps, warmup, device):
     return g, [a.elapsed_time(b) for a, b in ev]
 
 
+def size_sweep(device, steps):
+    """NVFP4 amax, RTN quantize (scale from that amax) and dequantize to bf16
+    of one bf16 Laplace matrix [n / 4096, 4096] per size of the 1 MiB - 4 GiB
+    sweep.  L2 is flushed (a 512 MB write) before every timed launch, so the
+    small sizes are measured from HBM too; the events bracket the kernel
+    alone."""
+    import torch
+    import block_scaled_fp4_e2m1_gb300 as m
+    from block_scaled_fp4_e2m1_gb300 import workloads as W
+    peak, kind = measured_peak()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    for nbytes in W.size_sweep_bytes():
+        n = nbytes // 2
+        w = W.laplace_weight(11, (n // 4096, 4096), device=device).view(-1)
+        a, t = torch.empty(1, device=device), torch.empty(1, device=device)
+        pk = torch.empty(n // 2, dtype=torch.uint8, device=device)
+        sc = torch.empty(n // 16, dtype=torch.uint8, device=device)
+        y = torch.empty(n, dtype=torch.bfloat16, device=device)
+        calls = {
+            "nvfp4_amax": (2.0 * n, lambda: m.nvfp4_amax(w, amax_ws=a)),
+            "nvfp4_quantize": (2.5625 * n, lambda: m.nvfp4_quantize(
+                w, tscale="from_amax", amax_ws=a, tensor_scale=t, packed=pk, scales=sc)),
+            "nvfp4_dequantize": (2.5625 * n, lambda: m.nvfp4_dequantize(
+                pk, sc, t, (n,), torch.bfloat16, out=y)),
+        }
+        for name, (byt, f) in calls.items():
+            for _ in range(3):
+                f()
+            times = []
+            for _ in range(steps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                f()
+                e1.record()
+                e1.synchronize()
+                times.append(e0.elapsed_time(e1))
+            ms = statistics.median(times)
+            gbs = byt / (ms * 1e-3) / 1e9
+            print(json.dumps({"kernel": name, "bytes": nbytes, "ms_median": round(ms, 4),
+                              "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                              "peak_kind": kind, "l2": "flushed before each launch"}),
+                  flush=True)
+        del w, pk, sc, y
+        torch.cuda.empty_cache()
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.kernel:
@@ -754,6 +804,12 @@ def main(argv=None):
                               "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
                               "peak_kind": kind}), flush=True)
             torch.cuda.empty_cache()
+        return 0
+    if args.sweep:
+        import torch
+        import __graft_entry__
+        __graft_entry__.build()
+        size_sweep(torch.device("cuda", 0), args.steps if args.steps != 60 else 10)
         return 0
     if args.quality:
         import torch

@@ -117,7 +117,12 @@ def laplace_weight(seed: int, shape, median_abs: float = 0.017, outliers: int = 
     # rand() can return exactly 0; keep |u| < 1/2 so that every weight is finite
     u = torch.rand(n, generator=g, device=device, dtype=torch.float32).clamp_(min=2.0 ** -25) - 0.5
     w = -b * torch.sign(u) * torch.log1p(-2.0 * u.abs())
-    pos = torch.randperm(n, generator=g, device=device)[:outliers]
+    if n <= 2 ** 31 - 1:
+        pos = torch.randperm(n, generator=g, device=device)[:outliers]
+    else:  # randperm's sort stops at 2^31 elements: one position per stratum
+        span = n // outliers
+        pos = (torch.randint(0, span, (outliers,), generator=g, device=device) +
+               span * torch.arange(outliers, device=device))
     mag = 0.3 + (max_abs - 0.3) * torch.rand(outliers, generator=g, device=device)
     mag[0] = max_abs
     sgn = torch.where(torch.rand(outliers, generator=g, device=device) < 0.5, -1.0, 1.0)
