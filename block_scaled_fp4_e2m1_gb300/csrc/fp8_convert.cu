@@ -129,9 +129,15 @@ __global__ void __launch_bounds__(kRowThreads)
 //     row's output start D is byte-aligned only, so each chunk is a window
 //     of two aligned tile pieces, and the row's last (D mod 16) bytes are
 //     carried, in a 16-byte slot before the row, to the next block of the
-//     same segment.  Inside a run every chunk is whole; only the first and
-//     last block of a run of one segment write partial chunks, as 32-bit
-//     words and bytes.
+//     same segment.
+// Inside a run every chunk is whole.  For a segment wholly inside the run,
+// the warp's 32 output rows are one contiguous byte range, so the partial
+// chunk where row r ends is the one where row r + 1 starts: the segment's
+// first block keeps each row's head chunk and its last block stores it
+// merged with the previous row's tail as one whole chunk; only the two ends
+// of the range, shared with other warps, go out byte by byte.  Where a
+// segment crosses a run's end (or has rows under 32 bytes), the partial
+// chunks there are clipped and stored as words and bytes.
 // No CTA barrier in the loop: the warps of a CTA are independent.  The 8
 // warps of a CTA take neighbouring feature blocks of the same run, so their
 // 16-byte row slices of the codes share one 128-byte line and their scale
@@ -260,9 +266,9 @@ __device__ __forceinline__ void col_issue(ColIn& in, const uint8_t* __restrict__
 
 // Converts and writes one token block of one 32-feature block (see above).
 __device__ __forceinline__ void col_block(const ColIn& in, const SegPos& p, int64_t fb, bool carry,
-                                          bool run_end, int64_t cols, int kb, int lane, int g,
-                                          int c, const uint2* lut2, uint32_t* tile,
-                                          uint8_t* __restrict__ fp8_t,
+                                          bool run_end, bool merge, int64_t cols, int kb, int lane,
+                                          int g, int c, const uint2* lut2, uint32_t* tile,
+                                          uint4* heads, uint8_t* __restrict__ fp8_t,
                                           float* __restrict__ fp8_t_scales) {
   const int64_t b = fb - p.sofs;  // block inside the segment
   const int64_t t0 = 128 * b;
@@ -314,10 +320,74 @@ __device__ __forceinline__ void col_block(const ColIn& in, const SegPos& p, int6
       const uint4* row = reinterpret_cast<const uint4*>(tile + r * kTileRow);  // row[0]: carry
       reinterpret_cast<uint4*>(D - a)[j] = window16(row[j], row[j + 1], 16u - a);
     }
+  } else if (merge) {
+    // first or last block of a segment whose rows are at least 32 bytes:
+    // the row's span in chunk coordinates u = x + a is [ulo, uhi); its
+    // whole chunks go out as above.  A row's partial head chunk (first
+    // block) is kept in heads[r]: the same 16 bytes hold the end of row
+    // r - 1, and the last block stores the two merged as one whole chunk.
+    // Only row 0's head and row 31's tail border other warps' rows; those
+    // bytes go out one at a time.
+    const int q = lane >> 3, j = lane & 7;
+#pragma unroll 4
+    for (int i = 0; i < 8; ++i) {
+      const int r = 4 * i + q;
+      uint8_t* const D = D0 + (int64_t)r * p.n_e;
+      const uint32_t a = (uint32_t)reinterpret_cast<uintptr_t>(D) & 15u;
+      const int ulo = carry ? 0 : (int)a;
+      const int uhi = run_end ? nv + (int)a : 128;
+      if (16 * j >= ulo && 16 * j + 16 <= uhi) {
+        const uint4* row = reinterpret_cast<const uint4*>(tile + r * kTileRow);  // row[0]: carry
+        reinterpret_cast<uint4*>(D - a)[j] = window16(row[j], row[j + 1], 16u - a);
+      }
+    }
+    uint8_t* const D = D0 + (int64_t)lane * p.n_e;
+    const uint32_t a = (uint32_t)reinterpret_cast<uintptr_t>(D) & 15u;
+    uint8_t* const G = D - a;  // byte u of the span is G[u]
+    const uint4* row = reinterpret_cast<const uint4*>(tile + lane * kTileRow);
+    if (!carry && a != 0u) {  // head chunk 0: bytes [a, 16) are this row's
+      const uint4 h = window16(row[0], row[1], 16u - a);
+      if (lane == 0) {
+        const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+        for (int m = 0; m < 16; ++m)
+          if (m >= (int)a) G[m] = (uint8_t)(hw[m >> 2] >> (8 * (m & 3)));
+      } else {
+        heads[lane] = h;
+      }
+    }
+    __syncwarp();
+    if (run_end) {
+      const int uhi = nv + (int)a;
+      const int kt = uhi >> 4, tl = uhi & 15;  // tail chunk kt: bytes [0, tl) are this row's
+      if (tl != 0) {
+        const uint4 nxt = kt < 8 ? row[kt + 1] : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 t = window16(row[kt], nxt, 16u - a);
+        if (lane < 31) {
+          // the rest of the chunk is the head of row r + 1 (it starts at
+          // byte tl of this chunk): one whole chunk
+          const uint4 h = heads[lane + 1];
+          const uint32_t tw[4] = {t.x, t.y, t.z, t.w}, hw[4] = {h.x, h.y, h.z, h.w};
+          uint32_t mw[4];
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const int lo = tl - 4 * w;  // bytes of word w taken from the tail
+            const uint32_t keep = lo >= 4 ? 0xFFFFFFFFu : (lo <= 0 ? 0u : (1u << (8 * lo)) - 1u);
+            mw[w] = (tw[w] & keep) | (hw[w] & ~keep);
+          }
+          reinterpret_cast<uint4*>(G)[kt] = make_uint4(mw[0], mw[1], mw[2], mw[3]);
+        } else {
+          const uint32_t tw[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+          for (int m = 0; m < 16; ++m)
+            if (m < tl) G[16 * kt + m] = (uint8_t)(tw[m >> 2] >> (8 * (m & 3)));
+        }
+      }
+    }
   } else {
-    // first or last block of a run: the same chunks (nine when the span
-    // ends past chunk 7), each clipped to the row bytes [lo, hi) this block
-    // writes
+    // first or last block of a segment with rows shorter than 32 bytes: the
+    // same chunks (nine when the span ends past chunk 7), each clipped to
+    // the row bytes [lo, hi) this block writes
     const int q = lane >> 3, j = lane & 7;
     for (int i = 0; i < 8; ++i) {
       const int r = 4 * i + q;
@@ -347,7 +417,10 @@ __device__ __forceinline__ void col_block(const ColIn& in, const SegPos& p, int6
 }
 
 // The loads of the next token block are issued before the current one is
-// converted and written (two register buffers, swapped by unrolling).
+// converted and written (two register buffers, swapped by unrolling).  A
+// segment that lies wholly inside the run (and has rows of 32 bytes or
+// more) merges its row ends; one that crosses the run's ends writes the
+// partial chunks there byte by byte.
 __global__ void __launch_bounds__(kColThreads)
     fp4_to_fp8_col_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ scales,
                           int64_t cols, const int64_t* __restrict__ seg_row_off,
@@ -356,10 +429,12 @@ __global__ void __launch_bounds__(kColThreads)
                           float* __restrict__ fp8_t_scales) {
   __shared__ __align__(8) uint8_t lut[128];
   __shared__ __align__(16) uint32_t tiles[kColThreads / 32][32 * kTileRow];
+  __shared__ uint4 head_tiles[kColThreads / 32][32];
   build_shift_tables(lut);
   __syncthreads();
   const uint2* lut2 = reinterpret_cast<const uint2*>(lut);
   uint32_t* const tile = tiles[threadIdx.x >> 5];
+  uint4* const heads = head_tiles[threadIdx.x >> 5];
   const int lane = threadIdx.x & 31;
   const int g = lane >> 1;  // tokens 8g .. 8g+7 of a block
   const int c = lane & 1;   // features 16c .. 16c+15 of the feature block
@@ -385,8 +460,9 @@ __global__ void __launch_bounds__(kColThreads)
       pb = pa;
       if (next) next = seg_advance(pb, fb + 1, nseg, seg_row_off, seg_scale_off);
       if (next) col_issue(B, packed, scales, pb, fb + 1, row_bytes, kblocks, kb, g, c);
-      col_block(A, pa, fb, fb != fb0 && fb != pa.sofs, !next || fb + 1 == pa.send, cols, kb, lane,
-                g, c, lut2, tile, fp8_t, fp8_t_scales);
+      col_block(A, pa, fb, fb != fb0 && fb != pa.sofs, !next || fb + 1 == pa.send,
+                pa.sofs >= fb0 && pa.send <= fb1 && pa.n_e >= 32, cols, kb, lane, g, c, lut2, tile,
+                heads, fp8_t, fp8_t_scales);
       if (!next) break;
       ++fb;
       // B holds block fb (segment pb); fetch fb + 1 into A
@@ -394,8 +470,9 @@ __global__ void __launch_bounds__(kColThreads)
       pa = pb;
       if (next) next = seg_advance(pa, fb + 1, nseg, seg_row_off, seg_scale_off);
       if (next) col_issue(A, packed, scales, pa, fb + 1, row_bytes, kblocks, kb, g, c);
-      col_block(B, pb, fb, fb != fb0 && fb != pb.sofs, !next || fb + 1 == pb.send, cols, kb, lane,
-                g, c, lut2, tile, fp8_t, fp8_t_scales);
+      col_block(B, pb, fb, fb != fb0 && fb != pb.sofs, !next || fb + 1 == pb.send,
+                pb.sofs >= fb0 && pb.send <= fb1 && pb.n_e >= 32, cols, kb, lane, g, c, lut2, tile,
+                heads, fp8_t, fp8_t_scales);
       if (!next) break;
       ++fb;
     }
