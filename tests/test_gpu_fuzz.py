@@ -140,3 +140,37 @@ def test_fuzz_qdq(trial):
                   seed=trial, step=3)
     assert_bits_equal(bf16_bits(wd), wb, f"qdq W {trial}")
     assert_bits_equal(to_f32_np(rd), rn, f"qdq residual {trial}")
+
+
+@pytest.mark.parametrize("trial", range(16))
+def test_fuzz_fp4_to_fp8_col(trial):
+    """FP4RowToFP8Col on random ragged segment sets: empty, tiny (rows under
+    32 bytes), medium and long segments (crossing several 32-block runs), an
+    output that starts at a random byte offset, canaries around it."""
+    m = fp4()
+    rng = np.random.default_rng(5000 + trial)
+    cols = int(rng.choice([128, 256, 384]))
+    nseg = int(rng.integers(1, 40))
+    kinds = rng.integers(0, 4, nseg)
+    sizes = np.where(kinds == 0, 0, np.where(kinds == 1, rng.integers(1, 32, nseg),
+                     np.where(kinds == 2, rng.integers(32, 700, nseg),
+                              rng.integers(700, 6000, nseg))))
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    R = int(off[-1])
+    packed = rng.integers(0, 256, (max(R, 1), cols // 2), dtype=np.uint8)[:R]
+    scales = rng.integers(110, 140, (max(R, 1), cols // 32), dtype=np.uint8)[:R]
+    segs = m.Segments(torch.from_numpy(off), dev())
+    pk = torch.from_numpy(np.ascontiguousarray(packed)).to(dev())
+    sc = torch.from_numpy(np.ascontiguousarray(scales)).to(dev())
+    shift = int(rng.integers(0, 16))
+    out = torch.full((cols * R + 96,), 0xA5, dtype=torch.uint8, device=dev())
+    osc = torch.full((cols * segs.total_blocks + 16,), -7.0, dtype=torch.float32, device=dev())
+    m.fp4_to_fp8_col(pk, sc, segs, out[32 + shift:32 + shift + cols * R],
+                     osc[8:8 + cols * segs.total_blocks])
+    wo, wsc = ora.fp4_to_fp8_col(packed, scales, off)
+    o = u8(out)
+    assert np.all(o[:32 + shift] == 0xA5) and np.all(o[32 + shift + cols * R:] == 0xA5)
+    assert_bits_equal(o[32 + shift:32 + shift + cols * R], wo, f"fp8_t {trial}")
+    s = to_f32_np(osc)
+    assert np.all(s[:8] == -7.0) and np.all(s[8 + cols * segs.total_blocks:] == -7.0)
+    assert_bits_equal(s[8:8 + cols * segs.total_blocks], wsc, f"fp8_t scales {trial}")
