@@ -167,3 +167,39 @@ def test_batched_rtn_ties_and_extreme_scales_full():
                                        tensor_scale=given[i])
         assert_bits_equal(u8(sc[i]), ws, f"scales {i}")
         assert_bits_equal(u8(pk[i]), wp, f"packed {i}")
+
+
+def test_batched_full_weight_set_sampled():
+    """The whole 36-layer Qwen3-8B-shaped weight set (252 bf16 matrices,
+    6.95 G weights) through the launches the benchmark times: one batched
+    amax, one batched quantize (tensor scales from that amax) and one batched
+    dequantize.  Every tensor scale against the oracle's, sampled blocks of
+    every matrix against the oracle bit for bit."""
+    m = fp4()
+    shapes = workloads.qwen3_8b_weight_shapes(layers=36)
+    mats = [workloads.laplace_weight(100 + i, s, device=dev()).view(-1)
+            for i, s in enumerate(shapes)]
+    pks = [torch.empty(w.numel() // 2, dtype=torch.uint8, device=dev()) for w in mats]
+    scs = [torch.empty(w.numel() // 16, dtype=torch.uint8, device=dev()) for w in mats]
+    ys = [torch.empty(w.numel(), dtype=torch.bfloat16, device=dev()) for w in mats]
+    qb = m.Batch(xs=mats, packed=pks, scales=scs)
+    db = m.Batch(packed=pks, scales=scs, ys=ys, sizes=[w.numel() for w in mats])
+    am = m.nvfp4_amax_batched(qb, torch.bfloat16)
+    ts = m.nvfp4_quantize_batched(qb, torch.bfloat16, tscale="from_amax", amax=am)
+    m.nvfp4_dequantize_batched(db, ts, torch.bfloat16)
+    rng = np.random.default_rng(36)
+    ts_h = ts.cpu().numpy()
+    for i, w in enumerate(mats):
+        nb = w.numel() // 16
+        # the oracle's amax over the whole matrix, on the host
+        wt = ora.nvfp4_tensor_scale(ora.nvfp4_amax(to_f32_np(w)))
+        assert np.float32(ts_h[i]) == np.float32(wt), i
+        for b0 in [0, nb - 32, int(rng.integers(0, nb - 32))]:
+            v = to_f32_np(w[16 * b0:16 * (b0 + 32)])
+            wp, wsc, wq = ora.nvfp4_blocks(v, b0, wt)
+            assert_bits_equal(u8(pks[i][8 * b0:8 * (b0 + 32)]), wp, f"packed {i} @{b0}")
+            assert_bits_equal(u8(scs[i][b0:b0 + 32]), wsc, f"scales {i} @{b0}")
+            assert_bits_equal(bf16_bits(ys[i][16 * b0:16 * (b0 + 32)]), ora.bf16_rn(wq),
+                              f"dequant {i} @{b0}")
+    del mats, pks, scs, ys
+    torch.cuda.empty_cache()
