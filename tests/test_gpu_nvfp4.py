@@ -227,6 +227,34 @@ def test_qdq_training_workload_steps():
         assert_bits_equal(u8(scales), ws, f"scales step {t}")
 
 
+def test_qdq_training_workload_100_steps_reduced():
+    """The training configuration's 100 steps of W <- qdq(W - 1e-4 G) (SR +
+    error feedback, a fresh gradient per step, the amax pass then the qdq
+    pass) on a [256, 2048] slice-sized weight of the same distribution: W,
+    the residual, the codes and the tensor scale equal the oracle's after
+    every step."""
+    m = fp4()
+    shape = (256, 2048)
+    w0 = workloads.nvfp4_train_weight(seed=3, shape=shape, device="cpu")
+    w = w0.to(dev()).view(-1)
+    r = torch.zeros(w.numel(), dtype=torch.float32, device=dev())
+    wb = bf16_bits(w0).ravel().copy()
+    rn = np.zeros(w.numel(), np.float32)
+    amax = torch.empty(1, dtype=torch.float32, device=dev())
+    ts = torch.empty(1, dtype=torch.float32, device=dev())
+    for t in range(100):
+        g = workloads.nvfp4_train_grad(3, t, shape=shape, device="cpu").view(-1)
+        gd = g.to(dev())
+        m.nvfp4_qdq_amax(w, gd, 1e-4, r, amax_ws=amax)
+        _, packed, _, _ = m.nvfp4_qdq(w, gd, 1e-4, r, rounding="sr", seed=11, step=t,
+                                      tscale="from_amax", amax_ws=amax, tensor_scale=ts)
+        wp, _, wt = ora.nvfp4_qdq(wb, g.numpy(), 1e-4, rn, rounding=ora.SR, seed=11, step=t)
+        assert np.float32(ts.item()) == np.float32(wt), t
+        assert_bits_equal(u8(packed), wp, f"packed step {t}")
+        assert_bits_equal(bf16_bits(w), wb, f"W step {t}")
+        assert_bits_equal(to_f32_np(r), rn, f"r step {t}")
+
+
 def test_qdq_sub_ulp_accumulation_on_gpu():
     """fp4-train "Correctness": a sub-ULP accumulation reaches 1.50 under EF
     and SR and stays at 0.50 under RTN (the same run as the oracle pin)."""
