@@ -592,7 +592,8 @@ KERNEL_STUDIES = ["nvfp4_amax", "nvfp4_quantize", "nvfp4_quantize_sr", "nvfp4_de
                   "fp4quant_decode_g64", "fp4quant_decode_g128", "fp4quant_decode_g256",
                   "nvfp4_amax_batched", "nvfp4_quantize_batched", "nvfp4_dequantize_batched",
                   "fp8_to_fp4_row", "mxfp4_dequantize", "nvfp4_quantize_blocked",
-                  "fp4_scales_to_blocked", "fp4_scales_from_blocked"]
+                  "fp4_scales_to_blocked", "fp4_scales_from_blocked",
+                  "nvfp4_quantize_batched_blocked"]
 
 
 def kernel_study(name, size_mb, steps, warmup, device):
@@ -700,6 +701,21 @@ def kernel_study(name, size_mb, steps, warmup, device):
         else:
             g = Group(name, "study", sc.numel() + blk.numel(),
                       [lambda: m.fp4_scales_from_blocked(blk, rows, 256, out=sc)])
+    elif name == "nvfp4_quantize_batched_blocked":
+        # whole layers of the weight set, scales straight into the blocked
+        # layout of block-scaled matmuls (a GEMM-ready copy of the model)
+        layers = max(1, int(round(size_mb / 386.0)))
+        shapes = W.qwen3_8b_weight_shapes(layers=layers)
+        mats = [W.laplace_weight(100 + i, s, device=device).view(-1) for i, s in enumerate(shapes)]
+        nq = sum(w.numel() for w in mats)
+        pks = [z(w.numel() // 2, u8) for w in mats]
+        blks = [z(m.fp4_blocked_scales_size(r, c // 16), u8) for r, c in shapes]
+        qb = m.Batch(xs=mats, packed=pks, scales=blks, ks=[c for _, c in shapes])
+        am, ts = z(len(mats), f32), z(len(mats), f32)
+        m.nvfp4_amax_batched(qb, bf16, amax=am)
+        g = Group(name, "study", 2.5 * nq + sum(b.numel() for b in blks),
+                  [lambda: m.nvfp4_quantize_batched_blocked(qb, bf16, tscale="from_amax",
+                                                            tensor_scale=ts, amax=am)])
     elif name.endswith("_batched"):
         # whole layers of the Qwen3-8B-shaped set (~386 MB of bf16 per layer)
         layers = max(1, int(round(size_mb / 386.0)))

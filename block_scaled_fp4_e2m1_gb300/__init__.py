@@ -11,7 +11,8 @@ from .codec import (Batch, Segments, fp4_blocked_scales_size, fp4_scaled_dequant
                     fp4quant_decode, fp4quant_encode, fp8_to_fp4_row, kernel_launches,
                     mxfp4_dequantize, mxfp4_quantize, nvfp4_amax, nvfp4_amax_batched,
                     nvfp4_dequantize, nvfp4_dequantize_batched, nvfp4_qdq, nvfp4_qdq_amax,
-                    nvfp4_quantize, nvfp4_quantize_batched, nvfp4_quantize_blocked,
+                    nvfp4_quantize, nvfp4_quantize_batched, nvfp4_quantize_batched_blocked,
+                    nvfp4_quantize_blocked,
                     nvfp4_quantize_noalloc)
 from .error_feedback import ErrorFeedback
 from .quality import fp4_quality
@@ -23,6 +24,7 @@ __all__ = [
     "fp4quant_decode", "fp4quant_encode", "fp8_to_fp4_row", "kernel_launches",
     "mxfp4_dequantize", "mxfp4_quantize", "nvfp4_amax", "nvfp4_amax_batched",
     "nvfp4_dequantize", "nvfp4_dequantize_batched", "nvfp4_qdq", "nvfp4_qdq_amax",
-    "nvfp4_quantize", "nvfp4_quantize_batched", "nvfp4_quantize_blocked",
+    "nvfp4_quantize", "nvfp4_quantize_batched", "nvfp4_quantize_batched_blocked",
+    "nvfp4_quantize_blocked",
     "nvfp4_quantize_noalloc",
 ]

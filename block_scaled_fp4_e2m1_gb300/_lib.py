@@ -37,6 +37,8 @@ SIGNATURES = {
     "fp4_batch_plan": (INT, [P, I32, P]),
     "nvfp4_amax_batched": (INT, [P, I32, I64, INT, P, P]),
     "nvfp4_quantize_batched": (INT, [P, I32, I64, INT, INT, U64, U64, INT, P, P, P]),
+    "nvfp4_quantize_batched_blocked": (INT, [P, P, I32, I64, INT, INT, U64, U64, INT, P, P, P]),
+    "fp4_batch_plan_blocked": (INT, [P, P, I32, P]),
     "nvfp4_dequantize_batched": (INT, [P, I32, I64, P, INT, P]),
     "mxfp4_quantize": (INT, [P, INT, I64, I64, P, P, P]),
     "fp4_to_fp8_row": (INT, [P, P, I64, I64, P, P, P]),

@@ -230,7 +230,8 @@ class Batch:
 
     DESC = None  # numpy dtype of fp4_tensor_desc, built on first use
 
-    def __init__(self, xs=None, packed=None, scales=None, ys=None, sizes=None, device=None):
+    def __init__(self, xs=None, packed=None, scales=None, ys=None, sizes=None, device=None,
+                 ks=None):
         import numpy as np
         if Batch.DESC is None:
             Batch.DESC = np.dtype([("x", "<u8"), ("packed", "<u8"), ("scales", "<u8"),
@@ -251,12 +252,21 @@ class Batch:
                     host[name][i] = t.data_ptr()
         host["n"] = self.sizes
         total = ctypes.c_int64(0)
-        call("fp4_batch_plan", host.ctypes.data, count, ctypes.addressof(total))
+        if ks is None:
+            call("fp4_batch_plan", host.ctypes.data, count, ctypes.addressof(total))
+        else:
+            # row lengths for the blocked scale layout (nvfp4_quantize_batched_blocked)
+            kh = np.ascontiguousarray(np.asarray(ks, dtype=np.int64))
+            if kh.size != count:
+                raise ValueError("ks needs one row length per tensor")
+            call("fp4_batch_plan_blocked", host.ctypes.data, kh.ctypes.data, count,
+                 ctypes.addressof(total))
         self.total_chunks = int(total.value)
         self.host = host
         dev = device if device is not None else (lists[0][0].device if lists and count else "cuda")
         self.desc = torch.from_numpy(host.view(np.uint8).copy()).to(dev)
         self.device = self.desc.device
+        self.kdev = None if ks is None else torch.from_numpy(kh).to(self.device)
 
 
 def nvfp4_amax_batched(batch: Batch, dtype: torch.dtype,
@@ -281,6 +291,26 @@ def nvfp4_quantize_batched(batch: Batch, dtype: torch.dtype, rounding: str = "rt
     call("nvfp4_quantize_batched", _ptr(batch.desc), batch.count, batch.total_chunks, _DT[dtype],
          _ROUND[rounding], seed, step, _TSCALE[tscale], _ptr(tensor_scale), _ptr(amax),
          _stream(dev))
+    return tensor_scale
+
+
+def nvfp4_quantize_batched_blocked(batch: Batch, dtype: torch.dtype, rounding: str = "rtn",
+                                   seed: int = 0, step: int = 0, tscale: str = "compute",
+                                   tensor_scale: Optional[torch.Tensor] = None,
+                                   amax: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """nvfp4_quantize_batched with every tensor's scales in the blocked layout
+    of its [n / k, k] matrix; the batch is built with ks (row lengths) and its
+    scales buffers hold fp4_blocked_scales_size(n / k, k / 16) bytes each."""
+    if batch.kdev is None:
+        raise ValueError("the batch was built without ks")
+    dev = batch.device
+    if tensor_scale is None:
+        tensor_scale = torch.ones(batch.count, dtype=torch.float32, device=dev)
+    if amax is None and tscale != "given":
+        amax = torch.empty(batch.count, dtype=torch.float32, device=dev)
+    call("nvfp4_quantize_batched_blocked", _ptr(batch.desc), _ptr(batch.kdev), batch.count,
+         batch.total_chunks, _DT[dtype], _ROUND[rounding], seed, step, _TSCALE[tscale],
+         _ptr(tensor_scale), _ptr(amax), _stream(dev))
     return tensor_scale
 
 

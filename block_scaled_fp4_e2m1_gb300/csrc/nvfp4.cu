@@ -106,59 +106,6 @@ constexpr int quantize_min_ctas() {
   return kRes ? 2 : ((kSR || !kBF16 || kBlk) ? 3 : 4);
 }
 
-// Where the block scales of a [rows, 16 * cols] matrix go in the blocked
-// layout (common.cuh).  A thread keeps its block's place as the byte offset
-// of its row tile, the row inside the tile and the scale column, and steps
-// it by the grid stride with adds and compares only: no division and no
-// 64-bit multiply per block.  cols < 2^24 keeps every offset inside a row
-// tile below 2^31.
-struct BlockedMap {
-  int64_t rows, cols, col_tiles;
-};
-
-struct BlockedCursor {
-  int64_t base;  // (row / 128) * col_tiles * 512
-  uint32_t rr;   // row % 128
-  uint32_t c;    // scale column
-};
-
-struct BlockedStep {
-  int64_t base;            // (stride rows / 128) * col_tiles * 512
-  int64_t tile_row_bytes;  // col_tiles * 512
-  uint32_t rr, c, cols;    // stride rows % 128, stride columns, cols
-};
-
-__device__ __forceinline__ BlockedCursor blocked_cursor(int64_t b, const BlockedMap& bm) {
-  const int64_t row = b / bm.cols;
-  return BlockedCursor{(row >> 7) * bm.col_tiles * 512, (uint32_t)(row & 127),
-                       (uint32_t)(b - row * bm.cols)};
-}
-
-__device__ __forceinline__ BlockedStep blocked_step(int64_t stride, const BlockedMap& bm) {
-  const int64_t rows = stride / bm.cols;
-  return BlockedStep{(rows >> 7) * bm.col_tiles * 512, bm.col_tiles * 512,
-                     (uint32_t)(rows & 127), (uint32_t)(stride - rows * bm.cols),
-                     (uint32_t)bm.cols};
-}
-
-// Byte offset of the cursor's scale: its row tile, then inside the tile the
-// column tile, the row group (row / 32), the row within it and the column
-// within the 4-byte word, which occupy disjoint bits.
-__device__ __forceinline__ int64_t blocked_at(const BlockedCursor& q) {
-  return q.base + (int64_t)(((q.c & ~3u) << 7) | ((q.rr & 31u) << 4) | ((q.rr >> 5) << 2) |
-                            (q.c & 3u));
-}
-
-__device__ __forceinline__ void blocked_advance(BlockedCursor& q, const BlockedStep& st) {
-  q.c += st.c;
-  const bool wrap = q.c >= st.cols;
-  q.c = wrap ? q.c - st.cols : q.c;
-  q.rr += st.rr + (wrap ? 1u : 0u);
-  const bool tile = q.rr >= 128u;
-  q.rr = tile ? q.rr - 128u : q.rr;
-  q.base += st.base + (tile ? st.tile_row_bytes : 0);
-}
-
 // A thread quantizes one block per grid-stride step; the loads of the next
 // kD blocks are in flight meanwhile.  The ring of kD + 1 buffers is walked
 // by a fully unrolled inner loop, so every buffer index is a constant and no

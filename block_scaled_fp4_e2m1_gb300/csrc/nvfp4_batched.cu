@@ -209,6 +209,74 @@ __global__ void __launch_bounds__(kBThreads, kSR ? 1 : (kBF16 ? 3 : 2))
   });
 }
 
+// The blocked-scale variant walks the tensors one after the other, each
+// with the whole grid in grid-stride order (the single-tensor kernel's
+// order), not in per-warp ranges.  A tensor's scale tiles are then
+// completed by the whole GPU within a pass or two, so their 16-byte lines
+// fill in L2 at once.  With per-warp ranges, thousands of warps each kept
+// their own row tiles half written, the partial lines overflowed L2, and
+// the kernel ran at 0.6 of the copy bandwidth.  tensor t's scales go to the
+// blocked layout of its [n_t / k_t, k_t] matrix (k: device array of the
+// k_t); padding is zeroed by the whole grid.
+template <bool kBF16, bool kSR>
+__global__ void __launch_bounds__(kBThreads, kSR ? 1 : (kBF16 ? 3 : 2))
+    quantize_batched_blocked_kernel(const fp4_tensor_desc* __restrict__ desc, int count,
+                                    const int64_t* __restrict__ kdim, uint64_t seed, uint64_t step,
+                                    int tscale_mode, float* __restrict__ tensor_scale,
+                                    const float* __restrict__ amax) {
+  constexpr int kD = kBF16 ? 2 : 1;  // blocks in flight ahead of the one being quantized
+  constexpr bool kFast = kBF16 && !kSR;
+  __shared__ EffEntry eff_tabs[kFast ? (kBThreads / 32) * kEffEntries : 1];
+  EffEntry* const tab = eff_tabs + (kFast ? (threadIdx.x >> 5) * kEffEntries : 0);
+  const uint32_t key0 = (uint32_t)seed, key1 = (uint32_t)(seed >> 32);
+  const uint32_t st0 = (uint32_t)step, st1 = (uint32_t)(step >> 32);
+  const int64_t stride = (int64_t)gridDim.x * kBThreads;
+  const int64_t gtid = (int64_t)blockIdx.x * kBThreads + threadIdx.x;
+  for (int t = 0; t < count; ++t) {
+    const float s_t = tscale_mode == FP4_TSCALE_GIVEN ? sanitize_scale(tensor_scale[t])
+                                                      : tensor_scale_from_amax(amax[t]);
+    if (tscale_mode != FP4_TSCALE_GIVEN && gtid == 0) tensor_scale[t] = s_t;
+    const int64_t nb = ldg_i64(&desc[t].n) / 16;
+    if (nb == 0) continue;
+    const ScaleDiv sd = make_scale_div(s_t);
+    if (kFast) build_eff_table(tab, s_t);
+    const void* x = ldg_ptr(&desc[t].x);
+    uint8_t* const packed = ldg_ptr(&desc[t].packed);
+    uint8_t* const scales = ldg_ptr(&desc[t].scales);
+    const int64_t kc = ldg_i64(&kdim[t]) / 16;  // block scales per row
+    const BlockedMap bm{nb / kc, kc, (kc + 3) / 4};
+    blocked_zero_padding(scales, bm.rows, bm.cols, bm.col_tiles, gtid, stride);
+    int64_t b = gtid;
+    BlockedCursor cur = blocked_cursor(b, bm);
+    const BlockedStep cstep = blocked_step(stride, bm);
+    BlockIn<kBF16, false> buf[kD + 1];
+#pragma unroll
+    for (int d = 0; d < kD; ++d) issue_block<kBF16, false>(x, nullptr, b + d * stride, nb, buf[d]);
+    for (;;) {
+#pragma unroll
+      for (int r = 0; r <= kD; ++r) {
+        if (b >= nb) goto tensor_done;
+        issue_block<kBF16, false>(x, nullptr, b + kD * stride, nb, buf[(r + kD) % (kD + 1)]);
+        uint2 out;
+        uint32_t sb;
+        if (kFast) {
+          sb = quantize_block_bf16_rtn(buf[r].x[0], sd, tab, out);
+        } else {
+          float v[16], rr[16], q[16];
+          unpack_block<kBF16, false>(buf[r], v, rr);
+          sb = quantize_block<kSR, false>(v, s_t, sd, (uint64_t)(16 * b), key0, key1, st0, st1,
+                                          out, q);
+        }
+        *reinterpret_cast<uint2*>(packed + 8 * b) = out;
+        scales[blocked_at(cur)] = (uint8_t)sb;
+        blocked_advance(cur, cstep);
+        b += stride;
+      }
+    }
+  tensor_done:;
+  }
+}
+
 template <bool kBF16Out>
 __global__ void __launch_bounds__(kBThreads)
     dequantize_batched_kernel(const fp4_tensor_desc* __restrict__ desc, int count,
@@ -276,6 +344,59 @@ fp4_status launch_amax_batched(const fp4_tensor_desc* desc, int32_t count, int64
                                             total_chunks, amax);
 }
 
+template <bool kBlk>
+fp4_status quantize_batched_common(const fp4_tensor_desc* desc, const int64_t* k, int32_t count,
+                                   int64_t total_chunks, int dtype, int rounding, uint64_t seed,
+                                   uint64_t step, int tscale_mode, float* tensor_scale,
+                                   float* amax, void* stream) {
+  if (!dtype_ok(dtype)) return FP4_ERR_DTYPE;
+  if (rounding != FP4_RTN && rounding != FP4_SR) return FP4_ERR_ARG;
+  if (tscale_mode != FP4_TSCALE_GIVEN && tscale_mode != FP4_TSCALE_COMPUTE &&
+      tscale_mode != FP4_TSCALE_FROM_AMAX)
+    return FP4_ERR_ARG;
+  if (const fp4_status st = check_desc(desc, count, total_chunks); st != FP4_OK) return st;
+  if (count > 0 && !tensor_scale) return FP4_ERR_NULL;
+  if (count > 0 && tscale_mode != FP4_TSCALE_GIVEN && !amax) return FP4_ERR_NULL;
+  if (!aligned(tensor_scale, 4) || !aligned(amax, 4)) return FP4_ERR_ALIGN;
+  cudaStream_t s = as_stream(stream);
+  if (tscale_mode == FP4_TSCALE_COMPUTE) {
+    const fp4_status st = launch_amax_batched(desc, count, total_chunks, dtype, amax, s);
+    if (st != FP4_OK) return st;
+  }
+  if (total_chunks == 0) return FP4_OK;
+  const int64_t units = total_chunks * kChunk;  // one thread per block of the flat space
+  if (kBlk) {
+    if (dtype == FP4_BF16) {
+      if (rounding == FP4_SR)
+        return launch<quantize_batched_blocked_kernel<true, true>>(
+            units, kBThreads, 0, s, desc, count, k, seed, step, tscale_mode, tensor_scale, amax);
+      return launch<quantize_batched_blocked_kernel<true, false>>(
+          units, kBThreads, 0, s, desc, count, k, seed, step, tscale_mode, tensor_scale, amax);
+    }
+    if (rounding == FP4_SR)
+      return launch<quantize_batched_blocked_kernel<false, true>>(
+          units, kBThreads, 0, s, desc, count, k, seed, step, tscale_mode, tensor_scale, amax);
+    return launch<quantize_batched_blocked_kernel<false, false>>(
+        units, kBThreads, 0, s, desc, count, k, seed, step, tscale_mode, tensor_scale, amax);
+  }
+  if (dtype == FP4_BF16) {
+    if (rounding == FP4_SR)
+      return launch<quantize_batched_kernel<true, true>>(units, kBThreads, 0, s, desc, count,
+                                                         total_chunks, seed, step, tscale_mode,
+                                                         tensor_scale, amax);
+    return launch<quantize_batched_kernel<true, false>>(units, kBThreads, 0, s, desc, count,
+                                                        total_chunks, seed, step, tscale_mode,
+                                                        tensor_scale, amax);
+  }
+  if (rounding == FP4_SR)
+    return launch<quantize_batched_kernel<false, true>>(units, kBThreads, 0, s, desc, count,
+                                                        total_chunks, seed, step, tscale_mode,
+                                                        tensor_scale, amax);
+  return launch<quantize_batched_kernel<false, false>>(units, kBThreads, 0, s, desc, count,
+                                                       total_chunks, seed, step, tscale_mode,
+                                                       tensor_scale, amax);
+}
+
 }  // namespace
 }  // namespace fp4
 
@@ -313,38 +434,29 @@ fp4_status nvfp4_amax_batched(const fp4_tensor_desc* desc, int32_t count, int64_
 fp4_status nvfp4_quantize_batched(const fp4_tensor_desc* desc, int32_t count, int64_t total_chunks,
                                   int dtype, int rounding, uint64_t seed, uint64_t step,
                                   int tscale_mode, float* tensor_scale, float* amax, void* stream) {
-  if (!dtype_ok(dtype)) return FP4_ERR_DTYPE;
-  if (rounding != FP4_RTN && rounding != FP4_SR) return FP4_ERR_ARG;
-  if (tscale_mode != FP4_TSCALE_GIVEN && tscale_mode != FP4_TSCALE_COMPUTE &&
-      tscale_mode != FP4_TSCALE_FROM_AMAX)
-    return FP4_ERR_ARG;
-  if (const fp4_status st = check_desc(desc, count, total_chunks); st != FP4_OK) return st;
-  if (count > 0 && !tensor_scale) return FP4_ERR_NULL;
-  if (count > 0 && tscale_mode != FP4_TSCALE_GIVEN && !amax) return FP4_ERR_NULL;
-  if (!aligned(tensor_scale, 4) || !aligned(amax, 4)) return FP4_ERR_ALIGN;
-  cudaStream_t s = as_stream(stream);
-  if (tscale_mode == FP4_TSCALE_COMPUTE) {
-    const fp4_status st = launch_amax_batched(desc, count, total_chunks, dtype, amax, s);
-    if (st != FP4_OK) return st;
+  return quantize_batched_common<false>(desc, nullptr, count, total_chunks, dtype, rounding, seed,
+                                        step, tscale_mode, tensor_scale, amax, stream);
+}
+
+fp4_status nvfp4_quantize_batched_blocked(const fp4_tensor_desc* desc, const int64_t* k,
+                                          int32_t count, int64_t total_chunks, int dtype,
+                                          int rounding, uint64_t seed, uint64_t step,
+                                          int tscale_mode, float* tensor_scale, float* amax,
+                                          void* stream) {
+  if (count > 0 && !k) return FP4_ERR_NULL;
+  if (!aligned(k, 8)) return FP4_ERR_ALIGN;
+  return quantize_batched_common<true>(desc, k, count, total_chunks, dtype, rounding, seed, step,
+                                       tscale_mode, tensor_scale, amax, stream);
+}
+
+fp4_status fp4_batch_plan_blocked(fp4_tensor_desc* host_desc, const int64_t* host_k, int32_t count,
+                                  int64_t* total_chunks) {
+  if (count > 0 && !host_k) return FP4_ERR_NULL;
+  for (int32_t t = 0; t < count && host_desc; ++t) {
+    const int64_t k = host_k[t], n = host_desc[t].n;
+    if (k <= 0 || k % 16 != 0 || k / 16 >= (INT64_C(1) << 24) || n % k != 0) return FP4_ERR_SHAPE;
   }
-  if (total_chunks == 0) return FP4_OK;
-  const int64_t units = total_chunks * kChunk;  // one thread per block of the flat space
-  if (dtype == FP4_BF16) {
-    if (rounding == FP4_SR)
-      return launch<quantize_batched_kernel<true, true>>(units, kBThreads, 0, s, desc, count,
-                                                         total_chunks, seed, step, tscale_mode,
-                                                         tensor_scale, amax);
-    return launch<quantize_batched_kernel<true, false>>(units, kBThreads, 0, s, desc, count,
-                                                        total_chunks, seed, step, tscale_mode,
-                                                        tensor_scale, amax);
-  }
-  if (rounding == FP4_SR)
-    return launch<quantize_batched_kernel<false, true>>(units, kBThreads, 0, s, desc, count,
-                                                        total_chunks, seed, step, tscale_mode,
-                                                        tensor_scale, amax);
-  return launch<quantize_batched_kernel<false, false>>(units, kBThreads, 0, s, desc, count,
-                                                       total_chunks, seed, step, tscale_mode,
-                                                       tensor_scale, amax);
+  return fp4_batch_plan(host_desc, count, total_chunks);
 }
 
 fp4_status nvfp4_dequantize_batched(const fp4_tensor_desc* desc, int32_t count,

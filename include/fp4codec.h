@@ -240,6 +240,24 @@ fp4_status nvfp4_quantize_batched(const fp4_tensor_desc* desc, int32_t count, in
                                   int dtype, int rounding, uint64_t seed, uint64_t step,
                                   int tscale_mode, float* tensor_scale, float* amax, void* stream);
 
+/* nvfp4_quantize_batched with every tensor's block scales written in the
+ * blocked layout of its [n_t / k_t, k_t] matrix, padding included (as
+ * nvfp4_quantize_blocked does for one matrix): desc[t].scales points at
+ * fp4_blocked_scales_size(n_t / k_t, k_t / 16) bytes (any alignment).
+ *   k  device array of count int64, the row length k_t of each tensor,
+ *      8-byte aligned; validated on the host by fp4_batch_plan_blocked.
+ * Codes, tensor scales and SR draws are those of nvfp4_quantize_batched. */
+fp4_status nvfp4_quantize_batched_blocked(const fp4_tensor_desc* desc, const int64_t* k,
+                                          int32_t count, int64_t total_chunks, int dtype,
+                                          int rounding, uint64_t seed, uint64_t step,
+                                          int tscale_mode, float* tensor_scale, float* amax,
+                                          void* stream);
+
+/* Host helper: fp4_batch_plan plus, for every tensor, k_t > 0, k_t % 16 == 0,
+ * k_t / 16 < 2^24 and n_t % k_t == 0 (FP4_ERR_SHAPE otherwise). */
+fp4_status fp4_batch_plan_blocked(fp4_tensor_desc* host_desc, const int64_t* host_k, int32_t count,
+                                  int64_t* total_chunks);
+
 /* nvfp4_dequantize on every tensor; tensor_scale is a device array of count
  * fp32, or NULL for scale 1. */
 fp4_status nvfp4_dequantize_batched(const fp4_tensor_desc* desc, int32_t count,

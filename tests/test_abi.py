@@ -213,3 +213,22 @@ def test_blocked_scale_layout_host_checks(L):
     assert call(mode=2, ws=None) == 1
     assert call(x=MIS) == 2
     assert call(pk=A + 8) == 2
+
+
+def test_batch_plan_blocked_host_helper(L):
+    import numpy as np
+    desc = np.dtype([("x", "<u8"), ("packed", "<u8"), ("scales", "<u8"), ("y", "<u8"),
+                     ("n", "<i8"), ("chunk_start", "<i8")])
+    d = np.zeros(3, desc)
+    d["n"] = [64, 4096 * 16, 0]
+    total = ctypes.c_int64(-1)
+    ok = np.array([32, 4096, 16], np.int64)
+    assert L.fp4_batch_plan_blocked(d.ctypes.data, ok.ctypes.data, 3, ctypes.addressof(total)) == 0
+    assert total.value == 1 + 16 + 0   # chunks of 256 blocks
+    for bad in ([48, 4096, 16], [24, 4096, 16], [32, 4096, 0], [32, 4096 * 3, 16]):
+        b = np.array(bad, np.int64)
+        assert L.fp4_batch_plan_blocked(d.ctypes.data, b.ctypes.data, 3,
+                                        ctypes.addressof(total)) == 3, bad
+    assert L.fp4_batch_plan_blocked(d.ctypes.data, None, 3, ctypes.addressof(total)) == 1
+    assert L.nvfp4_quantize_batched_blocked(A, None, 3, 2, 1, 0, 0, 0, 1, A, A, None) == 1
+    assert L.nvfp4_quantize_batched_blocked(A, A + 4, 3, 2, 1, 0, 0, 0, 1, A, A, None) == 2

@@ -198,3 +198,38 @@ def test_cuda_blocked_quantize_feeds_scaled_mm():
     wap, was, _ = ora.nvfp4_quantize(to_f32_np(a), tscale_mode=ora.TSCALE_GIVEN, tensor_scale=1.0)
     wbp, wbs, _ = ora.nvfp4_quantize(to_f32_np(b), tscale_mode=ora.TSCALE_GIVEN, tensor_scale=1.0)
     _check_product(got, _dequant_np(wap, was, M, K), _dequant_np(wbp, wbs, N, K))
+
+
+@pytest.mark.parametrize("rounding", ["rtn", "sr"])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_batched_blocked_matches_single_calls(rounding, dtype):
+    """nvfp4_quantize_batched_blocked over matrices of assorted shapes (rows
+    not a multiple of 128, k not a multiple of 64, one row, an empty
+    matrix): every tensor's codes, blocked scales (padding included) and
+    tensor scale equal nvfp4_quantize_blocked on it; guard bytes after each
+    blocked buffer stay untouched; one tensor against the oracle."""
+    m = fp4()
+    shapes = [(1024, 512), (130, 48), (1, 16), (300, 352), (0, 64), (257, 2064)]
+    xs = [_inputs(r, k, dtype, seed=40 + i).to(dev()) if r else
+          torch.empty(0, k, dtype=dtype, device=dev()) for i, (r, k) in enumerate(shapes)]
+    pks = [torch.full((r * k // 2,), 0x5A, dtype=torch.uint8, device=dev()) for r, k in shapes]
+    sizes = [m.fp4_blocked_scales_size(r, k // 16) for r, k in shapes]
+    bufs = [torch.full((sz + GUARD,), 0xA5, dtype=torch.uint8, device=dev()) for sz in sizes]
+    blks = [b[:sz] for b, sz in zip(bufs, sizes)]
+    batch = m.Batch(xs=[x.view(-1) for x in xs], packed=pks, scales=blks,
+                    ks=[k for _, k in shapes])
+    ts = m.nvfp4_quantize_batched_blocked(batch, dtype, rounding=rounding, seed=5, step=2,
+                                          tscale="compute")
+    for i, ((r, k), x) in enumerate(zip(shapes, xs)):
+        p1, b1, t1 = m.nvfp4_quantize_blocked(x, rounding=rounding, seed=5, step=2)
+        assert ts[i].item() == t1.item(), i
+        assert_bits_equal(u8(pks[i]), u8(p1).reshape(-1), f"packed {i}")
+        assert_bits_equal(u8(blks[i]), u8(b1), f"blocked {i}")
+        assert (bufs[i][sizes[i]:] == 0xA5).all(), i
+    r, k = shapes[5]
+    wp, ws, wt = ora.nvfp4_quantize(to_f32_np(xs[5]).reshape(-1),
+                                    rounding=ora.SR if rounding == "sr" else ora.RTN,
+                                    seed=5, step=2)
+    assert np.float32(ts[5].item()) == np.float32(wt)
+    assert_bits_equal(u8(pks[5]), wp, "oracle packed")
+    assert_bits_equal(u8(blks[5]), ora.scales_to_blocked(ws, r, k // 16), "oracle blocked")
