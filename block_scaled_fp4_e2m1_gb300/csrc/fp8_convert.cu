@@ -114,39 +114,63 @@ __global__ void __launch_bounds__(kRowThreads)
 
 // ------------------------------------------------------------------- col
 //
-// Work unit: one warp converts one 32-feature block (one MXFP4 scale column)
-// over a run of up to kColRun consecutive 128-token blocks of the global
-// block order (a run may cross segment boundaries).  Per token block:
-//   - lane (g, c) = (lane >> 1, lane & 1) loads the 16 codes of features
-//     16c .. 16c+15 (8 bytes) and the scale byte of tokens 8g .. 8g+7;
+// Output: for expert segment e (rows row0 .. row0 + n_e - 1 of the input),
+// feature f's n_e E4M3 bytes at fp8_t + cols * row0 + f * n_e.  Rows start
+// at arbitrary byte offsets, so the stores are organised around 32-byte
+// sectors: every store covers whole sectors, and a sector shared by two
+// rows is written once, merged.  (Measured: stores that leave sectors
+// half written cost the kernel a third of its time.)
+//
+// Work unit: one CTA converts a group of up to eight 32-feature blocks (one
+// MXFP4 scale column each, one per warp) over a run of up to kColRun
+// consecutive 128-token blocks of the global block order (a run may cross
+// segment boundaries).  Per token block:
+//   - the CTA copies the block's codes for its 256 features (128 tokens x
+//     128 bytes: whole lines) and their scale bytes into a shared-memory
+//     stage with cp.async, one block ahead of use; 16-byte chunk q of token
+//     t sits at chunk q ^ ((t >> 3) & 7) of its row, so the warps' reads
+//     are free of bank conflicts;
+//   - in warp w (feature block w of the group) lane (g, c) = (lane >> 1,
+//     lane & 1) reads the 16 codes of features 16c .. 16c+15 and the scale
+//     byte of tokens 8g .. 8g+7 from the stage;
 //   - the block's target scale S_t is one warp max reduction;
 //   - each lane converts its 8 tokens x 16 features through the shift
 //     tables and transposes them (4 x 4 byte transposes) into 16 feature
-//     rows x 8 token bytes, written to the warp's tile in shared memory
-//     (32 feature rows of 128 token bytes);
-//   - the warp then writes the 32 rows, four at a time, eight lanes per row
-//     each storing one aligned 16-byte chunk of the row's output span.  A
-//     row's output start D is byte-aligned only, so each chunk is a window
-//     of two aligned tile pieces, and the row's last (D mod 16) bytes are
-//     carried, in a 16-byte slot before the row, to the next block of the
-//     same segment.
-// Inside a run every chunk is whole.  For a segment wholly inside the run,
-// the warp's 32 output rows are one contiguous byte range, so the partial
-// chunk where row r ends is the one where row r + 1 starts: the segment's
-// first block keeps each row's head chunk and its last block stores it
-// merged with the previous row's tail as one whole chunk; only the two ends
-// of the range, shared with other warps, go out byte by byte.  Where a
-// segment crosses a run's end (or has rows under 32 bytes), the partial
-// chunks there are clipped and stored as words and bytes.
-// No CTA barrier in the loop: the warps of a CTA are independent.  The 8
-// warps of a CTA take neighbouring feature blocks of the same run, so their
-// 16-byte row slices of the codes share one 128-byte line and their scale
-// bytes one sector: those loads are cached in L1, so a line leaves L2 once
-// per CTA rather than once per warp.
+//     rows x 8 token bytes of the warp's tile in shared memory: 32 rows of
+//     a 32-byte carry (the previous block's last 32 tokens) and the block's
+//     128 token bytes (rows 16 .. 31 start 64 bytes further on, so the two
+//     halves of the warp write different banks);
+//   - eight lanes per row store the row's whole sectors that this block
+//     completes, as 16-byte windows of the tile row; the row's last
+//     (partial) sector is left to the next block through the carry.
+// At a segment's first block a row's first, partial sector (it begins
+// with the end of the previous row) is skipped, and the row's first 32
+// bytes are kept as its head.  At the segment's last block, lane r stores
+// row r's last partial sector merged with the head of row r + 1 (the next
+// warp's row 0 for r = 31).  Only where a CTA's group of features begins
+// and ends do partial sectors go out byte by byte.
+// A unit that starts inside a segment first converts, without storing,
+// the block before its run (for the carry) and, if the segment ends within
+// the run, the segment's first block (for the heads).  Segments under 32
+// tokens are written byte by byte.
+// One CTA barrier per token block publishes a stage and frees the one read
+// before; a segment of one block adds one between its heads and merges.
 
 constexpr int kColThreads = 256;
-constexpr int kColRun = 32;      // token blocks per unit
-constexpr int kTileRow = 36;     // tile words per feature row: 4 carry words, 32 data words
+constexpr int kColGroup = kColThreads / 32;  // feature blocks per CTA: one per warp
+constexpr int kColRun = 32;                  // token blocks per unit
+constexpr int kStageCodes = 128 * 16 * kColGroup;  // code bytes of one stage
+constexpr int kStageBytes = kStageCodes + 128 * kColGroup;  // + scale bytes
+constexpr int kTileRow = 40;  // tile words per feature row: 8 carry words, 32 data words
+constexpr int kTileWords = 32 * kTileRow + 16;  // rows 16 .. 31 shifted by 16 words
+constexpr int kHeadWords = 32 * 8;              // heads: 32 rows x 32 bytes
+constexpr size_t kColSmem =
+    2 * (size_t)kStageBytes + kColGroup * (kTileWords + kHeadWords) * 4 + 128;
+
+// Row r of a warp's tile, as 10 16-byte chunks: 0-1 carry, 2-9 data.
+__device__ __forceinline__ uint4* tile_row(uint32_t* tile, int r) {
+  return reinterpret_cast<uint4*>(tile + r * kTileRow + (r >= 16 ? 16 : 0));
+}
 
 // Largest e in [0, nseg) with off[e] <= v, for off non-decreasing, off[0] = 0
 // <= v < off[nseg]: a 32-way search by one warp.
@@ -166,7 +190,7 @@ __device__ __forceinline__ int find_segment(const int64_t* __restrict__ off, int
   return lo;
 }
 
-// Bytes o .. o+15 (1 <= o <= 16) of the 32-byte sequence x[0..3] | y[0..3].
+// Bytes o .. o+15 (0 <= o <= 16) of the 32-byte sequence x[0..3] | y[0..3].
 __device__ __forceinline__ uint4 window16(uint4 x, uint4 y, uint32_t o) {
   uint32_t w0 = x.x, w1 = x.y, w2 = x.z, w3 = x.w, w4 = y.x, w5 = y.y, w6 = y.z, w7 = y.w;
   if (o & 16u) return y;
@@ -181,6 +205,27 @@ __device__ __forceinline__ uint4 window16(uint4 x, uint4 y, uint32_t o) {
                     __funnelshift_r(w2, w3, sh), __funnelshift_r(w3, w4, sh));
 }
 
+// Bytes o .. o+31 (0 <= o <= 32) of the 64-byte sequence w[0..15], into
+// r[0..7].
+__device__ __forceinline__ void window32(const uint32_t w[16], uint32_t o, uint32_t r[8]) {
+  if (o & 32u) {  // the second half, whole
+#pragma unroll
+    for (int k = 0; k < 8; ++k) r[k] = w[8 + k];
+    return;
+  }
+  // v[0..8] = w[(o >> 2) .. (o >> 2) + 8], by shifts of 4, 2 and 1 words
+  uint32_t v[12];
+#pragma unroll
+  for (int k = 0; k < 12; ++k) v[k] = (o & 16u) ? w[k + 4] : w[k];
+#pragma unroll
+  for (int k = 0; k < 10; ++k) v[k] = (o & 8u) ? v[k + 2] : v[k];
+#pragma unroll
+  for (int k = 0; k < 9; ++k) v[k] = (o & 4u) ? v[k + 1] : v[k];
+  const uint32_t sh = 8u * (o & 3u);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) r[k] = __funnelshift_r(v[k], v[k + 1], sh);
+}
+
 // 4 x 4 byte transpose: x[i] holds bytes (i, 0..3); y[j] receives (0..3, j).
 __device__ __forceinline__ void transpose4(const uint32_t x[4], uint32_t y[4]) {
   const uint32_t a0 = __byte_perm(x[0], x[1], 0x5140u), a1 = __byte_perm(x[0], x[1], 0x7362u);
@@ -191,27 +236,11 @@ __device__ __forceinline__ void transpose4(const uint32_t x[4], uint32_t y[4]) {
   y[3] = __byte_perm(a1, a3, 0x7632u);
 }
 
-// Bytes lo .. hi-1 (0 <= lo < hi <= 16) of the 16-byte value v to the
-// 16-byte aligned p: one 128-bit store when the chunk is whole, otherwise
-// the whole 32-bit words inside [lo, hi) as word stores and the bytes of
-// the (at most two) edge words as byte stores.
-__device__ __forceinline__ void store_chunk(uint8_t* p, uint4 v, int lo, int hi) {
-  if (lo == 0 && hi == 16) {
-    *reinterpret_cast<uint4*>(p) = v;
-    return;
-  }
-  const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    const int b0 = 4 * t;
-    if (lo <= b0 && b0 + 4 <= hi) {
-      reinterpret_cast<uint32_t*>(p)[t] = vw[t];
-    } else {
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (b0 + q >= lo && b0 + q < hi) p[b0 + q] = (uint8_t)(vw[t] >> (8 * q));
-    }
-  }
+// Bytes [t_lo, t_hi) of tile row `row` (byte x holds token t0 - 32 + x) to
+// dst[t - t_lo] one byte at a time.
+__device__ __forceinline__ void store_bytes(uint8_t* dst, const uint4* row, int x_lo, int x_hi) {
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(row);
+  for (int x = x_lo; x < x_hi; ++x) dst[x - x_lo] = (uint8_t)(w[x >> 2] >> (8 * (x & 3)));
 }
 
 // The segment holding a token block, walked forward block by block.
@@ -241,242 +270,287 @@ __device__ __forceinline__ bool seg_advance(SegPos& p, int64_t fb, int nseg,
   return fb < p.send;
 }
 
-// Codes (16 features) and scale bytes of a lane's 8 tokens of one block.
-struct ColIn {
-  uint2 w[8];
-  uint32_t s[8];
-};
+// cp.async of `n` (16 or 4) bytes, the first `valid` of them from global
+// memory and the rest zero (valid = 0: nothing is read).
+template <int n>
+__device__ __forceinline__ void cp_async_zfill(void* smem, const void* gmem, int valid) {
+  const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+  if (n == 16)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(valid)
+                 : "memory");
+  else
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(s), "l"(gmem), "r"(valid)
+                 : "memory");
+}
 
-__device__ __forceinline__ void col_issue(ColIn& in, const uint8_t* __restrict__ packed,
+// The whole CTA copies token block fb of segment p for feature blocks
+// 8grp .. 8grp + nkb - 1 into stage `stg`: codes (16-byte chunk q of token
+// t at chunk q ^ ((t >> 3) & 7) of row t), then scale bytes (token t's from
+// 8 * (16 * (t & 7) + (t >> 3)) on, so that the 16 tokens 8g + i, g = 0..15,
+// a warp reads at once sit in different banks).  Missing tokens and feature
+// blocks are zero.
+__device__ __forceinline__ void col_stage(uint8_t* stg, const uint8_t* __restrict__ packed,
                                           const uint8_t* __restrict__ scales, const SegPos& p,
-                                          int64_t fb, int64_t row_bytes, int64_t kblocks, int kb,
-                                          int g, int c) {
+                                          int64_t fb, int64_t row_bytes, int64_t kblocks, int grp,
+                                          int nkb) {
   const int64_t t0 = 128 * (fb - p.sofs);
-  const int64_t left = p.n_e - t0 - 8 * g;  // tokens of this lane's 8 that exist
-  const int64_t r = p.row0 + t0 + 8 * g;
-  const uint8_t* pw = packed + r * row_bytes + 16 * kb + 8 * c;
-  const uint8_t* ps = scales + r * kblocks + kb;
+  const int nv = p.n_e - t0 < 128 ? (int)(p.n_e - t0) : 128;
+  const int64_t r0 = p.row0 + t0;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const bool ok = i < left;
-    in.w[i] = ok ? ld_shared_v2(pw + i * row_bytes) : make_uint2(0u, 0u);
-    in.s[i] = ok ? ld_shared_u8(ps + i * kblocks) : 0u;
+  for (int k = 0; k < 128 * kColGroup / kColThreads; ++k) {
+    const int idx = (int)threadIdx.x + kColThreads * k;
+    const int t = idx >> 3, q = idx & 7;
+    const bool ok = t < nv && q < nkb;
+    const uint8_t* src = ok ? packed + (r0 + t) * row_bytes + 16 * (kColGroup * grp + q) : packed;
+    cp_async_zfill<16>(stg + 128 * t + 16 * (q ^ ((t >> 3) & 7)), src, ok ? 16 : 0);
+  }
+  {
+    // thread (i, g, h) = (tid >> 5, (tid >> 1) & 15, tid & 1): token 8g + i,
+    // feature blocks 4h .. 4h+3
+    const int i = (int)threadIdx.x >> 5, gg = ((int)threadIdx.x >> 1) & 15;
+    const int h = (int)threadIdx.x & 1;
+    const int t = 8 * gg + i;
+    const bool ok = t < nv && 4 * h < nkb;
+    const uint8_t* src = ok ? scales + (r0 + t) * kblocks + kColGroup * grp + 4 * h : scales;
+    cp_async_zfill<4>(stg + kStageCodes + 8 * (16 * i + gg) + 4 * h, src, ok ? 4 : 0);
   }
 }
 
-// Converts and writes one token block of one 32-feature block (see above).
-__device__ __forceinline__ void col_block(const ColIn& in, const SegPos& p, int64_t fb, bool carry,
-                                          bool run_end, bool merge, int64_t cols, int kb, int lane,
-                                          int g, int c, const uint2* lut2, uint32_t* tile,
-                                          uint4* heads, uint8_t* __restrict__ fp8_t,
-                                          float* __restrict__ fp8_t_scales) {
-  const int64_t b = fb - p.sofs;  // block inside the segment
-  const int64_t t0 = 128 * b;
-  const int nv = p.n_e - t0 < 128 ? (int)(p.n_e - t0) : 128;  // tokens in this block
-  uint32_t st = in.s[0];
+// Converts staged token block b of a segment into the warp's tile (feature
+// block kbl of the stage); returns S_t.  At the segment's first block it
+// also keeps each row's first 32 bytes in heads.
+__device__ __forceinline__ uint32_t col_convert(const uint8_t* stg, int kbl, int g, int c, int lane,
+                                                bool keep_heads, const uint2* lut2,
+                                                uint32_t* tile, uint4* heads) {
+  uint2 w[8];
+  uint32_t sc[8];
 #pragma unroll
-  for (int i = 1; i < 8; ++i) st = max(st, in.s[i]);
+  for (int i = 0; i < 8; ++i) {
+    const int t = 8 * g + i;
+    w[i] = *reinterpret_cast<const uint2*>(stg + 128 * t + 16 * (kbl ^ (g & 7)) + 8 * c);
+    sc[i] = stg[kStageCodes + 8 * (16 * i + g) + kbl];
+  }
+  uint32_t st = sc[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) st = max(st, sc[i]);
   st = __reduce_max_sync(0xFFFFFFFFu, st);
-  fp8_t_scales[cols * p.sofs + (32 * kb + lane) * (p.send - p.sofs) + b] = ue8m0_to_f32(st);
 
-  // Convert and transpose into the tile: row 16c + f, token bytes 8g .. 8g+7.
+  // Convert and transpose: row 16c + f gets token bytes 8g .. 8g+7 at data
+  // words 2g (tokens 8g .. 8g+3) and 2g + 1.
+  uint32_t y[2][4][4];  // y[h][k][j]: row 16c + 4k + j, tokens 8g+4h .. 8g+4h+3
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     uint32_t x[4][4];  // x[i][k]: token 4h+i, features 4k .. 4k+3
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      uint32_t d = st - in.s[4 * h + i];
+      uint32_t d = st - sc[4 * h + i];
       d = d > 15u ? 15u : d;
       const uint2 l = lut2[d];
-      convert8(in.w[4 * h + i].x, l, x[i][0], x[i][1]);
-      convert8(in.w[4 * h + i].y, l, x[i][2], x[i][3]);
+      convert8(w[4 * h + i].x, l, x[i][0], x[i][1]);
+      convert8(w[4 * h + i].y, l, x[i][2], x[i][3]);
     }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const uint32_t xi[4] = {x[0][k], x[1][k], x[2][k], x[3][k]};
-      uint32_t y[4];
-      transpose4(xi, y);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) tile[(16 * c + 4 * k + j) * kTileRow + 4 + 2 * g + h] = y[j];
+      transpose4(xi, y[h][k]);
     }
   }
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      reinterpret_cast<uint2*>(tile_row(tile, 16 * c + 4 * k + j))[4 + g] =
+          make_uint2(y[0][k][j], y[1][k][j]);
   __syncwarp();
-
-  // Store the 32 rows: row r of this block covers output bytes
-  // [D, D + nv), D = fp8_t + cols*row0 + (32kb + r)*n_e + t0.  A tile row
-  // holds 16 carry bytes (bytes 112..127 of the previous block of the
-  // segment) and then the block's 128 bytes.
-  uint8_t* const D0 = fp8_t + cols * p.row0 + 32 * kb * p.n_e + t0;
-  if (carry && !run_end) {
-    // every chunk whole: row r writes the aligned 16-byte chunks j = 0..7
-    // of [D - a, D - a + 128), a = D mod 16, lanes 8q + j of step i take
-    // row 4i + q
-    const int q = lane >> 3, j = lane & 7;
-#pragma unroll 4
-    for (int i = 0; i < 8; ++i) {
-      const int r = 4 * i + q;
-      uint8_t* const D = D0 + (int64_t)r * p.n_e;
-      const uint32_t a = (uint32_t)reinterpret_cast<uintptr_t>(D) & 15u;
-      const uint4* row = reinterpret_cast<const uint4*>(tile + r * kTileRow);  // row[0]: carry
-      reinterpret_cast<uint4*>(D - a)[j] = window16(row[j], row[j + 1], 16u - a);
-    }
-  } else if (merge) {
-    // first or last block of a segment whose rows are at least 32 bytes:
-    // the row's span in chunk coordinates u = x + a is [ulo, uhi); its
-    // whole chunks go out as above.  A row's partial head chunk (first
-    // block) is kept in heads[r]: the same 16 bytes hold the end of row
-    // r - 1, and the last block stores the two merged as one whole chunk.
-    // Only row 0's head and row 31's tail border other warps' rows; those
-    // bytes go out one at a time.
-    const int q = lane >> 3, j = lane & 7;
-#pragma unroll 4
-    for (int i = 0; i < 8; ++i) {
-      const int r = 4 * i + q;
-      uint8_t* const D = D0 + (int64_t)r * p.n_e;
-      const uint32_t a = (uint32_t)reinterpret_cast<uintptr_t>(D) & 15u;
-      const int ulo = carry ? 0 : (int)a;
-      const int uhi = run_end ? nv + (int)a : 128;
-      if (16 * j >= ulo && 16 * j + 16 <= uhi) {
-        const uint4* row = reinterpret_cast<const uint4*>(tile + r * kTileRow);  // row[0]: carry
-        reinterpret_cast<uint4*>(D - a)[j] = window16(row[j], row[j + 1], 16u - a);
-      }
-    }
-    uint8_t* const D = D0 + (int64_t)lane * p.n_e;
-    const uint32_t a = (uint32_t)reinterpret_cast<uintptr_t>(D) & 15u;
-    uint8_t* const G = D - a;  // byte u of the span is G[u]
-    const uint4* row = reinterpret_cast<const uint4*>(tile + lane * kTileRow);
-    if (!carry && a != 0u) {  // head chunk 0: bytes [a, 16) are this row's
-      const uint4 h = window16(row[0], row[1], 16u - a);
-      if (lane == 0) {
-        const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
-#pragma unroll
-        for (int m = 0; m < 16; ++m)
-          if (m >= (int)a) G[m] = (uint8_t)(hw[m >> 2] >> (8 * (m & 3)));
-      } else {
-        heads[lane] = h;
-      }
-    }
-    __syncwarp();
-    if (run_end) {
-      const int uhi = nv + (int)a;
-      const int kt = uhi >> 4, tl = uhi & 15;  // tail chunk kt: bytes [0, tl) are this row's
-      if (tl != 0) {
-        const uint4 nxt = kt < 8 ? row[kt + 1] : make_uint4(0u, 0u, 0u, 0u);
-        const uint4 t = window16(row[kt], nxt, 16u - a);
-        if (lane < 31) {
-          // the rest of the chunk is the head of row r + 1 (it starts at
-          // byte tl of this chunk): one whole chunk
-          const uint4 h = heads[lane + 1];
-          const uint32_t tw[4] = {t.x, t.y, t.z, t.w}, hw[4] = {h.x, h.y, h.z, h.w};
-          uint32_t mw[4];
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const int lo = tl - 4 * w;  // bytes of word w taken from the tail
-            const uint32_t keep = lo >= 4 ? 0xFFFFFFFFu : (lo <= 0 ? 0u : (1u << (8 * lo)) - 1u);
-            mw[w] = (tw[w] & keep) | (hw[w] & ~keep);
-          }
-          reinterpret_cast<uint4*>(G)[kt] = make_uint4(mw[0], mw[1], mw[2], mw[3]);
-        } else {
-          const uint32_t tw[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-          for (int m = 0; m < 16; ++m)
-            if (m < tl) G[16 * kt + m] = (uint8_t)(tw[m >> 2] >> (8 * (m & 3)));
-        }
-      }
-    }
-  } else {
-    // first or last block of a segment with rows shorter than 32 bytes: the
-    // same chunks (nine when the span ends past chunk 7), each clipped to
-    // the row bytes [lo, hi) this block writes
-    const int q = lane >> 3, j = lane & 7;
-    for (int i = 0; i < 8; ++i) {
-      const int r = 4 * i + q;
-      uint8_t* const D = D0 + (int64_t)r * p.n_e;
-      const int a = (int)(reinterpret_cast<uintptr_t>(D) & 15u);
-      const int lo = carry ? -a : 0;  // without carry the bytes before t0 are not ours
-      const int hi = run_end ? nv : 128 - a;
-      const uint4* row = reinterpret_cast<const uint4*>(tile + r * kTileRow);
-#pragma unroll
-      for (int k = j; k < 9; k += 8) {  // chunk k: row bytes [16k - a, 16k - a + 16)
-        const int c0 = 16 * k - a;
-        const int blo = lo - c0 > 0 ? lo - c0 : 0;
-        const int bhi = hi - c0 < 16 ? hi - c0 : 16;
-        if (blo < bhi) {
-          const uint4 nxt = k + 1 < 9 ? row[k + 1] : make_uint4(0u, 0u, 0u, 0u);
-          store_chunk(D - a + 16 * k, window16(row[k], nxt, 16u - (uint32_t)a), blo, bhi);
-        }
-      }
-    }
+  if (keep_heads) {
+    const uint4* row = tile_row(tile, lane);
+    heads[2 * lane] = row[2];
+    heads[2 * lane + 1] = row[3];
   }
-  __syncwarp();
-  if (!run_end) {  // carry: lane r copies row r's last 16 bytes
-    uint4* row = reinterpret_cast<uint4*>(tile + lane * kTileRow);
-    row[0] = row[8];
-  }
-  __syncwarp();
+  return st;
 }
 
-// The loads of the next token block are issued before the current one is
-// converted and written (two register buffers, swapped by unrolling).  A
-// segment that lies wholly inside the run (and has rows of 32 bytes or
-// more) merges its row ends; one that crosses the run's ends writes the
-// partial chunks there byte by byte.
+// Stores token block b of segment p from the warp's tile (rows
+// R_r = base + r * n_e, block bytes from R_r + t0).  first / last: b is the
+// segment's first / last block; own_head: this warp writes row 0's first
+// partial sector (it begins a CTA's feature group); next_head: the head of
+// the row after row 31 (null where that row is another CTA's: row 31's
+// last partial sector is then written byte by byte).
+__device__ __forceinline__ void col_store(uint32_t* tile, const uint4* heads,
+                                          const uint4* next_head, uint8_t* base, int64_t n_e,
+                                          int64_t t0, int nv, bool first, bool last, bool own_head,
+                                          int lane) {
+  if (n_e < 32) {
+    // a single block; rows too short for whole sectors: lane r writes row r
+    uint8_t* const R = base + (int64_t)lane * n_e;
+    store_bytes(R, tile_row(tile, lane), 32, 32 + nv);
+    return;
+  }
+  // whole sectors: row 4i + q, chunk j of [L', L' + 128), L' = A rounded
+  // down to a sector, A = R_r + t0
+  const int q = lane >> 3, j = lane & 7;
+#pragma unroll 4
+  for (int i = 0; i < 8; ++i) {
+    const int r = 4 * i + q;
+    uint8_t* const A = base + (int64_t)r * n_e + t0;
+    const uint32_t a = (uint32_t)reinterpret_cast<uintptr_t>(A) & 31u;
+    uint8_t* const Lp = A - a;
+    // sectors [lo, hi) of the window are this block's to write
+    const int lo = first && a != 0u ? 1 : 0;
+    const int hi = last ? (int)((a + (uint32_t)nv) >> 5) : 4;
+    const int s = j >> 1;
+    if (s >= lo && s < hi) {
+      const uint32_t off = 32u - a + 16u * (uint32_t)j;  // tile byte of the chunk's first byte
+      const uint32_t k = off >> 4;
+      const uint4* row = tile_row(tile, r);
+      reinterpret_cast<uint4*>(Lp)[j] = window16(row[k], row[k + 1 < 10 ? k + 1 : 9], off & 15u);
+    }
+  }
+  const uint4* row = tile_row(tile, lane);
+  if (first && own_head && lane == 0) {
+    // row 0's first partial sector: bytes [A, A rounded up to a sector)
+    const uint32_t a = (uint32_t)reinterpret_cast<uintptr_t>(base) & 31u;
+    if (a != 0u) store_bytes(base, row, 32, 32 + (int)(32u - a));
+  }
+  if (last) {
+    // row r's last partial sector [E - m, E), E = R_{r+1}, merged with the
+    // first 32 - m bytes of row r + 1
+    uint8_t* const E = base + (int64_t)(lane + 1) * n_e;
+    const uint32_t m = (uint32_t)reinterpret_cast<uintptr_t>(E) & 31u;
+    if (m != 0u) {
+      const uint4* h = lane < 31 ? heads + 2 * (lane + 1) : next_head;
+      if (h == nullptr) {
+        store_bytes(E - m, row, 32 + nv - (int)m, 32 + nv);
+      } else {
+        // W = tile bytes [nv, nv + 32): the row's last 32 tokens
+        const uint32_t k = (uint32_t)nv >> 4;
+        const uint4 c0 = row[k], c1 = row[k + 1], c2 = row[k + 2 < 10 ? k + 2 : 9];
+        const uint4 w0 = window16(c0, c1, (uint32_t)nv & 15u);
+        const uint4 w1 = window16(c1, c2, (uint32_t)nv & 15u);
+        const uint4 h0 = h[0], h1 = h[1];
+        const uint32_t seq[16] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w,
+                                  h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+        uint32_t rr[8];
+        window32(seq, 32u - m, rr);
+        uint4* const S = reinterpret_cast<uint4*>(E - m);
+        S[0] = make_uint4(rr[0], rr[1], rr[2], rr[3]);
+        S[1] = make_uint4(rr[4], rr[5], rr[6], rr[7]);
+      }
+    }
+  }
+}
+
+// Block converted by item `it` of a unit (see the kernel).
+__device__ __forceinline__ int64_t col_item_block(int64_t it, int npre, bool pre_head,
+                                                  const SegPos& p0, int64_t fb0) {
+  if (it < npre) return (pre_head && it == 0) ? p0.sofs : fb0 - 1;
+  return fb0 + (it - npre);
+}
+
+// Stages item `it` into stage it & 1 (nothing past the run or the offsets)
+// and commits its cp.async group; ps follows the staged blocks' segments.
+__device__ __forceinline__ void col_stage_item(
+    int64_t it, int npre, bool pre_head, const SegPos& p0, SegPos& ps, int64_t fb0, int64_t fb1,
+    uint8_t* stages, const uint8_t* __restrict__ packed, const uint8_t* __restrict__ scales,
+    int64_t row_bytes, int64_t kblocks, int grp, int nkb, int nseg,
+    const int64_t* __restrict__ row_off, const int64_t* __restrict__ scale_off) {
+  const int64_t fb = col_item_block(it, npre, pre_head, p0, fb0);
+  bool ok = fb < fb1;
+  if (ok && it >= npre) ok = seg_advance(ps, fb, nseg, row_off, scale_off);
+  if (ok)
+    col_stage(stages + (it & 1) * kStageBytes, packed, scales, it < npre ? SegPos(p0) : SegPos(ps),
+              fb, row_bytes, kblocks, grp, nkb);
+  cp_async_commit();
+}
+
+// A unit's token blocks, in order: up to two blocks that are only
+// converted (the first segment's block 0 for the heads, the block before
+// the run for the carry), then the run's blocks.  The CTA stages each block
+// one ahead (one cp.async group per block, committed even when empty).
 __global__ void __launch_bounds__(kColThreads)
     fp4_to_fp8_col_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ scales,
                           int64_t cols, const int64_t* __restrict__ seg_row_off,
                           const int64_t* __restrict__ seg_scale_off, int nseg, int64_t total_blocks,
                           int64_t nunits, uint8_t* __restrict__ fp8_t,
                           float* __restrict__ fp8_t_scales) {
-  __shared__ __align__(8) uint8_t lut[128];
-  __shared__ __align__(16) uint32_t tiles[kColThreads / 32][32 * kTileRow];
-  __shared__ uint4 head_tiles[kColThreads / 32][32];
+  extern __shared__ __align__(16) uint8_t col_smem[];
+  uint8_t* const stages = col_smem;
+  uint32_t* const tiles = reinterpret_cast<uint32_t*>(col_smem + 2 * kStageBytes);
+  uint4* const all_heads = reinterpret_cast<uint4*>(tiles + kColGroup * kTileWords);
+  uint8_t* const lut = col_smem + kColSmem - 128;
   build_shift_tables(lut);
-  __syncthreads();
   const uint2* lut2 = reinterpret_cast<const uint2*>(lut);
-  uint32_t* const tile = tiles[threadIdx.x >> 5];
-  uint4* const heads = head_tiles[threadIdx.x >> 5];
   const int lane = threadIdx.x & 31;
+  const int wid = threadIdx.x >> 5;
+  uint32_t* const tile = tiles + wid * kTileWords;
+  uint4* const heads = all_heads + wid * (kHeadWords / 4);
   const int g = lane >> 1;  // tokens 8g .. 8g+7 of a block
   const int c = lane & 1;   // features 16c .. 16c+15 of the feature block
   const int64_t kblocks = cols / 32;
   const int64_t row_bytes = cols / 2;
-  const int64_t nwarps = (int64_t)gridDim.x * (kColThreads / 32);
-  for (int64_t unit = (int64_t)blockIdx.x * (kColThreads / 32) + (threadIdx.x >> 5); unit < nunits;
-       unit += nwarps) {
-    const int64_t run = unit / kblocks;
-    const int kb = (int)(unit - run * kblocks);
+  const int64_t ngroups = (kblocks + kColGroup - 1) / kColGroup;
+  for (int64_t unit = blockIdx.x; unit < nunits; unit += gridDim.x) {
+    __syncthreads();  // the previous unit is done with the stages and heads; tables built
+    const int64_t run = unit / ngroups;
+    const int grp = (int)(unit - run * ngroups);
+    const int nkb = (int)(kblocks - kColGroup * grp < kColGroup ? kblocks - kColGroup * grp
+                                                                : kColGroup);
+    const int kb = kColGroup * grp + wid;
+    const bool active = wid < nkb;
     const int64_t fb0 = run * kColRun;
     const int64_t fb1 = fb0 + kColRun < total_blocks ? fb0 + kColRun : total_blocks;
-    SegPos pa;
-    pa.e = find_segment(seg_scale_off, nseg, fb0);
-    seg_load(pa, seg_row_off, seg_scale_off);
-    if (!seg_advance(pa, fb0, nseg, seg_row_off, seg_scale_off)) continue;
-    ColIn A, B;
-    col_issue(A, packed, scales, pa, fb0, row_bytes, kblocks, kb, g, c);
-    SegPos pb = pa;
-    for (int64_t fb = fb0;;) {
-      // A holds block fb (segment pa); fetch fb + 1 into B
-      bool next = fb + 1 < fb1;
-      pb = pa;
-      if (next) next = seg_advance(pb, fb + 1, nseg, seg_row_off, seg_scale_off);
-      if (next) col_issue(B, packed, scales, pb, fb + 1, row_bytes, kblocks, kb, g, c);
-      col_block(A, pa, fb, fb != fb0 && fb != pa.sofs, !next || fb + 1 == pa.send,
-                pa.sofs >= fb0 && pa.send <= fb1 && pa.n_e >= 32, cols, kb, lane, g, c, lut2, tile,
-                heads, fp8_t, fp8_t_scales);
-      if (!next) break;
-      ++fb;
-      // B holds block fb (segment pb); fetch fb + 1 into A
-      next = fb + 1 < fb1;
-      pa = pb;
-      if (next) next = seg_advance(pa, fb + 1, nseg, seg_row_off, seg_scale_off);
-      if (next) col_issue(A, packed, scales, pa, fb + 1, row_bytes, kblocks, kb, g, c);
-      col_block(B, pb, fb, fb != fb0 && fb != pb.sofs, !next || fb + 1 == pb.send,
-                pb.sofs >= fb0 && pb.send <= fb1 && pb.n_e >= 32, cols, kb, lane, g, c, lut2, tile,
-                heads, fp8_t, fp8_t_scales);
-      if (!next) break;
-      ++fb;
+    SegPos p0;
+    p0.e = find_segment(seg_scale_off, nseg, fb0);
+    seg_load(p0, seg_row_off, seg_scale_off);
+    if (!seg_advance(p0, fb0, nseg, seg_row_off, seg_scale_off)) continue;
+    const int64_t blo = fb0 - p0.sofs;  // the run's first block inside its first segment
+    const bool pre_head = blo > 1 && p0.send <= fb1 && p0.n_e >= 32;
+    const int npre = (pre_head ? 1 : 0) + (blo > 0 ? 1 : 0);
+    // item it converts block item_block(it) (items < npre are in segment p0)
+    SegPos ps = p0;  // segment of the next block to stage
+    col_stage_item(0, npre, pre_head, p0, ps, fb0, fb1, stages, packed, scales, row_bytes, kblocks,
+                   grp, nkb, nseg, seg_row_off, seg_scale_off);
+    SegPos p = p0;
+    for (int64_t it = 0;; ++it) {
+      cp_async_wait<0>();
+      __syncthreads();  // block it is staged; block it - 1 is read
+      col_stage_item(it + 1, npre, pre_head, p0, ps, fb0, fb1, stages, packed, scales, row_bytes,
+                     kblocks, grp, nkb, nseg, seg_row_off, seg_scale_off);
+      const bool real = it >= npre;
+      const int64_t fb = col_item_block(it, npre, pre_head, p0, fb0);
+      if (real && !seg_advance(p, fb, nseg, seg_row_off, seg_scale_off)) break;
+      const SegPos sp = real ? p : p0;
+      const int64_t b = fb - sp.sofs;
+      const int64_t t0 = 128 * b;
+      const int nv = sp.n_e - t0 < 128 ? (int)(sp.n_e - t0) : 128;
+      const bool first = b == 0, last = fb + 1 == sp.send;
+      const uint8_t* const stg = stages + (it & 1) * kStageBytes;
+      if (active) {
+        const uint32_t st = col_convert(stg, wid, g, c, lane, first && sp.n_e >= 32, lut2, tile,
+                                        heads);
+        if (real)
+          fp8_t_scales[cols * sp.sofs + (32 * kb + lane) * (sp.send - sp.sofs) + b] =
+              ue8m0_to_f32(st);
+      }
+      // heads kept at this very block must be visible to the warp before
+      // (heads of an earlier block are, through the barrier above)
+      if (real && last && first && sp.n_e >= 32) __syncthreads();
+      if (active && real) {
+        uint8_t* const base = fp8_t + cols * sp.row0 + 32 * kb * sp.n_e;
+        const uint4* next_head = wid + 1 < nkb ? all_heads + (wid + 1) * (kHeadWords / 4) : nullptr;
+        col_store(tile, heads, next_head, base, sp.n_e, t0, nv, first, last, wid == 0, lane);
+      }
+      if (active) {
+        __syncwarp();
+        uint4* row = tile_row(tile, lane);  // carry: the block's last 32 bytes
+        row[0] = row[8];
+        row[1] = row[9];
+        __syncwarp();
+      }
+      if (real && fb + 1 >= fb1) break;
     }
   }
+  cp_async_wait<0>();
 }
 
 }  // namespace
@@ -512,11 +586,15 @@ fp4_status fp4_to_fp8_col(const uint8_t* packed, const uint8_t* scales, int64_t 
       !aligned(seg_row_off, 8) || !aligned(seg_scale_off, 8))
     return FP4_ERR_ALIGN;
   if (ntiles == 0 || num_segments == 0) return FP4_OK;
-  // one warp per (run of kColRun token blocks, 32-feature block)
-  const int64_t nunits = (total_blocks + kColRun - 1) / kColRun * (cols / 32);
-  return launch<fp4_to_fp8_col_kernel>(nunits * 32, kColThreads, 0, as_stream(stream), packed,
-                                       scales, cols, seg_row_off, seg_scale_off, num_segments,
-                                       total_blocks, nunits, fp8_t, fp8_t_scales);
+  // one CTA per (run of kColRun token blocks, group of kColGroup 32-feature blocks)
+  const int64_t kblocks = cols / 32;
+  const int64_t nunits =
+      (total_blocks + kColRun - 1) / kColRun * ((kblocks + kColGroup - 1) / kColGroup);
+  if (!allow_dynamic_smem<fp4_to_fp8_col_kernel>(kColSmem)) return FP4_ERR_CUDA;
+  return launch<fp4_to_fp8_col_kernel>(nunits * kColThreads, kColThreads, kColSmem,
+                                       as_stream(stream), packed, scales, cols, seg_row_off,
+                                       seg_scale_off, num_segments, total_blocks, nunits, fp8_t,
+                                       fp8_t_scales);
 }
 
 }  // extern "C"
