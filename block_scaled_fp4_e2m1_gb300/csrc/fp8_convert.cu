@@ -161,7 +161,10 @@ constexpr int kColGroup = kColThreads / 32;  // feature blocks per CTA: one per 
 constexpr int kColRun = 32;                  // token blocks per unit
 constexpr int kStageCodes = 128 * 16 * kColGroup;  // code bytes of one stage
 constexpr int kStageBytes = kStageCodes + 128 * kColGroup;  // + scale bytes
-constexpr int kTileRow = 40;  // tile words per feature row: 8 carry words, 32 data words
+// tile words per feature row: 8 carry words, 32 data words, 4 words of
+// padding (a pitch of 44 words puts 8 consecutive rows' 16-byte chunks in
+// different banks)
+constexpr int kTileRow = 44;
 constexpr int kTileWords = 32 * kTileRow + 16;  // rows 16 .. 31 shifted by 16 words
 constexpr int kHeadWords = 32 * 8;              // heads: 32 rows x 32 bytes
 constexpr size_t kColSmem =
