@@ -140,8 +140,8 @@ __global__ void __launch_bounds__(kRowThreads)
 //     a 32-byte carry (the previous block's last 32 tokens) and the block's
 //     128 token bytes (rows 16 .. 31 start 64 bytes further on, so the two
 //     halves of the warp write different banks);
-//   - eight lanes per row store the row's whole sectors that this block
-//     completes, as 16-byte windows of the tile row; the row's last
+//   - four lanes per row store the row's whole sectors that this block
+//     completes, each a 32-byte window of the tile row; the row's last
 //     (partial) sector is left to the next block through the carry.
 // At a segment's first block a row's first, partial sector (it begins
 // with the end of the previous row) is skipped, and the row's first 32
@@ -227,6 +227,20 @@ __device__ __forceinline__ void window32(const uint32_t w[16], uint32_t o, uint3
   const uint32_t sh = 8u * (o & 3u);
 #pragma unroll
   for (int k = 0; k < 8; ++k) r[k] = __funnelshift_r(v[k], v[k + 1], sh);
+}
+
+// Bytes o .. o+31 (0 <= o < 16) of the 48-byte sequence x | y | z.
+__device__ __forceinline__ U32x8 window32x(uint4 x, uint4 y, uint4 z, uint32_t o) {
+  uint32_t v[12] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w, z.x, z.y, z.z, z.w};
+#pragma unroll
+  for (int k = 0; k < 10; ++k) v[k] = (o & 8u) ? v[k + 2] : v[k];
+#pragma unroll
+  for (int k = 0; k < 9; ++k) v[k] = (o & 4u) ? v[k + 1] : v[k];
+  const uint32_t sh = 8u * (o & 3u);
+  U32x8 r;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) r.w[k] = __funnelshift_r(v[k], v[k + 1], sh);
+  return r;
 }
 
 // 4 x 4 byte transpose: x[i] holds bytes (i, 0..3); y[j] receives (0..3, j).
@@ -389,24 +403,24 @@ __device__ __forceinline__ void col_store(uint32_t* tile, const uint4* heads,
     store_bytes(R, tile_row(tile, lane), 32, 32 + nv);
     return;
   }
-  // whole sectors: row 4i + q, chunk j of [L', L' + 128), L' = A rounded
-  // down to a sector, A = R_r + t0
-  const int q = lane >> 3, j = lane & 7;
-#pragma unroll 4
-  for (int i = 0; i < 8; ++i) {
-    const int r = 4 * i + q;
+  // whole sectors: lane (q, s) = (lane >> 2, lane & 3) takes sector s of
+  // [L', L' + 128) of row 8i + q, L' = A rounded down to a sector,
+  // A = R_r + t0, as one 32-byte store
+  const int q = lane >> 2, s = lane & 3;
+#pragma unroll 2
+  for (int i = 0; i < 4; ++i) {
+    const int r = 8 * i + q;
     uint8_t* const A = base + (int64_t)r * n_e + t0;
     const uint32_t a = (uint32_t)reinterpret_cast<uintptr_t>(A) & 31u;
-    uint8_t* const Lp = A - a;
     // sectors [lo, hi) of the window are this block's to write
     const int lo = first && a != 0u ? 1 : 0;
     const int hi = last ? (int)((a + (uint32_t)nv) >> 5) : 4;
-    const int s = j >> 1;
     if (s >= lo && s < hi) {
-      const uint32_t off = 32u - a + 16u * (uint32_t)j;  // tile byte of the chunk's first byte
+      const uint32_t off = 32u - a + 32u * (uint32_t)s;  // tile byte of the sector's first byte
       const uint32_t k = off >> 4;
       const uint4* row = tile_row(tile, r);
-      reinterpret_cast<uint4*>(Lp)[j] = window16(row[k], row[k + 1 < 10 ? k + 1 : 9], off & 15u);
+      st_v8(A - a + 32 * s,
+            window32x(row[k], row[k + 1 < 10 ? k + 1 : 9], row[k + 2 < 10 ? k + 2 : 9], off & 15u));
     }
   }
   const uint4* row = tile_row(tile, lane);
