@@ -257,3 +257,44 @@ def test_moe_workload_full_size_sampled():
         nb = (n_e + 127) // 128
         gs = to_f32_np(fts[H * int(so[e]):H * (int(so[e]) + nb)]).reshape(H, nb)
         assert_bits_equal(gs, wsc, f"col scales segment {e}")
+
+
+# Segment layouts aimed at the column kernel's units of 32 token blocks
+# (blocks are numbered across segments, ceil(n_e / 128) per segment):
+#   - a segment that starts on a run's last block, so the next run begins
+#     one block into it (that run first converts the segment's block 0, for
+#     the carry and the row heads);
+#   - one that starts two blocks before a run's end and ends inside the next
+#     run (the next run converts block 0 for the heads and the block before
+#     it for the carry);
+#   - long segments across several runs; one-block segments of 31, 32, 33,
+#     127, 128 and 129 tokens; empty segments between them.
+RUN_LAYOUTS = [
+    [31 * 128, 128 + 50, 7],
+    [30 * 128, 3 * 128 + 5, 33, 0, 32],
+    [29 * 128 + 1, 70 * 128 + 77, 31, 129],
+    [127, 128, 129, 0, 31, 32, 33, 28 * 128 - 3, 40 * 128, 1, 300],
+    [5000, 6000, 0, 4096, 4095, 4097],
+]
+
+
+@pytest.mark.parametrize("sizes", RUN_LAYOUTS)
+@pytest.mark.parametrize("cols", [128, 384, 512])
+@pytest.mark.parametrize("shift", [0, 13])
+def test_fp4_to_fp8_col_run_boundaries(sizes, cols, shift):
+    m = fp4()
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    R = int(off[-1])
+    rng = np.random.default_rng(R + cols + shift)
+    packed = rng.integers(0, 256, (R, cols // 2), dtype=np.uint8)
+    scales = rng.integers(110, 140, (R, cols // 32), dtype=np.uint8)
+    segs = m.Segments(torch.from_numpy(off), dev())
+    pk = torch.from_numpy(packed).to(dev())
+    sc = torch.from_numpy(scales).to(dev())
+    out = torch.full((cols * R + 96,), 0xA5, dtype=torch.uint8, device=dev())
+    n = cols * R
+    m.fp4_to_fp8_col(pk, sc, segs, out[32 + shift:32 + shift + n])
+    wo, _ = ora.fp4_to_fp8_col(packed, scales, off)
+    o = u8(out)
+    assert np.all(o[:32 + shift] == 0xA5) and np.all(o[32 + shift + n:] == 0xA5)
+    assert_bits_equal(o[32 + shift:32 + shift + n], wo, f"fp8_t {sizes[:3]} {cols}")
