@@ -587,14 +587,21 @@ struct BlockedStep {
   uint32_t rr, c, cols;    // stride rows % 128, stride columns, cols
 };
 
+// a / d for a >= 0, d > 0; by 32-bit division when both fit (every weight
+// matrix of the workloads), the 64-bit form costing several times more.
+__device__ __forceinline__ int64_t div_nonneg(int64_t a, int64_t d) {
+  if (((a | d) >> 32) == 0) return (int64_t)((uint32_t)a / (uint32_t)d);
+  return a / d;
+}
+
 __device__ __forceinline__ BlockedCursor blocked_cursor(int64_t b, const BlockedMap& bm) {
-  const int64_t row = b / bm.cols;
+  const int64_t row = div_nonneg(b, bm.cols);
   return BlockedCursor{(row >> 7) * bm.col_tiles * 512, (uint32_t)(row & 127),
                        (uint32_t)(b - row * bm.cols)};
 }
 
 __device__ __forceinline__ BlockedStep blocked_step(int64_t stride, const BlockedMap& bm) {
-  const int64_t rows = stride / bm.cols;
+  const int64_t rows = div_nonneg(stride, bm.cols);
   return BlockedStep{(rows >> 7) * bm.col_tiles * 512, bm.col_tiles * 512,
                      (uint32_t)(rows & 127), (uint32_t)(stride - rows * bm.cols),
                      (uint32_t)bm.cols};
