@@ -74,31 +74,10 @@ __device__ __forceinline__ uint32_t ld_stream_u8(const void* p) {
   return r;
 }
 
-// Read-only loads cached in L1, for data that neighbouring warps of the CTA
-// read too (a line is fetched from L2 once per CTA instead of once per warp).
-__device__ __forceinline__ uint2 ld_shared_v2(const void* p) {
-  uint2 r;
-  asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t ld_shared_u8(const void* p) {
-  uint32_t r;
-  asm volatile("ld.global.nc.u8 %0, [%1];" : "=r"(r) : "l"(p));
-  return r;
-}
-
 // ---------------------------------------------------- asynchronous staging
 //
-// Streaming kernels keep several units of input per thread in flight by
-// copying them into shared memory with cp.async (16-byte copies that bypass
-// L1) a few units ahead of use.  Each thread only reads back what it copied
-// itself, so cp.async.wait_group is the only wait: no barrier, no spin loop.
-
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
-}
+// Group bookkeeping of cp.async copies into shared memory (the copies
+// themselves are issued where they are used).
 
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
@@ -108,19 +87,6 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
-
-// Ring of kStages slots of kPieces 16-byte pieces per thread in dynamic
-// shared memory; piece p of slot s of thread t is at
-// base[(s * kPieces + p) * kThreads + t], so each (slot, piece) is one
-// contiguous, conflict-free row of 16-byte words across the CTA.
-template <int kPieces, int kStages, int kThreads>
-struct StageRing {
-  static constexpr size_t kBytes = (size_t)kStages * kPieces * kThreads * 16;
-  uint4* base;
-  __device__ __forceinline__ uint4* at(int slot, int piece) const {
-    return base + (slot * kPieces + piece) * kThreads + threadIdx.x;
-  }
-};
 
 // ------------------------------------------------------ packed fp32 pairs
 //

@@ -31,26 +31,6 @@ __device__ __forceinline__ float tensor_scale_from_amax(float amax) {
   return sanitize_scale(__fdiv_rn(amax, 2688.0f));  // 6 * 448
 }
 
-template <bool kBF16>
-__device__ __forceinline__ void load_block(const void* x, int64_t b, float v[16]) {
-  if (kBF16) {
-    U32x8 r = ld_stream_v8(static_cast<const uint16_t*>(x) + 16 * b);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      v[2 * i] = bf16_lo(r.w[i]);
-      v[2 * i + 1] = bf16_hi(r.w[i]);
-    }
-  } else {
-    const float* p = static_cast<const float*>(x) + 16 * b;
-    U32x8 a = ld_stream_v8(p), c = ld_stream_v8(p + 8);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      v[i] = __uint_as_float(a.w[i]);
-      v[8 + i] = __uint_as_float(c.w[i]);
-    }
-  }
-}
-
 __device__ __forceinline__ void load_f32x16(const float* p, float v[16]) {
   U32x8 a = ld_v8(p), c = ld_v8(p + 8);
 #pragma unroll
@@ -258,21 +238,6 @@ __device__ __forceinline__ uint32_t settle_e2m1(float x, float eff, uint32_t cl,
     return (cl & 8u) | settle_midpoint(fabsf(x), eff, M, ml, ml + 1u);
   }
   return exact_e2m1_quotient(x, eff);
-}
-
-// One element under round-to-nearest: the code the fast path stores for it
-// (the lower bracket code) and its exact code.
-__device__ __forceinline__ void rtn_element(float x, float eff, uint32_t& stored, uint32_t& code) {
-  const Bracket k = make_bracket(eff);
-  const uint32_t c2 = cvt_e2m1x2(__fmul_rn(x, k.il), __fmul_rn(x, k.ih));
-  stored = c2 & 0xFu;
-  const uint32_t ch = c2 >> 4;
-  if (!bracket_certified(eff))  // the two bracket codes prove nothing here
-    code = exact_e2m1_quotient(x, eff);
-  else if (eff == 0.0f || stored == ch)
-    code = stored;
-  else
-    code = settle_e2m1(x, eff, stored, ch);
 }
 
 // Quantize one block v[16] (residual already added) under tensor scale s_t.
