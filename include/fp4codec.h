@@ -351,7 +351,12 @@ fp4_status fp4_to_fp8_row(const uint8_t* packed, const uint8_t* scales, int64_t 
  *   packed [total_rows, cols/2], scales [total_rows, cols/32] (as the row form)
  *   seg_row_off, seg_scale_off  device int64 [num_segments + 1]
  *   total_blocks  = seg_scale_off[num_segments] (host copy, sizes the grid)
- *   cols % 128 == 0.  Offsets are trusted: the device reads them as given. */
+ *   cols % 128 == 0.  Offsets are trusted: the device reads them as given.
+ * Alignment: packed 32 bytes, scales and fp8_t_scales 4, the offsets 8;
+ * fp8_t may start at any byte (the kernel stores whole 32-byte sectors and
+ * writes only the partial sectors at its ends byte by byte).  FP4_ERR_ALIGN
+ * otherwise; FP4_ERR_CUDA if the launch fails (it uses about 89 KB of
+ * shared memory per CTA). */
 fp4_status fp4_to_fp8_col(const uint8_t* packed, const uint8_t* scales, int64_t cols,
                           const int64_t* seg_row_off, const int64_t* seg_scale_off,
                           int32_t num_segments, int64_t total_rows, int64_t total_blocks,
