@@ -233,3 +233,43 @@ def test_batched_blocked_matches_single_calls(rounding, dtype):
     assert np.float32(ts[5].item()) == np.float32(wt)
     assert_bits_equal(u8(pks[5]), wp, "oracle packed")
     assert_bits_equal(u8(blks[5]), ora.scales_to_blocked(ws, r, k // 16), "oracle blocked")
+
+
+@pytest.mark.parametrize("mode", ["given", "from_amax"])
+def test_batched_blocked_tensor_scale_modes(mode):
+    """The other two tensor-scale modes of the batched blocked quantize.
+    given: per-tensor scales from the caller, among them 0 and NaN, which
+    both quantizers replace by 1 (reading R6); from_amax: the scales follow
+    from a preceding nvfp4_amax_batched.  Each tensor equals
+    nvfp4_quantize_blocked on it under the same mode and scale."""
+    m = fp4()
+    shapes = [(256, 256), (130, 48), (64, 1024), (3, 16)]
+    xs = [_inputs(r, k, torch.bfloat16, seed=70 + i).to(dev()) for i, (r, k) in enumerate(shapes)]
+    pks = [torch.empty(r * k // 2, dtype=torch.uint8, device=dev()) for r, k in shapes]
+    blks = [torch.empty(m.fp4_blocked_scales_size(r, k // 16), dtype=torch.uint8, device=dev())
+            for r, k in shapes]
+    batch = m.Batch(xs=[x.view(-1) for x in xs], packed=pks, scales=blks,
+                    ks=[k for _, k in shapes])
+    if mode == "given":
+        given = [0.003, 0.0, float("nan"), 17.5]
+        ts = torch.tensor(given, dtype=torch.float32, device=dev())
+        m.nvfp4_quantize_batched_blocked(batch, torch.bfloat16, tscale="given", tensor_scale=ts)
+        singles = [m.nvfp4_quantize_blocked(x, tscale="given",
+                                            tensor_scale=torch.tensor([g], dtype=torch.float32,
+                                                                      device=dev()))
+                   for x, g in zip(xs, given)]
+    else:
+        amax = m.nvfp4_amax_batched(batch, torch.bfloat16)
+        ts = m.nvfp4_quantize_batched_blocked(batch, torch.bfloat16, tscale="from_amax",
+                                              amax=amax)
+        singles = []
+        for i, x in enumerate(xs):
+            a1 = torch.zeros(1, dtype=torch.float32, device=dev())
+            m.nvfp4_amax(x.view(-1), amax_ws=a1)
+            assert a1.item() == amax[i].item(), i
+            singles.append(m.nvfp4_quantize_blocked(x, tscale="from_amax", amax_ws=a1))
+    for i, (p1, b1, t1) in enumerate(singles):
+        if mode != "given":
+            assert ts[i].item() == t1.item(), i
+        assert_bits_equal(u8(pks[i]), u8(p1).reshape(-1), f"packed {i}")
+        assert_bits_equal(u8(blks[i]), u8(b1), f"blocked {i}")
