@@ -118,8 +118,9 @@ __global__ void __launch_bounds__(kRowThreads)
 // feature f's n_e E4M3 bytes at fp8_t + cols * row0 + f * n_e.  Rows start
 // at arbitrary byte offsets, so the stores are organised around 32-byte
 // sectors: every store covers whole sectors, and a sector shared by two
-// rows is written once, merged.  (Measured: stores that leave sectors
-// half written cost the kernel a third of its time.)
+// rows is written once, merged.  (Measured: the same 16-byte stores ran
+// 14% faster when moved to 32-byte alignment, where they no longer left
+// sectors half written.)
 //
 // Work unit: one CTA converts a group of up to eight 32-feature blocks (one
 // MXFP4 scale column each, one per warp) over a run of up to kColRun
