@@ -22,6 +22,11 @@ int ora_mxfp4_quantize_row(const float* x, int64_t cols, uint8_t* packed,
     int E;
     if (bmax == 0.0f) {
       E = -127;
+    } else if (isinf(bmax)) {
+      /* the exponent field of an infinite amax is 255: floor(log2) read
+       * from it is 128 (frexpf leaves the exponent of an infinity
+       * unspecified); the infinite elements then saturate to +-6 */
+      E = 128 - 2;
     } else {
       int e2;
       frexpf(bmax, &e2);       /* bmax = f * 2^e2, f in [0.5, 1) */

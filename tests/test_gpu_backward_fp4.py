@@ -75,3 +75,49 @@ def test_backward_exchange_on_moe_shapes():
     assert_bits_equal(u8(p2), wp2, "packed")
     assert_bits_equal(u8(s2), ws2, "scales")
     assert_bits_equal(bf16_bits(y), ora.bf16_rn(ora.mxfp4_dequantize(wp2, ws2)), "y")
+
+
+def test_fp8_to_fp4_row_extreme_scales():
+    """FP8 -> MXFP4 where the products leave the normal range: per-128 scales
+    from the smallest subnormal up to the largest float, so that
+    e4m3 * scale underflows to subnormals or zero, or overflows to infinity
+    (which the MXFP4 rule saturates to +-6 under its largest exponent); also
+    all-zero blocks, blocks of -0 bytes and single-value blocks."""
+    m = fp4()
+    rows, cols = 48, 512
+    rng = np.random.default_rng(77)
+    b = rng.integers(0, 256, (rows, cols)).astype(np.uint8)
+    b[(b & 0x7F) == 0x7F] = 0x3C                       # no NaN bytes
+    b[0, :32] = 0
+    b[1, :32] = 0x80                                    # -0
+    b[2, :32] = 0
+    b[2, 5] = 0x7E                                      # 448 alone
+    b[3, 32:64] = 0xFE                                  # -448 everywhere
+    ext = np.array([2.0 ** -149, 2.0 ** -140, 2.0 ** -126, 1e-30, 1.0, 2.0 ** 60, 2.0 ** 100,
+                    2.0 ** 120, 2.0 ** 126, 2.0 ** 127, 3.4e38, 0.75 * 2.0 ** -133],
+                   dtype=np.float32)
+    s = ext[rng.integers(0, ext.size, (rows, cols // 128))]
+    pk, sc = m.fp8_to_fp4_row(torch.from_numpy(b).to(dev()), torch.from_numpy(s).to(dev()))
+    wp, ws = ora.fp8_to_fp4_row(b, s)
+    assert_bits_equal(u8(sc), ws, "scales")
+    assert_bits_equal(u8(pk), wp, "packed")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_mxfp4_quantize_infinite_inputs(dtype):
+    """mxfp4_quantize on blocks holding +-infinity beside finite values and
+    beside blocks without one: the same rule as the oracle (exponent from
+    the amax's exponent field, infinities saturated to +-6)."""
+    m = fp4()
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((16, 256)).astype(np.float32)
+    x[0, 3] = np.inf
+    x[1, 40] = -np.inf
+    x[2, :32] = np.inf
+    x[3, 100] = np.inf
+    x[3, 101] = -np.inf
+    xt = torch.from_numpy(x).to(dtype)
+    pk, sc = m.mxfp4_quantize(xt.to(dev()))
+    wp, ws = ora.mxfp4_quantize(to_f32_np(xt))
+    assert_bits_equal(u8(sc), ws, "scales")
+    assert_bits_equal(u8(pk), wp, "packed")

@@ -48,6 +48,26 @@ def test_mxfp4_zero_and_tiny_blocks():
     assert codes[33] == 0x8                              # sign of -0 kept
 
 
+def test_mxfp4_infinite_amax():
+    """A block holding an infinity: the exponent is read from the amax's
+    exponent field (reading R15), 255 for an infinity, so floor(log2) is 128,
+    E = 126 and the UE8M0 byte 253; the infinities saturate to +-6 (R2,
+    code 7 with the sign) and the finite elements, scaled by 2^-126, round
+    to zero.  A block of finite values beside it keeps its own exponent."""
+    x = np.zeros((1, 64), np.float32)
+    x[0, :32] = np.linspace(-3.0, 3.0, 32, dtype=np.float32)
+    x[0, 3] = np.inf
+    x[0, 9] = -np.inf
+    x[0, 32:] = 1.5
+    packed, scales = ora.mxfp4_quantize(x)
+    assert scales[0, 0] == 126 + 127 and scales[0, 1] == 0 - 2 + 127
+    codes = np.stack([packed & 0xF, packed >> 4], axis=-1).reshape(-1)
+    assert codes[3] == 0x7 and codes[9] == 0xF
+    finite = np.r_[0:3, 4:9, 10:32]
+    assert np.all((codes[finite] & 0x7) == 0)
+    assert np.all(codes[32:] == ora.e2m1_rn(np.full(32, 1.5 * 4.0, np.float32)))
+
+
 def _brute_e4m3(val: float) -> int:
     table = ora.e4m3_value(np.arange(256))
     fin = np.nonzero(~np.isnan(table))[0]
