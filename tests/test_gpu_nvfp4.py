@@ -152,6 +152,40 @@ def test_degenerate_blocks():
         assert_bits_equal(to_f32_np(y), ora.nvfp4_dequantize(wp, ws, wt, x.size), "dequant")
 
 
+@pytest.mark.parametrize("rounding", ["rtn", "sr"])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_infinite_inputs(rounding, dtype):
+    """Blocks holding +-infinity among finite values, and blocks without
+    one.  COMPUTE mode: the amax is infinite, so the tensor scale falls back
+    to 1; GIVEN mode: a finite scale.  The block amax saturates the e4m3
+    scale to 448, infinities encode as +-6 and the finite values beside them
+    shrink; the other blocks are untouched.  Codes, scales and the
+    dequantized values equal the oracle's."""
+    m = fp4()
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal(16 * 64) * 0.5).astype(np.float32)
+    x[3] = np.inf
+    x[16 * 5 + 7] = -np.inf
+    x[16 * 9:16 * 10] = np.inf
+    x[16 * 20 + 1] = np.inf
+    x[16 * 20 + 2] = -np.inf
+    xt = torch.from_numpy(x).to(dtype)
+    xn = to_f32_np(xt)
+    for mode, s_t in (("compute", 1.0), ("given", 0.01)):
+        ts = torch.tensor([s_t], dtype=torch.float32, device=dev())
+        packed, scales, tso = m.nvfp4_quantize(xt.to(dev()), rounding=rounding, seed=4, step=2,
+                                               tscale=mode, tensor_scale=ts)
+        wp, ws, wt = ora.nvfp4_quantize(xn, rounding=ora.SR if rounding == "sr" else ora.RTN,
+                                        seed=4, step=2,
+                                        tscale_mode=ora.TSCALE_COMPUTE if mode == "compute"
+                                        else ora.TSCALE_GIVEN, tensor_scale=s_t)
+        assert np.float32(tso.item()) == np.float32(wt), mode
+        assert_bits_equal(u8(scales), ws, f"scales {mode}")
+        assert_bits_equal(u8(packed), wp, f"packed {mode}")
+        y = m.nvfp4_dequantize(packed, scales, tso, (x.size,))
+        assert_bits_equal(to_f32_np(y), ora.nvfp4_dequantize(wp, ws, wt, x.size), f"y {mode}")
+
+
 def test_empty_tensor_publishes_unit_scale():
     m = fp4()
     x = torch.empty(0, dtype=torch.float32, device=dev())
