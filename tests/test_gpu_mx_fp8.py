@@ -298,3 +298,31 @@ def test_fp4_to_fp8_col_run_boundaries(sizes, cols, shift):
     o = u8(out)
     assert np.all(o[:32 + shift] == 0xA5) and np.all(o[32 + shift + n:] == 0xA5)
     assert_bits_equal(o[32 + shift:32 + shift + n], wo, f"fp8_t {sizes[:3]} {cols}")
+
+
+@pytest.mark.parametrize("cols", [128, 384])
+def test_fp4_to_fp8_full_range_scales(cols):
+    """Row and column FP4 -> FP8 with UE8M0 bytes over their whole range
+    0..255 (one block in eight at 0 or 255): shifts S_t - S_sub past 13 give
+    zeros, and the fp32 output scales reach 2^-127 (subnormal) and 2^128
+    (infinity).  Both forms against the oracle, bit for bit."""
+    m = fp4()
+    sizes = [300, 129, 0, 40, 1000]
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    R = int(off[-1])
+    rng = np.random.default_rng(cols + 3)
+    packed = rng.integers(0, 256, (R, cols // 2), dtype=np.uint8)
+    scales = rng.integers(0, 256, (R, cols // 32), dtype=np.uint8)
+    scales[rng.random(scales.shape) < 0.06] = 0
+    scales[rng.random(scales.shape) < 0.06] = 255
+    pk = torch.from_numpy(packed).to(dev())
+    sc = torch.from_numpy(scales).to(dev())
+    f8, f8s = m.fp4_to_fp8_row(pk, sc)
+    wo, wsc = ora.fp4_to_fp8_row(packed, scales)
+    assert_bits_equal(u8(f8), wo, "row fp8")
+    assert_bits_equal(to_f32_np(f8s), wsc, "row scales")
+    segs = m.Segments(torch.from_numpy(off), dev())
+    ft, fts = m.fp4_to_fp8_col(pk, sc, segs)
+    wo, wsc = ora.fp4_to_fp8_col(packed, scales, off)
+    assert_bits_equal(u8(ft), wo, "col fp8")
+    assert_bits_equal(to_f32_np(fts), wsc, "col scales")
