@@ -74,3 +74,38 @@ def test_activation_workload_full_size_sampled(G):
     assert_bits_equal(u8(packed[rows]), wp, "packed")
     wy = ora.fp4quant_decode(wp, w1, w2, G)
     assert_bits_equal(bf16_bits(y[rows]), ora.bf16_rn(wy), "decoded")
+
+
+@pytest.mark.parametrize("G", [64, 128, 256])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_groups_at_the_fp32_range_ends(G, out_dtype):
+    """Groups whose sum of squares leaves the fp32 range: values near 2^64
+    overflow it (RMS infinite, reciprocal 0, every transformed value 0, and
+    the decode's 0 * infinity is NaN), values near 2^-64 underflow it (RMS
+    0, the same zero path, decoding to zeros), and groups just inside both
+    ends.  Codes and scales must match the oracle bit for bit; decoded
+    values too, except that a NaN only has to be a NaN (its payload is not
+    fixed)."""
+    m = fp4()
+    rng = np.random.default_rng(G)
+    x = rng.standard_normal((6, 2 * G)).astype(np.float32)
+    x[0, :G] *= np.float32(2.0 ** 64)          # squares overflow
+    x[1, G:] *= np.float32(2.0 ** 60)          # inside
+    x[2, :G] *= np.float32(2.0 ** -64)         # squares underflow to zero / subnormals
+    x[3, G:] *= np.float32(2.0 ** -60)         # inside
+    x[4, :G] = np.float32(3.0e38) * np.sign(x[4, :G])
+    xt = torch.from_numpy(x)
+    packed, s1, s2 = m.fp4quant_encode(xt.to(dev()), G)
+    wp, w1, w2 = ora.fp4quant_encode(x, G)
+    assert_bits_equal(to_f32_np(s1), w1, "s1")
+    assert_bits_equal(to_f32_np(s2), w2, "s2")
+    assert_bits_equal(u8(packed), wp, "packed")
+    y = m.fp4quant_decode(packed, s1, s2, G, out_dtype)
+    wy = ora.fp4quant_decode(wp, w1, w2, G)
+    got = to_f32_np(y).astype(np.float32)
+    nan = np.isnan(wy)
+    assert np.array_equal(np.isnan(got), nan)
+    if out_dtype == torch.bfloat16:
+        assert_bits_equal(bf16_bits(y)[~nan], ora.bf16_rn(wy)[~nan], "decoded bf16")
+    else:
+        assert_bits_equal(got[~nan], wy[~nan], "decoded f32")
