@@ -234,6 +234,34 @@ def test_qdq_matches_oracle(rounding, with_g, with_r):
         assert_bits_equal(to_f32_np(rd), rn, "residual")
 
 
+@pytest.mark.parametrize("rounding", ["rtn", "sr"])
+def test_qdq_infinite_gradient(rounding):
+    """A training step whose gradient holds infinities (and one block of
+    them): v = W - lr*G is infinite there, the amax too, so the tensor scale
+    falls back to 1; those elements store +-6 * eff in W and an infinite
+    residual.  W, residual, codes and scales equal the oracle's."""
+    m = fp4()
+    n = 16 * 200
+    w0 = workloads.nvfp4_train_weight(seed=3, shape=(n // 64, 64), device="cpu").view(-1)
+    g = workloads.nvfp4_train_grad(3, 0, shape=(n,), device="cpu").clone()
+    g[7] = float("inf")
+    g[16 * 50 + 3] = -float("inf")
+    g[16 * 90:16 * 91] = float("inf")
+    r0 = torch.randn(n, generator=torch.Generator().manual_seed(4)) * 1e-4
+    w, rd = w0.to(dev()), r0.to(dev())
+    _, packed, scales, ts = m.nvfp4_qdq(w, g.to(dev()), 1e-4, rd, rounding=rounding, seed=6,
+                                        step=1)
+    wb = bf16_bits(w0).copy()
+    rn = r0.numpy().copy()
+    wp, ws, wt = ora.nvfp4_qdq(wb, g.numpy(), 1e-4, rn,
+                               rounding=ora.SR if rounding == "sr" else ora.RTN, seed=6, step=1)
+    assert np.float32(ts.item()) == np.float32(wt) == np.float32(1.0)
+    assert_bits_equal(u8(packed), wp, "packed")
+    assert_bits_equal(u8(scales), ws, "scales")
+    assert_bits_equal(bf16_bits(w), wb, "W")
+    assert_bits_equal(to_f32_np(rd), rn, "residual")
+
+
 def test_qdq_training_workload_steps():
     """The bf16 [6144, 2048] N(0, 0.02) weight with G_t ~ N(0, 1), lr 1e-4,
     SR + error feedback: 3 full-size steps bit-exact, with the amax pass and
