@@ -95,3 +95,34 @@ def test_fp4quant_encode_past_2_31():
         assert_bits_equal(to_f32_np(s1[r:r + 1]), w1, f"s1 row {r}")
         assert_bits_equal(to_f32_np(s2[r:r + 1]), w2, f"s2 row {r}")
         assert_bits_equal(u8(packed[r:r + 1]), wp, f"packed row {r}")
+
+
+def test_fp4_to_fp8_col_past_2_31_output_bytes():
+    """The ragged column conversion with more than 2^31 output bytes: 64
+    segments of random lengths over 299,600 dispatched rows x 7168.  The
+    first and last segments, and the one holding output byte 2^31, against
+    the per-segment oracle."""
+    m = fp4()
+    cols = 7168
+    R = E31 // cols + 4000
+    rng = np.random.default_rng(4)
+    off = np.concatenate([[0], np.sort(rng.integers(0, R, 63)), [R]]).astype(np.int64)
+    g = torch.Generator(device=dev()).manual_seed(5)
+    pk = torch.randint(0, 256, (R, cols // 2), generator=g, device=dev(), dtype=torch.uint8)
+    sc = torch.randint(110, 140, (R, cols // 32), generator=g, device=dev(), dtype=torch.uint8)
+    segs = m.Segments(torch.from_numpy(off), dev())
+    ft, fts = m.fp4_to_fp8_col(pk, sc, segs)
+    sizes = np.diff(off)
+    e_mid = int(np.searchsorted(off * cols, E31, side="right") - 1)
+    assert off[e_mid] * cols <= E31 < off[e_mid + 1] * cols
+    for e in sorted({0, e_mid, len(sizes) - 1}):
+        row0, n_e = int(off[e]), int(sizes[e])
+        if n_e == 0:
+            continue
+        wo, wsc = ora.fp4_to_fp8_col_segment(u8(pk[row0:row0 + n_e]), u8(sc[row0:row0 + n_e]),
+                                             0, n_e)
+        assert_bits_equal(u8(ft[cols * row0:cols * (row0 + n_e)]).reshape(cols, n_e), wo,
+                          f"segment {e}")
+        s0, nb = int(segs.scale_off_host[e]), (n_e + 127) // 128
+        assert_bits_equal(to_f32_np(fts[cols * s0:cols * (s0 + nb)]).reshape(cols, nb), wsc,
+                          f"segment {e} scales")
