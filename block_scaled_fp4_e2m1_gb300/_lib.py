@@ -46,6 +46,8 @@ SIGNATURES = {
     "mxfp4_dequantize": (INT, [P, P, I64, I64, P, INT, P]),
     "fp4_scaled_quantize": (INT, [P, INT, I64, ctypes.c_float, P, P]),
     "fp4_scaled_dequantize": (INT, [P, I64, ctypes.c_float, P, INT, P]),
+    "fp4_scaled_quantize_amax": (INT, [P, INT, I64, P, P, P, P]),
+    "fp4_scaled_dequantize_dev": (INT, [P, I64, P, P, INT, P]),
     "fp4_to_fp8_col": (INT, [P, P, I64, P, P, I32, I64, I64, P, P, P]),
     "fp4_seg_scale_offsets": (INT, [P, I32, P]),
     "fp4quant_encode": (INT, [P, INT, I64, I64, INT, P, P, P, P]),

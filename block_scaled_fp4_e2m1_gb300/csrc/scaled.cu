@@ -4,6 +4,9 @@
 // "Sixteen values aren't enough": the comparison points of block scaling.
 // Codes are RN_e2m1(RN(x / s)) with one correctly rounded division per
 // element; s = 1 rounds straight to FP4.  Dequantize: value(code) * s.
+// The scale is a host value, or is read from the device: the one-scale-per-
+// matrix choice s = RN(amax / 6) is formed from a tensor amax in device
+// memory (the largest magnitude lands on 6, the largest E2M1 value).
 //
 // One thread per 16 elements: one 256-bit load of bf16 (two of fp32), an
 // 8-byte store of codes; the inverse reads 8 bytes and writes 32 (bf16) or
@@ -18,10 +21,23 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// s = RN(amax / 6), or 1 when that is not finite and > 0 (amax 0, say).
+__device__ __forceinline__ float scale_from_amax(float amax) {
+  const float s = __fdiv_rn(amax, 6.0f);
+  return (s > 0.0f && s <= 3.40282347e38f) ? s : 1.0f;
+}
+
+// amax == NULL: the scale is s; otherwise s = scale_from_amax(*amax), which
+// the first thread also writes to *scale_out.
 template <bool kBF16>
 __global__ void __launch_bounds__(kThreads)
     scaled_quantize_kernel(const void* __restrict__ x, int64_t nunits, float s,
+                           const float* __restrict__ amax, float* __restrict__ scale_out,
                            uint8_t* __restrict__ packed) {
+  if (amax) {
+    s = scale_from_amax(*amax);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *scale_out = s;
+  }
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   for (int64_t u = (int64_t)blockIdx.x * kThreads + threadIdx.x; u < nunits; u += stride) {
     float v[16];
@@ -49,10 +65,12 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// s_dev != NULL: the scale is *s_dev instead of s.
 template <bool kBF16Out>
 __global__ void __launch_bounds__(kThreads)
     scaled_dequantize_kernel(const uint8_t* __restrict__ packed, int64_t nunits, float s,
-                             void* __restrict__ y) {
+                             const float* __restrict__ s_dev, void* __restrict__ y) {
+  if (s_dev) s = *s_dev;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   for (int64_t u = (int64_t)blockIdx.x * kThreads + threadIdx.x; u < nunits; u += stride) {
     const uint2 p = ld_stream_v2(packed + 8 * u);
@@ -95,6 +113,25 @@ __global__ void __launch_bounds__(kThreads)
 
 bool scale_ok(float s) { return s > 0.0f && s <= 3.40282347e38f; }
 
+fp4_status launch_scaled_quantize(const void* x, int dtype, int64_t n, float scale,
+                                  const float* amax, float* scale_out, uint8_t* packed,
+                                  cudaStream_t s) {
+  const int64_t nu = n / 16;
+  if (dtype == FP4_BF16)
+    return launch<scaled_quantize_kernel<true>>(nu, kThreads, 0, s, x, nu, scale, amax,
+                                                scale_out, packed);
+  return launch<scaled_quantize_kernel<false>>(nu, kThreads, 0, s, x, nu, scale, amax, scale_out,
+                                               packed);
+}
+
+fp4_status launch_scaled_dequantize(const uint8_t* packed, int64_t n, float scale,
+                                    const float* s_dev, void* y, int out_dtype, cudaStream_t s) {
+  const int64_t nu = n / 16;
+  if (out_dtype == FP4_BF16)
+    return launch<scaled_dequantize_kernel<true>>(nu, kThreads, 0, s, packed, nu, scale, s_dev, y);
+  return launch<scaled_dequantize_kernel<false>>(nu, kThreads, 0, s, packed, nu, scale, s_dev, y);
+}
+
 }  // namespace
 }  // namespace fp4
 
@@ -110,11 +147,18 @@ fp4_status fp4_scaled_quantize(const void* x, int dtype, int64_t n, float scale,
   if (n > 0 && (!x || !packed)) return FP4_ERR_NULL;
   if (!aligned(x, 32) || !aligned(packed, 8)) return FP4_ERR_ALIGN;
   if (n == 0) return FP4_OK;
-  const int64_t nu = n / 16;
-  cudaStream_t s = as_stream(stream);
-  if (dtype == FP4_BF16)
-    return launch<scaled_quantize_kernel<true>>(nu, kThreads, 0, s, x, nu, scale, packed);
-  return launch<scaled_quantize_kernel<false>>(nu, kThreads, 0, s, x, nu, scale, packed);
+  return launch_scaled_quantize(x, dtype, n, scale, nullptr, nullptr, packed, as_stream(stream));
+}
+
+fp4_status fp4_scaled_quantize_amax(const void* x, int dtype, int64_t n, const float* amax,
+                                    float* scale_out, uint8_t* packed, void* stream) {
+  if (!dtype_ok(dtype)) return FP4_ERR_DTYPE;
+  if (n < 0 || n % 16 != 0) return FP4_ERR_SHAPE;
+  if (!amax || !scale_out || (n > 0 && (!x || !packed))) return FP4_ERR_NULL;
+  if (!aligned(x, 32) || !aligned(packed, 8) || !aligned(amax, 4) || !aligned(scale_out, 4))
+    return FP4_ERR_ALIGN;
+  // an empty tensor still publishes its scale: one CTA, no units
+  return launch_scaled_quantize(x, dtype, n, 1.0f, amax, scale_out, packed, as_stream(stream));
 }
 
 fp4_status fp4_scaled_dequantize(const uint8_t* packed, int64_t n, float scale, void* y,
@@ -125,11 +169,17 @@ fp4_status fp4_scaled_dequantize(const uint8_t* packed, int64_t n, float scale, 
   if (n > 0 && (!packed || !y)) return FP4_ERR_NULL;
   if (!aligned(packed, 8) || !aligned(y, 32)) return FP4_ERR_ALIGN;
   if (n == 0) return FP4_OK;
-  const int64_t nu = n / 16;
-  cudaStream_t s = as_stream(stream);
-  if (out_dtype == FP4_BF16)
-    return launch<scaled_dequantize_kernel<true>>(nu, kThreads, 0, s, packed, nu, scale, y);
-  return launch<scaled_dequantize_kernel<false>>(nu, kThreads, 0, s, packed, nu, scale, y);
+  return launch_scaled_dequantize(packed, n, scale, nullptr, y, out_dtype, as_stream(stream));
+}
+
+fp4_status fp4_scaled_dequantize_dev(const uint8_t* packed, int64_t n, const float* scale,
+                                     void* y, int out_dtype, void* stream) {
+  if (!dtype_ok(out_dtype)) return FP4_ERR_DTYPE;
+  if (n < 0 || n % 16 != 0) return FP4_ERR_SHAPE;
+  if (!scale || (n > 0 && (!packed || !y))) return FP4_ERR_NULL;
+  if (!aligned(packed, 8) || !aligned(y, 32) || !aligned(scale, 4)) return FP4_ERR_ALIGN;
+  if (n == 0) return FP4_OK;
+  return launch_scaled_dequantize(packed, n, 1.0f, scale, y, out_dtype, as_stream(stream));
 }
 
 }  // extern "C"

@@ -16,8 +16,9 @@ from typing import Dict
 
 import torch
 
-from .codec import (fp4_scaled_dequantize, fp4_scaled_quantize, mxfp4_dequantize,
-                    mxfp4_quantize, nvfp4_amax, nvfp4_dequantize, nvfp4_quantize)
+from .codec import (fp4_scaled_dequantize, fp4_scaled_dequantize_dev, fp4_scaled_quantize,
+                    fp4_scaled_quantize_amax, mxfp4_dequantize, mxfp4_quantize, nvfp4_amax,
+                    nvfp4_dequantize, nvfp4_quantize)
 
 METHODS = ("straight", "per_matrix", "mxfp4", "nvfp4")
 
@@ -28,13 +29,13 @@ def round_trips(w: torch.Tensor) -> Dict[str, torch.Tensor]:
     rows, cols = w.shape
     x = w.contiguous().view(-1)
     n = x.numel()
-    amax = float(nvfp4_amax(x).item())
-    if not math.isfinite(amax):
+    amax = nvfp4_amax(x)
+    if not math.isfinite(float(amax.item())):
         raise ValueError("the matrix holds a non-finite value")
-    s = float(torch.tensor(amax, dtype=torch.float32) / 6.0) if amax > 0 else 1.0
+    pk, s = fp4_scaled_quantize_amax(x, amax)  # s = RN(amax / 6), on the device
     out = {
         "straight": fp4_scaled_dequantize(fp4_scaled_quantize(x, 1.0), n, 1.0),
-        "per_matrix": fp4_scaled_dequantize(fp4_scaled_quantize(x, s), n, s),
+        "per_matrix": fp4_scaled_dequantize_dev(pk, n, s),
     }
     pk, sc = mxfp4_quantize(w.contiguous())
     out["mxfp4"] = mxfp4_dequantize(pk, sc, torch.float32).view(-1)

@@ -145,7 +145,11 @@ fp4_status nvfp4_qdq(uint16_t* w_bf16, const float* g, float lr, int64_t n, floa
  *   Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  *   The first call on each device looks the array's device address up with
  *   cudaGetSymbolAddress (with that device current) and caches it; make that
- *   first call before any stream capture on the device.
+ *   first call before any stream capture on the device.  The cached address
+ *   belongs to the device's context as it was at that first call: after a
+ *   cudaDeviceReset (or any other reset of that context) in the same
+ *   process it is stale, and the process must not call this entry point on
+ *   that device again.
  *   Every call on a device shares the one slot, which the call clears before
  *   use; calls whose work overlaps on the GPU (other streams, or two host
  *   threads) race on it and must be serialized by the caller. */
@@ -277,6 +281,21 @@ fp4_status fp4_scaled_quantize(const void* x, int dtype, int64_t n, float scale,
                                uint8_t* packed, void* stream);
 fp4_status fp4_scaled_dequantize(const uint8_t* packed, int64_t n, float scale, void* y,
                                  int out_dtype, void* stream);
+
+/* The same two operations with the scale in device memory, so that the one
+ * scale per matrix is chosen without a round trip to the host.
+ * fp4_scaled_quantize_amax: scale = RN(*amax / 6) (the largest magnitude,
+ * e.g. from nvfp4_amax on x, lands on 6, the largest E2M1 value); a scale
+ * that is not finite and > 0 (amax 0) is used as 1.  The scale used is
+ * written to *scale_out (also for n = 0).
+ *   amax, scale_out  1 fp32 each on the device, 4-byte aligned
+ * fp4_scaled_dequantize_dev: value(code) * (*scale), scale a device fp32
+ * (4-byte aligned) that is finite and > 0, e.g. the scale_out above.
+ * Other arguments as fp4_scaled_quantize / fp4_scaled_dequantize. */
+fp4_status fp4_scaled_quantize_amax(const void* x, int dtype, int64_t n, const float* amax,
+                                    float* scale_out, uint8_t* packed, void* stream);
+fp4_status fp4_scaled_dequantize_dev(const uint8_t* packed, int64_t n, const float* scale,
+                                     void* y, int out_dtype, void* stream);
 
 /* ------------------------------------------------------------------ MXFP4
  * [MoE-FP4] "方法概述" / "核心技术贡献" 2 (BF16ToFP4Row): each row in

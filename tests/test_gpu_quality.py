@@ -69,3 +69,29 @@ def test_quality_report_round_trips_and_stats():
     # the page's ordering: block scaling far ahead, NVFP4 ahead of MXFP4
     assert rep["straight"]["zero"] > 0.99 and rep["per_matrix"]["zero"] > 0.5
     assert rep["nvfp4"]["error"] < rep["mxfp4"]["error"] < rep["per_matrix"]["error"]
+
+
+def test_scale_from_amax_on_the_device():
+    """fp4_scaled_quantize_amax forms RN(amax / 6) on the device: codes and
+    the published scale equal the oracle's with that scale; an all-zero
+    tensor (amax 0) and an empty one publish scale 1."""
+    m = fp4()
+    x = workloads.laplace_weight(21, (64, 256), device=dev()).view(-1)
+    xn = to_f32_np(x)
+    amax = m.nvfp4_amax(x)
+    pk, s = m.fp4_scaled_quantize_amax(x, amax)
+    want_s = np.float32(np.float32(np.abs(xn).max()) / np.float32(6.0))
+    assert np.float32(s.item()) == want_s
+    assert_bits_equal(u8(pk), ora.fp4_scaled_quantize(xn, float(want_s)), "codes")
+    for od in (torch.float32, torch.bfloat16):
+        y = m.fp4_scaled_dequantize_dev(pk, x.numel(), s, od)
+        wy = ora.fp4_scaled_dequantize(u8(pk), x.numel(), float(want_s))
+        got = to_f32_np(y) if od == torch.float32 else bf16_bits(y)
+        assert_bits_equal(got, wy if od == torch.float32 else ora.bf16_rn(wy), str(od))
+    zero = torch.zeros(256, dtype=torch.bfloat16, device=dev())
+    _, s0 = m.fp4_scaled_quantize_amax(zero, m.nvfp4_amax(zero))
+    assert s0.item() == 1.0
+    empty = torch.empty(0, dtype=torch.float32, device=dev())
+    s1 = torch.full((1,), -3.0, device=dev())
+    m.fp4_scaled_quantize_amax(empty, torch.zeros(1, device=dev()), scale_out=s1)
+    assert s1.item() == 1.0

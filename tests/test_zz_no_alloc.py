@@ -102,3 +102,45 @@ def test_noalloc_argument_checks():
     assert f(A, 1, 16, None, 0, 0, 0, None, A, A, None) == 1   # tensor_scale
     assert f(A + 8, 1, 16, None, 0, 0, 0, A, A, A, None) == 2  # x alignment
     assert f(A, 9, 16, None, 0, 0, 0, A, A, A, None) == 4      # dtype
+
+
+def test_noalloc_empty_tensor_publishes_scale_one():
+    """n = 0: nothing to quantize, but the tensor scale is still written
+    (amax 0 gives scale 1), as nvfp4_quantize does in COMPUTE mode."""
+    L = _lib()
+    dev = torch.device("cuda", 0)
+    for dtype in (torch.bfloat16, torch.float32):
+        x = torch.empty(0, dtype=dtype, device=dev)
+        _, _, ts = _call_noalloc(L, x, None, 0, 0, 0)
+        _, _, ts_want = _call_existing(L, x, None, 0, 0, 0)
+        torch.cuda.synchronize()
+        assert ts.item() == 1.0 and ts_want.item() == 1.0
+
+
+def test_noalloc_allocates_nothing():
+    """Warmed-up calls leave the device's free memory and PyTorch's
+    allocator exactly as they were."""
+    L = _lib()
+    dev = torch.device("cuda", 0)
+    x = (torch.randn(16 * 4096, generator=torch.Generator().manual_seed(3)) * 0.1).to(dev)
+    n = x.numel()
+    ts = torch.empty(1, dtype=torch.float32, device=dev)
+    packed = torch.empty(n // 2, dtype=torch.uint8, device=dev)
+    scales = torch.empty(n // 16, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+
+    def call():
+        st = L.lib().nvfp4_quantize_noalloc(x.data_ptr(), 0, n, None, 0, 0, 0, ts.data_ptr(),
+                                            packed.data_ptr(), scales.data_ptr(), stream)
+        assert st == 0
+
+    call()
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info(dev)
+    alloc0 = torch.cuda.memory_allocated(dev)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info(dev)
+    assert free1 == free0
+    assert torch.cuda.memory_allocated(dev) == alloc0
