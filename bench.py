@@ -5,16 +5,26 @@ One step runs every kernel of the codec once on its workload:
   nvfp4_roundtrip   fp32 [1024, 1024]: amax, quantize (RTN), dequantize -> fp32
   fp4quant_acts     bf16 [16384, 4096], G = 64, 128, 256: encode, decode -> bf16
   nvfp4_train       bf16 W [6144, 2048] + fp32 G_t + fp32 residual: amax pass,
-                    fused qdq step (stochastic rounding + error feedback)
+                    fused qdq step (stochastic rounding + error feedback); step
+                    k of the bench is training step t = k mod 100 of the
+                    100-step schedule, with its own gradient G_t (seed + 1 + t,
+                    all 100 drawn once, before timing, and resident in HBM)
   moe_tokens        bf16 [32768, 7168] -> MXFP4; the top-8 dispatch of 262144
                     rows (gathered once, outside the timed region) -> FP8 E4M3
                     row form and ragged column form
   qwen3_8b_weights  252 bf16 matrices (6.95 G weights): amax, quantize (RTN),
                     dequantize -> bf16
-Inputs are resident in HBM; the step touches ~58 GB, far more than the 129 MB
-L2, so no explicit flush is needed.  Each kernel group is bracketed by CUDA
-events on the launching stream; `value` is the step's algorithmic bytes
-(read + written) over the device time of the step.
+The step's order keeps every consumer away from its producer: the FP4Quant
+decodes and the qdq pass run after the MoE kernels (about 2.5 GB of other
+traffic), so no kernel reads another's output, or its own input, from the
+129 MB L2.  Inputs are resident in HBM and the step touches ~58 GB.
+
+Timing: the step loop is bracketed by CUDA events (value, ms_per_step).  The
+per-kernel figures (`kernels`, `roofline`) come from a second pass in which
+L2 is flushed before every kernel group: a 512 MB buffer (four times L2) is
+written and then read back, outside the group's events, so the group starts
+with no line of its inputs in L2 and no dirty line of earlier work left to
+write back.
 
 Prints one JSON line (rank 0).  --impl reference times the CPU oracle on a
 bounded sample of the same workload instead.
@@ -61,6 +71,10 @@ def parse_args(argv=None):
     p.add_argument("--quality", action="store_true",
                    help="print the FP4 quality table (zero share, average error) of the four "
                         "methods on layer-18-shaped synthetic weights, one JSON line per matrix")
+    p.add_argument("--train-report", action="store_true",
+                   help="run the training workload's 100 steps under SR+EF, RTN+EF and RTN and "
+                        "print the share of weights changed per step and the drift of mean(W) "
+                        "against the fp32 reference, one JSON line per mode")
     p.add_argument("--source-hash", metavar="GROUP",
                    help="print the source hash a traffic figure of GROUP must carry")
     p.add_argument("--summarize-launches", metavar="CSV",
@@ -108,78 +122,85 @@ class Group:
         return self.bytes_per_launch * len(self.calls)
 
 
+TRAIN_STEPS = 100  # the training workload's schedule: 100 steps, G_t from seed + 1 + t
+
+
 def build_suite(device, rank=0, small=False, host_inputs=False):
     """Allocate inputs and outputs on `device` and return (groups, state).
-    With host_inputs, also keep pinned host copies of every input and output
-    for the end-to-end measurement."""
+    The groups are in step order (see the module docstring)."""
     import torch
     import block_scaled_fp4_e2m1_gb300 as m
     from block_scaled_fp4_e2m1_gb300 import workloads as W
 
     seed = 1000 * rank
-    groups = []
-    st = {"inputs": [], "outputs": []}   # (device tensor) lists for e2e copies
+    by = {}
+    st = {}
     f32, bf16, u8 = torch.float32, torch.bfloat16, torch.uint8
 
     def zeros(shape, dt):
         return torch.empty(shape, dtype=dt, device=device)
+
+    def add(g):
+        by[g.name] = g
+        return g
 
     # nvfp4_roundtrip: fp32 [1024, 1024]
     x1 = W.nvfp4_roundtrip(seed=seed, device=device).view(-1)
     n1 = x1.numel()
     a1, t1 = zeros(1, f32), zeros(1, f32)
     p1, s1, y1 = zeros(n1 // 2, u8), zeros(n1 // 16, u8), zeros(n1, f32)
-    st["inputs"] += [x1]
-    st["outputs"] += [p1, s1, y1, t1]
-    groups.append(Group("nvfp4_amax", "nvfp4_roundtrip", 4 * n1,
-                        [lambda: m.nvfp4_amax(x1, amax_ws=a1)]))
-    groups.append(Group("nvfp4_quantize", "nvfp4_roundtrip", n1 * (4 + 0.5 + 1 / 16),
-                        [lambda: m.nvfp4_quantize(x1, tscale="from_amax", amax_ws=a1,
-                                                  tensor_scale=t1, packed=p1, scales=s1)]))
-    groups.append(Group("nvfp4_dequantize", "nvfp4_roundtrip", n1 * (0.5 + 1 / 16 + 4),
-                        [lambda: m.nvfp4_dequantize(p1, s1, t1, (n1,), f32, out=y1)]))
+    add(Group("nvfp4_amax", "nvfp4_roundtrip", 4 * n1, [lambda: m.nvfp4_amax(x1, amax_ws=a1)]))
+    add(Group("nvfp4_quantize", "nvfp4_roundtrip", n1 * (4 + 0.5 + 1 / 16),
+              [lambda: m.nvfp4_quantize(x1, tscale="from_amax", amax_ws=a1, tensor_scale=t1,
+                                        packed=p1, scales=s1)]))
+    add(Group("nvfp4_dequantize", "nvfp4_roundtrip", n1 * (0.5 + 1 / 16 + 4),
+              [lambda: m.nvfp4_dequantize(p1, s1, t1, (n1,), f32, out=y1)]))
 
     # fp4quant_acts: bf16 [16384, 4096]
     T2, H2 = (1024, 4096) if small else (16384, 4096)
     x2 = W.fp4quant_acts(seed=seed, tokens=T2, hidden=H2, device=device)
-    st["inputs"] += [x2]
     n2 = x2.numel()
     fq_out = []
     for G in (64, 128, 256):
         pk, q1, q2 = zeros((T2, H2 // 2), u8), zeros((T2, H2 // G), f32), zeros((T2, H2 // G), f32)
         yy = zeros((T2, H2), bf16)
-        st["outputs"] += [pk, q1, q2, yy]
         fq_out += [pk, q1, q2, yy]
         b = n2 * (2 + 0.5 + 8 / G)
-        groups.append(Group(f"fp4quant_encode_g{G}", "fp4quant_acts", b,
-                            [lambda G=G, pk=pk, q1=q1, q2=q2: m.fp4quant_encode(x2, G, pk, q1, q2)]))
-        groups.append(Group(f"fp4quant_decode_g{G}", "fp4quant_acts", b,
-                            [lambda G=G, pk=pk, q1=q1, q2=q2, yy=yy:
-                             m.fp4quant_decode(pk, q1, q2, G, bf16, out=yy)]))
+        add(Group(f"fp4quant_encode_g{G}", "fp4quant_acts", b,
+                  [lambda G=G, pk=pk, q1=q1, q2=q2: m.fp4quant_encode(x2, G, pk, q1, q2)]))
+        add(Group(f"fp4quant_decode_g{G}", "fp4quant_acts", b,
+                  [lambda G=G, pk=pk, q1=q1, q2=q2, yy=yy:
+                   m.fp4quant_decode(pk, q1, q2, G, bf16, out=yy)]))
 
-    # nvfp4_train: bf16 W [6144, 2048], one SR + EF step per bench step
+    # nvfp4_train: bf16 W [6144, 2048]; bench step k is training step
+    # t = k mod 100 with its own gradient G_t, all drawn before timing
     shp3 = (6144, 2048)
     w3 = W.nvfp4_train_weight(seed=seed, shape=shp3, device=device).view(-1)
     n3 = w3.numel()
-    g3 = W.nvfp4_train_grad(seed, 0, shape=shp3, device=device).view(-1)
+    ng = 10 if small else TRAIN_STEPS
+    gbank = [W.nvfp4_train_grad(seed, t, shape=shp3, device=device).view(-1) for t in range(ng)]
     r3 = torch.zeros(n3, dtype=f32, device=device)
     a3, t3 = zeros(1, f32), zeros(1, f32)
     p3, s3 = zeros(n3 // 2, u8), zeros(n3 // 16, u8)
-    st["inputs"] += [w3, g3, r3]
-    st["outputs"] += [w3, r3, p3, s3, t3]
     st["train_step"] = [0]
+    st["g_override"] = None   # the end-to-end run feeds its uploaded gradient here
+
+    def cur_g():
+        if st["g_override"] is not None:
+            return st["g_override"]
+        return gbank[st["train_step"][0] % ng]
 
     def qdq_amax():
-        m.nvfp4_qdq_amax(w3, g3, 1e-4, r3, amax_ws=a3)
+        m.nvfp4_qdq_amax(w3, cur_g(), 1e-4, r3, amax_ws=a3)
 
     def qdq():
         k = st["train_step"][0]
-        m.nvfp4_qdq(w3, g3, 1e-4, r3, rounding="sr", seed=seed, step=k, tscale="from_amax",
-                    amax_ws=a3, tensor_scale=t3, packed=p3, scales=s3)
+        m.nvfp4_qdq(w3, cur_g(), 1e-4, r3, rounding="sr", seed=seed, step=k % ng,
+                    tscale="from_amax", amax_ws=a3, tensor_scale=t3, packed=p3, scales=s3)
         st["train_step"][0] = k + 1
 
-    groups.append(Group("nvfp4_qdq_amax", "nvfp4_train", n3 * (2 + 4 + 4), [qdq_amax]))
-    groups.append(Group("nvfp4_qdq", "nvfp4_train", n3 * (10 + 2 + 4 + 0.5 + 1 / 16), [qdq]))
+    add(Group("nvfp4_qdq_amax", "nvfp4_train", n3 * (2 + 4 + 4), [qdq_amax]))
+    add(Group("nvfp4_qdq", "nvfp4_train", n3 * (10 + 2 + 4 + 0.5 + 1 / 16), [qdq]))
 
     # moe_tokens: bf16 [32768, 7168], top-8 of 256 Zipf experts
     T4, H4, E4 = (2048, 7168, 256) if small else (32768, 7168, 256)
@@ -194,17 +215,14 @@ def build_suite(device, rank=0, small=False, host_inputs=False):
     segs = m.Segments(row_off, device)
     f8, f8s = zeros((R4, H4), u8), zeros((R4, H4 // 128), f32)
     ft, fts = zeros(H4 * R4, u8), zeros(H4 * segs.total_blocks, f32)
-    st["inputs"] += [x4, dp, ds]
-    st["outputs"] += [mp, ms, f8, f8s, ft, fts]
     n4 = x4.numel()
-    groups.append(Group("mxfp4_quantize", "moe_tokens", n4 * (2 + 0.5 + 1 / 32),
-                        [lambda: m.mxfp4_quantize(x4, mp, ms)]))
+    add(Group("mxfp4_quantize", "moe_tokens", n4 * (2 + 0.5 + 1 / 32),
+              [lambda: m.mxfp4_quantize(x4, mp, ms)]))
     nd = R4 * H4
-    groups.append(Group("fp4_to_fp8_row", "moe_tokens", nd * (0.5 + 1 / 32 + 1 + 4 / 128),
-                        [lambda: m.fp4_to_fp8_row(dp, ds, f8, f8s)]))
-    groups.append(Group("fp4_to_fp8_col", "moe_tokens",
-                        nd * (0.5 + 1 / 32 + 1) + 4 * H4 * segs.total_blocks,
-                        [lambda: m.fp4_to_fp8_col(dp, ds, segs, ft, fts)]))
+    add(Group("fp4_to_fp8_row", "moe_tokens", nd * (0.5 + 1 / 32 + 1 + 4 / 128),
+              [lambda: m.fp4_to_fp8_row(dp, ds, f8, f8s)]))
+    add(Group("fp4_to_fp8_col", "moe_tokens", nd * (0.5 + 1 / 32 + 1) + 4 * H4 * segs.total_blocks,
+              [lambda: m.fp4_to_fp8_col(dp, ds, segs, ft, fts)]))
 
     # qwen3_8b_weights: 252 Laplace bf16 matrices, one batched launch per pass
     shapes = W.qwen3_8b_weight_shapes(layers=2 if small else 36)
@@ -219,28 +237,45 @@ def build_suite(device, rank=0, small=False, host_inputs=False):
     amax5, ts5 = zeros(k5, f32), zeros(k5, f32)
     qbatch = m.Batch(xs=mats, packed=pk5, scales=sc5)
     dbatch = m.Batch(packed=pk5, scales=sc5, ys=out5, sizes=[w.numel() for w in mats])
-    st["inputs"] += mats
-    st["outputs"] += pk5 + sc5 + out5 + [ts5]
     n5 = sum(w.numel() for w in mats)
-    groups.append(Group("nvfp4_amax", "qwen3_8b_weights", 2 * n5,
-                        [lambda: m.nvfp4_amax_batched(qbatch, bf16, amax=amax5)]))
-    groups.append(Group("nvfp4_quantize", "qwen3_8b_weights", n5 * (2 + 0.5 + 1 / 16),
-                        [lambda: m.nvfp4_quantize_batched(qbatch, bf16, tscale="from_amax",
-                                                          tensor_scale=ts5, amax=amax5)]))
-    groups.append(Group("nvfp4_dequantize", "qwen3_8b_weights", n5 * (0.5 + 1 / 16 + 2),
-                        [lambda: m.nvfp4_dequantize_batched(dbatch, ts5, bf16)]))
+    add(Group("nvfp4_amax", "qwen3_8b_weights", 2 * n5,
+              [lambda: m.nvfp4_amax_batched(qbatch, bf16, amax=amax5)]))
+    add(Group("nvfp4_quantize", "qwen3_8b_weights", n5 * (2 + 0.5 + 1 / 16),
+              [lambda: m.nvfp4_quantize_batched(qbatch, bf16, tscale="from_amax",
+                                                tensor_scale=ts5, amax=amax5)]))
+    add(Group("nvfp4_dequantize", "qwen3_8b_weights", n5 * (0.5 + 1 / 16 + 2),
+              [lambda: m.nvfp4_dequantize_batched(dbatch, ts5, bf16)]))
     st["elements"] = {"nvfp4_roundtrip": n1, "fp4quant_acts": n2, "nvfp4_train": n3,
                       "moe_tokens": n4, "moe_dispatched": nd, "qwen3_8b_weights": n5}
+
+    order = (["nvfp4_amax@nvfp4_roundtrip", "nvfp4_quantize@nvfp4_roundtrip",
+              "nvfp4_dequantize@nvfp4_roundtrip"] +
+             [f"fp4quant_encode_g{G}@fp4quant_acts" for G in (64, 128, 256)] +
+             ["nvfp4_qdq_amax@nvfp4_train", "mxfp4_quantize@moe_tokens",
+              "fp4_to_fp8_row@moe_tokens", "fp4_to_fp8_col@moe_tokens"] +
+             [f"fp4quant_decode_g{G}@fp4quant_acts" for G in (64, 128, 256)] +
+             ["nvfp4_qdq@nvfp4_train", "nvfp4_amax@qwen3_8b_weights",
+              "nvfp4_quantize@qwen3_8b_weights", "nvfp4_dequantize@qwen3_8b_weights"])
+    assert sorted(order) == sorted(by)
+    groups = [by[k] for k in order]
 
     # The same work cut into stages for the end-to-end pipeline: each stage
     # has its inputs, its calls and its outputs.  The weight set goes in
     # chunks of whole layers (each chunk one batched launch per pass), so
     # that one chunk's upload, another's kernels and a third's download can
-    # overlap.
-    stages = [([x1], [g.calls[0] for g in groups[0:3]], [p1, s1, y1, t1])]
-    stages.append(([x2], [g.calls[0] for g in groups[3:9]], fq_out))
-    stages.append(([w3, g3, r3], [qdq_amax, qdq], [w3, r3, p3, s3, t3]))
-    stages.append(([x4, dp, ds], [g.calls[0] for g in groups[11:14]], [mp, ms, f8, f8s, ft, fts]))
+    # overlap.  The training stage uploads its gradient into g_e2e.
+    calls = lambda *names: [by[nm].calls[0] for nm in names]
+    g_e2e = zeros(n3, f32)
+    st["g_e2e"] = g_e2e
+    stages = [([x1], calls("nvfp4_amax@nvfp4_roundtrip", "nvfp4_quantize@nvfp4_roundtrip",
+                           "nvfp4_dequantize@nvfp4_roundtrip"), [p1, s1, y1, t1])]
+    stages.append(([x2], [c for G in (64, 128, 256)
+                          for c in calls(f"fp4quant_encode_g{G}@fp4quant_acts",
+                                         f"fp4quant_decode_g{G}@fp4quant_acts")], fq_out))
+    stages.append(([w3, g_e2e, r3], [qdq_amax, qdq], [w3, r3, p3, s3, t3]))
+    stages.append(([x4, dp, ds], calls("mxfp4_quantize@moe_tokens", "fp4_to_fp8_row@moe_tokens",
+                                       "fp4_to_fp8_col@moe_tokens"),
+                   [mp, ms, f8, f8s, ft, fts]))
     per_layer = 7
     layers = k5 // per_layer
     chunk_layers = max(1, min(4, layers))
@@ -257,7 +292,26 @@ def build_suite(device, rank=0, small=False, host_inputs=False):
                         lambda db=db, ts=ts: m.nvfp4_dequantize_batched(db, ts, bf16)],
                        pk5[i0:i1] + sc5[i0:i1] + out5[i0:i1] + [ts]))
     st["stages"] = stages
+    st["gbank0"] = gbank[0]
     return groups, st
+
+
+class L2Flush:
+    """Leaves L2 holding only clean lines of a 512 MB buffer (four times the
+    129 MB L2): the buffer is written, which evicts everything, then read
+    back, which writes the dirty lines to HBM.  The next kernel therefore
+    finds none of its inputs in L2 and pays for no earlier work's
+    write-backs."""
+
+    def __init__(self, device, nbytes=512 << 20):
+        import torch
+        self.buf = torch.empty(nbytes // 8, dtype=torch.int64, device=device)
+        self.sink = torch.empty((), dtype=torch.int64, device=device)
+
+    def __call__(self):
+        import torch
+        self.buf.zero_()
+        torch.sum(self.buf, dim=0, out=self.sink)
 
 
 def run_step(groups, events):
@@ -327,79 +381,153 @@ class ClockSampler:
 
 # --------------------------------------------------------------- CPU side
 
-def cpu_oracle_rates(budget_s=12.0):
-    """Time the CPU oracle (single-threaded C) on bounded samples of each
-    kernel's workload; returns {group name: GB/s} and a sample description."""
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_oracle_rates(big_mb=256.0, small_scale=1.0, parallel=True):
+    """Time the CPU oracle (plain single-threaded C) on bounded slices of each
+    kernel's workload.  Returns (single, multi, sample, cores): GB/s per
+    group on one core, GB/s per group with the slice's rows split over
+    `cores` threads (each thread runs the same C oracle on its rows; the
+    ctypes calls release the GIL), a description of the slices, and the
+    thread count.  The weight-set and MoE slices hold big_mb MB of input;
+    the others are scaled by small_scale.  Quantize passes take the tensor
+    scale as given (computed before timing), as the bench's quantize
+    kernels take it from the preceding amax pass."""
+    from concurrent.futures import ThreadPoolExecutor
+
     import numpy as np
     import torch
     import oracle as ora
     from block_scaled_fp4_e2m1_gb300 import workloads as W
 
     ora.build()
-    rates = {}
-    per = budget_s / 9.0
+    cores = host_cores() if parallel else 1
+    pool = ThreadPoolExecutor(max_workers=cores) if cores > 1 else None
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    single, multi = {}, {}
 
-    def timed(fn, nbytes):
-        # repeat until ~per seconds
+    def parts(n, unit):
+        """[a, b) ranges of n rows (multiples of unit) over `cores` threads."""
+        k = max(1, min(cores, n // unit))
+        cuts = [((n // unit) * i // k) * unit for i in range(k)] + [n]
+        return list(zip(cuts, cuts[1:]))
+
+    def timed(name, nbytes, fn, part_fn=None, ranges=None):
         t0 = time.perf_counter()
         reps = 0
-        while True:
+        while True:   # tiny slices repeat up to ~0.2 s
             fn()
             reps += 1
             el = time.perf_counter() - t0
-            if el >= per or reps >= 50:
+            if el >= 0.2 or reps >= 20:
                 break
-        return nbytes * reps / el / 1e9
+        single[name] = nbytes * reps / el / 1e9
+        if pool is not None and part_fn is not None:
+            t0 = time.perf_counter()
+            list(pool.map(lambda ab: part_fn(*ab), ranges))
+            multi[name] = nbytes / (time.perf_counter() - t0) / 1e9
 
-    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
-    # nvfp4 round-trip (fp32, 256K elements)
-    x = W.nvfp4_roundtrip(seed=0, shape=(256, 1024)).numpy().ravel()
+    G_ = ora.TSCALE_GIVEN
+    # nvfp4 round-trip: fp32 [1024 * small_scale, 1024]
+    r1 = max(16, int(1024 * small_scale))
+    x = W.nvfp4_roundtrip(seed=0, shape=(r1, 1024)).numpy().ravel()
     n = x.size
-    rates["nvfp4_amax@nvfp4_roundtrip"] = timed(lambda: ora.nvfp4_amax(x), 4 * n)
-    pq = ora.nvfp4_quantize(x)
-    rates["nvfp4_quantize@nvfp4_roundtrip"] = timed(lambda: ora.nvfp4_quantize(x), 4.5625 * n)
-    rates["nvfp4_dequantize@nvfp4_roundtrip"] = timed(
-        lambda: ora.nvfp4_dequantize(pq[0], pq[1], pq[2], n), 4.5625 * n)
-    # fp4quant (64 tokens of 4096)
-    a = ora.bf16_to_f32(bits(W.fp4quant_acts(seed=0, tokens=64, hidden=4096)))
+    ts = ora.nvfp4_tensor_scale(ora.nvfp4_amax(x))
+    rg = parts(n, 4096)
+    timed("nvfp4_amax@nvfp4_roundtrip", 4 * n, lambda: ora.nvfp4_amax(x),
+          lambda a, b: ora.nvfp4_amax(x[a:b]), rg)
+    pq = ora.nvfp4_quantize(x, tscale_mode=G_, tensor_scale=ts)
+    timed("nvfp4_quantize@nvfp4_roundtrip", 4.5625 * n,
+          lambda: ora.nvfp4_quantize(x, tscale_mode=G_, tensor_scale=ts),
+          lambda a, b: ora.nvfp4_quantize(x[a:b], tscale_mode=G_, tensor_scale=ts), rg)
+    timed("nvfp4_dequantize@nvfp4_roundtrip", 4.5625 * n,
+          lambda: ora.nvfp4_dequantize(pq[0], pq[1], ts, n),
+          lambda a, b: ora.nvfp4_dequantize(pq[0][a // 2:b // 2], pq[1][a // 16:b // 16], ts,
+                                            b - a), rg)
+    # FP4Quant activations: [1024 * small_scale, 4096] tokens
+    t2 = max(16, int(1024 * small_scale))
+    a = ora.bf16_to_f32(bits(W.fp4quant_acts(seed=0, tokens=t2, hidden=4096)))
+    rg = parts(t2, 1)
     for G in (64, 128, 256):
         enc = ora.fp4quant_encode(a, G)
-        b = a.size * (2.5 + 8 / G)
-        rates[f"fp4quant_encode_g{G}@fp4quant_acts"] = timed(lambda: ora.fp4quant_encode(a, G), b)
-        rates[f"fp4quant_decode_g{G}@fp4quant_acts"] = timed(
-            lambda: ora.fp4quant_decode(*enc, G), b)
-    # training step (64K elements)
-    w = bits(W.nvfp4_train_weight(seed=0, shape=(32, 2048))).ravel().copy()
-    g = W.nvfp4_train_grad(0, 0, shape=(32, 2048)).numpy().ravel()
+        b_ = a.size * (2.5 + 8 / G)
+        timed(f"fp4quant_encode_g{G}@fp4quant_acts", b_, lambda: ora.fp4quant_encode(a, G),
+              lambda i, j: ora.fp4quant_encode(a[i:j], G), rg)
+        timed(f"fp4quant_decode_g{G}@fp4quant_acts", b_, lambda: ora.fp4quant_decode(*enc, G),
+              lambda i, j: ora.fp4quant_decode(enc[0][i:j], enc[1][i:j], enc[2][i:j], G), rg)
+    # training step: [512 * small_scale, 2048] of W, G_0, r
+    r3 = max(16, int(512 * small_scale))
+    w = bits(W.nvfp4_train_weight(seed=0, shape=(r3, 2048))).ravel().copy()
+    g = W.nvfp4_train_grad(0, 0, shape=(r3, 2048)).numpy().ravel()
     r = np.zeros(w.size, np.float32)
-    rates["nvfp4_qdq_amax@nvfp4_train"] = timed(lambda: ora.nvfp4_qdq_amax(w, g, 1e-4, r),
-                                                10 * w.size)
-    rates["nvfp4_qdq@nvfp4_train"] = timed(
-        lambda: ora.nvfp4_qdq(w, g, 1e-4, r, rounding=ora.SR), 16.5625 * w.size)
-    # MoE (16 tokens, then 128 dispatched rows)
-    t = ora.bf16_to_f32(bits(W.moe_tokens(seed=0, tokens=16, hidden=7168)))
+    ts3 = ora.nvfp4_tensor_scale(ora.nvfp4_qdq_amax(w, g, 1e-4, r))
+    rg = parts(w.size, 4096)
+    timed("nvfp4_qdq_amax@nvfp4_train", 10 * w.size, lambda: ora.nvfp4_qdq_amax(w, g, 1e-4, r),
+          lambda i, j: ora.nvfp4_qdq_amax(w[i:j], g[i:j], 1e-4, r[i:j]), rg)
+    timed("nvfp4_qdq@nvfp4_train", 16.5625 * w.size,
+          lambda: ora.nvfp4_qdq(w, g, 1e-4, r, rounding=ora.SR, tscale_mode=G_,
+                                tensor_scale=ts3),
+          lambda i, j: ora.nvfp4_qdq(w[i:j], g[i:j], 1e-4, r[i:j], rounding=ora.SR,
+                                     tscale_mode=G_, tensor_scale=ts3), rg)
+    # MoE: big_mb MB of bf16 tokens; then big_mb MB of dispatched MXFP4 rows
+    # (0.53125 B per element), cut into expert segments of the workload's
+    # mean length (1024 rows)
+    t4 = max(8, int(big_mb * 1e6 / (2 * 7168)))
+    t = ora.bf16_to_f32(bits(W.moe_tokens(seed=0, tokens=t4, hidden=7168)))
+    timed("mxfp4_quantize@moe_tokens", t.size * 2.53125, lambda: ora.mxfp4_quantize(t),
+          lambda i, j: ora.mxfp4_quantize(t[i:j]), parts(t4, 1))
     mp, ms = ora.mxfp4_quantize(t)
-    rates["mxfp4_quantize@moe_tokens"] = timed(lambda: ora.mxfp4_quantize(t), t.size * 2.53125)
-    dp = np.repeat(mp, 8, axis=0)
-    dsc = np.repeat(ms, 8, axis=0)
-    nd = dp.shape[0] * 7168
-    rates["fp4_to_fp8_row@moe_tokens"] = timed(lambda: ora.fp4_to_fp8_row(dp, dsc), nd * 1.5625)
-    off = np.array([0, 40, 128], np.int64)
-    rates["fp4_to_fp8_col@moe_tokens"] = timed(lambda: ora.fp4_to_fp8_col(dp, dsc, off),
-                                               nd * 1.5625)
-    # weight set (one [64, 4096] slice)
-    wq = ora.bf16_to_f32(bits(W.laplace_weight(0, (64, 4096)))).ravel()
+    del t
+    rd = max(128, int(big_mb * 1e6 / (0.53125 * 7168)))
+    reps = -(-rd // t4)
+    dp = np.ascontiguousarray(np.tile(mp, (reps, 1))[:rd])
+    dsc = np.ascontiguousarray(np.tile(ms, (reps, 1))[:rd])
+    del mp, ms
+    nd = rd * 7168
+    timed("fp4_to_fp8_row@moe_tokens", nd * 1.5625, lambda: ora.fp4_to_fp8_row(dp, dsc),
+          lambda i, j: ora.fp4_to_fp8_row(dp[i:j], dsc[i:j]), parts(rd, 1))
+    off = np.array(list(range(0, rd, 1024)) + [rd], np.int64)
+    segs = list(zip(off[:-1], off[1:]))
+    seg_ranges = parts(len(segs), 1)
+
+    def col_part(i, j):
+        for a_, b_ in segs[i:j]:
+            ora.fp4_to_fp8_col_segment(dp, dsc, int(a_), int(b_ - a_))
+
+    timed("fp4_to_fp8_col@moe_tokens", nd * 1.5625, lambda: ora.fp4_to_fp8_col(dp, dsc, off),
+          col_part, seg_ranges)
+    del dp, dsc
+    # weight set: big_mb MB of one Laplace matrix [., 4096]
+    r5 = max(16, int(big_mb * 1e6 / (2 * 4096)))
+    wq = ora.bf16_to_f32(bits(W.laplace_weight(0, (r5, 4096)))).ravel()
     nq = wq.size
-    rates["nvfp4_amax@qwen3_8b_weights"] = timed(lambda: ora.nvfp4_amax(wq), 2 * nq)
-    pw = ora.nvfp4_quantize(wq)
-    rates["nvfp4_quantize@qwen3_8b_weights"] = timed(lambda: ora.nvfp4_quantize(wq), 2.5625 * nq)
-    rates["nvfp4_dequantize@qwen3_8b_weights"] = timed(
-        lambda: ora.nvfp4_dequantize(pw[0], pw[1], pw[2], nq), 2.5625 * nq)
-    sample = ("single-threaded C oracle on slices of each workload: 256x1024 fp32 round-trip, "
-              "64x4096 activations per G, 32x2048 training step, 16x7168 tokens and 128 "
-              "dispatched rows, 64x4096 of a weight matrix; whole-step GB/s = step bytes / "
-              "sum over kernels of (kernel bytes / oracle GB/s)")
-    return rates, sample
+    ts5 = ora.nvfp4_tensor_scale(ora.nvfp4_amax(wq))
+    rg = parts(nq, 4096)
+    timed("nvfp4_amax@qwen3_8b_weights", 2 * nq, lambda: ora.nvfp4_amax(wq),
+          lambda i, j: ora.nvfp4_amax(wq[i:j]), rg)
+    pw = ora.nvfp4_quantize(wq, tscale_mode=G_, tensor_scale=ts5)
+    timed("nvfp4_quantize@qwen3_8b_weights", 2.5625 * nq,
+          lambda: ora.nvfp4_quantize(wq, tscale_mode=G_, tensor_scale=ts5),
+          lambda i, j: ora.nvfp4_quantize(wq[i:j], tscale_mode=G_, tensor_scale=ts5), rg)
+    timed("nvfp4_dequantize@qwen3_8b_weights", 2.5625 * nq,
+          lambda: ora.nvfp4_dequantize(pw[0], pw[1], ts5, nq),
+          lambda i, j: ora.nvfp4_dequantize(pw[0][i // 2:j // 2], pw[1][i // 16:j // 16], ts5,
+                                            j - i), rg)
+    if pool is not None:
+        pool.shutdown()
+    mb = lambda v: f"{v / 1e6:.0f} MB"
+    sample = (f"the C oracle on slices of each workload: fp32 round-trip [{r1}, 1024], "
+              f"activations [{t2}, 4096] per G, training step [{r3}, 2048], MoE tokens "
+              f"[{t4}, 7168] ({mb(2 * t4 * 7168)} bf16) and {rd} dispatched MXFP4 rows "
+              f"({mb(0.53125 * nd)}, segments of 1024 rows), weights [{r5}, 4096] "
+              f"({mb(2 * nq)} bf16); one pass per slice (tiny ones repeated to 0.2 s); "
+              f"step GB/s = step bytes / sum over kernels of (kernel bytes / oracle GB/s)")
+    return single, multi, sample, cores
 
 
 def combine_rate(groups, rates):
@@ -414,26 +542,36 @@ def reference_arm(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    import types
     # the step's byte mix (shapes only; nothing allocated)
     groups = suite_shapes()
     steps, warm = max(1, args.steps), max(0, args.warmup)
-    budget = max(0.6, min(6.0, 150.0 / (steps + warm)))
-    vals = []
+    # each step: the oracle on slices sized so that the whole run ends in a
+    # few minutes (about 150 s of CPU work over all steps)
+    budget = max(1.0, min(30.0, 150.0 / (steps + warm)))
+    big_mb = max(2.0, 256.0 * budget / 30.0)
+    small = max(0.02, budget / 30.0)
+    vals, walls = [], []
     sample = ""
     for i in range(warm + steps):
-        rates, sample = cpu_oracle_rates(budget_s=budget)
+        t0 = time.perf_counter()
+        rates, _, sample, _ = cpu_oracle_rates(big_mb=big_mb, small_scale=small, parallel=False)
+        wall = time.perf_counter() - t0
         if i >= warm:
             vals.append(combine_rate(groups, rates))
+            walls.append(wall)
     v = statistics.median(vals)
+    full_ms = sum(g.bytes_per_step for g in groups) / (v * 1e9) * 1e3
     line = {
         "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s",
         "n_gpus": args.gpus, "steps": steps, "warmup": warm,
-        "ms_per_step": round(sum(g.bytes_per_step for g in groups) / (v * 1e9) * 1e3, 3),
+        "ms_per_step": round(statistics.median(walls) * 1e3, 1),
+        "ms_per_step_kind": ("measured wall time of one sampled step (the oracle on a slice "
+                             "of every kernel's workload, plus drawing the slices)"),
+        "full_step_ms_extrapolated": round(full_ms, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": {"workload": WORKLOAD},
         "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                         "host_cores": host_cores(), "sample": sample},
         "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -501,6 +639,8 @@ def e2e_measure(groups, st, steps, warmup, device):
     d2h = sum(t.numel() * t.element_size() for ts in outs for t in ts)
     if host_mem_available() < 1.5 * (h2d + d2h):
         return None, h2d, d2h
+    st["g_e2e"].copy_(st["gbank0"])
+    st["g_override"] = st["g_e2e"]
     h_in = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ts] for ts in ins]
     h_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ts] for ts in outs]
     for hs, ts in zip(h_in, ins):
@@ -541,7 +681,13 @@ def e2e_measure(groups, st, steps, warmup, device):
             if t.numel() * t.element_size() <= (256 << 20) and not torch.equal(h.to(device), t):
                 raise RuntimeError(f"e2e stage {k}: a downloaded output differs from the device")
     del h_in, h_out
+    st["g_override"] = None
     return statistics.median(times), h2d, d2h
+
+
+def kernel_pass_steps(steps):
+    """Steps of the L2-flushed per-kernel pass that follows the timed steps."""
+    return max(5, min(steps, 30))
 
 
 def summarize_launches(path, steps, warmup):
@@ -566,13 +712,15 @@ def summarize_launches(path, steps, warmup):
         ns = v * {"ns": 1.0, "us": 1e3, "usecond": 1e3, "ms": 1e6, "msecond": 1e6}.get(unit, 1.0)
         rows.append((short, ns, r["Grid Size"], r["Block Size"]))
     # the run is: one setup launch (the MXFP4 quantize feeding the dispatch
-    # gather), max(3, warmup) warm-up steps, then the timed steps
+    # gather), max(3, warmup) warm-up steps, the timed steps, then the
+    # L2-flushed per-kernel pass of kernel_pass_steps(steps) steps
     total = len(rows)
-    nsteps = max(3, warmup) + steps
+    warm = max(3, warmup)
+    nsteps = warm + steps + kernel_pass_steps(steps)
     per_step = (total - 1) // nsteps
     if per_step * nsteps + 1 != total:
         raise ValueError(f"{total} launches do not split into {nsteps} steps + 1")
-    sel = rows[total - per_step * steps:]
+    sel = rows[1 + warm * per_step:1 + (warm + steps) * per_step]
     agg = {}
     for short, ns, grid, block in sel:
         a = agg.setdefault(short, [0, 0.0, grid, block])
@@ -598,8 +746,8 @@ KERNEL_STUDIES = ["nvfp4_amax", "nvfp4_quantize", "nvfp4_quantize_sr", "nvfp4_de
 
 def kernel_study(name, size_mb, steps, warmup, device):
     """One kernel on a bf16 input of ~size_mb MB (the shapes of its bench
-    workload, rows scaled), timed per launch with CUDA events.  Returns
-    (group, per-launch ms list)."""
+    workload, rows scaled), timed per launch with CUDA events, L2 flushed
+    (L2Flush) before every launch.  Returns (group, per-launch ms list)."""
     import torch
     import block_scaled_fp4_e2m1_gb300 as m
     from block_scaled_fp4_e2m1_gb300 import workloads as W
@@ -745,8 +893,10 @@ def kernel_study(name, size_mb, steps, warmup, device):
         g.calls[0]()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
+    flush = L2Flush(device)
     torch.cuda.synchronize()
     for s in range(steps):
+        flush()
         ev[s][0].record()
         g.calls[0]()
         ev[s][1].record()
@@ -757,14 +907,15 @@ def kernel_study(name, size_mb, steps, warmup, device):
 def size_sweep(device, steps):
     """NVFP4 amax, RTN quantize (scale from that amax) and dequantize to bf16
     of one bf16 Laplace matrix [n / 4096, 4096] per size of the 1 MiB - 4 GiB
-    sweep.  L2 is flushed (a 512 MB write) before every timed launch, so the
-    small sizes are measured from HBM too; the events bracket the kernel
-    alone."""
+    sweep.  L2 is flushed (L2Flush: 512 MB written, then read back) before
+    every timed launch, so the small sizes are measured from HBM too and no
+    write-back of the flush lands in the kernel's time; the events bracket
+    the kernel alone."""
     import torch
     import block_scaled_fp4_e2m1_gb300 as m
     from block_scaled_fp4_e2m1_gb300 import workloads as W
     peak, kind = measured_peak()
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    flush = L2Flush(device)
     for nbytes in W.size_sweep_bytes():
         n = nbytes // 2
         w = W.laplace_weight(11, (n // 4096, 4096), device=device).view(-1)
@@ -784,7 +935,7 @@ def size_sweep(device, steps):
                 f()
             times = []
             for _ in range(steps):
-                flush.zero_()
+                flush()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record()
                 f()
@@ -799,6 +950,87 @@ def size_sweep(device, steps):
                   flush=True)
         del w, pk, sc, y
         torch.cuda.empty_cache()
+
+
+def train_report(device, steps=TRAIN_STEPS, check_elems=65536):
+    """The training workload run for its full schedule: W <- qdq(W - lr G_t)
+    on the bf16 [6144, 2048] weight, lr 1e-4, G_t ~ N(0, 1) from seed 1 + t,
+    under SR + error feedback, RTN + error feedback and plain RTN ([fp4-train]
+    "Correctness": RTN stalls on updates below one quantization step, EF and
+    SR do not), each with the tensor scale computed from every step's amax
+    and with it held at its step-0 value.  Per step: the share of weights
+    whose stored bf16 value changed and mean(W) minus the mean of the
+    unquantized fp32 reference W_ref <- W_ref - lr G_t; at the end, the share
+    of the reference's total update that W followed,
+    <W_T - W_0, R_T - W_0> / |R_T - W_0|^2.  The first check_elems weights
+    and residuals are compared with the CPU oracle at every step, with the
+    tensor scale the GPU used.  One JSON line per run."""
+    import numpy as np
+    import torch
+    import block_scaled_fp4_e2m1_gb300 as m
+    import oracle as ora
+    from block_scaled_fp4_e2m1_gb300 import workloads as W
+
+    ora.build()
+    shp = (6144, 2048)
+    lr = 1e-4
+    w0 = W.nvfp4_train_weight(seed=0, shape=shp, device=device).view(-1)
+    n = w0.numel()
+    grads = [W.nvfp4_train_grad(0, t, shape=shp, device=device).view(-1) for t in range(steps)]
+    ref = w0.float()
+    ref_mean = [float(ref.double().mean())]
+    for t in range(steps):
+        ref = ref - lr * grads[t]
+        ref_mean.append(float(ref.double().mean()))
+    ref_upd = ref.double() - w0.double()
+    bits = lambda t: t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    for tsmode in ("computed", "fixed"):
+        for mode, rnd, ef in (("sr+ef", "sr", True), ("rtn+ef", "rtn", True),
+                              ("rtn", "rtn", False)):
+            w = w0.clone()
+            r = torch.zeros(n, dtype=torch.float32, device=device) if ef else None
+            amax, ts = torch.empty(1, device=device), torch.empty(1, device=device)
+            m.nvfp4_qdq_amax(w, grads[0], lr, r, amax_ws=amax)
+            ts_fixed = torch.tensor([ora.nvfp4_tensor_scale(float(amax.item()))],
+                                    dtype=torch.float32, device=device)
+            ow = bits(w0)[:check_elems].copy()
+            orr = np.zeros(check_elems, np.float32) if ef else None
+            changed, drift, mismatch = [], [], 0
+            for t in range(steps):
+                prev = w.clone()
+                if tsmode == "computed":
+                    m.nvfp4_qdq_amax(w, grads[t], lr, r, amax_ws=amax)
+                    m.nvfp4_qdq(w, grads[t], lr, r, rounding=rnd, seed=0, step=t,
+                                tscale="from_amax", amax_ws=amax, tensor_scale=ts,
+                                want_packed=False)
+                else:
+                    ts.copy_(ts_fixed)
+                    m.nvfp4_qdq(w, grads[t], lr, r, rounding=rnd, seed=0, step=t,
+                                tscale="given", tensor_scale=ts, want_packed=False)
+                changed.append(float((w.view(torch.int16) != prev.view(torch.int16))
+                                     .double().mean()))
+                drift.append(float(w.double().mean()) - ref_mean[t + 1])
+                ora.nvfp4_qdq(ow, grads[t][:check_elems].cpu().numpy(), lr, orr,
+                              rounding=ora.SR if rnd == "sr" else ora.RTN, seed=0, step=t,
+                              tscale_mode=ora.TSCALE_GIVEN, tensor_scale=float(ts.item()))
+                same = np.array_equal(bits(w)[:check_elems], ow)
+                if ef:
+                    same = same and np.array_equal(
+                        r[:check_elems].cpu().numpy().view(np.uint32), orr.view(np.uint32))
+                mismatch += 0 if same else 1
+            upd = w.double() - w0.double()
+            print(json.dumps({
+                "train_report": mode, "tensor_scale": tsmode, "steps": steps, "lr": lr,
+                "shape": list(shp),
+                "changed_mean": round(statistics.mean(changed), 6),
+                "changed_first5": [round(c, 6) for c in changed[:5]],
+                "changed_last5": [round(c, 6) for c in changed[-5:]],
+                "update_followed": float((upd * ref_upd).sum() / (ref_upd * ref_upd).sum()),
+                "mean_w_minus_ref_final": drift[-1],
+                "mean_abs_w_minus_ref_final": float((w.double() - ref.double()).abs().mean()),
+                "drift_every20": [drift[i] for i in range(19, steps, 20)],
+                "oracle_slice": check_elems, "oracle_steps_mismatched": mismatch,
+            }), flush=True)
 
 
 def main(argv=None):
@@ -826,6 +1058,12 @@ def main(argv=None):
         import __graft_entry__
         __graft_entry__.build()
         size_sweep(torch.device("cuda", 0), args.steps if args.steps != 60 else 10)
+        return 0
+    if args.train_report:
+        import torch
+        import __graft_entry__
+        __graft_entry__.build()
+        train_report(torch.device("cuda", 0))
         return 0
     if args.quality:
         import torch
@@ -897,18 +1135,38 @@ def main(argv=None):
     ms_per_step = total_ms / steps
 
     for gi, g in enumerate(groups):
-        g.times_ms = [events[s][gi][0].elapsed_time(events[s][gi][1]) for s in range(steps)]
+        g.step_times_ms = [events[s][gi][0].elapsed_time(events[s][gi][1]) for s in range(steps)]
     bytes_step = sum(g.bytes_per_step for g in groups)
     value = job_gbs(bytes_step, world, ms_per_step)
     peak, peak_kind = measured_peak()
+
+    # per-kernel pass: L2 flushed (clean) before every group, outside its events
+    flush = L2Flush(device)
+    kpass = kernel_pass_steps(steps)
+    kev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in groups] for _ in range(kpass)]
+    for s_ in range(kpass):
+        for gi, g in enumerate(groups):
+            flush()
+            kev[s_][gi][0].record()
+            for c in g.calls:
+                c()
+            kev[s_][gi][1].record()
+    torch.cuda.synchronize()
+    del flush
+    for gi, g in enumerate(groups):
+        g.times_ms = [kev[s_][gi][0].elapsed_time(kev[s_][gi][1]) for s_ in range(kpass)]
 
     kernels = {}
     for g in groups:
         t = statistics.median(g.times_ms)
         gbs = g.bytes_per_step / (t * 1e-3) / 1e9
+        t_step = statistics.median(g.step_times_ms)
         kernels[g.name] = {"gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
                            "ms": round(t, 4), "launches": len(g.calls),
-                           "bytes_per_launch": int(g.bytes_per_launch)}
+                           "bytes_per_launch": int(g.bytes_per_launch),
+                           "ms_in_step": round(t_step, 4),
+                           "frac_in_step": round(g.bytes_per_step / (t_step * 1e-3) / 1e9 / peak, 4)}
     dom = max(groups, key=lambda g: statistics.mean(g.times_ms))
     dom_launch_ms = statistics.mean(dom.times_ms) / len(dom.calls)
     achieved = dom.bytes_per_launch / (dom_launch_ms * 1e-3) / 1e9
@@ -935,9 +1193,15 @@ def main(argv=None):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rates, sample = cpu_oracle_rates()
+        rates, mrates, sample, cores = cpu_oracle_rates()
         cpu = {"value": round(combine_rate(groups, rates), 4), "unit": "GB/s", "cores": 1,
-               "kind": "oracle", "sample": sample}
+               "kind": "oracle", "host_cores": host_cores(), "sample": sample,
+               "per_kernel_gbs": {k: round(v, 4) for k, v in rates.items()}}
+        if mrates:
+            cpu["all_cores"] = {"value": round(combine_rate(groups, mrates), 4), "unit": "GB/s",
+                                "cores": cores,
+                                "how": "the same C oracle on each slice, rows split over "
+                                       "threads"}
 
     if rank == 0:
         line = {
@@ -947,7 +1211,12 @@ def main(argv=None):
             "data": "synthetic",
             "config": {"workload": WORKLOAD + ("_small" if args.small else ""),
                        "elements": st["elements"], "bytes_per_step": int(bytes_step),
-                       "l2": "inputs larger than L2 (the step touches ~58 GB; L2 is 129 MB)",
+                       "l2": ("step: inputs larger than L2 (~58 GB per step, L2 129 MB; every "
+                              "consumer separated from its producer by >= 2.5 GB of other "
+                              "traffic); kernels and roofline: L2 flushed before every group "
+                              "(512 MB written then read back)"),
+                       "train": (f"bench step k = training step k mod {TRAIN_STEPS} of one SR+EF "
+                                 "qdq (amax pass + qdq pass), gradient G_t resident"),
                        "parallelism": f"replicas{world}"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": int(launches), "clocks": clocks, "kernels": kernels,

@@ -214,7 +214,7 @@ def test_nvfp4_roundtrip_workload_full():
 def test_qdq_matches_oracle(rounding, with_g, with_r):
     m = fp4()
     n = 16 * (256 * 4 + 3)
-    w0 = workloads.nvfp4_train_weight(seed=1, shape=(n // 64, 64), device="cpu").view(-1)
+    w0 = workloads.nvfp4_train_weight(seed=1, shape=(n // 16, 16), device="cpu").view(-1)
     g = workloads.nvfp4_train_grad(1, 0, shape=(n,), device="cpu") if with_g else None
     r0 = (torch.randn(n, generator=torch.Generator().manual_seed(2)) * 1e-4) if with_r else None
     w = w0.to(dev())
