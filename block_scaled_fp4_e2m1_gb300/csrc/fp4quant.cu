@@ -4,24 +4,29 @@
 // gets an RMS scale, then a normalized Walsh-Hadamard transform made of
 // additions and subtractions, then an absmax scale into the E2M1 range; both
 // scales travel with the codes.  "Making compression cheap enough to help":
-// the transform exchanges values between the threads of a warp by register
-// shuffles, codes are paired and packed two per byte in registers, and the
-// receiver unpacks, dequantizes and runs the inverse transform.
+// the transform's early stages stay inside a thread, the stages that span
+// threads exchange values through on-chip memory, codes are packed two per
+// byte in registers, and the receiver unpacks, dequantizes and runs the
+// inverse transform.
 //
-// Layout: a thread owns 32 consecutive elements of a group (two 256-bit
-// loads of bf16), so a group of G spans G/32 consecutive lanes (2, 4 or 8)
-// and never leaves its warp: no shared memory and no CTA barrier.
-//   - sum of squares: a balanced pairwise tree over adjacent elements, first
-//     inside the thread (32 -> 1), then across lanes by xor-shuffle 1, 2, ...;
-//   - transform: butterfly stages h = 1 .. 16 inside the thread, stages
-//     h = 32, 64, ... across lanes (lane xor h/32), in the natural
-//     (Sylvester) order; the lower partner keeps a + b, the upper a - b,
-//     computed as one correctly rounded fma(+-1, own, partner).  Holding 32
-//     elements keeps one more stage inside the thread than 16 would: the
-//     shuffles, which bound these kernels, drop by a quarter to a half;
-//   - each thread packs its 32 codes into 16 bytes and stores them directly.
-// The arithmetic order (reciprocal scales, the tree, the stage order) is the
-// one the CPU oracle follows, so codes and scales are bit-exact.
+// Layout.  A group of G elements spans L = G/32 consecutive lanes (2, 4 or
+// 8), never leaving its warp: no CTA barrier.  The transform's stages run in
+// the natural (Sylvester) order h = 1, 2, ..., G/2, which the CPU oracle
+// follows, in two phases:
+//   - phase 1: lane l holds the 32 consecutive elements 32 l .. 32 l + 31 of
+//     the group (two 256-bit loads of bf16), so the sum of squares and the
+//     stages h = 1 .. 16 are in-thread;
+//   - a transpose through a warp-private shared-memory tile: lane l then
+//     holds, for every lane i of its group, the 32/L consecutive elements
+//     32 i + l (32/L) .. of i's chunk; the tile's 16-byte units are placed
+//     so that every 128-bit store and load of a warp is free of bank
+//     conflicts;
+//   - phase 2: the stages h = 32 .. G/2 pair elements of chunks i and
+//     i xor (h/32), now in the same thread.
+// Each stage is one correctly rounded add and subtract per pair, two pairs
+// per packed f32x2 instruction.  The codes (encode) and the values (decode)
+// leave phase 2 as one store per source chunk of 32/L codes or values, the
+// L lanes of a group covering each chunk's row contiguously.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -31,6 +36,9 @@ namespace fp4 {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kE = 32;                      // elements per lane
+constexpr int kTileUnits = 32 * kE / 4;     // 16-byte units of a warp's tile (4 KB)
 
 template <int G>
 __device__ __forceinline__ float wht_norm() {
@@ -38,54 +46,111 @@ __device__ __forceinline__ float wht_norm() {
   return G == 64 ? 0.125f : (G == 256 ? 0.0625f : __uint_as_float(0x3DB504F3u));
 }
 
-// A thread's 32 elements as 16 packed pairs P[i] = (y[i], y[i + 16]), so
-// that the butterfly stages h = 1 .. 8, the cross-lane stages and the final
-// scalings run two elements per instruction; stage h = 16 pairs the two
-// halves of each P[i].  A product that feeds an addition is always formed
-// by a scalar multiply: the compiler may fuse a packed multiply into the
-// packed addition that consumes it (one rounding instead of two), which
-// would break the exact operation order.
-constexpr int kE = 32;  // elements per thread
-
-struct Row32 {
-  F2 p[16];
-  __device__ __forceinline__ float& at(int i) { return i < 16 ? p[i].x : p[i - 16].y; }
-};
-
 __device__ __forceinline__ F2 splat(float v) { return F2{v, v}; }
 
-// Normalized Walsh-Hadamard transform of the group whose elements
-// 32*(lane % (G/32)) .. +31 this thread holds.
+// 32 elements of a lane as 16 packed pairs.  Phase 1: p[t] holds elements
+// 2t, 2t + 1 of the lane's chunk.  Phase 2: p[i * B/2 + t] holds elements
+// 2t, 2t + 1 of the lane's block of chunk i of the group (B = 32/L).
+struct Row32 {
+  F2 p[16];
+};
+
+// A product that feeds an addition is always formed by a scalar multiply:
+// the compiler may fuse a packed multiply into the packed addition that
+// consumes it (one rounding instead of two), which would break the exact
+// operation order.
+
+// Stages h = 1 .. 16 of the transform, inside the thread (phase 1).
+__device__ __forceinline__ void wht_in_thread(Row32& y) {
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {  // h = 1: the two halves of each pair
+    const float a = y.p[t].x, b = y.p[t].y;
+    y.p[t] = F2{__fadd_rn(a, b), __fsub_rn(a, b)};
+  }
+#pragma unroll
+  for (int hp = 1; hp < 16; hp <<= 1) {  // h = 2 hp
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      if (t & hp) continue;
+      const F2 a = y.p[t], b = y.p[t + hp];
+      y.p[t] = add2(a, b);
+      y.p[t + hp] = sub2(a, b);
+    }
+  }
+}
+
+// Stages h = 32 .. G/2 on the phase-2 layout: chunk index bit m of the
+// group is the register block index bit m.
 template <int G>
-__device__ __forceinline__ void wht_group(Row32& y, int lane) {
+__device__ __forceinline__ void wht_across_chunks(Row32& y) {
+  constexpr int L = G / kE, BP = 16 / L;  // pairs per chunk block
 #pragma unroll
-  for (int h = 1; h < 16; h <<= 1) {
+  for (int m = 1; m < L; m <<= 1) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      if (i & h) continue;
-      const F2 a = y.p[i], b = y.p[i + h];
-      y.p[i] = add2(a, b);
-      y.p[i + h] = sub2(a, b);
+    for (int i = 0; i < L; ++i) {
+      if (i & m) continue;
+#pragma unroll
+      for (int t = 0; t < BP; ++t) {
+        const F2 a = y.p[i * BP + t], b = y.p[(i + m) * BP + t];
+        y.p[i * BP + t] = add2(a, b);
+        y.p[(i + m) * BP + t] = sub2(a, b);
+      }
     }
   }
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, F2 a, F2 b) {
+  asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a.x), "f"(a.y),
+               "f"(b.x), "f"(b.y)
+               : "memory");
+}
+
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, F2& a, F2& b) {
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(a.x), "=f"(a.y), "=f"(b.x), "=f"(b.y)
+               : "r"(addr)
+               : "memory");
+}
+
+// The phase-1 -> phase-2 transpose through the warp's tile (kTileUnits
+// 16-byte units at byte address tile).  Row k of a group's region receives
+// block k (elements k B .. k B + B - 1) of every lane of the group; lane
+// src's block goes to column src xor k, and within it 16-byte half h to
+// unit S col + (h xor (g mod S)), S = 8/L units per block.  For a fixed
+// instruction the eight lanes of each quarter-warp then hit eight different
+// units mod 8: no bank conflict, stores and loads alike.
+template <int G>
+__device__ __forceinline__ void transpose_to_blocks(Row32& y, uint32_t tile, int lane) {
+  constexpr int L = G / kE, B = kE / L, S = 8 / L;
+  const int g = lane / L, l = lane % L;
+  const uint32_t region = tile + (uint32_t)(g * L * 8) * 16u;
+  const int hs = g % S;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {  // h = 16
-    const float a = y.p[i].x, b = y.p[i].y;
-    y.p[i] = F2{__fadd_rn(a, b), __fsub_rn(a, b)};
-  }
+  for (int k = 0; k < L; ++k) {
 #pragma unroll
-  for (int m = 1; m < G / kE; m <<= 1) {
-    const F2 sgn = splat((lane & m) ? -1.0f : 1.0f);  // upper partner: partner - own
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const F2 q{__shfl_xor_sync(0xFFFFFFFFu, y.p[i].x, m),
-                 __shfl_xor_sync(0xFFFFFFFFu, y.p[i].y, m)};
-      y.p[i] = fma2(sgn, y.p[i], q);
+    for (int h = 0; h < S; ++h) {
+      const int unit = k * 8 + S * (l ^ k) + (h ^ hs);
+      st_shared_v4(region + 16u * unit, y.p[k * B / 2 + 2 * h], y.p[k * B / 2 + 2 * h + 1]);
     }
   }
-  const F2 c = splat(wht_norm<G>());
+  __syncwarp();
 #pragma unroll
-  for (int i = 0; i < 16; ++i) y.p[i] = mul2(y.p[i], c);
+  for (int i = 0; i < L; ++i) {
+#pragma unroll
+    for (int h = 0; h < S; ++h) {
+      const int unit = l * 8 + S * (i ^ l) + (h ^ hs);
+      ld_shared_v4(region + 16u * unit, y.p[i * B / 2 + 2 * h], y.p[i * B / 2 + 2 * h + 1]);
+    }
+  }
+  __syncwarp();
+}
+
+// max(m, |a|, |b|) in one three-input max (exact; the order of a max does
+// not matter).
+__device__ __forceinline__ float max3_abs(float m, float a, float b) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(m), "f"(fabsf(a)), "f"(fabsf(b)));
+  return r;
 }
 
 template <int G>
@@ -102,78 +167,113 @@ __device__ __forceinline__ float group_max(float v) {
   return v;
 }
 
-template <bool kBF16>
-__device__ __forceinline__ void load32(const void* x, int64_t u, Row32& y) {
-  if (kBF16) {
-    const uint16_t* p = static_cast<const uint16_t*>(x) + kE * u;
-    const U32x8 a = ld_stream_v8(p), b = ld_stream_v8(p + 16);
+// Per-warp staging ring in shared memory for a kernel's input.  A tile is
+// what the warp's 32 lanes consume in one loop step, P 16-byte pieces per
+// lane, contiguous in global memory (lane c's pieces at 16 (P c + q)).  The
+// warp copies a tile with cp.async, piece 32 k + lane in instruction k, so
+// each copy instruction reads 512 contiguous bytes; tiles are copied NS - 1
+// steps ahead of their use, so several tiles per warp are in flight without
+// holding registers.  In shared memory lane c's piece q sits at unit
+// P c + (q xor sw(c)), sw(c) = (c / (8/P)) mod P: the eight lanes of a
+// quarter-warp then touch eight different 16-byte units mod 128 bytes, for
+// the copies and for each lane's 128-bit reads of its own pieces.
+template <int P>
+__device__ __forceinline__ int ring_unit(int c, int q) {
+  return P * c + (q ^ ((c / (8 / P)) & (P - 1)));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool ok) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(ok ? 16 : 0)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool ok) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
+               "r"(ok ? 4 : 0)
+               : "memory");
+}
+
+// Copies the tile at src (valid: its first `valid` bytes exist, a multiple
+// of 16; the rest is zero-filled without reading) into the slot at byte
+// address dst.
+template <int P>
+__device__ __forceinline__ void ring_copy(uint32_t dst, const uint8_t* src, int64_t valid,
+                                          int lane) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      y.p[2 * i].x = bf16_lo(a.w[i]);
-      y.p[2 * i + 1].x = bf16_hi(a.w[i]);
-      y.p[2 * i].y = bf16_lo(b.w[i]);
-      y.p[2 * i + 1].y = bf16_hi(b.w[i]);
+  for (int k = 0; k < P; ++k) {
+    const int p = 32 * k + lane;
+    const bool ok = 16 * (int64_t)p < valid;
+    cp_async16(dst + 16u * ring_unit<P>(p / P, p % P), ok ? src + 16 * p : src, ok);
+  }
+}
+
+template <int P>
+__device__ __forceinline__ void ring_read(uint32_t slot, int lane, uint4 v[P]) {
+#pragma unroll
+  for (int q = 0; q < P; ++q)
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v[q].x), "=r"(v[q].y), "=r"(v[q].z), "=r"(v[q].w)
+                 : "r"(slot + 16u * ring_unit<P>(lane, q))
+                 : "memory");
+}
+
+__device__ __forceinline__ float bf16_lo_(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi_(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// A lane's 32 input elements from its P = 4 (bf16) or 8 (fp32) pieces.
+template <bool kBF16>
+__device__ __forceinline__ void unpack_chunk(const uint4* v, Row32& y) {
+  if (kBF16) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) y.p[4 * q + i] = F2{bf16_lo_(w[i]), bf16_hi_(w[i])};
     }
   } else {
-    const float* p = static_cast<const float*>(x) + kE * u;
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const U32x8 a = ld_stream_v8(p + 8 * k), b = ld_stream_v8(p + 16 + 8 * k);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        y.p[8 * k + i].x = __uint_as_float(a.w[i]);
-        y.p[8 * k + i].y = __uint_as_float(b.w[i]);
-      }
+    for (int q = 0; q < 8; ++q) {
+      y.p[2 * q] = F2{__uint_as_float(v[q].x), __uint_as_float(v[q].y)};
+      y.p[2 * q + 1] = F2{__uint_as_float(v[q].z), __uint_as_float(v[q].w)};
     }
   }
 }
 
-// The raw words of a chunk, fetched one grid-stride step ahead of their use
-// so that a thread's next loads are in flight while it transforms the
-// current chunk (bf16 input: two 256-bit words; fp32 input is loaded when
-// used, four words would cost too many registers).
-struct RawBF16 {
-  U32x8 a, b;
-};
-
-__device__ __forceinline__ void fetch_bf16(const void* x, int64_t u, bool ok, RawBF16& r) {
-  if (ok) {
-    const uint16_t* p = static_cast<const uint16_t*>(x) + kE * u;
-    r.a = ld_stream_v8(p);
-    r.b = ld_stream_v8(p + 16);
+// Stores the B codes of each source chunk of the group: B = 4 -> 2 bytes,
+// 8 -> 4 bytes, 16 -> 8 bytes at byte l B / 2 of the chunk's 16-byte row.
+template <int B>
+__device__ __forceinline__ void store_codes(uint8_t* row, int l, const uint32_t* w) {
+  if (B == 4) {
+    *reinterpret_cast<uint16_t*>(row + 2 * l) = (uint16_t)w[0];
+  } else if (B == 8) {
+    *reinterpret_cast<uint32_t*>(row + 4 * l) = w[0];
+  } else {
+    *reinterpret_cast<uint2*>(row + 8 * l) = make_uint2(w[0], w[1]);
   }
 }
 
-__device__ __forceinline__ void unpack_bf16(const RawBF16& r, bool ok, Row32& y) {
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    y.p[2 * i].x = ok ? bf16_lo(r.a.w[i]) : 0.0f;
-    y.p[2 * i + 1].x = ok ? bf16_hi(r.a.w[i]) : 0.0f;
-    y.p[2 * i].y = ok ? bf16_lo(r.b.w[i]) : 0.0f;
-    y.p[2 * i + 1].y = ok ? bf16_hi(r.b.w[i]) : 0.0f;
-  }
-}
-
-// Units are 32-element chunks; the loop is warp-uniform so that every lane
-// takes part in the shuffles, and lanes past the end compute on zeros
-// without storing (the chunk count is a multiple of G/32, so a group is
-// either entirely inside or entirely past the end).
-// Encodes the chunk u (32 elements in y) and stores its codes and, from the
-// group's first lane, its two scales.
+// Encodes the group chunk set this warp holds (lane chunk u, valid when
+// inside the tensor) and stores codes and scales.  Lanes past the end
+// compute on zeros and store nothing (the chunk count is a multiple of L, so
+// a group is either entirely inside or entirely past the end).
 template <int G>
 __device__ __forceinline__ void encode_chunk(Row32& y, int64_t u, bool valid, int lane,
-                                             uint8_t* __restrict__ packed,
+                                             uint32_t tile, uint8_t* __restrict__ packed,
                                              float* __restrict__ s1_out,
                                              float* __restrict__ s2_out) {
-  constexpr int LPG = G / kE;
-  // RMS scale: the pairwise tree over adjacent squares, levels 1-4 two
-  // sums per instruction ((0..15 | 16..31) halves side by side)
-  F2 sq[16];
+  constexpr int L = G / kE, B = kE / L;
+  // RMS scale: the pairwise tree over adjacent squares, levels 2-5 two sums
+  // per instruction (the halves 0..15 | 16..31 side by side)
+  F2 sq[8];
 #pragma unroll
-  for (int i = 0; i < 16; ++i)
-    sq[i] = F2{__fmul_rn(y.p[i].x, y.p[i].x), __fmul_rn(y.p[i].y, y.p[i].y)};
+  for (int i = 0; i < 8; ++i) {
+    const F2 a = y.p[i], b = y.p[8 + i];
+    sq[i] = F2{__fadd_rn(__fmul_rn(a.x, a.x), __fmul_rn(a.y, a.y)),
+               __fadd_rn(__fmul_rn(b.x, b.x), __fmul_rn(b.y, b.y))};
+  }
 #pragma unroll
-  for (int w = 16; w > 1; w >>= 1) {
+  for (int w = 8; w > 1; w >>= 1) {
 #pragma unroll
     for (int i = 0; i < w / 2; ++i) sq[i] = add2(sq[2 * i], sq[2 * i + 1]);
   }
@@ -182,70 +282,96 @@ __device__ __forceinline__ void encode_chunk(Row32& y, int64_t u, bool valid, in
   const float inv1 = rms == 0.0f ? 0.0f : __frcp_rn(rms);
 #pragma unroll
   for (int i = 0; i < 16; ++i) y.p[i] = F2{__fmul_rn(y.p[i].x, inv1), __fmul_rn(y.p[i].y, inv1)};
-  // transform
-  wht_group<G>(y, lane);
+  // transform: stages 1..16, transpose, stages 32..G/2, normalization
+  wht_in_thread(y);
+  transpose_to_blocks<G>(y, tile, lane);
+  wht_across_chunks<G>(y);
+  const F2 c = splat(wht_norm<G>());
+#pragma unroll
+  for (int i = 0; i < 16; ++i) y.p[i] = mul2(y.p[i], c);
   // absmax scale into [-6, 6]
   float zmax = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) zmax = fmaxf(zmax, fmaxf(fabsf(y.p[i].x), fabsf(y.p[i].y)));
+  for (int i = 0; i < 16; ++i) zmax = max3_abs(zmax, y.p[i].x, y.p[i].y);
   zmax = group_max<G>(zmax);
   const float sc2 = __fdiv_rn(zmax, 6.0f);
   const F2 inv2 = splat(sc2 == 0.0f ? 0.0f : __frcp_rn(sc2));
 #pragma unroll
   for (int i = 0; i < 16; ++i) y.p[i] = mul2(y.p[i], inv2);
-  uint32_t w[4];
+  if (!valid) return;
+  const int l = lane % L;
+  uint8_t* const rows = packed + 16 * (u - l);  // the group's first chunk
 #pragma unroll
-  for (int k = 0; k < 4; ++k)
-    w[k] = cvt_e2m1x8(y.at(8 * k), y.at(8 * k + 1), y.at(8 * k + 2), y.at(8 * k + 3),
-                      y.at(8 * k + 4), y.at(8 * k + 5), y.at(8 * k + 6), y.at(8 * k + 7));
-  if (valid) {
-    *reinterpret_cast<uint4*>(packed + 16 * u) = make_uint4(w[0], w[1], w[2], w[3]);
-    if ((lane & (LPG - 1)) == 0) {
-      s1_out[u / LPG] = rms;
-      s2_out[u / LPG] = sc2;
+  for (int i = 0; i < L; ++i) {
+    const F2* q = y.p + i * (B / 2);
+    uint32_t w[2];
+    if (B == 4) {
+      w[0] = cvt_e2m1x2(q[0].x, q[0].y) | (cvt_e2m1x2(q[1].x, q[1].y) << 8);
+    } else {
+#pragma unroll
+      for (int k = 0; k < B / 8; ++k)
+        w[k] = cvt_e2m1x8(q[4 * k].x, q[4 * k].y, q[4 * k + 1].x, q[4 * k + 1].y,
+                          q[4 * k + 2].x, q[4 * k + 2].y, q[4 * k + 3].x, q[4 * k + 3].y);
     }
+    store_codes<B>(rows + 16 * i, l, w);
+  }
+  if (l == 0) {
+    s1_out[u / L] = rms;
+    s2_out[u / L] = sc2;
   }
 }
 
-// bf16 input keeps the next chunk's loads in flight (a two-buffer ring
-// walked by an unrolled loop, so no registers are copied); fp32 input loads
-// each chunk when it is used.
+// Input pieces per lane and staged tiles per warp of the encode kernels.
+// (bf16: 8 KB per warp with the transpose tile, three CTAs of 256 threads
+// per SM at 80 registers; fp32: 12 KB per warp, two CTAs.  Measured on
+// GB300: a third staged tile or two CTAs of up to 128 registers ran no
+// faster.)
+template <bool kBF16>
+struct EncRing {
+  static constexpr int P = kBF16 ? 4 : 8;            // 64 or 128 bytes per lane
+  static constexpr int NS = 2;                       // tiles per warp ring
+  static constexpr int kSlot = 32 * 16 * P;          // bytes per tile
+  static constexpr size_t kSmem = (size_t)kWarps * (NS * kSlot + 16 * kTileUnits);
+};
+
+// The loop walks 32-chunk tiles, one per warp per grid-stride step, and is
+// warp-uniform so that every lane takes part in the exchanges.  Each warp
+// stages its tiles NS - 1 steps ahead in its shared-memory ring (one
+// cp.async group per tile, committed even when empty); the transpose's
+// __syncwarp calls order a slot's reads before its next copy.
 template <int G, bool kBF16>
-__global__ void __launch_bounds__(kThreads, kBF16 ? 2 : 3)
+__global__ void __launch_bounds__(kThreads, kBF16 ? 3 : 2)
     encode_kernel(const void* __restrict__ x, int64_t nchunks, uint8_t* __restrict__ packed,
                   float* __restrict__ s1_out, float* __restrict__ s2_out) {
-  const int lane = threadIdx.x & 31;
+  using R = EncRing<kBF16>;
+  extern __shared__ __align__(16) uint8_t enc_smem[];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const uint32_t smem = (uint32_t)__cvta_generic_to_shared(enc_smem);
+  const uint32_t ring = smem + (uint32_t)(wid * R::NS * R::kSlot);
+  const uint32_t tile = smem + (uint32_t)(kWarps * R::NS * R::kSlot + wid * 16 * kTileUnits);
   const int64_t stride = (int64_t)gridDim.x * kThreads;
+  const int64_t ubytes = 16 * R::P;  // input bytes per chunk
+  const uint8_t* const xb = static_cast<const uint8_t*>(x);
   int64_t u0 = (int64_t)blockIdx.x * kThreads + (threadIdx.x & ~31);
-  if (kBF16) {
-    RawBF16 ring[2];
-    fetch_bf16(x, u0 + lane, u0 + lane < nchunks, ring[0]);
-    for (;;) {
+  auto stage = [&](int64_t t0, int slot) {
+    if (t0 < nchunks)
+      ring_copy<R::P>(ring + slot * R::kSlot, xb + ubytes * t0, (nchunks - t0) * ubytes, lane);
+    cp_async_commit();
+  };
 #pragma unroll
-      for (int s = 0; s < 2; ++s) {
-        if (u0 >= nchunks) return;
-        const int64_t u = u0 + lane;
-        fetch_bf16(x, u + stride, u + stride < nchunks, ring[s ^ 1]);
-        Row32 y;
-        unpack_bf16(ring[s], u < nchunks, y);
-        encode_chunk<G>(y, u, u < nchunks, lane, packed, s1_out, s2_out);
-        u0 += stride;
-      }
-    }
-  } else {
-    for (; u0 < nchunks; u0 += stride) {
-      const int64_t u = u0 + lane;
-      const bool valid = u < nchunks;
-      Row32 y;
-      if (valid) {
-        load32<false>(x, u, y);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) y.p[i] = splat(0.0f);
-      }
-      encode_chunk<G>(y, u, valid, lane, packed, s1_out, s2_out);
-    }
+  for (int k = 0; k < R::NS - 1; ++k) stage(u0 + k * stride, k);
+  for (int t = 0; u0 < nchunks; ++t, u0 += stride) {
+    stage(u0 + (R::NS - 1) * stride, (t + R::NS - 1) % R::NS);
+    cp_async_wait<R::NS - 1>();
+    __syncwarp();
+    const int64_t u = u0 + lane;
+    uint4 v[R::P];
+    ring_read<R::P>(ring + (t % R::NS) * R::kSlot, lane, v);
+    Row32 y;
+    unpack_chunk<kBF16>(v, y);
+    encode_chunk<G>(y, u, u < nchunks, lane, tile, packed, s1_out, s2_out);
   }
+  cp_async_wait<0>();
 }
 
 // The 8 codes of w (code i in bits 4i+3..4i) as exact floats, through the
@@ -264,100 +390,158 @@ __device__ __forceinline__ void e2m1x8_values(uint32_t w, float o[8]) {
   }
 }
 
-// A chunk's codes and its group's two scales.
-struct DecIn {
-  uint4 p;
-  float sc1, sc2;
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// Staged tiles of the decode kernels: per tile the 32 chunks' codes (16
+// bytes per lane) and the s1, s2 of its 32/L groups.
+template <int G>
+struct DecRing {
+  static constexpr int L = G / kE, NG = 32 / L;
+  static constexpr int NS = 4;                       // tiles per warp ring
+  static constexpr int kSlot = 512 + 8 * NG;         // bytes per tile (multiple of 16)
+  static constexpr size_t kSmem = (size_t)kWarps * (NS * kSlot + 16 * kTileUnits);
 };
 
-template <int G>
-__device__ __forceinline__ void fetch_dec(const uint8_t* __restrict__ packed,
-                                          const float* __restrict__ s1_in,
-                                          const float* __restrict__ s2_in, int64_t u, bool ok,
-                                          DecIn& d) {
-  constexpr int LPG = G / kE;
-  if (ok) {
-    d.p = ld_stream_v4(packed + 16 * u);
-    d.sc1 = s1_in[u / LPG];
-    d.sc2 = s2_in[u / LPG];
+// Stores the B values of each source chunk: bf16 B = 4, 8, 16 -> 8, 16, 32
+// bytes; fp32 -> 16, 32, 64 bytes, at element l B of the chunk's row.
+template <int B, bool kBF16Out>
+__device__ __forceinline__ void store_values(void* out, int64_t chunk, int l, const F2* q) {
+  if (kBF16Out) {
+    uint16_t* o = static_cast<uint16_t*>(out) + kE * chunk + B * l;
+    uint32_t w[B / 2];
+#pragma unroll
+    for (int t = 0; t < B / 2; ++t) w[t] = pack_bf16x2(q[t].x, q[t].y);
+    if (B == 4) {
+      *reinterpret_cast<uint2*>(o) = make_uint2(w[0], w[1]);
+    } else if (B == 8) {
+      *reinterpret_cast<uint4*>(o) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+      U32x8 v;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) v.w[t] = w[t];
+      st_v8(o, v);
+    }
   } else {
-    d.p = make_uint4(0u, 0u, 0u, 0u);
-    d.sc1 = d.sc2 = 0.0f;
+    float* o = static_cast<float*>(out) + kE * chunk + B * l;
+    if (B == 4) {
+      *reinterpret_cast<float4*>(o) = make_float4(q[0].x, q[0].y, q[1].x, q[1].y);
+    } else {
+#pragma unroll
+      for (int k = 0; k < B / 8; ++k) {
+        U32x8 v;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          v.w[2 * t] = __float_as_uint(q[4 * k + t].x);
+          v.w[2 * t + 1] = __float_as_uint(q[4 * k + t].y);
+        }
+        st_v8(o + 8 * k, v);
+      }
+    }
   }
 }
 
-// The next chunk's codes and scales are in flight while the current one is
-// decoded (a two-buffer ring walked by an unrolled loop).
+// Tiles are staged NS - 1 loop steps ahead in the warp's ring, as in the
+// encode kernels.
 template <int G, bool kBF16Out>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const uint8_t* __restrict__ packed, const float* __restrict__ s1_in,
                   const float* __restrict__ s2_in, int64_t nchunks, void* __restrict__ out) {
-  const int lane = threadIdx.x & 31;
+  using R = DecRing<G>;
+  constexpr int L = G / kE, B = kE / L, NG = R::NG;
+  extern __shared__ __align__(16) uint8_t dec_smem[];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int l = lane % L;
+  const uint32_t smem = (uint32_t)__cvta_generic_to_shared(dec_smem);
+  const uint32_t ring = smem + (uint32_t)(wid * R::NS * R::kSlot);
+  const uint32_t tile = smem + (uint32_t)(kWarps * R::NS * R::kSlot + wid * 16 * kTileUnits);
   const int64_t stride = (int64_t)gridDim.x * kThreads;
+  const int64_t ngroups = nchunks / L;
   int64_t u0 = (int64_t)blockIdx.x * kThreads + (threadIdx.x & ~31);
-  DecIn ring[2];
-  fetch_dec<G>(packed, s1_in, s2_in, u0 + lane, u0 + lane < nchunks, ring[0]);
-  for (;;) {
+  auto stage = [&](int64_t t0, int slot) {
+    if (t0 < nchunks) {
+      const uint32_t dst = ring + slot * R::kSlot;
+      ring_copy<1>(dst, packed + 16 * t0, (nchunks - t0) * 16, lane);
+      const int64_t gi = t0 / L + (lane % NG);
+      const bool ok = lane < 2 * NG && gi < ngroups;
+      const float* src = lane < NG ? s1_in : s2_in;
+      if (lane < 2 * NG) cp_async4(dst + 512u + 4u * lane, ok ? src + gi : src, ok);
+    }
+    cp_async_commit();
+  };
 #pragma unroll
-    for (int s = 0; s < 2; ++s) {
-      if (u0 >= nchunks) return;
-      const int64_t u = u0 + lane;
-      const bool valid = u < nchunks;
-      fetch_dec<G>(packed, s1_in, s2_in, u + stride, u + stride < nchunks, ring[s ^ 1]);
-      const DecIn& d = ring[s];
-      float v[32];
-      e2m1x8_values(d.p.x, v);
-      e2m1x8_values(d.p.y, v + 8);
-      e2m1x8_values(d.p.z, v + 16);
-      e2m1x8_values(d.p.w, v + 24);
-      Row32 z;
+  for (int k = 0; k < R::NS - 1; ++k) stage(u0 + k * stride, k);
+  for (int t = 0; u0 < nchunks; ++t, u0 += stride) {
+    stage(u0 + (R::NS - 1) * stride, (t + R::NS - 1) % R::NS);
+    cp_async_wait<R::NS - 1>();
+    __syncwarp();
+    const int64_t u = u0 + lane;
+    const bool valid = u < nchunks;
+    const uint32_t slot = ring + (t % R::NS) * R::kSlot;
+    uint4 pk[1];
+    ring_read<1>(slot, lane, pk);
+    const float sc1 = ld_shared_f32(slot + 512u + 4u * (lane / L));
+    const float sc2 = ld_shared_f32(slot + 512u + 4u * (NG + lane / L));
+    Row32 z;
+    const uint32_t words[4] = {pk[0].x, pk[0].y, pk[0].z, pk[0].w};
 #pragma unroll
-      for (int i = 0; i < 16; ++i) z.p[i] = F2{__fmul_rn(v[i], d.sc2), __fmul_rn(v[i + 16], d.sc2)};
-      wht_group<G>(z, lane);
-      const F2 m1 = splat(d.sc1);
+    for (int k = 0; k < 4; ++k) {
+      float v[8];
+      e2m1x8_values(words[k], v);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) z.p[i] = mul2(z.p[i], m1);
-      if (valid) {
-        if (kBF16Out) {
-          uint16_t* o = static_cast<uint16_t*>(out) + kE * u;
+      for (int i = 0; i < 4; ++i)
+        z.p[4 * k + i] = F2{__fmul_rn(v[2 * i], sc2), __fmul_rn(v[2 * i + 1], sc2)};
+    }
+    wht_in_thread(z);
+    transpose_to_blocks<G>(z, tile, lane);
+    wht_across_chunks<G>(z);
+    const F2 m = splat(wht_norm<G>());
 #pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            U32x8 w;
+    for (int i = 0; i < 16; ++i) z.p[i] = mul2(z.p[i], m);
+    // x' = y' s1 with the group's s1 (every lane of a group holds it)
+    const F2 m1 = splat(sc1);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              w.w[i] = pack_bf16x2(z.at(16 * k + 2 * i), z.at(16 * k + 2 * i + 1));
-            st_v8(o + 16 * k, w);
-          }
-        } else {
-          float* o = static_cast<float*>(out) + kE * u;
+    for (int i = 0; i < 16; ++i) z.p[i] = mul2(z.p[i], m1);
+    if (valid) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            U32x8 w;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) w.w[i] = __float_as_uint(z.at(8 * k + i));
-            st_v8(o + 8 * k, w);
-          }
-        }
-      }
-      u0 += stride;
+      for (int i = 0; i < L; ++i) store_values<B, kBF16Out>(out, u - l + i, l, z.p + i * (B / 2));
     }
   }
+  cp_async_wait<0>();
+}
+
+template <int G, bool kBF16>
+fp4_status launch_encode_t(const void* x, int64_t nchunks, uint8_t* packed, float* s1, float* s2,
+                           cudaStream_t s) {
+  constexpr size_t smem = EncRing<kBF16>::kSmem;
+  if (!allow_dynamic_smem<encode_kernel<G, kBF16>>(smem)) return FP4_ERR_CUDA;
+  return launch<encode_kernel<G, kBF16>>(nchunks, kThreads, smem, s, x, nchunks, packed, s1, s2);
 }
 
 template <int G>
 fp4_status launch_encode(const void* x, int dtype, int64_t nchunks, uint8_t* packed, float* s1,
                          float* s2, cudaStream_t s) {
-  if (dtype == FP4_BF16)
-    return launch<encode_kernel<G, true>>(nchunks, kThreads, 0, s, x, nchunks, packed, s1, s2);
-  return launch<encode_kernel<G, false>>(nchunks, kThreads, 0, s, x, nchunks, packed, s1, s2);
+  if (dtype == FP4_BF16) return launch_encode_t<G, true>(x, nchunks, packed, s1, s2, s);
+  return launch_encode_t<G, false>(x, nchunks, packed, s1, s2, s);
+}
+
+template <int G, bool kBF16Out>
+fp4_status launch_decode_t(const uint8_t* packed, const float* s1, const float* s2,
+                           int64_t nchunks, void* y, cudaStream_t s) {
+  constexpr size_t smem = DecRing<G>::kSmem;
+  if (!allow_dynamic_smem<decode_kernel<G, kBF16Out>>(smem)) return FP4_ERR_CUDA;
+  return launch<decode_kernel<G, kBF16Out>>(nchunks, kThreads, smem, s, packed, s1, s2, nchunks,
+                                            y);
 }
 
 template <int G>
 fp4_status launch_decode(const uint8_t* packed, const float* s1, const float* s2, int64_t nchunks,
                          void* y, int dtype, cudaStream_t s) {
-  if (dtype == FP4_BF16)
-    return launch<decode_kernel<G, true>>(nchunks, kThreads, 0, s, packed, s1, s2, nchunks, y);
-  return launch<decode_kernel<G, false>>(nchunks, kThreads, 0, s, packed, s1, s2, nchunks, y);
+  if (dtype == FP4_BF16) return launch_decode_t<G, true>(packed, s1, s2, nchunks, y, s);
+  return launch_decode_t<G, false>(packed, s1, s2, nchunks, y, s);
 }
 
 bool group_ok(int g) { return g == 64 || g == 128 || g == 256; }
