@@ -74,10 +74,14 @@ float ora_bf16_value(uint16_t b);
  * random numbers: as easy as 1, 2, 3" (SC'11). */
 void ora_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
 
-/* The 32-bit random word for flat element index g of a tensor quantized at
- * (seed, step): counter (g>>2 lo, g>>2 hi, step lo, step hi), key (seed lo,
- * seed hi), word g & 3.  [fp4-train] "How it works" (counter-based RNG keyed
- * on seed, step and global index). */
+/* The random word for flat element index g of a tensor quantized at (seed,
+ * step): a 16-bit uniform h, returned as h << 16 so that the stochastic rule's
+ * u = (word >> 8) * 2^-24 is h * 2^-16.  h is half g & 1 (low half first) of
+ * word (g >> 1) & 3 of Philox4x32-10 at counter (g>>3 lo, g>>3 hi, step lo,
+ * step hi), key (seed lo, seed hi): one call serves eight elements.
+ * [fp4-train] "How it works" (counter-based RNG keyed on seed, step and
+ * global index; the upper neighbour taken with probability equal to the
+ * fractional distance, here to within 2^-16). */
 uint32_t ora_rng_word(uint64_t seed, uint64_t step, uint64_t g);
 
 /* ------------------------------------------------------------------ NVFP4 */

@@ -35,11 +35,14 @@ void ora_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t ou
 }
 
 uint32_t ora_rng_word(uint64_t seed, uint64_t step, uint64_t g) {
-  uint64_t quad = g >> 2;
-  uint32_t ctr[4] = {(uint32_t)quad, (uint32_t)(quad >> 32), (uint32_t)step,
+  /* eight elements per Philox call: element g takes the 16-bit half g & 1 of
+   * word (g >> 1) & 3 of the block at counter g >> 3 */
+  uint64_t oct = g >> 3;
+  uint32_t ctr[4] = {(uint32_t)oct, (uint32_t)(oct >> 32), (uint32_t)step,
                      (uint32_t)(step >> 32)};
   uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
   uint32_t out[4];
   ora_philox4x32_10(ctr, key, out);
-  return out[g & 3];
+  uint32_t h = (out[(g >> 1) & 3] >> (16 * (g & 1))) & 0xFFFFu;
+  return h << 16;
 }

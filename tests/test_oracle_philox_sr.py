@@ -60,26 +60,33 @@ def test_philox_matches_curand_host(seed):
 
 
 def test_rng_word_layout():
-    # element g draws word g & 3 of Philox(counter = (g>>2, step), key = seed)
+    # element g takes the 16-bit half g & 1 of word (g >> 1) & 3 of
+    # Philox(counter = (g >> 3, step), key = seed), in the word's top half
     seed, step = 0xDEADBEEF12345678, (7 << 32) | 3
-    g = np.array([0, 1, 2, 3, 4, 5, (1 << 33) + 2], np.uint64)
+    g = np.array([0, 1, 2, 3, 4, 5, 6, 7, 8, 9, (1 << 33) + 2, (1 << 33) + 7], np.uint64)
     words = ora.rng_words(seed, step, g)
     key = [seed & 0xFFFFFFFF, seed >> 32]
     for gi, w in zip(g.tolist(), words.tolist()):
-        q = gi >> 2
-        blk = ora.philox4x32_10([q & 0xFFFFFFFF, q >> 32, step & 0xFFFFFFFF, step >> 32], key)
-        assert w == int(blk[gi & 3])
+        o = gi >> 3
+        blk = ora.philox4x32_10([o & 0xFFFFFFFF, o >> 32, step & 0xFFFFFFFF, step >> 32], key)
+        h = (int(blk[(gi >> 1) & 3]) >> (16 * (gi & 1))) & 0xFFFF
+        assert w == h << 16
 
 
 def test_philox_uniformity_chi_square():
     g = np.arange(1 << 18, dtype=np.uint64)
     w = ora.rng_words(0, 0, g)
+    assert np.all((w & 0xFFFF) == 0)
     top = (w >> 24).astype(np.int64)          # 256 bins of the top byte
     counts = np.bincount(top, minlength=256)
     chi2, p = stats.chisquare(counts)
     assert p > 1e-4, (chi2, p)
-    bits = np.unpackbits(w.view(np.uint8)).reshape(-1, 32).mean(axis=0)
+    h = (w >> 16).astype(np.uint16)
+    bits = np.unpackbits(h.view(np.uint8)).reshape(-1, 16).mean(axis=0)
     assert np.all(np.abs(bits - 0.5) < 0.01)
+    # the two halves of one Philox word and the 8 elements of one call are
+    # unrelated: neighbouring elements agree no more often than chance
+    assert np.mean(h[0::2] == h[1::2]) < 1e-3
     # different steps give unrelated streams
     w2 = ora.rng_words(0, 1, g)
     assert np.mean(w == w2) < 1e-3
