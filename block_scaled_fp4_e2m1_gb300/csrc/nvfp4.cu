@@ -103,7 +103,7 @@ struct QuantPipe {
 // few more registers than 64.
 template <bool kBF16, bool kSR, bool kRes, bool kBlk>
 constexpr int quantize_min_ctas() {
-  return kRes ? 2 : ((kSR || !kBF16 || kBlk) ? 3 : 4);
+  return (kRes || kSR) ? 2 : ((!kBF16 || kBlk) ? 3 : 4);
 }
 
 // A thread quantizes one block per grid-stride step; the loads of the next

@@ -134,7 +134,7 @@ __device__ __noinline__ uint32_t exact_e2m1_quotient(float x, float y) {
 }
 
 // The stochastic-rounding code of RN(x / y) by the rule of e2m1_sr, with an
-// exact division (the fallback of sr_code_certified).
+// exact division (the fallback of sr_codes8).
 __device__ __noinline__ uint32_t exact_e2m1_sr_quotient(float x, float y, uint32_t rw) {
   return e2m1_sr(y == 0.0f ? __fmul_rn(x, 0.0f) : __fdiv_rn(x, y), rw);
 }
@@ -142,35 +142,88 @@ __device__ __noinline__ uint32_t exact_e2m1_sr_quotient(float x, float y, uint32
 // Stochastic rounding without a division.  For m = |a| < 6 the code of
 // e2m1_sr is c + [u < frac], c the grid interval of m and frac its position
 // in it; with the position s = c + frac that is ceil(s - u) (u < 1), and
-// s(m) is piecewise linear: 2m below 2, m + 2 on [2, 4), m/2 + 4 on [4, 6),
-// and 7 from 6 on (code 7), which is min(2m, m + 2, m/2 + 4, 7).  Here a = RN(x / eff) is replaced by
+// s(m) is piecewise linear and continuous: 2m below 2, m + 2 on [2, 4),
+// m/2 + 4 on [4, 6), and 7 from 6 on (code 7), which is
+// min(2m, m + 2, m/2 + 4, 7).  Here a = RN(x / eff) is replaced by
 // q = RN(x * inv), inv = RN(1/eff) with eff in [2^-125, 2^125]:
-// |q - a| <= 1.5 * 2^-23 |x / eff|, so with slopes <= 2 the position moves
-// by at most 1.5 * 2^-21, and the two fp32 roundings of s and s - u add at
-// most 2^-21.  Hence when t = s(q) - u lies more than 2^-19 from every
-// integer, ceil(t) is the code of a; returns false otherwise (and for NaN),
-// which is about one element in 10^5.  Subnormal quotients have absolute
-// errors far below the margin.
+// |q - a| <= 1.5 * 2^-23 |x / eff|, and with slopes <= 2 the position moves
+// by at most 1.5 * 2^-21.  The code is taken as RN(T) with
+// T = RN(min(2m + 1/2, m + 5/2, m/2 + 9/2, 15/2) - u) ~ ceil(s - u) + ...:
+// ceil(t) = RN(t + 1/2) for non-integer t.  The roundings of the pieces and
+// of the difference add at most 2^-21 + 2^-22, so T is within 2^-19 of
+// t + 1/2, t = s(a) - u; when T lies more than 2^-19 inside its rounding
+// interval, RN(T) is a's code.  Otherwise (about one element in 10^5, and
+// NaN) the element is settled exactly.
 //
-// Two equal ways to form s: kMin takes the least of the pieces (s is
-// concave, and RN is monotone, so the least rounded piece is the rounded
-// least piece), the other selects the piece by comparing m.  Measured on
-// GB300, the least-of form is faster in the plain stochastic quantizer and
-// the selecting form in the error-feedback kernels.
-template <bool kMin>
-__device__ __forceinline__ bool sr_code_certified(float x, float inv, uint32_t rw,
-                                                  uint32_t& code) {
-  const float m = fabsf(__fmul_rn(x, inv));
-  const float s = kMin ? fminf(fminf(__fmul_rn(m, 2.0f), __fadd_rn(m, 2.0f)),
-                               fminf(__fmaf_rn(m, 0.5f, 4.0f), 7.0f))
-                       : (m < 2.0f   ? __fmul_rn(m, 2.0f)
-                          : m < 4.0f ? __fadd_rn(m, 2.0f)
-                          : m < 6.0f ? __fmaf_rn(m, 0.5f, 4.0f)
-                                     : 7.0f);
-  const float t = __fsub_rn(s, __fmul_rn((float)(rw >> 8), 0x1p-24f));
-  const float r = __fsub_rn(t, rintf(t));
-  code = ((__float_as_uint(x) >> 28) & 8u) | (uint32_t)(int)ceilf(t);
-  return fabsf(r) > 0x1p-19f && m == m;
+// The arithmetic is branch-free and mostly packed:
+//   - u = h 2^-16, the 16-bit uniform, as (128 + h 2^-16) - 128, where the
+//     float 128 + h 2^-16 is the bit pattern 0x4300 0000 | h (one byte
+//     permute);
+//   - RN(T) lands in the low bits of F = T + C, C = 1.5 * 2^23 (+8 for a
+//     negative x, so the low nibble of F is the whole E2M1 code);
+//   - T - (F - C) is exact and is T's distance from its rounded value;
+//   - each nibble is inserted into the code word with one bit-field insert.
+
+__device__ __forceinline__ uint32_t prmt_bytes(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+// min(a, b, c) with NaN propagated (a NaN position is never certified).
+__device__ __forceinline__ float min3_nan(float a, float b, float c) {
+  float r;
+  asm("min.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+__device__ __forceinline__ float min_nan(float a, float b) {
+  float r;
+  asm("min.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+constexpr uint32_t kSrMagic = 0x4B400000u;  // 1.5 * 2^23
+
+// Bits pos .. pos+3 of b replaced by the low four bits of a.
+__device__ __forceinline__ uint32_t insert_nibble(uint32_t a, uint32_t b, uint32_t pos) {
+  uint32_t r;
+  asm("bfi.b32 %0, %1, %2, %3, 4;" : "=r"(r) : "r"(a), "r"(b), "r"(pos));
+  return r;
+}
+
+// The stochastic codes of the eight elements x[0..7] (a multiple of eight
+// apart from the tensor's start) from one Philox block r, by the certified
+// rule above: element i draws the 16-bit half i & 1 (low first) of word
+// i >> 1.  Returns the eight codes as nibbles; bit i of pend is set where
+// element i is not certified and its nibble must be replaced.
+__device__ __forceinline__ uint32_t sr_codes8(const float x[8], float inv, const Philox4& r,
+                                              uint32_t& pend) {
+  const uint32_t words[4] = {r.x, r.y, r.z, r.w};
+  uint32_t acc = 0u;
+  pend = 0u;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int i = 2 * k;
+    const F2 ux{__uint_as_float(prmt_bytes(words[k], 0x43000000u, 0x7410u)),
+                __uint_as_float(prmt_bytes(words[k], 0x43000000u, 0x7432u))};
+    const F2 u = sub2(ux, F2{128.0f, 128.0f});                        // exact
+    const F2 m{fabsf(__fmul_rn(x[i], inv)), fabsf(__fmul_rn(x[i + 1], inv))};
+    const F2 p2 = fma2(m, F2{2.0f, 2.0f}, F2{0.5f, 0.5f});
+    const F2 p1 = add2(m, F2{2.5f, 2.5f});
+    const F2 ph = fma2(m, F2{0.5f, 0.5f}, F2{4.5f, 4.5f});
+    const F2 sh{min_nan(min3_nan(p2.x, p1.x, ph.x), 7.5f), min_nan(min3_nan(p2.y, p1.y, ph.y), 7.5f)};
+    const F2 T = sub2(sh, u);
+    const F2 C{__uint_as_float(kSrMagic | ((__float_as_uint(x[i]) >> 28) & 8u)),
+               __uint_as_float(kSrMagic | ((__float_as_uint(x[i + 1]) >> 28) & 8u))};
+    const F2 F = add2(T, C);
+    const F2 d = sub2(T, sub2(F, C));
+    acc = insert_nibble(__float_as_uint(F.x), acc, 4 * i);
+    acc = insert_nibble(__float_as_uint(F.y), acc, 4 * i + 4);
+    if (!(fabsf(d.x) < 0.5f - 0x1p-19f)) pend |= 1u << i;
+    if (!(fabsf(d.y) < 0.5f - 0x1p-19f)) pend |= 2u << i;
+  }
+  return acc;
 }
 
 // Settling a bracket that straddles a rounding midpoint, without dividing.
@@ -255,31 +308,25 @@ __device__ __forceinline__ uint32_t quantize_block(const float v[16], float s_t,
   const float eff = __fmul_rn(e4m3_value(sb), s_t);
   uint32_t w0, w1;
   if (kSR) {
-    // codes by sr_code_certified; the few uncertified elements (and every
-    // element when eff is outside the certified range) take the exact
-    // division afterwards, their random word drawn again
+    // codes by sr_codes8, eight elements per Philox block at counter
+    // (g0 >> 3) + k; the few uncertified elements (and every element when
+    // eff is outside the certified range) take the exact division
+    // afterwards, their random half drawn again
     const bool fast = eff >= 0x1p-125f && eff <= 0x1p125f;
     const float inv = fast ? __frcp_rn(eff) : 0.0f;
     uint32_t pend = 0u;  // bit i: element i still to settle
-    w0 = w1 = 0;
+    uint32_t ww[2];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint64_t quad = (g0 >> 2) + (uint64_t)k;
-      const Philox4 r = philox4x32_10((uint32_t)quad, (uint32_t)(quad >> 32), step0, step1, key0,
+    for (int k = 0; k < 2; ++k) {
+      const uint64_t oct = (g0 >> 3) + (uint64_t)k;
+      const Philox4 r = philox4x32_10((uint32_t)oct, (uint32_t)(oct >> 32), step0, step1, key0,
                                       key1);
-      const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int i = 4 * k + j;
-        uint32_t code;
-        const bool ok = sr_code_certified<!kEF>(v[i], inv, rw[j], code) && fast;
-        if (i < 8)
-          w0 |= (ok ? code : 0u) << (4 * i);
-        else
-          w1 |= (ok ? code : 0u) << (4 * (i - 8));
-        pend |= (ok ? 0u : 1u) << i;
-      }
+      uint32_t pk;
+      ww[k] = sr_codes8(v + 8 * k, inv, r, pk);
+      pend |= (fast ? pk : 0xFFu) << (8 * k);
     }
+    w0 = ww[0];
+    w1 = ww[1];
     while (pend != 0u) {
       const int i = __ffs(pend) - 1;
       pend &= pend - 1u;
@@ -293,16 +340,18 @@ __device__ __forceinline__ uint32_t quantize_block(const float v[16], float s_t,
 #pragma unroll
       for (int t = 0; t < 2; ++t) e[t] = b2 ? e[2 * t + 1] : e[2 * t];
       const float xi = b3 ? e[1] : e[0];
-      const uint64_t quad = (g0 >> 2) + (uint64_t)(i >> 2);
-      const Philox4 r = philox4x32_10((uint32_t)quad, (uint32_t)(quad >> 32), step0, step1, key0,
+      const uint64_t oct = (g0 >> 3) + (uint64_t)(i >> 3);
+      const Philox4 r = philox4x32_10((uint32_t)oct, (uint32_t)(oct >> 32), step0, step1, key0,
                                       key1);
-      const int j = i & 3;
-      const uint32_t rwi = j == 0 ? r.x : j == 1 ? r.y : j == 2 ? r.z : r.w;
+      const int j = (i >> 1) & 3;
+      const uint32_t wj = j == 0 ? r.x : j == 1 ? r.y : j == 2 ? r.z : r.w;
+      const uint32_t rwi = (i & 1) ? (wj & 0xFFFF0000u) : (wj << 16);
       const uint32_t code = exact_e2m1_sr_quotient(xi, eff, rwi);
+      const int sh = 4 * (i & 7);
       if (i < 8)
-        w0 |= code << (4 * i);
+        w0 = (w0 & ~(0xFu << sh)) | (code << sh);
       else
-        w1 |= code << (4 * (i - 8));
+        w1 = (w1 & ~(0xFu << sh)) | (code << sh);
     }
   } else if (eff >= 0x1p-125f && eff <= 0x1p125f) {
     // RTN codes of RN(v / eff) through the certified bracket, 8 at a time
