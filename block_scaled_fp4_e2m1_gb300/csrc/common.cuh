@@ -252,9 +252,10 @@ __device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint3
   return Philox4{c0, c1, c2, c3};
 }
 
-// Stochastic E2M1 encode of a with the 32-bit random word rw: between grid
-// neighbours lo <= |a| < hi the upper one is taken iff
-// (rw >> 8) * 2^-24 < (|a| - lo) / (hi - lo); |a| >= 6 gives 6.
+// Stochastic E2M1 encode of a with the random word rw (a 16-bit uniform h
+// as h << 16): between grid neighbours lo <= |a| < hi the upper one is taken
+// iff (rw >> 8) * 2^-24 = h * 2^-16 < (|a| - lo) / (hi - lo); |a| >= 6
+// gives 6.
 __device__ __forceinline__ uint32_t e2m1_sr(float a, uint32_t rw) {
   uint32_t sign = (__float_as_uint(a) >> 28) & 8u;
   float m = fabsf(a);

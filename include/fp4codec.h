@@ -89,8 +89,11 @@ fp4_status nvfp4_amax(const void* x, int dtype, int64_t n, const float* residual
  *   x            [n] fp32 or bf16 (dtype), 32-byte aligned
  *   residual     [n] fp32 error-feedback residual, read and updated in place
  *                (r <- (x + r) - dequant(code)), 32-byte aligned, or NULL
- *   rounding     FP4_RTN or FP4_SR; SR draws Philox4x32-10 with key = seed and
- *                counter = (g >> 2, step), g the flat element index, word g & 3
+ *   rounding     FP4_RTN or FP4_SR; SR draws a 16-bit uniform h per element
+ *                from Philox4x32-10 with key = seed and counter = (g >> 3,
+ *                step), g the flat element index: half g & 1 (low first) of
+ *                word (g >> 1) & 3; the upper grid neighbour is taken iff
+ *                h * 2^-16 < the fractional distance
  *   tscale_mode  fp4_tscale; tensor_scale: 1 fp32 on the device (read for
  *                GIVEN, written otherwise); amax_ws: 1 fp32 workspace, needed
  *                for COMPUTE and FROM_AMAX (may be NULL for GIVEN)
