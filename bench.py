@@ -1201,7 +1201,8 @@ def main(argv=None):
             cpu["all_cores"] = {"value": round(combine_rate(groups, mrates), 4), "unit": "GB/s",
                                 "cores": cores,
                                 "how": "the same C oracle on each slice, rows split over "
-                                       "threads"}
+                                       "threads",
+                                "per_kernel_gbs": {k: round(v, 4) for k, v in mrates.items()}}
 
     if rank == 0:
         line = {
