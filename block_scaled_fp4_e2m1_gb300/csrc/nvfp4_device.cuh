@@ -153,16 +153,16 @@ __device__ __noinline__ uint32_t exact_e2m1_sr_quotient(float x, float y, uint32
 // of the difference add at most 2^-21 + 2^-22, so T is within 2^-19 of
 // t + 1/2, t = s(a) - u; when T lies more than 2^-19 inside its rounding
 // interval, RN(T) is a's code.  Otherwise (about one element in 10^5, and
-// NaN) the element is settled exactly.
+// NaN) the element's group of eight is settled exactly.
 //
 // The arithmetic is branch-free and mostly packed:
 //   - u = h 2^-16, the 16-bit uniform, as (128 + h 2^-16) - 128, where the
 //     float 128 + h 2^-16 is the bit pattern 0x4300 0000 | h (one byte
 //     permute);
-//   - RN(T) lands in the low bits of F = T + C, C = 1.5 * 2^23 (+8 for a
-//     negative x, so the low nibble of F is the whole E2M1 code);
-//   - T - (F - C) is exact and is T's distance from its rounded value;
-//   - each nibble is inserted into the code word with one bit-field insert.
+//   - RN(T) lands in the low bits of T + 1.5 * 2^23 (see sr_codes8 for the
+//     sign);
+//   - T - RN(T) is exact, and the largest of its eight magnitudes
+//     certifies a group of eight at once.
 
 __device__ __forceinline__ uint32_t prmt_bytes(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;
@@ -185,23 +185,31 @@ __device__ __forceinline__ float min_nan(float a, float b) {
 
 constexpr uint32_t kSrMagic = 0x4B400000u;  // 1.5 * 2^23
 
-// Bits pos .. pos+3 of b replaced by the low four bits of a.
-__device__ __forceinline__ uint32_t insert_nibble(uint32_t a, uint32_t b, uint32_t pos) {
-  uint32_t r;
-  asm("bfi.b32 %0, %1, %2, %3, 4;" : "=r"(r) : "r"(a), "r"(b), "r"(pos));
+// max(m, |a|, |b|) with NaN propagated.
+__device__ __forceinline__ float max3_abs_nan(float m, float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(m), "f"(fabsf(a)), "f"(fabsf(b)));
   return r;
 }
 
 // The stochastic codes of the eight elements x[0..7] (a multiple of eight
 // apart from the tensor's start) from one Philox block r, by the certified
 // rule above: element i draws the 16-bit half i & 1 (low first) of word
-// i >> 1.  Returns the eight codes as nibbles; bit i of pend is set where
-// element i is not certified and its nibble must be replaced.
+// i >> 1.  Returns the eight codes as nibbles, valid only when all eight are
+// certified: that is when the returned largest distance |T - RN(T)| is
+// below 1/2 - 2^-19 (NaN when an element is NaN); otherwise the caller
+// settles all eight exactly.
+//   RN(T) is formed as F1 = RN(T + 12582916) (1.5 * 2^23 + 4), and the code
+// nibble as F1 - copysign(4, x): 1.5 * 2^23 + RN(T) for x >= 0, the same +8
+// for x < 0, so the low nibble of its bits is the signed E2M1 code.  The
+// nibbles are summed into the word by integer multiply-adds of the raw
+// bits; the constant part of the bits (0x4B40 0000 at every nibble) is
+// removed once.  A certified nibble is at most 15, so nothing carries.
 __device__ __forceinline__ uint32_t sr_codes8(const float x[8], float inv, const Philox4& r,
-                                              uint32_t& pend) {
+                                              float& dmax) {
   const uint32_t words[4] = {r.x, r.y, r.z, r.w};
   uint32_t acc = 0u;
-  pend = 0u;
+  float dm = 0.0f;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int i = 2 * k;
@@ -214,16 +222,17 @@ __device__ __forceinline__ uint32_t sr_codes8(const float x[8], float inv, const
     const F2 ph = fma2(m, F2{0.5f, 0.5f}, F2{4.5f, 4.5f});
     const F2 sh{min_nan(min3_nan(p2.x, p1.x, ph.x), 7.5f), min_nan(min3_nan(p2.y, p1.y, ph.y), 7.5f)};
     const F2 T = sub2(sh, u);
-    const F2 C{__uint_as_float(kSrMagic | ((__float_as_uint(x[i]) >> 28) & 8u)),
-               __uint_as_float(kSrMagic | ((__float_as_uint(x[i + 1]) >> 28) & 8u))};
-    const F2 F = add2(T, C);
-    const F2 d = sub2(T, sub2(F, C));
-    acc = insert_nibble(__float_as_uint(F.x), acc, 4 * i);
-    acc = insert_nibble(__float_as_uint(F.y), acc, 4 * i + 4);
-    if (!(fabsf(d.x) < 0.5f - 0x1p-19f)) pend |= 1u << i;
-    if (!(fabsf(d.y) < 0.5f - 0x1p-19f)) pend |= 2u << i;
+    const F2 F1 = add2(T, F2{12582916.0f, 12582916.0f});
+    const F2 d = sub2(T, sub2(F1, F2{12582916.0f, 12582916.0f}));
+    dm = max3_abs_nan(dm, d.x, d.y);
+    const F2 sg{__uint_as_float((__float_as_uint(x[i]) & 0x80000000u) | 0x40800000u),
+                __uint_as_float((__float_as_uint(x[i + 1]) & 0x80000000u) | 0x40800000u)};
+    const F2 F = sub2(F1, sg);
+    acc += __float_as_uint(F.x) * (1u << (4 * i));
+    acc += __float_as_uint(F.y) * (1u << (4 * i + 4));
   }
-  return acc;
+  dmax = dm;
+  return acc - kSrMagic * 0x11111111u;
 }
 
 // Settling a bracket that straddles a rounding midpoint, without dividing.
@@ -321,9 +330,9 @@ __device__ __forceinline__ uint32_t quantize_block(const float v[16], float s_t,
       const uint64_t oct = (g0 >> 3) + (uint64_t)k;
       const Philox4 r = philox4x32_10((uint32_t)oct, (uint32_t)(oct >> 32), step0, step1, key0,
                                       key1);
-      uint32_t pk;
-      ww[k] = sr_codes8(v + 8 * k, inv, r, pk);
-      pend |= (fast ? pk : 0xFFu) << (8 * k);
+      float dmax;
+      ww[k] = sr_codes8(v + 8 * k, inv, r, dmax);
+      pend |= (fast && dmax < 0.5f - 0x1p-19f ? 0u : 0xFFu) << (8 * k);
     }
     w0 = ww[0];
     w1 = ww[1];
