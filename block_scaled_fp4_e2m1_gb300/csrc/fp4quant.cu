@@ -38,7 +38,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kE = 32;                      // elements per lane
-constexpr int kTileUnits = 32 * kE / 4;     // 16-byte units of a warp's tile (4 KB)
 
 template <int G>
 __device__ __forceinline__ float wht_norm() {
@@ -55,10 +54,10 @@ struct Row32 {
   F2 p[16];
 };
 
-// A product that feeds an addition is always formed by a scalar multiply:
-// the compiler may fuse a packed multiply into the packed addition that
-// consumes it (one rounding instead of two), which would break the exact
-// operation order.
+// No packed product feeds a packed addition: the compiler may fuse the two
+// into one packed fma (one rounding instead of two), which would break the
+// exact operation order.  A packed product may feed the scalar addition of
+// its own two halves (stage h = 1), which no fma can absorb.
 
 // Stages h = 1 .. 16 of the transform, inside the thread (phase 1).
 __device__ __forceinline__ void wht_in_thread(Row32& y) {
@@ -99,38 +98,34 @@ __device__ __forceinline__ void wht_across_chunks(Row32& y) {
   }
 }
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, F2 a, F2 b) {
-  asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a.x), "f"(a.y),
-               "f"(b.x), "f"(b.y)
-               : "memory");
-}
-
-__device__ __forceinline__ void ld_shared_v4(uint32_t addr, F2& a, F2& b) {
-  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(a.x), "=f"(a.y), "=f"(b.x), "=f"(b.y)
-               : "r"(addr)
-               : "memory");
-}
-
-// The phase-1 -> phase-2 transpose through the warp's tile (kTileUnits
-// 16-byte units at byte address tile).  Row k of a group's region receives
-// block k (elements k B .. k B + B - 1) of every lane of the group; lane
-// src's block goes to column src xor k, and within it 16-byte half h to
-// unit S col + (h xor (g mod S)), S = 8/L units per block.  For a fixed
-// instruction the eight lanes of each quarter-warp then hit eight different
-// units mod 8: no bank conflict, stores and loads alike.
+// The phase-1 -> phase-2 transpose through the warp's shared tile.  Lane l
+// of group g writes its block k (elements k B .. k B + B - 1), in S = 8/L
+// 16-byte halves h, to unit S l + h + (8 + S) k of the group's region of R
+// units; lane l then reads lane i's block l half h from unit
+// S i + h + (8 + S) l.  Both sides are a per-lane base plus a constant, so no
+// address is computed per access.  The units of one region are distinct
+// ((8 + S) k leaves room for the 8 units S l + h of a block), and with R odd
+// the eight lanes of a quarter-warp (S groups of L lanes) touch eight
+// different units mod 8 on every store and load: no bank conflict.
 template <int G>
-__device__ __forceinline__ void transpose_to_blocks(Row32& y, uint32_t tile, int lane) {
-  constexpr int L = G / kE, B = kE / L, S = 8 / L;
+struct TTile {
+  static constexpr int L = G / kE, S = 8 / L;
+  static constexpr int R = ((8 + S) * (L - 1) + 8) | 1;  // units per group region
+  static constexpr int kBytes = 16 * (32 / L) * R;        // per warp
+};
+
+template <int G>
+__device__ __forceinline__ void transpose_to_blocks(Row32& y, float4* tile, int lane) {
+  constexpr int L = G / kE, B = kE / L, S = 8 / L, R = TTile<G>::R;
   const int g = lane / L, l = lane % L;
-  const uint32_t region = tile + (uint32_t)(g * L * 8) * 16u;
-  const int hs = g % S;
+  float4* const st = tile + g * R + S * l;
+  const float4* const ld = tile + g * R + (8 + S) * l;
 #pragma unroll
   for (int k = 0; k < L; ++k) {
 #pragma unroll
     for (int h = 0; h < S; ++h) {
-      const int unit = k * 8 + S * (l ^ k) + (h ^ hs);
-      st_shared_v4(region + 16u * unit, y.p[k * B / 2 + 2 * h], y.p[k * B / 2 + 2 * h + 1]);
+      const F2 a = y.p[k * B / 2 + 2 * h], b = y.p[k * B / 2 + 2 * h + 1];
+      st[h + (8 + S) * k] = make_float4(a.x, a.y, b.x, b.y);
     }
   }
   __syncwarp();
@@ -138,8 +133,9 @@ __device__ __forceinline__ void transpose_to_blocks(Row32& y, uint32_t tile, int
   for (int i = 0; i < L; ++i) {
 #pragma unroll
     for (int h = 0; h < S; ++h) {
-      const int unit = l * 8 + S * (i ^ l) + (h ^ hs);
-      ld_shared_v4(region + 16u * unit, y.p[i * B / 2 + 2 * h], y.p[i * B / 2 + 2 * h + 1]);
+      const float4 v = ld[S * i + h];
+      y.p[i * B / 2 + 2 * h] = F2{v.x, v.y};
+      y.p[i * B / 2 + 2 * h + 1] = F2{v.z, v.w};
     }
   }
   __syncwarp();
@@ -194,6 +190,28 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool ok
                : "memory");
 }
 
+__device__ __forceinline__ void cp_async16_all(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Byte offset in a slot of piece 32 k + lane: 512 (k - k mod M) plus a lane
+// offset that depends on k only through k mod M (M = 2 for P = 8, else 1),
+// so every copy of a tile is one per-lane base plus a constant.
+template <int P>
+__device__ __forceinline__ uint32_t ring_piece_off(int lane, int k) {
+  constexpr int M = P == 8 ? 2 : 1;
+  const int p = 32 * (k % M) + lane;
+  return 16u * (uint32_t)ring_unit<P>(p / P, p % P) + 512u * (uint32_t)(k - k % M);
+}
+
+// Copies a whole tile (lane's pieces at src_lane + 512 k) into the slot at
+// byte address dst.
+template <int P>
+__device__ __forceinline__ void ring_copy_full(uint32_t dst, const uint8_t* src_lane, int lane) {
+#pragma unroll
+  for (int k = 0; k < P; ++k) cp_async16_all(dst + ring_piece_off<P>(lane, k), src_lane + 512 * k);
+}
+
 // Copies the tile at src (valid: its first `valid` bytes exist, a multiple
 // of 16; the rest is zero-filled without reading) into the slot at byte
 // address dst.
@@ -204,17 +222,20 @@ __device__ __forceinline__ void ring_copy(uint32_t dst, const uint8_t* src, int6
   for (int k = 0; k < P; ++k) {
     const int p = 32 * k + lane;
     const bool ok = 16 * (int64_t)p < valid;
-    cp_async16(dst + 16u * ring_unit<P>(p / P, p % P), ok ? src + 16 * p : src, ok);
+    cp_async16(dst + ring_piece_off<P>(lane, k), ok ? src + 16 * p : src, ok);
   }
 }
 
+// Lane's P pieces of the tile in the slot at byte address slot (64-byte
+// aligned): piece q at (slot + 16 P lane + 16 sw) xor 16 q.
 template <int P>
 __device__ __forceinline__ void ring_read(uint32_t slot, int lane, uint4 v[P]) {
+  const uint32_t a = slot + 16u * (uint32_t)ring_unit<P>(lane, 0);
 #pragma unroll
   for (int q = 0; q < P; ++q)
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v[q].x), "=r"(v[q].y), "=r"(v[q].z), "=r"(v[q].w)
-                 : "r"(slot + 16u * ring_unit<P>(lane, q))
+                 : "r"(a ^ (16u * (uint32_t)q))
                  : "memory");
 }
 
@@ -253,13 +274,14 @@ __device__ __forceinline__ void store_codes(uint8_t* row, int l, const uint32_t*
   }
 }
 
-// Encodes the group chunk set this warp holds (lane chunk u, valid when
-// inside the tensor) and stores codes and scales.  Lanes past the end
-// compute on zeros and store nothing (the chunk count is a multiple of L, so
-// a group is either entirely inside or entirely past the end).
+// Encodes the group chunk set this warp holds (tile t: lane's chunk
+// 32 t + lane, valid when inside the tensor) and stores codes and scales.
+// Lanes past the end compute on zeros and store nothing (the chunk count is
+// a multiple of L, so a group is either entirely inside or entirely past the
+// end).
 template <int G>
-__device__ __forceinline__ void encode_chunk(Row32& y, int64_t u, bool valid, int lane,
-                                             uint32_t tile, uint8_t* __restrict__ packed,
+__device__ __forceinline__ void encode_chunk(Row32& y, int t, bool valid, int lane, float4* tile,
+                                             uint8_t* __restrict__ packed,
                                              float* __restrict__ s1_out,
                                              float* __restrict__ s2_out) {
   constexpr int L = G / kE, B = kE / L;
@@ -281,95 +303,121 @@ __device__ __forceinline__ void encode_chunk(Row32& y, int64_t u, bool valid, in
   const float rms = __fsqrt_rn(__fmul_rn(ss, 1.0f / (float)G));
   const float inv1 = rms == 0.0f ? 0.0f : __frcp_rn(rms);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) y.p[i] = F2{__fmul_rn(y.p[i].x, inv1), __fmul_rn(y.p[i].y, inv1)};
+  for (int i = 0; i < 16; ++i) y.p[i] = mul2(y.p[i], splat(inv1));
   // transform: stages 1..16, transpose, stages 32..G/2, normalization
   wht_in_thread(y);
   transpose_to_blocks<G>(y, tile, lane);
   wht_across_chunks<G>(y);
-  const F2 c = splat(wht_norm<G>());
+  // normalization and absmax scale into [-6, 6].  z = RN(w c) and
+  // max|z| = RN(max|w| c) (RN is monotone).  For G = 64 and 256, c is a
+  // power of two: when 2^-20 <= max|z| <= 2^100, RN(z inv2) = RN(w (c inv2))
+  // for every element (c inv2 is exact; where w c is normal, z = w c
+  // exactly; where it is subnormal, both products are below 2^-100 and
+  // round to a zero code of w's sign), so the two scalings fold into one.
+  const float c = wht_norm<G>();
+  float wmax = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) y.p[i] = mul2(y.p[i], c);
-  // absmax scale into [-6, 6]
-  float zmax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) zmax = max3_abs(zmax, y.p[i].x, y.p[i].y);
-  zmax = group_max<G>(zmax);
+  for (int i = 0; i < 16; ++i) wmax = max3_abs(wmax, y.p[i].x, y.p[i].y);
+  const float zmax = __fmul_rn(group_max<G>(wmax), c);
   const float sc2 = __fdiv_rn(zmax, 6.0f);
-  const F2 inv2 = splat(sc2 == 0.0f ? 0.0f : __frcp_rn(sc2));
+  const float inv2 = sc2 == 0.0f ? 0.0f : __frcp_rn(sc2);
+  if (G != 128 && zmax >= 0x1p-20f && zmax <= 0x1p100f) {
+    const F2 m = splat(__fmul_rn(inv2, c));
 #pragma unroll
-  for (int i = 0; i < 16; ++i) y.p[i] = mul2(y.p[i], inv2);
+    for (int i = 0; i < 16; ++i) y.p[i] = mul2(y.p[i], m);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) y.p[i] = mul2(mul2(y.p[i], splat(c)), splat(inv2));
+  }
   if (!valid) return;
   const int l = lane % L;
-  uint8_t* const rows = packed + 16 * (u - l);  // the group's first chunk
+  // the group's first chunk row
+  uint8_t* const rows = packed + 16 * ((int64_t)t * 32 + (lane - l));
+  if (B == 4) {
+    // two source chunks' 4 codes per conversion word, stored as halves
 #pragma unroll
-  for (int i = 0; i < L; ++i) {
-    const F2* q = y.p + i * (B / 2);
-    uint32_t w[2];
-    if (B == 4) {
-      w[0] = cvt_e2m1x2(q[0].x, q[0].y) | (cvt_e2m1x2(q[1].x, q[1].y) << 8);
-    } else {
+    for (int i = 0; i < L; i += 2) {
+      const F2* q = y.p + i * 2;
+      const uint32_t w = cvt_e2m1x8(q[0].x, q[0].y, q[1].x, q[1].y, q[2].x, q[2].y, q[3].x,
+                                    q[3].y);
+      *reinterpret_cast<uint16_t*>(rows + 16 * i + 2 * l) = (uint16_t)w;
+      *reinterpret_cast<uint16_t*>(rows + 16 * (i + 1) + 2 * l) = (uint16_t)(w >> 16);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < L; ++i) {
+      const F2* q = y.p + i * (B / 2);
+      uint32_t w[2];
 #pragma unroll
       for (int k = 0; k < B / 8; ++k)
         w[k] = cvt_e2m1x8(q[4 * k].x, q[4 * k].y, q[4 * k + 1].x, q[4 * k + 1].y,
                           q[4 * k + 2].x, q[4 * k + 2].y, q[4 * k + 3].x, q[4 * k + 3].y);
+      store_codes<B>(rows + 16 * i, l, w);
     }
-    store_codes<B>(rows + 16 * i, l, w);
   }
   if (l == 0) {
-    s1_out[u / L] = rms;
-    s2_out[u / L] = sc2;
+    const int64_t gi = (int64_t)t * (32 / L) + lane / L;
+    s1_out[gi] = rms;
+    s2_out[gi] = sc2;
   }
 }
 
 // Input pieces per lane and staged tiles per warp of the encode kernels.
-// (bf16: 8 KB per warp with the transpose tile, three CTAs of 256 threads
-// per SM at 80 registers; fp32: 12 KB per warp, two CTAs.  Measured on
-// GB300: a third staged tile or two CTAs of up to 128 registers ran no
-// faster.)
-template <bool kBF16>
+// (bf16: 4 KB of ring and a 4.4-5.3 KB transpose tile per warp, three CTAs
+// of 256 threads per SM at 80 registers; fp32: 8 KB of ring, two CTAs.
+// Measured on GB300: a third staged tile or two CTAs of up to 128 registers
+// ran no faster.)
+template <int G, bool kBF16>
 struct EncRing {
   static constexpr int P = kBF16 ? 4 : 8;            // 64 or 128 bytes per lane
   static constexpr int NS = 2;                       // tiles per warp ring
   static constexpr int kSlot = 32 * 16 * P;          // bytes per tile
-  static constexpr size_t kSmem = (size_t)kWarps * (NS * kSlot + 16 * kTileUnits);
+  static constexpr size_t kSmem = (size_t)kWarps * (NS * kSlot + TTile<G>::kBytes);
 };
 
 // The loop walks 32-chunk tiles, one per warp per grid-stride step, and is
 // warp-uniform so that every lane takes part in the exchanges.  Each warp
 // stages its tiles NS - 1 steps ahead in its shared-memory ring (one
 // cp.async group per tile, committed even when empty); the transpose's
-// __syncwarp calls order a slot's reads before its next copy.
+// __syncwarp calls order a slot's reads before its next copy.  Tile
+// indices are 32-bit (the entry point admits fewer than 2^35 chunks).
 template <int G, bool kBF16>
 __global__ void __launch_bounds__(kThreads, kBF16 ? 3 : 2)
     encode_kernel(const void* __restrict__ x, int64_t nchunks, uint8_t* __restrict__ packed,
                   float* __restrict__ s1_out, float* __restrict__ s2_out) {
-  using R = EncRing<kBF16>;
-  extern __shared__ __align__(16) uint8_t enc_smem[];
+  using R = EncRing<G, kBF16>;
+  constexpr int P = R::P, NS = R::NS;
+  extern __shared__ __align__(128) uint8_t enc_smem[];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const uint32_t smem = (uint32_t)__cvta_generic_to_shared(enc_smem);
-  const uint32_t ring = smem + (uint32_t)(wid * R::NS * R::kSlot);
-  const uint32_t tile = smem + (uint32_t)(kWarps * R::NS * R::kSlot + wid * 16 * kTileUnits);
-  const int64_t stride = (int64_t)gridDim.x * kThreads;
-  const int64_t ubytes = 16 * R::P;  // input bytes per chunk
-  const uint8_t* const xb = static_cast<const uint8_t*>(x);
-  int64_t u0 = (int64_t)blockIdx.x * kThreads + (threadIdx.x & ~31);
-  auto stage = [&](int64_t t0, int slot) {
-    if (t0 < nchunks)
-      ring_copy<R::P>(ring + slot * R::kSlot, xb + ubytes * t0, (nchunks - t0) * ubytes, lane);
+  const uint32_t ring =
+      (uint32_t)__cvta_generic_to_shared(enc_smem) + (uint32_t)(wid * NS * R::kSlot);
+  float4* const tile =
+      reinterpret_cast<float4*>(enc_smem + kWarps * NS * R::kSlot + wid * TTile<G>::kBytes);
+  const int ntiles = (int)((nchunks + 31) >> 5), nfull = (int)(nchunks >> 5);
+  const int rem = (int)(nchunks & 31);
+  const int tstride = (int)gridDim.x * kWarps;
+  const int64_t step = (int64_t)tstride * R::kSlot;  // input bytes between a warp's tiles
+  int t = (int)blockIdx.x * kWarps + wid;
+  const uint8_t* src = static_cast<const uint8_t*>(x) + (int64_t)t * R::kSlot;
+  auto stage = [&](int tt, const uint8_t* s, int slot) {
+    const uint32_t dst = ring + (uint32_t)(slot * R::kSlot);
+    if (tt < nfull)
+      ring_copy_full<P>(dst, s + 16 * lane, lane);
+    else if (tt < ntiles)
+      ring_copy<P>(dst, s, (nchunks - 32 * (int64_t)tt) * (16 * P), lane);
     cp_async_commit();
   };
 #pragma unroll
-  for (int k = 0; k < R::NS - 1; ++k) stage(u0 + k * stride, k);
-  for (int t = 0; u0 < nchunks; ++t, u0 += stride) {
-    stage(u0 + (R::NS - 1) * stride, (t + R::NS - 1) % R::NS);
-    cp_async_wait<R::NS - 1>();
+  for (int k = 0; k < NS - 1; ++k) stage(t + k * tstride, src + k * step, k);
+  for (int it = 0; t < ntiles; ++it, t += tstride, src += step) {
+    stage(t + (NS - 1) * tstride, src + (NS - 1) * step, (it + NS - 1) % NS);
+    cp_async_wait<NS - 1>();
     __syncwarp();
-    const int64_t u = u0 + lane;
-    uint4 v[R::P];
-    ring_read<R::P>(ring + (t % R::NS) * R::kSlot, lane, v);
+    uint4 v[P];
+    ring_read<P>(ring + (uint32_t)((it % NS) * R::kSlot), lane, v);
     Row32 y;
     unpack_chunk<kBF16>(v, y);
-    encode_chunk<G>(y, u, u < nchunks, lane, tile, packed, s1_out, s2_out);
+    encode_chunk<G>(y, t, t < nfull || lane < rem, lane, tile, packed, s1_out, s2_out);
   }
   cp_async_wait<0>();
 }
@@ -403,7 +451,7 @@ struct DecRing {
   static constexpr int L = G / kE, NG = 32 / L;
   static constexpr int NS = 4;                       // tiles per warp ring
   static constexpr int kSlot = 512 + 8 * NG;         // bytes per tile (multiple of 16)
-  static constexpr size_t kSmem = (size_t)kWarps * (NS * kSlot + 16 * kTileUnits);
+  static constexpr size_t kSmem = (size_t)kWarps * (NS * kSlot + TTile<G>::kBytes);
 };
 
 // Stores the B values of each source chunk: bf16 B = 4, 8, 16 -> 8, 16, 32
@@ -457,7 +505,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int l = lane % L;
   const uint32_t smem = (uint32_t)__cvta_generic_to_shared(dec_smem);
   const uint32_t ring = smem + (uint32_t)(wid * R::NS * R::kSlot);
-  const uint32_t tile = smem + (uint32_t)(kWarps * R::NS * R::kSlot + wid * 16 * kTileUnits);
+  float4* const tile =
+      reinterpret_cast<float4*>(dec_smem + kWarps * R::NS * R::kSlot + wid * TTile<G>::kBytes);
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   const int64_t ngroups = nchunks / L;
   int64_t u0 = (int64_t)blockIdx.x * kThreads + (threadIdx.x & ~31);
@@ -516,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int G, bool kBF16>
 fp4_status launch_encode_t(const void* x, int64_t nchunks, uint8_t* packed, float* s1, float* s2,
                            cudaStream_t s) {
-  constexpr size_t smem = EncRing<kBF16>::kSmem;
+  constexpr size_t smem = EncRing<G, kBF16>::kSmem;
   if (!allow_dynamic_smem<encode_kernel<G, kBF16>>(smem)) return FP4_ERR_CUDA;
   return launch<encode_kernel<G, kBF16>>(nchunks, kThreads, smem, s, x, nchunks, packed, s1, s2);
 }
@@ -558,6 +607,7 @@ fp4_status fp4quant_encode(const void* x, int dtype, int64_t rows, int64_t cols,
   if (!dtype_ok(dtype)) return FP4_ERR_DTYPE;
   if (!group_ok(group)) return FP4_ERR_ARG;
   if (rows < 0 || cols < 0 || cols % group != 0) return FP4_ERR_SHAPE;
+  if (cols > 0 && rows > ((int64_t)1 << 40) / cols) return FP4_ERR_SHAPE;
   const int64_t nchunks = rows * cols / kE;
   if (nchunks > 0 && (!x || !packed || !s1 || !s2)) return FP4_ERR_NULL;
   if (!aligned(x, 32) || !aligned(packed, 16) || !aligned(s1, 4) || !aligned(s2, 4))
