@@ -141,12 +141,35 @@ __device__ __forceinline__ void transpose_to_blocks(Row32& y, float4* tile, int 
   __syncwarp();
 }
 
-// max(m, |a|, |b|) in one three-input max (exact; the order of a max does
-// not matter).
-__device__ __forceinline__ float max3_abs(float m, float a, float b) {
+// max(|a|, |b|, |c|) and max(a, b, c) in one three-input max (exact; the
+// order of a max does not matter; a NaN operand is ignored).
+__device__ __forceinline__ float max3_abs(float a, float b, float c) {
   float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(m), "f"(fabsf(a)), "f"(fabsf(b)));
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(fabsf(a)), "f"(fabsf(b)), "f"(fabsf(c)));
   return r;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// max(0, |v|) over a lane's 32 values, as a tree of three-input maxima (16
+// instructions, 4 deep) rather than a chain.
+__device__ __forceinline__ float absmax32(const Row32& y) {
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    v[2 * i] = y.p[i].x;
+    v[2 * i + 1] = y.p[i].y;
+  }
+  float a[10];
+#pragma unroll
+  for (int k = 0; k < 10; ++k) a[k] = max3_abs(v[3 * k], v[3 * k + 1], v[3 * k + 2]);
+  const float b0 = max3(a[0], a[1], a[2]), b1 = max3(a[3], a[4], a[5]);
+  const float b2 = max3(a[6], a[7], a[8]), b3 = max3_abs(a[9], v[30], v[31]);
+  return max3(max3(b0, b1, b2), b3, 0.0f);
 }
 
 template <int G>
@@ -290,9 +313,8 @@ __device__ __forceinline__ void encode_chunk(Row32& y, int t, bool valid, int la
   F2 sq[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const F2 a = y.p[i], b = y.p[8 + i];
-    sq[i] = F2{__fadd_rn(__fmul_rn(a.x, a.x), __fmul_rn(a.y, a.y)),
-               __fadd_rn(__fmul_rn(b.x, b.x), __fmul_rn(b.y, b.y))};
+    const F2 a = mul2(y.p[i], y.p[i]), b = mul2(y.p[8 + i], y.p[8 + i]);
+    sq[i] = F2{__fadd_rn(a.x, a.y), __fadd_rn(b.x, b.y)};
   }
 #pragma unroll
   for (int w = 8; w > 1; w >>= 1) {
@@ -315,10 +337,7 @@ __device__ __forceinline__ void encode_chunk(Row32& y, int t, bool valid, int la
   // exactly; where it is subnormal, both products are below 2^-100 and
   // round to a zero code of w's sign), so the two scalings fold into one.
   const float c = wht_norm<G>();
-  float wmax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) wmax = max3_abs(wmax, y.p[i].x, y.p[i].y);
-  const float zmax = __fmul_rn(group_max<G>(wmax), c);
+  const float zmax = __fmul_rn(group_max<G>(absmax32(y)), c);
   const float sc2 = __fdiv_rn(zmax, 6.0f);
   const float inv2 = sc2 == 0.0f ? 0.0f : __frcp_rn(sc2);
   if (G != 128 && zmax >= 0x1p-20f && zmax <= 0x1p100f) {
@@ -493,26 +512,34 @@ __device__ __forceinline__ void store_values(void* out, int64_t chunk, int l, co
 }
 
 // Tiles are staged NS - 1 loop steps ahead in the warp's ring, as in the
-// encode kernels.
+// encode kernels; tile indices are 32-bit likewise.
 template <int G, bool kBF16Out>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, (kBF16Out && G == 256) ? 4 : 1)
     decode_kernel(const uint8_t* __restrict__ packed, const float* __restrict__ s1_in,
                   const float* __restrict__ s2_in, int64_t nchunks, void* __restrict__ out) {
   using R = DecRing<G>;
-  constexpr int L = G / kE, B = kE / L, NG = R::NG;
-  extern __shared__ __align__(16) uint8_t dec_smem[];
+  constexpr int L = G / kE, B = kE / L, NG = R::NG, NS = R::NS;
+  extern __shared__ __align__(128) uint8_t dec_smem[];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int l = lane % L;
-  const uint32_t smem = (uint32_t)__cvta_generic_to_shared(dec_smem);
-  const uint32_t ring = smem + (uint32_t)(wid * R::NS * R::kSlot);
+  const uint32_t ring =
+      (uint32_t)__cvta_generic_to_shared(dec_smem) + (uint32_t)(wid * NS * R::kSlot);
   float4* const tile =
-      reinterpret_cast<float4*>(dec_smem + kWarps * R::NS * R::kSlot + wid * TTile<G>::kBytes);
-  const int64_t stride = (int64_t)gridDim.x * kThreads;
+      reinterpret_cast<float4*>(dec_smem + kWarps * NS * R::kSlot + wid * TTile<G>::kBytes);
+  const int ntiles = (int)((nchunks + 31) >> 5), nfull = (int)(nchunks >> 5);
+  const int rem = (int)(nchunks & 31);
   const int64_t ngroups = nchunks / L;
-  int64_t u0 = (int64_t)blockIdx.x * kThreads + (threadIdx.x & ~31);
-  auto stage = [&](int64_t t0, int slot) {
-    if (t0 < nchunks) {
-      const uint32_t dst = ring + slot * R::kSlot;
+  const int tstride = (int)gridDim.x * kWarps;
+  int t = (int)blockIdx.x * kWarps + wid;
+  // lanes 0 .. NG-1 stage the tile's s1 words, lanes NG .. 2 NG-1 its s2 words
+  const float* const ssrc = (lane < NG ? s1_in : s2_in) + (lane % NG);
+  auto stage = [&](int tt, int slot) {
+    const uint32_t dst = ring + (uint32_t)(slot * R::kSlot);
+    if (tt < nfull) {
+      cp_async16_all(dst + 16u * lane, packed + 512 * (int64_t)tt + 16 * lane);
+      if (lane < 2 * NG) cp_async4(dst + 512u + 4u * lane, ssrc + (int64_t)tt * NG, true);
+    } else if (tt < ntiles) {
+      const int64_t t0 = 32 * (int64_t)tt;
       ring_copy<1>(dst, packed + 16 * t0, (nchunks - t0) * 16, lane);
       const int64_t gi = t0 / L + (lane % NG);
       const bool ok = lane < 2 * NG && gi < ngroups;
@@ -522,14 +549,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     cp_async_commit();
   };
 #pragma unroll
-  for (int k = 0; k < R::NS - 1; ++k) stage(u0 + k * stride, k);
-  for (int t = 0; u0 < nchunks; ++t, u0 += stride) {
-    stage(u0 + (R::NS - 1) * stride, (t + R::NS - 1) % R::NS);
-    cp_async_wait<R::NS - 1>();
+  for (int k = 0; k < NS - 1; ++k) stage(t + k * tstride, k);
+  for (int it = 0; t < ntiles; ++it, t += tstride) {
+    stage(t + (NS - 1) * tstride, (it + NS - 1) % NS);
+    cp_async_wait<NS - 1>();
     __syncwarp();
-    const int64_t u = u0 + lane;
-    const bool valid = u < nchunks;
-    const uint32_t slot = ring + (t % R::NS) * R::kSlot;
+    const bool valid = t < nfull || lane < rem;
+    const uint32_t slot = ring + (uint32_t)((it % NS) * R::kSlot);
     uint4 pk[1];
     ring_read<1>(slot, lane, pk);
     const float sc1 = ld_shared_f32(slot + 512u + 4u * (lane / L));
@@ -541,22 +567,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       float v[8];
       e2m1x8_values(words[k], v);
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        z.p[4 * k + i] = F2{__fmul_rn(v[2 * i], sc2), __fmul_rn(v[2 * i + 1], sc2)};
+      for (int i = 0; i < 4; ++i) z.p[4 * k + i] = mul2(F2{v[2 * i], v[2 * i + 1]}, splat(sc2));
     }
     wht_in_thread(z);
     transpose_to_blocks<G>(z, tile, lane);
     wht_across_chunks<G>(z);
-    const F2 m = splat(wht_norm<G>());
+    // normalization, then x' = y' s1 with the group's s1 (every lane of a
+    // group holds it).  For G = 64 and 256, c is a power of two; when
+    // s2 = 0 or |s2| >= 2^-60 every nonzero transform output w is a multiple
+    // of 2^-84 (the values z are RN(v s2) >= 2^-61 in magnitude, and sums of
+    // multiples of 2^-84 stay multiples of it), so w c is exact, and when
+    // s1 = 0 or |s1| >= 2^-120 so is c s1: then RN(RN(w c) s1) = RN(w (c s1))
+    // and one scaling does both.
+    const float c = wht_norm<G>();
+    const bool fold_ok = (sc2 == 0.0f || fabsf(sc2) >= 0x1p-60f) &&
+                         (sc1 == 0.0f || fabsf(sc1) >= 0x1p-120f);
+    if (G != 128 && __all_sync(0xFFFFFFFFu, fold_ok)) {
+      const F2 m = splat(__fmul_rn(c, sc1));
 #pragma unroll
-    for (int i = 0; i < 16; ++i) z.p[i] = mul2(z.p[i], m);
-    // x' = y' s1 with the group's s1 (every lane of a group holds it)
-    const F2 m1 = splat(sc1);
+      for (int i = 0; i < 16; ++i) z.p[i] = mul2(z.p[i], m);
+    } else {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) z.p[i] = mul2(z.p[i], m1);
+      for (int i = 0; i < 16; ++i) z.p[i] = mul2(mul2(z.p[i], splat(c)), splat(sc1));
+    }
     if (valid) {
 #pragma unroll
-      for (int i = 0; i < L; ++i) store_values<B, kBF16Out>(out, u - l + i, l, z.p + i * (B / 2));
+      for (int i = 0; i < L; ++i)
+        store_values<B, kBF16Out>(out, (int64_t)t * 32 + (lane - l) + i, l, z.p + i * (B / 2));
     }
   }
   cp_async_wait<0>();
