@@ -31,6 +31,7 @@
 
 #include "common.cuh"
 #include "host_common.h"
+#include "rn_math.cuh"
 
 namespace fp4 {
 namespace {
@@ -98,34 +99,33 @@ __device__ __forceinline__ void wht_across_chunks(Row32& y) {
   }
 }
 
-// The phase-1 -> phase-2 transpose through the warp's shared tile.  Lane l
-// of group g writes its block k (elements k B .. k B + B - 1), in S = 8/L
-// 16-byte halves h, to unit S l + h + (8 + S) k of the group's region of R
-// units; lane l then reads lane i's block l half h from unit
-// S i + h + (8 + S) l.  Both sides are a per-lane base plus a constant, so no
-// address is computed per access.  The units of one region are distinct
-// ((8 + S) k leaves room for the 8 units S l + h of a block), and with R odd
+// The phase-1 -> phase-2 transpose through the warp's 4.5 KB shared tile.
+// Group g owns the 9 L units from unit 9 L g.  Lane l of the group writes its
+// block k (elements k B .. k B + B - 1), in S = 8/L 16-byte halves h, to unit
+// l + L h + 9 k of the group's region, and reads lane i's block l half h
+// from unit i + L h + 9 l.  Both sides are a per-lane base plus a constant,
+// so no address is computed per access.  l + L h covers 0 .. 7 once, so the
+// blocks (9 units apart) do not overlap; and since 9 L = L and 9 = 1 mod 8,
 // the eight lanes of a quarter-warp (S groups of L lanes) touch eight
 // different units mod 8 on every store and load: no bank conflict.
 template <int G>
 struct TTile {
-  static constexpr int L = G / kE, S = 8 / L;
-  static constexpr int R = ((8 + S) * (L - 1) + 8) | 1;  // units per group region
-  static constexpr int kBytes = 16 * (32 / L) * R;        // per warp
+  static constexpr int L = G / kE;
+  static constexpr int kBytes = 16 * 32 * 9;  // per warp: 32/L regions of 9 L units
 };
 
 template <int G>
 __device__ __forceinline__ void transpose_to_blocks(Row32& y, float4* tile, int lane) {
-  constexpr int L = G / kE, B = kE / L, S = 8 / L, R = TTile<G>::R;
+  constexpr int L = G / kE, B = kE / L, S = 8 / L;
   const int g = lane / L, l = lane % L;
-  float4* const st = tile + g * R + S * l;
-  const float4* const ld = tile + g * R + (8 + S) * l;
+  float4* const st = tile + 9 * L * g + l;
+  const float4* const ld = tile + 9 * L * g + 9 * l;
 #pragma unroll
   for (int k = 0; k < L; ++k) {
 #pragma unroll
     for (int h = 0; h < S; ++h) {
       const F2 a = y.p[k * B / 2 + 2 * h], b = y.p[k * B / 2 + 2 * h + 1];
-      st[h + (8 + S) * k] = make_float4(a.x, a.y, b.x, b.y);
+      st[L * h + 9 * k] = make_float4(a.x, a.y, b.x, b.y);
     }
   }
   __syncwarp();
@@ -133,7 +133,7 @@ __device__ __forceinline__ void transpose_to_blocks(Row32& y, float4* tile, int 
   for (int i = 0; i < L; ++i) {
 #pragma unroll
     for (int h = 0; h < S; ++h) {
-      const float4 v = ld[S * i + h];
+      const float4 v = ld[i + L * h];
       y.p[i * B / 2 + 2 * h] = F2{v.x, v.y};
       y.p[i * B / 2 + 2 * h + 1] = F2{v.z, v.w};
     }
@@ -322,8 +322,8 @@ __device__ __forceinline__ void encode_chunk(Row32& y, int t, bool valid, int la
     for (int i = 0; i < w / 2; ++i) sq[i] = add2(sq[2 * i], sq[2 * i + 1]);
   }
   const float ss = group_sum<G>(__fadd_rn(sq[0].x, sq[0].y));
-  const float rms = __fsqrt_rn(__fmul_rn(ss, 1.0f / (float)G));
-  const float inv1 = rms == 0.0f ? 0.0f : __frcp_rn(rms);
+  const float rms = sqrt_rn(__fmul_rn(ss, 1.0f / (float)G));
+  const float inv1 = rms == 0.0f ? 0.0f : rcp_rn(rms);
 #pragma unroll
   for (int i = 0; i < 16; ++i) y.p[i] = mul2(y.p[i], splat(inv1));
   // transform: stages 1..16, transpose, stages 32..G/2, normalization
@@ -338,8 +338,8 @@ __device__ __forceinline__ void encode_chunk(Row32& y, int t, bool valid, int la
   // round to a zero code of w's sign), so the two scalings fold into one.
   const float c = wht_norm<G>();
   const float zmax = __fmul_rn(group_max<G>(absmax32(y)), c);
-  const float sc2 = __fdiv_rn(zmax, 6.0f);
-  const float inv2 = sc2 == 0.0f ? 0.0f : __frcp_rn(sc2);
+  const float sc2 = div6_rn(zmax);
+  const float inv2 = sc2 == 0.0f ? 0.0f : rcp_rn(sc2);
   if (G != 128 && zmax >= 0x1p-20f && zmax <= 0x1p100f) {
     const F2 m = splat(__fmul_rn(inv2, c));
 #pragma unroll
@@ -381,59 +381,56 @@ __device__ __forceinline__ void encode_chunk(Row32& y, int t, bool valid, int la
   }
 }
 
-// Input pieces per lane and staged tiles per warp of the encode kernels.
-// (bf16: 4 KB of ring and a 4.4-5.3 KB transpose tile per warp, three CTAs
-// of 256 threads per SM at 80 registers; fp32: 8 KB of ring, two CTAs.
-// Measured on GB300: a third staged tile or two CTAs of up to 128 registers
-// ran no faster.)
+// Input pieces per lane and the shared memory of the encode kernels: one
+// staging slot per warp plus its transpose tile.  (bf16: 6.5 KB per warp,
+// four CTAs of 256 threads per SM at 64 registers; fp32: 8.5 KB per warp,
+// two CTAs.)
 template <int G, bool kBF16>
 struct EncRing {
   static constexpr int P = kBF16 ? 4 : 8;            // 64 or 128 bytes per lane
-  static constexpr int NS = 2;                       // tiles per warp ring
   static constexpr int kSlot = 32 * 16 * P;          // bytes per tile
-  static constexpr size_t kSmem = (size_t)kWarps * (NS * kSlot + TTile<G>::kBytes);
+  static constexpr size_t kSmem = (size_t)kWarps * (kSlot + TTile<G>::kBytes);
 };
 
 // The loop walks 32-chunk tiles, one per warp per grid-stride step, and is
 // warp-uniform so that every lane takes part in the exchanges.  Each warp
-// stages its tiles NS - 1 steps ahead in its shared-memory ring (one
-// cp.async group per tile, committed even when empty); the transpose's
-// __syncwarp calls order a slot's reads before its next copy.  Tile
-// indices are 32-bit (the entry point admits fewer than 2^35 chunks).
+// stages its next tile into its one shared slot as soon as it has read the
+// current tile out of it (one cp.async group per tile, committed even when
+// empty), so the copy runs under the current tile's arithmetic without
+// holding registers.  Tile indices are 32-bit (the entry point admits fewer
+// than 2^35 chunks).
 template <int G, bool kBF16>
-__global__ void __launch_bounds__(kThreads, kBF16 ? 3 : 2)
+__global__ void __launch_bounds__(kThreads, kBF16 ? 4 : 2)
     encode_kernel(const void* __restrict__ x, int64_t nchunks, uint8_t* __restrict__ packed,
                   float* __restrict__ s1_out, float* __restrict__ s2_out) {
   using R = EncRing<G, kBF16>;
-  constexpr int P = R::P, NS = R::NS;
+  constexpr int P = R::P;
   extern __shared__ __align__(128) uint8_t enc_smem[];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const uint32_t ring =
-      (uint32_t)__cvta_generic_to_shared(enc_smem) + (uint32_t)(wid * NS * R::kSlot);
+  const uint32_t slot = (uint32_t)__cvta_generic_to_shared(enc_smem) + (uint32_t)(wid * R::kSlot);
   float4* const tile =
-      reinterpret_cast<float4*>(enc_smem + kWarps * NS * R::kSlot + wid * TTile<G>::kBytes);
+      reinterpret_cast<float4*>(enc_smem + kWarps * R::kSlot + wid * TTile<G>::kBytes);
   const int ntiles = (int)((nchunks + 31) >> 5), nfull = (int)(nchunks >> 5);
   const int rem = (int)(nchunks & 31);
   const int tstride = (int)gridDim.x * kWarps;
   const int64_t step = (int64_t)tstride * R::kSlot;  // input bytes between a warp's tiles
   int t = (int)blockIdx.x * kWarps + wid;
   const uint8_t* src = static_cast<const uint8_t*>(x) + (int64_t)t * R::kSlot;
-  auto stage = [&](int tt, const uint8_t* s, int slot) {
-    const uint32_t dst = ring + (uint32_t)(slot * R::kSlot);
+  auto stage = [&](int tt, const uint8_t* s) {
     if (tt < nfull)
-      ring_copy_full<P>(dst, s + 16 * lane, lane);
+      ring_copy_full<P>(slot, s + 16 * lane, lane);
     else if (tt < ntiles)
-      ring_copy<P>(dst, s, (nchunks - 32 * (int64_t)tt) * (16 * P), lane);
+      ring_copy<P>(slot, s, (nchunks - 32 * (int64_t)tt) * (16 * P), lane);
     cp_async_commit();
   };
-#pragma unroll
-  for (int k = 0; k < NS - 1; ++k) stage(t + k * tstride, src + k * step, k);
-  for (int it = 0; t < ntiles; ++it, t += tstride, src += step) {
-    stage(t + (NS - 1) * tstride, src + (NS - 1) * step, (it + NS - 1) % NS);
-    cp_async_wait<NS - 1>();
+  stage(t, src);
+  for (; t < ntiles; t += tstride, src += step) {
+    cp_async_wait<0>();
     __syncwarp();
     uint4 v[P];
-    ring_read<P>(ring + (uint32_t)((it % NS) * R::kSlot), lane, v);
+    ring_read<P>(slot, lane, v);
+    __syncwarp();  // every lane's reads of the slot before its next copy
+    stage(t + tstride, src + step);
     Row32 y;
     unpack_chunk<kBF16>(v, y);
     encode_chunk<G>(y, t, t < nfull || lane < rem, lane, tile, packed, s1_out, s2_out);
@@ -514,7 +511,7 @@ __device__ __forceinline__ void store_values(void* out, int64_t chunk, int l, co
 // Tiles are staged NS - 1 loop steps ahead in the warp's ring, as in the
 // encode kernels; tile indices are 32-bit likewise.
 template <int G, bool kBF16Out>
-__global__ void __launch_bounds__(kThreads, (kBF16Out && G == 256) ? 4 : 1)
+__global__ void __launch_bounds__(kThreads, kBF16Out ? 4 : 1)
     decode_kernel(const uint8_t* __restrict__ packed, const float* __restrict__ s1_in,
                   const float* __restrict__ s2_in, int64_t nchunks, void* __restrict__ out) {
   using R = DecRing<G>;
