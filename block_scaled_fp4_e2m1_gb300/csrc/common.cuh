@@ -88,6 +88,20 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// max(|a|, |b|, |c|) and max(a, b, c) in one three-input max (exact; the
+// order of a max does not matter; a NaN operand is ignored).
+__device__ __forceinline__ float max3_abs(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(fabsf(a)), "f"(fabsf(b)), "f"(fabsf(c)));
+  return r;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // ------------------------------------------------------ packed fp32 pairs
 //
 // Two fp32 values in one 64-bit register pair, operated on by the packed

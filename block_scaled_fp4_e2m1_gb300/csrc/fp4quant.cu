@@ -141,20 +141,6 @@ __device__ __forceinline__ void transpose_to_blocks(Row32& y, float4* tile, int 
   __syncwarp();
 }
 
-// max(|a|, |b|, |c|) and max(a, b, c) in one three-input max (exact; the
-// order of a max does not matter; a NaN operand is ignored).
-__device__ __forceinline__ float max3_abs(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(fabsf(a)), "f"(fabsf(b)), "f"(fabsf(c)));
-  return r;
-}
-
-__device__ __forceinline__ float max3(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
-
 // max(0, |v|) over a lane's 32 values, as a tree of three-input maxima (16
 // instructions, 4 deep) rather than a chain.
 __device__ __forceinline__ float absmax32(const Row32& y) {

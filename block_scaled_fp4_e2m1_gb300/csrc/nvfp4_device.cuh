@@ -15,6 +15,7 @@
 #include <type_traits>
 
 #include "common.cuh"
+#include "rn_math.cuh"
 
 namespace fp4 {
 namespace {
@@ -302,6 +303,15 @@ __device__ __forceinline__ uint32_t settle_e2m1(float x, float eff, uint32_t cl,
   return exact_e2m1_quotient(x, eff);
 }
 
+// max(0, |v[i]|) over a block (a NaN element is ignored, as by fmaxf), as a
+// tree of three-input maxima.
+__device__ __forceinline__ float absmax16(const float v[16]) {
+  float a[5];
+#pragma unroll
+  for (int k = 0; k < 5; ++k) a[k] = max3_abs(v[3 * k], v[3 * k + 1], v[3 * k + 2]);
+  return max3(max3(a[0], a[1], a[2]), max3(a[3], a[4], fabsf(v[15])), 0.0f);
+}
+
 // Quantize one block v[16] (residual already added) under tensor scale s_t.
 // Writes the 8 packed bytes as two words, returns the e4m3 scale byte, and
 // (kEF) leaves the dequantized values in q[16].
@@ -310,9 +320,7 @@ __device__ __forceinline__ uint32_t quantize_block(const float v[16], float s_t,
                                                    uint64_t g0, uint32_t key0, uint32_t key1,
                                                    uint32_t step0, uint32_t step1, uint2& out,
                                                    float q[16]) {
-  float bmax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(v[i]));
+  const float bmax = absmax16(v);
   const uint32_t sb = block_scale_code(bmax, sd);
   const float eff = __fmul_rn(e4m3_value(sb), s_t);
   uint32_t w0, w1;
@@ -322,7 +330,7 @@ __device__ __forceinline__ uint32_t quantize_block(const float v[16], float s_t,
     // eff is outside the certified range) take the exact division
     // afterwards, their random half drawn again
     const bool fast = eff >= 0x1p-125f && eff <= 0x1p125f;
-    const float inv = fast ? __frcp_rn(eff) : 0.0f;
+    const float inv = fast ? rcp_rn(eff) : 0.0f;
     uint32_t pend = 0u;  // bit i: element i still to settle
     uint32_t ww[2];
 #pragma unroll
@@ -364,7 +372,7 @@ __device__ __forceinline__ uint32_t quantize_block(const float v[16], float s_t,
     }
   } else if (eff >= 0x1p-125f && eff <= 0x1p125f) {
     // RTN codes of RN(v / eff) through the certified bracket, 8 at a time
-    const float inv = __frcp_rn(eff);
+    const float inv = rcp_rn(eff);
     const float il = __fmul_rn(inv, 0x1.fffffp-1f);   // 1 - 2^-21
     const float ih = __fmul_rn(inv, 0x1.000008p+0f);  // 1 + 2^-21
     uint32_t lo[2], hi[2];
