@@ -102,6 +102,27 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return r;
 }
 
+// The 8 codes of w (code i in bits 4i+3..4i) as exact floats, through the
+// hardware e2m1x2 -> f16x2 conversion of each byte of w.
+__device__ __forceinline__ void e2m1x8_to_f32(uint32_t w, float o[8]) {
+  uint32_t h[4];
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "cvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
+        : "=f"(o[2 * k]), "=f"(o[2 * k + 1])
+        : "r"(h[k]));
+  }
+}
+
 // ------------------------------------------------------ packed fp32 pairs
 //
 // Two fp32 values in one 64-bit register pair, operated on by the packed

@@ -424,22 +424,6 @@ __global__ void __launch_bounds__(kThreads, kBF16 ? 4 : 2)
   cp_async_wait<0>();
 }
 
-// The 8 codes of w (code i in bits 4i+3..4i) as exact floats, through the
-// hardware e2m1x2 -> f16x2 conversion.
-__device__ __forceinline__ void e2m1x8_values(uint32_t w, float o[8]) {
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    uint32_t h2;
-    const uint16_t byte = (uint16_t)((w >> (8 * k)) & 0xFFu);
-    asm("{\n\t.reg .b8 b;\n\tcvt.u8.u16 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}"
-        : "=r"(h2)
-        : "h"(byte));
-    const uint16_t lo = (uint16_t)(h2 & 0xFFFFu), hi = (uint16_t)(h2 >> 16);
-    asm("cvt.f32.f16 %0, %1;" : "=f"(o[2 * k]) : "h"(lo));
-    asm("cvt.f32.f16 %0, %1;" : "=f"(o[2 * k + 1]) : "h"(hi));
-  }
-}
-
 __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
   float v;
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
@@ -550,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, (kBF16Out && G != 64) ? 4 : 1)
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       float v[8];
-      e2m1x8_values(words[k], v);
+      e2m1x8_to_f32(words[k], v);
 #pragma unroll
       for (int i = 0; i < 4; ++i) z.p[4 * k + i] = mul2(F2{v[2 * i], v[2 * i + 1]}, splat(sc2));
     }

@@ -131,19 +131,9 @@ __global__ void __launch_bounds__(kThreads)
     float o[32];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
+      e2m1x8_to_f32(words[k], o + 8 * k);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t h2;
-        const uint16_t byte = (uint16_t)((words[k] >> (8 * j)) & 0xFFu);
-        asm("{\n\t.reg .b8 c;\n\tcvt.u8.u16 c, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, c;\n\t}"
-            : "=r"(h2)
-            : "h"(byte));
-        float lo, hi;
-        asm("cvt.f32.f16 %0, %1;" : "=f"(lo) : "h"((uint16_t)(h2 & 0xFFFFu)));
-        asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"((uint16_t)(h2 >> 16)));
-        o[8 * k + 2 * j] = __fmul_rn(lo, f);
-        o[8 * k + 2 * j + 1] = __fmul_rn(hi, f);
-      }
+      for (int j = 0; j < 8; ++j) o[8 * k + j] = __fmul_rn(o[8 * k + j], f);
     }
     const bool nan = S == 255u;
     if (kBF16Out) {

@@ -561,22 +561,6 @@ __device__ __forceinline__ uint32_t quantize_block_bf16_rtn(const U32x8& raw, co
   return sb;
 }
 
-// Decode the 8 codes of w (code i in bits 4i+3..4i) to exact floats via the
-// hardware e2m1x2 -> f16x2 conversion.
-__device__ __forceinline__ void e2m1x8_to_f32(uint32_t w, float o[8]) {
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    uint32_t h2;
-    const uint16_t byte = (uint16_t)((w >> (8 * k)) & 0xFFu);
-    asm("{\n\t.reg .b8 b;\n\tcvt.u8.u16 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}"
-        : "=r"(h2)
-        : "h"(byte));
-    uint16_t lo = (uint16_t)(h2 & 0xFFFFu), hi = (uint16_t)(h2 >> 16);
-    asm("cvt.f32.f16 %0, %1;" : "=f"(o[2 * k]) : "h"(lo));
-    asm("cvt.f32.f16 %0, %1;" : "=f"(o[2 * k + 1]) : "h"(hi));
-  }
-}
-
 template <bool kBF16Out>
 __device__ __forceinline__ void dequantize_store(uint32_t w0, uint32_t w1, float eff, void* y,
                                                  int64_t b) {

@@ -78,19 +78,9 @@ __global__ void __launch_bounds__(kThreads)
     float o[16];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
+      e2m1x8_to_f32(words[h], o + 8 * h);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        uint32_t h2;
-        const uint16_t byte = (uint16_t)((words[h] >> (8 * k)) & 0xFFu);
-        asm("{\n\t.reg .b8 c;\n\tcvt.u8.u16 c, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, c;\n\t}"
-            : "=r"(h2)
-            : "h"(byte));
-        float lo, hi;
-        asm("cvt.f32.f16 %0, %1;" : "=f"(lo) : "h"((uint16_t)(h2 & 0xFFFFu)));
-        asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"((uint16_t)(h2 >> 16)));
-        o[8 * h + 2 * k] = __fmul_rn(lo, s);
-        o[8 * h + 2 * k + 1] = __fmul_rn(hi, s);
-      }
+      for (int k = 0; k < 8; ++k) o[8 * h + k] = __fmul_rn(o[8 * h + k], s);
     }
     if (kBF16Out) {
       U32x8 w;
