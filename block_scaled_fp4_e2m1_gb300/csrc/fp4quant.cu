@@ -630,6 +630,7 @@ fp4_status fp4quant_decode(const uint8_t* packed, const float* s1, const float* 
   if (!dtype_ok(out_dtype)) return FP4_ERR_DTYPE;
   if (!group_ok(group)) return FP4_ERR_ARG;
   if (rows < 0 || cols < 0 || cols % group != 0) return FP4_ERR_SHAPE;
+  if (cols > 0 && rows > ((int64_t)1 << 40) / cols) return FP4_ERR_SHAPE;
   const int64_t nchunks = rows * cols / kE;
   if (nchunks > 0 && (!y || !packed || !s1 || !s2)) return FP4_ERR_NULL;
   if (!aligned(y, 32) || !aligned(packed, 16) || !aligned(s1, 4) || !aligned(s2, 4))

@@ -403,8 +403,8 @@ fp4_status fp4_seg_scale_offsets(const int64_t* host_row_off, int32_t num_segmen
  *   packed  [rows, cols/2], 16-byte aligned
  *   s1, s2  [rows, cols/G] fp32, 4-byte aligned
  *   cols % G == 0
- * Errors: FP4_ERR_SHAPE for negative sizes, cols % G != 0 or (encode only)
- * rows * cols above 2^40 elements. */
+ * Errors: FP4_ERR_SHAPE for negative sizes, cols % G != 0 or rows * cols
+ * above 2^40 elements. */
 fp4_status fp4quant_encode(const void* x, int dtype, int64_t rows, int64_t cols, int group,
                            uint8_t* packed, float* s1, float* s2, void* stream);
 fp4_status fp4quant_decode(const uint8_t* packed, const float* s1, const float* s2,

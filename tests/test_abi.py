@@ -135,9 +135,11 @@ def test_mx_fp8_fp4quant_argument_checks(L):
     assert enc(A, 1, 2, 96, 64, A, A, A, None) == 3              # cols % group
     assert enc(A, 1, 2, 128, 64, A, None, A, None) == 1
     assert enc(MIS, 1, 2, 128, 64, A, A, A, None) == 2
+    assert enc(A, 1, 1 << 34, 1 << 7, 64, A, A, A, None) == 3    # above 2^40 elements
     dec = L.fp4quant_decode
     assert dec(A, A, A, 2, 128, 512, A, 1, None) == 5
     assert dec(A, A, A, 2, 128, 64, A, 9, None) == 4
+    assert dec(A, A, A, 1 << 34, 1 << 7, 64, A, 1, None) == 3    # above 2^40 elements
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
