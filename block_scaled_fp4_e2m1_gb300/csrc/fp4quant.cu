@@ -14,13 +14,14 @@
 // the natural (Sylvester) order h = 1, 2, ..., G/2, which the CPU oracle
 // follows, in two phases:
 //   - phase 1: lane l holds the 32 consecutive elements 32 l .. 32 l + 31 of
-//     the group (two 256-bit loads of bf16), so the sum of squares and the
-//     stages h = 1 .. 16 are in-thread;
+//     the group (staged through shared memory by cp.async), so the sum of
+//     squares and the stages h = 1 .. 16 are in-thread;
 //   - a transpose through a warp-private shared-memory tile: lane l then
 //     holds, for every lane i of its group, the 32/L consecutive elements
 //     32 i + l (32/L) .. of i's chunk; the tile's 16-byte units are placed
-//     so that every 128-bit store and load of a warp is free of bank
-//     conflicts;
+//     so that the eight lanes of a quarter-warp touch eight different bank
+//     groups on every 128-bit store and load, at addresses that are a
+//     per-lane base plus a constant;
 //   - phase 2: the stages h = 32 .. G/2 pair elements of chunks i and
 //     i xor (h/32), now in the same thread.
 // Each stage is one correctly rounded add and subtract per pair, two pairs
