@@ -109,9 +109,7 @@ __device__ __forceinline__ void wht_across_chunks(Row32& y) {
 // blocks (9 units apart) do not overlap; and since 9 L = L and 9 = 1 mod 8,
 // the eight lanes of a quarter-warp (S groups of L lanes) touch eight
 // different units mod 8 on every store and load: no bank conflict.
-template <int G>
 struct TTile {
-  static constexpr int L = G / kE;
   static constexpr int kBytes = 16 * 32 * 9;  // per warp: 32/L regions of 9 L units
 };
 
@@ -159,33 +157,19 @@ __device__ __forceinline__ float absmax32(const Row32& y) {
   return max3(max3(b0, b1, b2), b3, 0.0f);
 }
 
-template <int G>
-__device__ __forceinline__ float group_sum(float v) {
-#pragma unroll
-  for (int m = 1; m < G / kE; m <<= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, m));
-  return v;
-}
-
-template <int G>
-__device__ __forceinline__ float group_max(float v) {
-#pragma unroll
-  for (int m = 1; m < G / kE; m <<= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, m));
-  return v;
-}
-
 // Per-warp staging ring in shared memory for a kernel's input.  A tile is
 // what the warp's 32 lanes consume in one loop step, P 16-byte pieces per
 // lane, contiguous in global memory (lane c's pieces at 16 (P c + q)).  The
 // warp copies a tile with cp.async, piece 32 k + lane in instruction k, so
-// each copy instruction reads 512 contiguous bytes; tiles are copied NS - 1
-// steps ahead of their use, so several tiles per warp are in flight without
-// holding registers.  In shared memory lane c's piece q sits at unit
-// P c + (q xor sw(c)), sw(c) = (c / (8/P)) mod P: the eight lanes of a
-// quarter-warp then touch eight different 16-byte units mod 128 bytes, for
-// the copies and for each lane's 128-bit reads of its own pieces.
+// each copy instruction reads 512 contiguous bytes; tiles are copied ahead of
+// their use, so tiles are in flight without holding registers.  In shared
+// memory lane c's piece q sits at unit P c + (q xor sw(c)), with
+// sw(c) = (c / (8/P)) mod P for P <= 8 and c mod 8 for P = 16, 32: the eight
+// lanes of a quarter-warp then touch eight different 16-byte units mod 128
+// bytes, for the copies and for each lane's 128-bit reads of its own pieces.
 template <int P>
 __device__ __forceinline__ int ring_unit(int c, int q) {
-  return P * c + (q ^ ((c / (8 / P)) & (P - 1)));
+  return P * c + (q ^ (P <= 8 ? ((c / (8 / P)) & (P - 1)) : (c & 7)));
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool ok) {
@@ -205,11 +189,11 @@ __device__ __forceinline__ void cp_async16_all(uint32_t dst, const void* src) {
 }
 
 // Byte offset in a slot of piece 32 k + lane: 512 (k - k mod M) plus a lane
-// offset that depends on k only through k mod M (M = 2 for P = 8, else 1),
-// so every copy of a tile is one per-lane base plus a constant.
+// offset that depends on k only through k mod M (M = P/4 for P >= 8, else
+// 1), so every copy of a tile is one per-lane base plus a constant.
 template <int P>
 __device__ __forceinline__ uint32_t ring_piece_off(int lane, int k) {
-  constexpr int M = P == 8 ? 2 : 1;
+  constexpr int M = P >= 8 ? P / 4 : 1;
   const int p = 32 * (k % M) + lane;
   return 16u * (uint32_t)ring_unit<P>(p / P, p % P) + 512u * (uint32_t)(k - k % M);
 }
@@ -236,8 +220,8 @@ __device__ __forceinline__ void ring_copy(uint32_t dst, const uint8_t* src, int6
   }
 }
 
-// Lane's P pieces of the tile in the slot at byte address slot (64-byte
-// aligned): piece q at (slot + 16 P lane + 16 sw) xor 16 q.
+// Lane's P pieces of the tile in the slot at byte address slot (aligned to
+// 16 P bytes): piece q at (slot + 16 P lane + 16 sw) xor 16 q.
 template <int P>
 __device__ __forceinline__ void ring_read(uint32_t slot, int lane, uint4 v[P]) {
   const uint32_t a = slot + 16u * (uint32_t)ring_unit<P>(lane, 0);
@@ -252,164 +236,163 @@ __device__ __forceinline__ void ring_read(uint32_t slot, int lane, uint4 v[P]) {
 __device__ __forceinline__ float bf16_lo_(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi_(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// A lane's 32 input elements from its P = 4 (bf16) or 8 (fp32) pieces.
-template <bool kBF16>
-__device__ __forceinline__ void unpack_chunk(const uint4* v, Row32& y) {
-  if (kBF16) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint32_t w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) y.p[4 * q + i] = F2{bf16_lo_(w[i]), bf16_hi_(w[i])};
-    }
-  } else {
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      y.p[2 * q] = F2{__uint_as_float(v[q].x), __uint_as_float(v[q].y)};
-      y.p[2 * q + 1] = F2{__uint_as_float(v[q].z), __uint_as_float(v[q].w)};
-    }
-  }
-}
-
-// Stores the B codes of each source chunk of the group: B = 4 -> 2 bytes,
-// 8 -> 4 bytes, 16 -> 8 bytes at byte l B / 2 of the chunk's 16-byte row.
-template <int B>
-__device__ __forceinline__ void store_codes(uint8_t* row, int l, const uint32_t* w) {
-  if (B == 4) {
-    *reinterpret_cast<uint16_t*>(row + 2 * l) = (uint16_t)w[0];
-  } else if (B == 8) {
-    *reinterpret_cast<uint32_t*>(row + 4 * l) = w[0];
-  } else {
-    *reinterpret_cast<uint2*>(row + 8 * l) = make_uint2(w[0], w[1]);
-  }
-}
-
-// Encodes the group chunk set this warp holds (tile t: lane's chunk
-// 32 t + lane, valid when inside the tensor) and stores codes and scales.
-// Lanes past the end compute on zeros and store nothing (the chunk count is
-// a multiple of L, so a group is either entirely inside or entirely past the
-// end).
+// ------------------------------------------------------------------ encode
+//
+// Each lane holds whole chunk pairs of its group: 64 elements (G = 64 and
+// 256: L = G/64 lanes per group) or 128 (G = 128: one lane per group).
+// Chunk pair m (chunks 2m, 2m + 1) sits in 32 packed pairs
+// p[32 h + j] = (chunk 2m element j, chunk 2m + 1 element j), h = m - NP l
+// (NP = chunk pairs per lane).  Stages h = 1 .. 16 then pair registers, both
+// chunks at once; stage h = 32 pairs the two halves of each register; stage
+// h = 64 of G = 128 pairs the lane's two chunk pairs.  For G = 256 the
+// stages h = 64, 128 follow a transpose (transpose_wide), after which lane k
+// holds positions 8 k .. 8 k + 7 of every chunk pair m as
+// p[8 m + b] = (chunk 2m, chunk 2m + 1 at position 8 k + b).
+//
+// Every product that feeds a packed addition (the squares, the RMS scaling)
+// is a packed fma with the runtime -0 addend nz: fma(a, b, -0) = RN(a b)
+// exactly, and the compiler cannot fold nz away, so no multiply fuses into
+// an add.  More elements per lane mean fewer lanes per group: G = 64 and 128
+// need no cross-lane exchange at all.
 template <int G>
-__device__ __forceinline__ void encode_chunk(Row32& y, int t, bool valid, int lane, float4* tile,
-                                             uint8_t* __restrict__ packed,
-                                             float* __restrict__ s1_out,
-                                             float* __restrict__ s2_out) {
-  constexpr int L = G / kE, B = kE / L;
-  // RMS scale: the pairwise tree over adjacent squares, levels 2-5 two sums
-  // per instruction (the halves 0..15 | 16..31 side by side)
-  F2 sq[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const F2 a = mul2(y.p[i], y.p[i]), b = mul2(y.p[8 + i], y.p[8 + i]);
-    sq[i] = F2{__fadd_rn(a.x, a.y), __fadd_rn(b.x, b.y)};
-  }
-#pragma unroll
-  for (int w = 8; w > 1; w >>= 1) {
-#pragma unroll
-    for (int i = 0; i < w / 2; ++i) sq[i] = add2(sq[2 * i], sq[2 * i + 1]);
-  }
-  const float ss = group_sum<G>(__fadd_rn(sq[0].x, sq[0].y));
-  const float rms = sqrt_rn(__fmul_rn(ss, 1.0f / (float)G));
-  const float inv1 = rms == 0.0f ? 0.0f : rcp_rn(rms);
-#pragma unroll
-  for (int i = 0; i < 16; ++i) y.p[i] = mul2(y.p[i], splat(inv1));
-  // transform: stages 1..16, transpose, stages 32..G/2, normalization
-  wht_in_thread(y);
-  transpose_to_blocks<G>(y, tile, lane);
-  wht_across_chunks<G>(y);
-  // normalization and absmax scale into [-6, 6].  z = RN(w c) and
-  // max|z| = RN(max|w| c) (RN is monotone).  For G = 64 and 256, c is a
-  // power of two: when 2^-20 <= max|z| <= 2^100, RN(z inv2) = RN(w (c inv2))
-  // for every element (c inv2 is exact; where w c is normal, z = w c
-  // exactly; where it is subnormal, both products are below 2^-100 and
-  // round to a zero code of w's sign), so the two scalings fold into one.
-  const float c = wht_norm<G>();
-  const float zmax = __fmul_rn(group_max<G>(absmax32(y)), c);
-  const float sc2 = div6_rn(zmax);
-  const float inv2 = sc2 == 0.0f ? 0.0f : rcp_rn(sc2);
-  if (G != 128 && zmax >= 0x1p-20f && zmax <= 0x1p100f) {
-    const F2 m = splat(__fmul_rn(inv2, c));
-#pragma unroll
-    for (int i = 0; i < 16; ++i) y.p[i] = mul2(y.p[i], m);
-  } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) y.p[i] = mul2(mul2(y.p[i], splat(c)), splat(inv2));
-  }
-  if (!valid) return;
-  const int l = lane % L;
-  // the group's first chunk row
-  uint8_t* const rows = packed + 16 * ((int64_t)t * 32 + (lane - l));
-  if (B == 4) {
-    // two source chunks' 4 codes per conversion word, stored as halves
-#pragma unroll
-    for (int i = 0; i < L; i += 2) {
-      const F2* q = y.p + i * 2;
-      const uint32_t w = cvt_e2m1x8(q[0].x, q[0].y, q[1].x, q[1].y, q[2].x, q[2].y, q[3].x,
-                                    q[3].y);
-      *reinterpret_cast<uint16_t*>(rows + 16 * i + 2 * l) = (uint16_t)w;
-      *reinterpret_cast<uint16_t*>(rows + 16 * (i + 1) + 2 * l) = (uint16_t)(w >> 16);
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < L; ++i) {
-      const F2* q = y.p + i * (B / 2);
-      uint32_t w[2];
-#pragma unroll
-      for (int k = 0; k < B / 8; ++k)
-        w[k] = cvt_e2m1x8(q[4 * k].x, q[4 * k].y, q[4 * k + 1].x, q[4 * k + 1].y,
-                          q[4 * k + 2].x, q[4 * k + 2].y, q[4 * k + 3].x, q[4 * k + 3].y);
-      store_codes<B>(rows + 16 * i, l, w);
-    }
-  }
-  if (l == 0) {
-    const int64_t gi = (int64_t)t * (32 / L) + lane / L;
-    s1_out[gi] = rms;
-    s2_out[gi] = sc2;
-  }
-}
-
-// Input pieces per lane and the shared memory of the encode kernels: one
-// staging slot per warp plus its transpose tile.  (bf16: 6.5 KB per warp,
-// four CTAs of 256 threads per SM at 64 registers; fp32: 8.5 KB per warp,
-// two CTAs.)
-template <int G, bool kBF16>
-struct EncRing {
-  static constexpr int P = kBF16 ? 4 : 8;            // 64 or 128 bytes per lane
-  static constexpr int kSlot = 32 * 16 * P;          // bytes per tile
-  static constexpr size_t kSmem = (size_t)kWarps * (kSlot + TTile<G>::kBytes);
+struct Wide {
+  static constexpr int EPL = G == 128 ? 128 : 64;  // elements per lane
+  static constexpr int NP = EPL / 64;               // chunk pairs per lane
+  static constexpr int L = G / EPL;                 // lanes per group
+  static constexpr int B = 32 / L;                  // positions per chunk after the transpose
 };
 
-// The loop walks 32-chunk tiles, one per warp per grid-stride step, and is
-// warp-uniform so that every lane takes part in the exchanges.  Each warp
-// stages its next tile into its one shared slot as soon as it has read the
-// current tile out of it (one cp.async group per tile, committed even when
-// empty), so the copy runs under the current tile's arithmetic without
-// holding registers.  Tile indices are 32-bit (the entry point admits fewer
-// than 2^35 chunks).
+template <int G>
+struct WideRow {
+  F2 p[16 * Wide<G>::NP * 2];
+};
+
+// Input pieces per lane and shared memory of the encode: one staging slot
+// per warp (bf16: 8 or 16 pieces per lane, fp32 twice that), plus for
+// G = 256 the transpose tile.
 template <int G, bool kBF16>
-__global__ void __launch_bounds__(kThreads, kBF16 ? 4 : 2)
-    encode_kernel(const void* __restrict__ x, int64_t nchunks, uint8_t* __restrict__ packed,
-                  float* __restrict__ s1_out, float* __restrict__ s2_out) {
-  using R = EncRing<G, kBF16>;
-  constexpr int P = R::P;
-  extern __shared__ __align__(128) uint8_t enc_smem[];
+struct EncSmem {
+  static constexpr int P = Wide<G>::EPL * (kBF16 ? 2 : 4) / 16;
+  static constexpr int kSlot = 32 * 16 * P;
+  static constexpr int kTile = Wide<G>::L > 1 ? 16 * 17 * 32 : 0;
+  static constexpr size_t kSmem = (size_t)kWarps * (kSlot + kTile);
+};
+
+// The lane's chunk pairs from its staged pieces: chunk c's 32 elements are
+// pieces 4c .. 4c + 3 (bf16) or 8c .. 8c + 7 (fp32).
+template <int G, bool kBF16>
+__device__ __forceinline__ void unpack_wide(const uint4* v, WideRow<G>& y) {
+  constexpr int NP = Wide<G>::NP;
+#pragma unroll
+  for (int h = 0; h < NP; ++h) {
+    if (kBF16) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 a = v[8 * h + q], b = v[8 * h + 4 + q];
+        const uint32_t lo[4] = {a.x, a.y, a.z, a.w};
+        const uint32_t hi[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int i = 4 * q + k;  // word i: elements 2i, 2i + 1 of each chunk
+          y.p[32 * h + 2 * i] = F2{bf16_lo_(lo[k]), bf16_lo_(hi[k])};
+          y.p[32 * h + 2 * i + 1] = F2{bf16_hi_(lo[k]), bf16_hi_(hi[k])};
+        }
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const uint4 a = v[16 * h + q], b = v[16 * h + 8 + q];
+        y.p[32 * h + 4 * q] = F2{__uint_as_float(a.x), __uint_as_float(b.x)};
+        y.p[32 * h + 4 * q + 1] = F2{__uint_as_float(a.y), __uint_as_float(b.y)};
+        y.p[32 * h + 4 * q + 2] = F2{__uint_as_float(a.z), __uint_as_float(b.z)};
+        y.p[32 * h + 4 * q + 3] = F2{__uint_as_float(a.w), __uint_as_float(b.w)};
+      }
+    }
+  }
+}
+
+// G = 256 transpose: group g owns 17 L = 68 16-byte units from unit 68 g;
+// writer l puts its unit h (h < 4: positions 8 k + 2h, 8 k + 2h + 1 of its
+// chunk pair) for reader k at l + L h + 17 k, reader k takes writer m's unit
+// h from there.  Both sides are a lane base plus a constant, and since
+// 17 = 1 mod 8 the eight lanes of a quarter-warp touch eight different units
+// mod 8 on every access.
+template <int G>
+__device__ __forceinline__ void transpose_wide(WideRow<G>& y, float4* tile, int lane) {
+  constexpr int L = Wide<G>::L, B = Wide<G>::B, S = B / 2;
+  const int g = lane / L, l = lane % L;
+  float4* const st = tile + 17 * L * g + l;
+  const float4* const ld = tile + 17 * L * g + 17 * l;
+#pragma unroll
+  for (int k = 0; k < L; ++k) {
+#pragma unroll
+    for (int h = 0; h < S; ++h) {
+      const F2 a = y.p[B * k + 2 * h], b = y.p[B * k + 2 * h + 1];
+      st[L * h + 17 * k] = make_float4(a.x, a.y, b.x, b.y);
+    }
+  }
+  __syncwarp();
+#pragma unroll
+  for (int m = 0; m < L; ++m) {
+#pragma unroll
+    for (int h = 0; h < S; ++h) {
+      const float4 v = ld[m + L * h];
+      y.p[B * m + 2 * h] = F2{v.x, v.y};
+      y.p[B * m + 2 * h + 1] = F2{v.z, v.w};
+    }
+  }
+  __syncwarp();
+}
+
+template <int G>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+  for (int m = 1; m < Wide<G>::L; m <<= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, m));
+  return v;
+}
+
+template <int G>
+__device__ __forceinline__ float group_max(float v) {
+#pragma unroll
+  for (int m = 1; m < Wide<G>::L; m <<= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, m));
+  return v;
+}
+
+// The loop walks tiles of 32 lanes' slices, one per warp per grid-stride
+// step, warp-uniform so that every lane takes part in the exchanges.  Each
+// warp stages its next tile into its one shared slot as soon as it has read
+// the current tile out of it (one cp.async group per tile, committed even
+// when empty), so the copy runs under the current tile's arithmetic.  Lanes
+// past the end compute on zeros and store nothing (the slice count is a
+// multiple of L, so a group is entirely inside or entirely past the end).
+// Tile indices are 32-bit (the entry point admits fewer than 2^40 elements).
+template <int G, bool kBF16>
+__global__ void __launch_bounds__(kThreads, G == 128 ? 1 : 2)
+    encode_kernel(const void* __restrict__ x, int64_t nslices, uint8_t* __restrict__ packed,
+                  float* __restrict__ s1_out, float* __restrict__ s2_out, float nz) {
+  using W = Wide<G>;
+  using M = EncSmem<G, kBF16>;
+  constexpr int NP = W::NP, L = W::L, B = W::B, P = M::P, NR = 32 * NP;
+  extern __shared__ __align__(512) uint8_t enc_smem[];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const uint32_t slot = (uint32_t)__cvta_generic_to_shared(enc_smem) + (uint32_t)(wid * R::kSlot);
+  const uint32_t slot =
+      (uint32_t)__cvta_generic_to_shared(enc_smem) + (uint32_t)(wid * M::kSlot);
   float4* const tile =
-      reinterpret_cast<float4*>(enc_smem + kWarps * R::kSlot + wid * TTile<G>::kBytes);
-  const int ntiles = (int)((nchunks + 31) >> 5), nfull = (int)(nchunks >> 5);
-  const int rem = (int)(nchunks & 31);
+      reinterpret_cast<float4*>(enc_smem + kWarps * M::kSlot + wid * M::kTile);
+  const int ntiles = (int)((nslices + 31) >> 5), nfull = (int)(nslices >> 5);
+  const int rem = (int)(nslices & 31);
   const int tstride = (int)gridDim.x * kWarps;
-  const int64_t step = (int64_t)tstride * R::kSlot;  // input bytes between a warp's tiles
+  const int64_t step = (int64_t)tstride * M::kSlot;  // input bytes between a warp's tiles
   int t = (int)blockIdx.x * kWarps + wid;
-  const uint8_t* src = static_cast<const uint8_t*>(x) + (int64_t)t * R::kSlot;
+  const uint8_t* src = static_cast<const uint8_t*>(x) + (int64_t)t * M::kSlot;
   auto stage = [&](int tt, const uint8_t* s) {
     if (tt < nfull)
       ring_copy_full<P>(slot, s + 16 * lane, lane);
     else if (tt < ntiles)
-      ring_copy<P>(slot, s, (nchunks - 32 * (int64_t)tt) * (16 * P), lane);
+      ring_copy<P>(slot, s, (nslices - 32 * (int64_t)tt) * (16 * P), lane);
     cp_async_commit();
   };
+  const F2 nz2{nz, nz};
   stage(t, src);
   for (; t < ntiles; t += tstride, src += step) {
     cp_async_wait<0>();
@@ -418,9 +401,135 @@ __global__ void __launch_bounds__(kThreads, kBF16 ? 4 : 2)
     ring_read<P>(slot, lane, v);
     __syncwarp();  // every lane's reads of the slot before its next copy
     stage(t + tstride, src + step);
-    Row32 y;
-    unpack_chunk<kBF16>(v, y);
-    encode_chunk<G>(y, t, t < nfull || lane < rem, lane, tile, packed, s1_out, s2_out);
+    WideRow<G> y;
+    unpack_wide<G, kBF16>(v, y);
+    // RMS: the pairwise tree over adjacent squares, both chunks of a pair side
+    // by side (levels 1 - 5), then the pair, the lane's pairs and the lanes
+    float pair[NP];
+#pragma unroll
+    for (int h = 0; h < NP; ++h) {
+      F2 sq[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const F2 a = y.p[32 * h + 2 * i], b = y.p[32 * h + 2 * i + 1];
+        sq[i] = add2(fma2(a, a, nz2), fma2(b, b, nz2));
+      }
+#pragma unroll
+      for (int w = 16; w > 1; w >>= 1) {
+#pragma unroll
+        for (int i = 0; i < w / 2; ++i) sq[i] = add2(sq[2 * i], sq[2 * i + 1]);
+      }
+      pair[h] = __fadd_rn(sq[0].x, sq[0].y);
+    }
+    const float ss = group_sum<G>(NP == 2 ? __fadd_rn(pair[0], pair[NP - 1]) : pair[0]);
+    const float rms = sqrt_rn(__fmul_rn(ss, 1.0f / (float)G));
+    const float inv1 = rms == 0.0f ? 0.0f : rcp_rn(rms);
+    const F2 i1 = splat(inv1);
+#pragma unroll
+    for (int j = 0; j < NR; ++j) y.p[j] = fma2(y.p[j], i1, nz2);
+    // stages h = 1 .. 16, h = 32 (the halves), h = 64 inside the lane (G = 128)
+#pragma unroll
+    for (int hp = 1; hp < 32; hp <<= 1) {
+#pragma unroll
+      for (int j = 0; j < NR; ++j) {
+        if (j & hp) continue;
+        const F2 a = y.p[j], b = y.p[j + hp];
+        y.p[j] = add2(a, b);
+        y.p[j + hp] = sub2(a, b);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < NR; ++j) {
+      const float a = y.p[j].x, b = y.p[j].y;
+      y.p[j] = F2{__fadd_rn(a, b), __fsub_rn(a, b)};
+    }
+    if (NP == 2) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const F2 a = y.p[j], b = y.p[32 + j];
+        y.p[j] = add2(a, b);
+        y.p[32 + j] = sub2(a, b);
+      }
+    }
+    if (L > 1) {
+      // stages h = 64 (chunk pairs m, m xor 1) and h = 128 (m, m xor 2)
+      transpose_wide<G>(y, tile, lane);
+#pragma unroll
+      for (int mm = 1; mm < L; mm <<= 1) {
+#pragma unroll
+        for (int m = 0; m < L; ++m) {
+          if (m & mm) continue;
+#pragma unroll
+          for (int b = 0; b < B; ++b) {
+            const F2 a = y.p[m * B + b], c = y.p[(m + mm) * B + b];
+            y.p[m * B + b] = add2(a, c);
+            y.p[(m + mm) * B + b] = sub2(a, c);
+          }
+        }
+      }
+    }
+    // normalization and absmax scale into [-6, 6].  z = RN(w c) and
+    // max|z| = RN(max|w| c) (RN is monotone).  For G = 64 and 256, c is a
+    // power of two: when 2^-20 <= max|z| <= 2^100, RN(z inv2) = RN(w (c inv2))
+    // for every element (c inv2 is exact; where w c is normal, z = w c
+    // exactly; where it is subnormal, both products are below 2^-100 and
+    // round to a zero code of w's sign), so the two scalings fold into one.
+    float am = 0.0f;
+#pragma unroll
+    for (int q = 0; q < NR / 16; ++q) {
+      const Row32& h = *reinterpret_cast<const Row32*>(y.p + 16 * q);
+      am = fmaxf(am, absmax32(h));
+    }
+    const float c = wht_norm<G>();
+    const float zmax = __fmul_rn(group_max<G>(am), c);
+    const float sc2 = div6_rn(zmax);
+    const float inv2 = sc2 == 0.0f ? 0.0f : rcp_rn(sc2);
+    if (G != 128 && zmax >= 0x1p-20f && zmax <= 0x1p100f) {
+      const F2 m = splat(__fmul_rn(inv2, c));
+#pragma unroll
+      for (int j = 0; j < NR; ++j) y.p[j] = mul2(y.p[j], m);
+    } else {
+#pragma unroll
+      for (int j = 0; j < NR; ++j) y.p[j] = mul2(mul2(y.p[j], splat(c)), splat(inv2));
+    }
+    if (!(t < nfull || lane < rem)) continue;
+    const int l = lane % L;
+    const int64_t sl = (int64_t)t * 32 + lane;                    // the lane's slice
+    uint8_t* const grp = packed + (int64_t)(W::EPL / 2) * (sl - l);  // the group's codes
+    if (L == 1) {
+      // the lane's chunks in order, 32 or 64 bytes
+#pragma unroll
+      for (int h = 0; h < NP; ++h) {
+        uint32_t wd[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const F2* q = y.p + 32 * h + 8 * k;
+          wd[k] = cvt_e2m1x8(q[0].x, q[1].x, q[2].x, q[3].x, q[4].x, q[5].x, q[6].x, q[7].x);
+          wd[4 + k] = cvt_e2m1x8(q[0].y, q[1].y, q[2].y, q[3].y, q[4].y, q[5].y, q[6].y, q[7].y);
+        }
+        uint4* const o = reinterpret_cast<uint4*>(grp + 32 * h);
+        o[0] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+        o[1] = make_uint4(wd[4], wd[5], wd[6], wd[7]);
+      }
+    } else {
+      // chunk 2m: p[8 m + b].x, chunk 2m + 1: .y, positions 8 l + b: four
+      // bytes at byte 4 l of each chunk's 16-byte row
+#pragma unroll
+      for (int m = 0; m < L; ++m) {
+        const F2* q = y.p + m * B;
+        const uint32_t wx =
+            cvt_e2m1x8(q[0].x, q[1].x, q[2].x, q[3].x, q[4].x, q[5].x, q[6].x, q[7].x);
+        const uint32_t wy =
+            cvt_e2m1x8(q[0].y, q[1].y, q[2].y, q[3].y, q[4].y, q[5].y, q[6].y, q[7].y);
+        *reinterpret_cast<uint32_t*>(grp + 32 * m + 4 * l) = wx;
+        *reinterpret_cast<uint32_t*>(grp + 32 * m + 16 + 4 * l) = wy;
+      }
+    }
+    if (l == 0) {
+      const int64_t gi = sl / L;
+      s1_out[gi] = rms;
+      s2_out[gi] = sc2;
+    }
   }
   cp_async_wait<0>();
 }
@@ -438,7 +547,7 @@ struct DecRing {
   static constexpr int L = G / kE, NG = 32 / L;
   static constexpr int NS = 4;                       // tiles per warp ring
   static constexpr int kSlot = 512 + 8 * NG;         // bytes per tile (multiple of 16)
-  static constexpr size_t kSmem = (size_t)kWarps * (NS * kSlot + TTile<G>::kBytes);
+  static constexpr size_t kSmem = (size_t)kWarps * (NS * kSlot + TTile::kBytes);
 };
 
 // Stores the B values of each source chunk: bf16 B = 4, 8, 16 -> 8, 16, 32
@@ -495,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, (kBF16Out && G != 64) ? 4 : 1)
   const uint32_t ring =
       (uint32_t)__cvta_generic_to_shared(dec_smem) + (uint32_t)(wid * NS * R::kSlot);
   float4* const tile =
-      reinterpret_cast<float4*>(dec_smem + kWarps * NS * R::kSlot + wid * TTile<G>::kBytes);
+      reinterpret_cast<float4*>(dec_smem + kWarps * NS * R::kSlot + wid * TTile::kBytes);
   const int ntiles = (int)((nchunks + 31) >> 5), nfull = (int)(nchunks >> 5);
   const int rem = (int)(nchunks & 31);
   const int64_t ngroups = nchunks / L;
@@ -572,9 +681,11 @@ __global__ void __launch_bounds__(kThreads, (kBF16Out && G != 64) ? 4 : 1)
 template <int G, bool kBF16>
 fp4_status launch_encode_t(const void* x, int64_t nchunks, uint8_t* packed, float* s1, float* s2,
                            cudaStream_t s) {
-  constexpr size_t smem = EncRing<G, kBF16>::kSmem;
+  constexpr size_t smem = EncSmem<G, kBF16>::kSmem;
   if (!allow_dynamic_smem<encode_kernel<G, kBF16>>(smem)) return FP4_ERR_CUDA;
-  return launch<encode_kernel<G, kBF16>>(nchunks, kThreads, smem, s, x, nchunks, packed, s1, s2);
+  const int64_t nslices = nchunks / (Wide<G>::EPL / kE);
+  return launch<encode_kernel<G, kBF16>>(nslices, kThreads, smem, s, x, nslices, packed, s1, s2,
+                                         -0.0f);
 }
 
 template <int G>
