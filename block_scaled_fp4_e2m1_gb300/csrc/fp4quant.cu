@@ -267,6 +267,13 @@ struct WideRow {
   F2 p[16 * Wide<G>::NP * 2];
 };
 
+// Transpose tile of the encode (see transpose_wide): C L units per group.
+template <int G>
+struct WideTile {
+  static constexpr int C = 16 * Wide<G>::NP + 1;
+  static constexpr int kBytes = Wide<G>::L > 1 ? 16 * C * 32 : 0;  // per warp
+};
+
 // Input pieces per lane and shared memory of the encode: one staging slot
 // per warp (bf16: 8 or 16 pieces per lane, fp32 twice that), plus for
 // G = 256 the transpose tile.
@@ -274,7 +281,7 @@ template <int G, bool kBF16>
 struct EncSmem {
   static constexpr int P = Wide<G>::EPL * (kBF16 ? 2 : 4) / 16;
   static constexpr int kSlot = 32 * 16 * P;
-  static constexpr int kTile = Wide<G>::L > 1 ? 16 * 17 * 32 : 0;
+  static constexpr int kTile = WideTile<G>::kBytes;
   static constexpr size_t kSmem = (size_t)kWarps * (kSlot + kTile);
 };
 
@@ -311,34 +318,44 @@ __device__ __forceinline__ void unpack_wide(const uint4* v, WideRow<G>& y) {
   }
 }
 
-// G = 256 transpose: group g owns 17 L = 68 16-byte units from unit 68 g;
-// writer l puts its unit h (h < 4: positions 8 k + 2h, 8 k + 2h + 1 of its
-// chunk pair) for reader k at l + L h + 17 k, reader k takes writer m's unit
-// h from there.  Both sides are a lane base plus a constant, and since
-// 17 = 1 mod 8 the eight lanes of a quarter-warp touch eight different units
-// mod 8 on every access.
+// Transpose of the encode when a group spans L > 1 lanes.  Writer l holds
+// chunk pairs NP l + h (h < NP); reader k is to hold positions
+// B k .. B k + B - 1 of every chunk pair.  Writer l's unit s for reader k
+// (s = h B/2 + u: positions B k + 2u, B k + 2u + 1 of its pair h) goes to
+// unit l + L s + C k of the group's region of C L units, C the smallest
+// number >= 16 NP that is 1 mod 8; reader k takes it from there into its
+// registers for pair NP m + h.  Both sides are a lane base plus a constant,
+// and since L s + l covers 0 .. 16 NP - 1 once and C = 1 mod 8, the eight
+// lanes of a quarter-warp touch eight different units mod 8 on every access.
 template <int G>
 __device__ __forceinline__ void transpose_wide(WideRow<G>& y, float4* tile, int lane) {
-  constexpr int L = Wide<G>::L, B = Wide<G>::B, S = B / 2;
+  constexpr int NP = Wide<G>::NP, L = Wide<G>::L, B = Wide<G>::B, H = B / 2;
+  constexpr int C = WideTile<G>::C;
   const int g = lane / L, l = lane % L;
-  float4* const st = tile + 17 * L * g + l;
-  const float4* const ld = tile + 17 * L * g + 17 * l;
+  float4* const st = tile + C * L * g + l;
+  const float4* const ld = tile + C * L * g + C * l;
 #pragma unroll
   for (int k = 0; k < L; ++k) {
 #pragma unroll
-    for (int h = 0; h < S; ++h) {
-      const F2 a = y.p[B * k + 2 * h], b = y.p[B * k + 2 * h + 1];
-      st[L * h + 17 * k] = make_float4(a.x, a.y, b.x, b.y);
+    for (int h = 0; h < NP; ++h) {
+#pragma unroll
+      for (int u = 0; u < H; ++u) {
+        const F2 a = y.p[32 * h + B * k + 2 * u], b = y.p[32 * h + B * k + 2 * u + 1];
+        st[L * (H * h + u) + C * k] = make_float4(a.x, a.y, b.x, b.y);
+      }
     }
   }
   __syncwarp();
 #pragma unroll
   for (int m = 0; m < L; ++m) {
 #pragma unroll
-    for (int h = 0; h < S; ++h) {
-      const float4 v = ld[m + L * h];
-      y.p[B * m + 2 * h] = F2{v.x, v.y};
-      y.p[B * m + 2 * h + 1] = F2{v.z, v.w};
+    for (int h = 0; h < NP; ++h) {
+#pragma unroll
+      for (int u = 0; u < H; ++u) {
+        const float4 v = ld[m + L * (H * h + u)];
+        y.p[(NP * m + h) * B + 2 * u] = F2{v.x, v.y};
+        y.p[(NP * m + h) * B + 2 * u + 1] = F2{v.z, v.w};
+      }
     }
   }
   __syncwarp();
@@ -367,7 +384,7 @@ __device__ __forceinline__ float group_max(float v) {
 // multiple of L, so a group is entirely inside or entirely past the end).
 // Tile indices are 32-bit (the entry point admits fewer than 2^40 elements).
 template <int G, bool kBF16>
-__global__ void __launch_bounds__(kThreads, G == 128 ? 1 : 2)
+__global__ void __launch_bounds__(kThreads, Wide<G>::EPL == 128 ? 1 : 2)
     encode_kernel(const void* __restrict__ x, int64_t nslices, uint8_t* __restrict__ packed,
                   float* __restrict__ s1_out, float* __restrict__ s2_out, float nz) {
   using W = Wide<G>;
@@ -452,12 +469,12 @@ __global__ void __launch_bounds__(kThreads, G == 128 ? 1 : 2)
       }
     }
     if (L > 1) {
-      // stages h = 64 (chunk pairs m, m xor 1) and h = 128 (m, m xor 2)
+      // the stages that pair chunk pairs of different lanes (M, M xor mm)
       transpose_wide<G>(y, tile, lane);
 #pragma unroll
-      for (int mm = 1; mm < L; mm <<= 1) {
+      for (int mm = NP; mm < NP * L; mm <<= 1) {
 #pragma unroll
-        for (int m = 0; m < L; ++m) {
+        for (int m = 0; m < NP * L; ++m) {
           if (m & mm) continue;
 #pragma unroll
           for (int b = 0; b < B; ++b) {
@@ -512,17 +529,27 @@ __global__ void __launch_bounds__(kThreads, G == 128 ? 1 : 2)
         o[1] = make_uint4(wd[4], wd[5], wd[6], wd[7]);
       }
     } else {
-      // chunk 2m: p[8 m + b].x, chunk 2m + 1: .y, positions 8 l + b: four
-      // bytes at byte 4 l of each chunk's 16-byte row
+      // chunk 2M: p[M B + b].x, chunk 2M + 1: .y, positions B l + b: B/2
+      // bytes at byte B l / 2 of each chunk's 16-byte row
 #pragma unroll
-      for (int m = 0; m < L; ++m) {
+      for (int m = 0; m < NP * L; ++m) {
         const F2* q = y.p + m * B;
-        const uint32_t wx =
-            cvt_e2m1x8(q[0].x, q[1].x, q[2].x, q[3].x, q[4].x, q[5].x, q[6].x, q[7].x);
-        const uint32_t wy =
-            cvt_e2m1x8(q[0].y, q[1].y, q[2].y, q[3].y, q[4].y, q[5].y, q[6].y, q[7].y);
-        *reinterpret_cast<uint32_t*>(grp + 32 * m + 4 * l) = wx;
-        *reinterpret_cast<uint32_t*>(grp + 32 * m + 16 + 4 * l) = wy;
+        uint32_t wx[B / 8], wy[B / 8];
+#pragma unroll
+        for (int k = 0; k < B / 8; ++k) {
+          wx[k] = cvt_e2m1x8(q[8 * k].x, q[8 * k + 1].x, q[8 * k + 2].x, q[8 * k + 3].x,
+                             q[8 * k + 4].x, q[8 * k + 5].x, q[8 * k + 6].x, q[8 * k + 7].x);
+          wy[k] = cvt_e2m1x8(q[8 * k].y, q[8 * k + 1].y, q[8 * k + 2].y, q[8 * k + 3].y,
+                             q[8 * k + 4].y, q[8 * k + 5].y, q[8 * k + 6].y, q[8 * k + 7].y);
+        }
+        uint8_t* const r0 = grp + 32 * m + (B / 2) * l;
+        if (B == 16) {
+          *reinterpret_cast<uint2*>(r0) = make_uint2(wx[0], wx[1]);
+          *reinterpret_cast<uint2*>(r0 + 16) = make_uint2(wy[0], wy[1]);
+        } else {
+          *reinterpret_cast<uint32_t*>(r0) = wx[0];
+          *reinterpret_cast<uint32_t*>(r0 + 16) = wy[0];
+        }
       }
     }
     if (l == 0) {
@@ -682,6 +709,7 @@ template <int G, bool kBF16>
 fp4_status launch_encode_t(const void* x, int64_t nchunks, uint8_t* packed, float* s1, float* s2,
                            cudaStream_t s) {
   constexpr size_t smem = EncSmem<G, kBF16>::kSmem;
+  static_assert(smem <= 227 * 1024, "one CTA's shared memory must fit an SM");
   if (!allow_dynamic_smem<encode_kernel<G, kBF16>>(smem)) return FP4_ERR_CUDA;
   const int64_t nslices = nchunks / (Wide<G>::EPL / kE);
   return launch<encode_kernel<G, kBF16>>(nslices, kThreads, smem, s, x, nslices, packed, s1, s2,
@@ -699,6 +727,7 @@ template <int G, bool kBF16Out>
 fp4_status launch_decode_t(const uint8_t* packed, const float* s1, const float* s2,
                            int64_t nchunks, void* y, cudaStream_t s) {
   constexpr size_t smem = DecRing<G>::kSmem;
+  static_assert(smem <= 227 * 1024, "one CTA's shared memory must fit an SM");
   if (!allow_dynamic_smem<decode_kernel<G, kBF16Out>>(smem)) return FP4_ERR_CUDA;
   return launch<decode_kernel<G, kBF16Out>>(nchunks, kThreads, smem, s, packed, s1, s2, nchunks,
                                             y);
