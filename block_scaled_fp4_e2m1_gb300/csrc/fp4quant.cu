@@ -616,11 +616,11 @@ __device__ __forceinline__ void store_values(void* out, int64_t chunk, int l, co
 }
 
 // Tiles are staged NS - 1 loop steps ahead in the warp's ring, as in the
-// encode kernels; tile indices are 32-bit likewise.  The bf16-output
-// kernels for G = 128 and 256 are held to 64 registers (four CTAs per SM);
-// for G = 64 three CTAs at 71 registers measured faster.
+// encode kernels; tile indices are 32-bit likewise.  The bf16-output kernel
+// for G = 256 is held to 64 registers (four CTAs per SM); for G = 64 and 128
+// three CTAs at 71-72 registers measured faster.
 template <int G, bool kBF16Out>
-__global__ void __launch_bounds__(kThreads, (kBF16Out && G != 64) ? 4 : 1)
+__global__ void __launch_bounds__(kThreads, (kBF16Out && G == 256) ? 4 : 1)
     decode_kernel(const uint8_t* __restrict__ packed, const float* __restrict__ s1_in,
                   const float* __restrict__ s2_in, int64_t nchunks, void* __restrict__ out) {
   using R = DecRing<G>;
