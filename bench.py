@@ -24,7 +24,9 @@ per-kernel figures (`kernels`, `roofline`) come from a second pass in which
 L2 is flushed before every kernel group: a 512 MB buffer (four times L2) is
 written and then read back, outside the group's events, so the group starts
 with no line of its inputs in L2 and no dirty line of earlier work left to
-write back.
+write back.  Beside each group's figure, `copy_same_bytes` is a plain device
+copy of the same number of bytes per launch, timed the same way: the
+ceiling of a memory-bound kernel at that size (launches up to 4 GB).
 
 Prints one JSON line (rank 0).  --impl reference times the CPU oracle on a
 bounded sample of the same workload instead.
@@ -112,6 +114,7 @@ class Group:
         self.bytes_per_launch = bytes_per_launch
         self.calls = calls          # list of zero-arg callables
         self.times_ms = []
+        self.copy_ms = None         # size-matched copy (copy_at_sizes), when timed
 
     @property
     def name(self):
@@ -312,6 +315,43 @@ class L2Flush:
         import torch
         self.buf.zero_()
         torch.sum(self.buf, dim=0, out=self.sink)
+
+
+COPY_MAX_BYTES = 4 << 30  # size-matched copies only for launches up to this many bytes
+
+
+def copy_at_sizes(nbytes, device, passes, flush):
+    """Median CUDA-event time (ms) of a plain device copy moving each of the
+    byte counts in `nbytes` (half read, half written: torch's bf16 copy_,
+    the kernel behind the measured copy bandwidth), timed as the kernels
+    are: L2 flushed before every launch, events around it.  It is the
+    ceiling of a memory-bound kernel at that size: at tens of MB the fixed
+    cost of a launch (launch, CTA ramp, the first loads' latency, the tail)
+    is a visible share of it.  Returns {nbytes: ms}."""
+    import torch
+    sizes = sorted({int(b) for b in nbytes if 0 < b <= COPY_MAX_BYTES})
+    if not sizes:
+        return {}
+    elems = {b: max(8, b // 4 // 8 * 8) for b in sizes}  # bf16 elements copied
+    top = max(elems.values())
+    src = torch.ones(top, dtype=torch.bfloat16, device=device)
+    dst = torch.empty_like(src)
+    out = {}
+    for b in sizes:
+        k = elems[b]
+        s, d = src[:k], dst[:k]
+        d.copy_(s)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(passes)]
+        for p in range(passes):
+            flush()
+            ev[p][0].record()
+            d.copy_(s)
+            ev[p][1].record()
+        torch.cuda.synchronize()
+        out[b] = statistics.median(a.elapsed_time(e) for a, e in ev)
+    del src, dst
+    return out
 
 
 def run_step(groups, events):
@@ -918,6 +958,8 @@ def kernel_study(name, size_mb, steps, warmup, device):
         g.calls[0]()
         ev[s][1].record()
     torch.cuda.synchronize()
+    g.copy_ms = copy_at_sizes([int(g.bytes_per_launch)], device, steps, flush).get(
+        int(g.bytes_per_launch))
     return g, [a.elapsed_time(b) for a, b in ev]
 
 
@@ -1063,11 +1105,16 @@ def main(argv=None):
             g, ts = kernel_study(nm, args.size_mb, args.steps, args.warmup, dev)
             t = statistics.median(ts)
             gbs = g.bytes_per_launch / (t * 1e-3) / 1e9
-            print(json.dumps({"kernel": nm, "size_mb": args.size_mb,
-                              "bytes_per_launch": int(g.bytes_per_launch),
-                              "ms_median": round(t, 4), "ms_min": round(min(ts), 4),
-                              "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
-                              "peak_kind": kind}), flush=True)
+            rec = {"kernel": nm, "size_mb": args.size_mb,
+                   "bytes_per_launch": int(g.bytes_per_launch),
+                   "ms_median": round(t, 4), "ms_min": round(min(ts), 4),
+                   "gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "peak_kind": kind}
+            if g.copy_ms is not None:
+                cgbs = g.bytes_per_launch / (g.copy_ms * 1e-3) / 1e9
+                rec["copy_same_bytes"] = {"ms": round(g.copy_ms, 4),
+                                          "frac": round(cgbs / peak, 4),
+                                          "kernel_over_copy": round(gbs / cgbs, 4)}
+            print(json.dumps(rec), flush=True)
             torch.cuda.empty_cache()
         return 0
     if args.sweep:
@@ -1170,9 +1217,10 @@ def main(argv=None):
                 c()
             kev[s_][gi][1].record()
     torch.cuda.synchronize()
-    del flush
     for gi, g in enumerate(groups):
         g.times_ms = [kev[s_][gi][0].elapsed_time(kev[s_][gi][1]) for s_ in range(kpass)]
+    copy_ms = copy_at_sizes([int(g.bytes_per_launch) for g in groups], device, kpass, flush)
+    del flush
 
     kernels = {}
     for g in groups:
@@ -1184,6 +1232,12 @@ def main(argv=None):
                            "bytes_per_launch": int(g.bytes_per_launch),
                            "ms_in_step": round(t_step, 4),
                            "frac_in_step": round(g.bytes_per_step / (t_step * 1e-3) / 1e9 / peak, 4)}
+        tc = copy_ms.get(int(g.bytes_per_launch))
+        if tc is not None:
+            cgbs = g.bytes_per_launch / (tc * 1e-3) / 1e9
+            kernels[g.name]["copy_same_bytes"] = {"ms": round(tc, 4),
+                                                  "frac": round(cgbs / peak, 4),
+                                                  "kernel_over_copy": round(gbs / cgbs, 4)}
     dom = max(groups, key=lambda g: statistics.mean(g.times_ms))
     dom_launch_ms = statistics.mean(dom.times_ms) / len(dom.calls)
     achieved = dom.bytes_per_launch / (dom_launch_ms * 1e-3) / 1e9

@@ -49,6 +49,7 @@ SIGNATURES = {
     "fp4_scaled_quantize_amax": (INT, [P, INT, I64, P, P, P, P]),
     "fp4_scaled_dequantize_dev": (INT, [P, I64, P, P, INT, P]),
     "fp4_to_fp8_col": (INT, [P, P, I64, P, P, I32, I64, I64, P, P, P]),
+    "fp4_to_fp8_col_runs": (INT, [P, P, I64, P, P, I32, I64, I64, I32, P, P, P]),
     "fp4_seg_scale_offsets": (INT, [P, I32, P]),
     "fp4quant_encode": (INT, [P, INT, I64, I64, INT, P, P, P, P]),
     "fp4quant_decode": (INT, [P, P, P, I64, I64, INT, P, INT, P]),

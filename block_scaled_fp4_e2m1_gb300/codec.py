@@ -658,10 +658,14 @@ class Segments:
 
 def fp4_to_fp8_col(packed: torch.Tensor, scales: torch.Tensor, segments: Segments,
                    fp8_t: Optional[torch.Tensor] = None,
-                   fp8_t_scales: Optional[torch.Tensor] = None):
+                   fp8_t_scales: Optional[torch.Tensor] = None, run_blocks: int = 0):
     """Per segment e: [cols, n_e] E4M3 at fp8_t[cols*row_off[e]:] and
     [cols, ceil(n_e/128)] fp32 scales at fp8_t_scales[cols*scale_off[e]:]
-    (flat outputs).  The segments must cover exactly the rows of packed."""
+    (flat outputs).  The segments must cover exactly the rows of packed.
+    run_blocks fixes the token blocks per CTA work unit (0: the library's
+    choice); the output does not depend on it."""
+    if not 0 <= int(run_blocks) <= 1 << 20:
+        raise ValueError(f"run_blocks must be in [0, 2^20], got {run_blocks}")
     rows, cols, dev = _mx_source(packed, scales)
     if segments.total_rows != rows:
         raise ValueError(f"the segments cover {segments.total_rows} rows, packed has {rows}")
@@ -673,9 +677,15 @@ def fp4_to_fp8_col(packed: torch.Tensor, scales: torch.Tensor, segments: Segment
              if fp8_t is None else fp8_t)
     fp8_t_scales = (torch.empty(cols * segments.total_blocks, dtype=_F32, device=dev)
                     if fp8_t_scales is None else fp8_t_scales)
-    call("fp4_to_fp8_col", _ptr(packed), _ptr(scales), cols, _ptr(segments.row_off),
-         _ptr(segments.scale_off), segments.num_segments, segments.total_rows,
-         segments.total_blocks, _ptr(fp8_t), _ptr(fp8_t_scales), _stream(dev))
+    if run_blocks:
+        call("fp4_to_fp8_col_runs", _ptr(packed), _ptr(scales), cols, _ptr(segments.row_off),
+             _ptr(segments.scale_off), segments.num_segments, segments.total_rows,
+             segments.total_blocks, int(run_blocks), _ptr(fp8_t), _ptr(fp8_t_scales),
+             _stream(dev))
+    else:
+        call("fp4_to_fp8_col", _ptr(packed), _ptr(scales), cols, _ptr(segments.row_off),
+             _ptr(segments.scale_off), segments.num_segments, segments.total_rows,
+             segments.total_blocks, _ptr(fp8_t), _ptr(fp8_t_scales), _stream(dev))
     return fp8_t, fp8_t_scales
 
 

@@ -123,9 +123,10 @@ __global__ void __launch_bounds__(kRowThreads)
 // sectors half written.)
 //
 // Work unit: one CTA converts a group of up to eight 32-feature blocks (one
-// MXFP4 scale column each, one per warp) over a run of up to kColRun
-// consecutive 128-token blocks of the global block order (a run may cross
-// segment boundaries).  Per token block:
+// MXFP4 scale column each, one per warp) over a run of consecutive 128-token
+// blocks of the global block order (a run may cross segment boundaries).
+// The run length is chosen per launch (col_run_blocks) so that the units
+// fill whole waves of resident CTAs.  Per token block:
 //   - the CTA copies the block's codes for its 256 features (128 tokens x
 //     128 bytes: whole lines) and their scale bytes into a shared-memory
 //     stage with cp.async, one block ahead of use; 16-byte chunk q of token
@@ -159,7 +160,10 @@ __global__ void __launch_bounds__(kRowThreads)
 
 constexpr int kColThreads = 256;
 constexpr int kColGroup = kColThreads / 32;  // feature blocks per CTA: one per warp
-constexpr int kColRun = 32;                  // token blocks per unit
+constexpr int kColRunMin = 8;   // token blocks per unit: at least
+constexpr int kColRunMax = 40;  // and at most (a unit converts up to two
+                                // extra blocks for its carry and heads)
+constexpr int kColRunLimit = 1 << 20;  // largest run a caller may fix
 constexpr int kStageCodes = 128 * 16 * kColGroup;  // code bytes of one stage
 constexpr int kStageBytes = kStageCodes + 128 * kColGroup;  // + scale bytes
 // tile words per feature row: 8 carry words, 32 data words, 4 words of
@@ -228,20 +232,6 @@ __device__ __forceinline__ void window32(const uint32_t w[16], uint32_t o, uint3
   const uint32_t sh = 8u * (o & 3u);
 #pragma unroll
   for (int k = 0; k < 8; ++k) r[k] = __funnelshift_r(v[k], v[k + 1], sh);
-}
-
-// Bytes o .. o+31 (0 <= o < 16) of the 48-byte sequence x | y | z.
-__device__ __forceinline__ U32x8 window32x(uint4 x, uint4 y, uint4 z, uint32_t o) {
-  uint32_t v[12] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w, z.x, z.y, z.z, z.w};
-#pragma unroll
-  for (int k = 0; k < 10; ++k) v[k] = (o & 8u) ? v[k + 2] : v[k];
-#pragma unroll
-  for (int k = 0; k < 9; ++k) v[k] = (o & 4u) ? v[k + 1] : v[k];
-  const uint32_t sh = 8u * (o & 3u);
-  U32x8 r;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) r.w[k] = __funnelshift_r(v[k], v[k + 1], sh);
-  return r;
 }
 
 // 4 x 4 byte transpose: x[i] holds bytes (i, 0..3); y[j] receives (0..3, j).
@@ -417,11 +407,20 @@ __device__ __forceinline__ void col_store(uint32_t* tile, const uint4* heads,
     const int lo = first && a != 0u ? 1 : 0;
     const int hi = last ? (int)((a + (uint32_t)nv) >> 5) : 4;
     if (s >= lo && s < hi) {
-      const uint32_t off = 32u - a + 32u * (uint32_t)s;  // tile byte of the sector's first byte
-      const uint32_t k = off >> 4;
-      const uint4* row = tile_row(tile, r);
-      st_v8(A - a + 32 * s,
-            window32x(row[k], row[k + 1 < 10 ? k + 1 : 9], row[k + 2 < 10 ? k + 2 : 9], off & 15u));
+      // the sector's first byte is tile byte off (1 <= off <= 128): words
+      // off/4 .. off/4 + 8 of the row (the ninth, read only when off < 128
+      // needs it, is at most word 40, the row's first padding word),
+      // shifted down by off mod 4 bytes
+      const uint32_t off = 32u - a + 32u * (uint32_t)s;
+      const uint32_t* w = reinterpret_cast<const uint32_t*>(tile_row(tile, r)) + (off >> 2);
+      uint32_t v[9];
+#pragma unroll
+      for (int j = 0; j < 9; ++j) v[j] = w[j];
+      const uint32_t sh = 8u * (off & 3u);
+      U32x8 o;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) o.w[j] = __funnelshift_r(v[j], v[j + 1], sh);
+      st_v8(A - a + 32 * s, o);
     }
   }
   const uint4* row = tile_row(tile, lane);
@@ -489,7 +488,7 @@ __global__ void __launch_bounds__(kColThreads)
     fp4_to_fp8_col_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ scales,
                           int64_t cols, const int64_t* __restrict__ seg_row_off,
                           const int64_t* __restrict__ seg_scale_off, int nseg, int64_t total_blocks,
-                          int64_t nunits, uint8_t* __restrict__ fp8_t,
+                          int64_t run_len, int64_t nunits, uint8_t* __restrict__ fp8_t,
                           float* __restrict__ fp8_t_scales) {
   extern __shared__ __align__(16) uint8_t col_smem[];
   uint8_t* const stages = col_smem;
@@ -515,8 +514,8 @@ __global__ void __launch_bounds__(kColThreads)
                                                                 : kColGroup);
     const int kb = kColGroup * grp + wid;
     const bool active = wid < nkb;
-    const int64_t fb0 = run * kColRun;
-    const int64_t fb1 = fb0 + kColRun < total_blocks ? fb0 + kColRun : total_blocks;
+    const int64_t fb0 = run * run_len;
+    const int64_t fb1 = fb0 + run_len < total_blocks ? fb0 + run_len : total_blocks;
     SegPos p0;
     p0.e = find_segment(seg_scale_off, nseg, fb0);
     seg_load(p0, seg_row_off, seg_scale_off);
@@ -571,6 +570,22 @@ __global__ void __launch_bounds__(kColThreads)
   cp_async_wait<0>();
 }
 
+// Token blocks per unit for a launch over total_blocks blocks and ngroups
+// feature groups on `wave` resident CTAs: the longest run up to kColRunMax
+// whose units fill whole waves (k waves: at most k * wave units, the last
+// wave nearly full), for the smallest such k.  A last wave of a few units
+// would otherwise run alone on an idle GPU: at 616 units on 304 resident
+// CTAs, eight units made a third wave.  Never below kColRunMin.
+int64_t col_run_blocks(int64_t total_blocks, int64_t ngroups, int64_t wave) {
+  for (int64_t k = 1; k <= 4096; ++k) {
+    const int64_t nruns = k * wave / ngroups;
+    if (nruns < 1) continue;
+    const int64_t r = (total_blocks + nruns - 1) / nruns;
+    if (r <= kColRunMax) return r < kColRunMin ? kColRunMin : r;
+  }
+  return kColRunMax;
+}
+
 }  // namespace
 }  // namespace fp4
 
@@ -590,11 +605,13 @@ fp4_status fp4_to_fp8_row(const uint8_t* packed, const uint8_t* scales, int64_t 
                                        nspans, fp8, fp8_scales);
 }
 
-fp4_status fp4_to_fp8_col(const uint8_t* packed, const uint8_t* scales, int64_t cols,
-                          const int64_t* seg_row_off, const int64_t* seg_scale_off,
-                          int32_t num_segments, int64_t total_rows, int64_t total_blocks,
-                          uint8_t* fp8_t, float* fp8_t_scales, void* stream) {
-  if (cols < 0 || cols % 128 != 0 || num_segments < 0 || total_rows < 0 || total_blocks < 0)
+fp4_status fp4_to_fp8_col_runs(const uint8_t* packed, const uint8_t* scales, int64_t cols,
+                               const int64_t* seg_row_off, const int64_t* seg_scale_off,
+                               int32_t num_segments, int64_t total_rows, int64_t total_blocks,
+                               int32_t run_blocks, uint8_t* fp8_t, float* fp8_t_scales,
+                               void* stream) {
+  if (cols < 0 || cols % 128 != 0 || num_segments < 0 || total_rows < 0 || total_blocks < 0 ||
+      run_blocks < 0 || run_blocks > kColRunLimit)
     return FP4_ERR_SHAPE;
   if (total_blocks > total_rows / 128 + num_segments) return FP4_ERR_SHAPE;
   if (!seg_row_off || !seg_scale_off) return FP4_ERR_NULL;
@@ -604,15 +621,27 @@ fp4_status fp4_to_fp8_col(const uint8_t* packed, const uint8_t* scales, int64_t 
       !aligned(seg_row_off, 8) || !aligned(seg_scale_off, 8))
     return FP4_ERR_ALIGN;
   if (ntiles == 0 || num_segments == 0) return FP4_OK;
-  // one CTA per (run of kColRun token blocks, group of kColGroup 32-feature blocks)
-  const int64_t kblocks = cols / 32;
-  const int64_t nunits =
-      (total_blocks + kColRun - 1) / kColRun * ((kblocks + kColGroup - 1) / kColGroup);
   if (!allow_dynamic_smem<fp4_to_fp8_col_kernel>(kColSmem)) return FP4_ERR_CUDA;
+  // one CTA per (run of token blocks, group of kColGroup 32-feature blocks)
+  const int64_t ngroups = (cols / 32 + kColGroup - 1) / kColGroup;
+  const int64_t run =
+      run_blocks > 0
+          ? run_blocks
+          : col_run_blocks(total_blocks, ngroups,
+                           wave_ctas<fp4_to_fp8_col_kernel>(kColThreads, kColSmem));
+  const int64_t nunits = (total_blocks + run - 1) / run * ngroups;
   return launch<fp4_to_fp8_col_kernel>(nunits * kColThreads, kColThreads, kColSmem,
                                        as_stream(stream), packed, scales, cols, seg_row_off,
-                                       seg_scale_off, num_segments, total_blocks, nunits, fp8_t,
-                                       fp8_t_scales);
+                                       seg_scale_off, num_segments, total_blocks, run, nunits,
+                                       fp8_t, fp8_t_scales);
+}
+
+fp4_status fp4_to_fp8_col(const uint8_t* packed, const uint8_t* scales, int64_t cols,
+                          const int64_t* seg_row_off, const int64_t* seg_scale_off,
+                          int32_t num_segments, int64_t total_rows, int64_t total_blocks,
+                          uint8_t* fp8_t, float* fp8_t_scales, void* stream) {
+  return fp4_to_fp8_col_runs(packed, scales, cols, seg_row_off, seg_scale_off, num_segments,
+                             total_rows, total_blocks, 0, fp8_t, fp8_t_scales, stream);
 }
 
 }  // extern "C"

@@ -41,13 +41,19 @@ inline bool allow_dynamic_smem(size_t smem) {
   return ok;
 }
 
+// CTAs of `Kernel` resident on the whole GPU at once (one full wave).
+template <auto Kernel>
+inline int64_t wave_ctas(int threads, size_t smem) {
+  static const int occ = occupancy(Kernel, threads, smem);
+  return (int64_t)sm_count() * occ;
+}
+
 // Grid for a grid-stride loop over `units` thread-level work units: one
 // thread per unit up to one full wave of resident CTAs on every SM.
 template <auto Kernel>
 inline unsigned grid_for_kernel(int64_t units, int threads, size_t smem) {
-  static const int occ = occupancy(Kernel, threads, smem);
   int64_t want = (units + threads - 1) / threads;
-  int64_t cap = (int64_t)sm_count() * occ;
+  const int64_t cap = wave_ctas<Kernel>(threads, smem);
   if (want > cap) want = cap;
   if (want < 1) want = 1;
   return (unsigned)want;

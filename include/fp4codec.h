@@ -384,6 +384,19 @@ fp4_status fp4_to_fp8_col(const uint8_t* packed, const uint8_t* scales, int64_t 
                           int32_t num_segments, int64_t total_rows, int64_t total_blocks,
                           uint8_t* fp8_t, float* fp8_t_scales, void* stream);
 
+/* FP4RowToFP8Col with the kernel's work split fixed by the caller: one CTA
+ * converts a run of run_blocks consecutive 128-token blocks (in the global
+ * block order of seg_scale_off) for 256 features at a time.  run_blocks = 0
+ * lets the library choose (fp4_to_fp8_col does): the run length, between 8
+ * and 40 blocks, whose units fill whole waves of resident CTAs.  The output
+ * does not depend on it.  Errors as fp4_to_fp8_col, and FP4_ERR_SHAPE for
+ * run_blocks < 0 or above 2^20. */
+fp4_status fp4_to_fp8_col_runs(const uint8_t* packed, const uint8_t* scales, int64_t cols,
+                               const int64_t* seg_row_off, const int64_t* seg_scale_off,
+                               int32_t num_segments, int64_t total_rows, int64_t total_blocks,
+                               int32_t run_blocks, uint8_t* fp8_t, float* fp8_t_scales,
+                               void* stream);
+
 /* Host helper: host_scale_off[0] = 0, host_scale_off[e+1] = host_scale_off[e]
  * + ceil((host_row_off[e+1] - host_row_off[e]) / 128).  Returns FP4_ERR_SHAPE
  * on a decreasing offset. */

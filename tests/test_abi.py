@@ -31,6 +31,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ["nvfp4_amax", "nvfp4_quantize", "nvfp4_dequantize", "nvfp4_qdq_amax",
                  "nvfp4_qdq", "mxfp4_quantize", "fp4_to_fp8_row", "fp4_to_fp8_col",
+                 "fp4_to_fp8_col_runs",
                  "fp4_seg_scale_offsets", "fp4quant_encode", "fp4quant_decode",
                  "fp4_status_string", "fp4_abi_version", "fp4_kernel_launches",
                  "fp4_blocked_scales_size", "fp4_scales_to_blocked", "fp4_scales_from_blocked",
@@ -130,6 +131,11 @@ def test_mx_fp8_fp4quant_argument_checks(L):
     assert col(A, A, 128, None, A, 2, 10, 2, A, A, None) == 1
     assert col(A, A, 128, A, A, 2, 10, 5, A, A, None) == 3       # too many blocks
     assert col(A, A, 128, A + 4, A, 2, 10, 2, A, A, None) == 2
+    runs = L.fp4_to_fp8_col_runs
+    assert runs(A, A, 128, A, A, 2, 10, 2, -1, A, A, None) == 3      # run_blocks < 0
+    assert runs(A, A, 128, A, A, 2, 10, 2, (1 << 20) + 1, A, A, None) == 3
+    assert runs(A, A, 96, A, A, 2, 10, 2, 8, A, A, None) == 3
+    assert runs(A, A, 128, A + 4, A, 2, 10, 2, 8, A, A, None) == 2
     enc = L.fp4quant_encode
     assert enc(A, 1, 2, 128, 32, A, A, A, None) == 5             # group
     assert enc(A, 1, 2, 96, 64, A, A, A, None) == 3              # cols % group

@@ -259,8 +259,9 @@ def test_moe_workload_full_size_sampled():
         assert_bits_equal(gs, wsc, f"col scales segment {e}")
 
 
-# Segment layouts aimed at the column kernel's units of 32 token blocks
-# (blocks are numbered across segments, ceil(n_e / 128) per segment):
+# Segment layouts aimed at the column kernel's units, run with runs of 32
+# token blocks (blocks are numbered across segments, ceil(n_e / 128) per
+# segment):
 #   - a segment that starts on a run's last block, so the next run begins
 #     one block into it (that run first converts the segment's block 0, for
 #     the carry and the row heads);
@@ -293,11 +294,41 @@ def test_fp4_to_fp8_col_run_boundaries(sizes, cols, shift):
     sc = torch.from_numpy(scales).to(dev())
     out = torch.full((cols * R + 96,), 0xA5, dtype=torch.uint8, device=dev())
     n = cols * R
-    m.fp4_to_fp8_col(pk, sc, segs, out[32 + shift:32 + shift + n])
+    m.fp4_to_fp8_col(pk, sc, segs, out[32 + shift:32 + shift + n], run_blocks=32)
     wo, _ = ora.fp4_to_fp8_col(packed, scales, off)
     o = u8(out)
     assert np.all(o[:32 + shift] == 0xA5) and np.all(o[32 + shift + n:] == 0xA5)
     assert_bits_equal(o[32 + shift:32 + shift + n], wo, f"fp8_t {sizes[:3]} {cols}")
+
+
+@pytest.mark.parametrize("run", [0, 1, 2, 3, 7, 8, 29, 33, 40, 1000])
+def test_fp4_to_fp8_col_any_run_length(run):
+    """The column form does not depend on how the token blocks are cut into
+    CTA work units: runs of 1 .. 1000 blocks (and the library's own choice,
+    0) on segment layouts with long, one-block, short (< 32 tokens) and
+    empty segments, against the oracle bit for bit, codes and scales, with
+    the output at an odd byte offset."""
+    m = fp4()
+    rng = np.random.default_rng(run + 77)
+    sizes = [31 * 128, 128 + 50, 7, 0, 29 * 128 + 1, 33, 128, 129, 300, 12, 4095, 5000, 1]
+    sizes += rng.integers(0, 700, 12).tolist()
+    cols = 384
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    R = int(off[-1])
+    packed = rng.integers(0, 256, (R, cols // 2), dtype=np.uint8)
+    scales = rng.integers(110, 140, (R, cols // 32), dtype=np.uint8)
+    segs = m.Segments(torch.from_numpy(off), dev())
+    pk = torch.from_numpy(packed).to(dev())
+    sc = torch.from_numpy(scales).to(dev())
+    n = cols * R
+    out = torch.full((n + 64,), 0xA5, dtype=torch.uint8, device=dev())
+    fts = torch.empty(cols * segs.total_blocks, dtype=torch.float32, device=dev())
+    m.fp4_to_fp8_col(pk, sc, segs, out[5:5 + n], fts, run_blocks=run)
+    wo, wsc = ora.fp4_to_fp8_col(packed, scales, off)
+    o = u8(out)
+    assert np.all(o[:5] == 0xA5) and np.all(o[5 + n:] == 0xA5)
+    assert_bits_equal(o[5:5 + n], wo, f"fp8_t run {run}")
+    assert_bits_equal(to_f32_np(fts), wsc, f"fp8_t scales run {run}")
 
 
 @pytest.mark.parametrize("cols", [128, 384])
