@@ -153,8 +153,10 @@ __global__ void __launch_bounds__(kRowThreads)
 // and ends do partial sectors go out byte by byte.
 // A unit that starts inside a segment first converts, without storing,
 // the block before its run (for the carry) and, if the segment ends within
-// the run, the segment's first block (for the heads).  Segments under 32
-// tokens are written byte by byte.
+// the run, the segment's first block (for the heads).  A segment under 32
+// tokens is one contiguous span of the CTA's rows: they are laid out in
+// order in shared memory and the span goes out as whole sectors
+// (col_store_short).
 // One CTA barrier per token block publishes a stage and frees the one read
 // before; a segment of one block adds one between its heads and merges.
 
@@ -388,12 +390,6 @@ __device__ __forceinline__ void col_store(uint32_t* tile, const uint4* heads,
                                           const uint4* next_head, uint8_t* base, int64_t n_e,
                                           int64_t t0, int nv, bool first, bool last, bool own_head,
                                           int lane) {
-  if (n_e < 32) {
-    // a single block; rows too short for whole sectors: lane r writes row r
-    uint8_t* const R = base + (int64_t)lane * n_e;
-    store_bytes(R, tile_row(tile, lane), 32, 32 + nv);
-    return;
-  }
   // whole sectors: lane (q, s) = (lane >> 2, lane & 3) takes sector s of
   // [L', L' + 128) of row 8i + q, L' = A rounded down to a sector,
   // A = R_r + t0, as one 32-byte store
@@ -455,6 +451,46 @@ __device__ __forceinline__ void col_store(uint32_t* tile, const uint4* heads,
       }
     }
   }
+}
+
+// Stores a segment of n_e < 32 tokens (one block) for the CTA's nkb
+// feature blocks.  Their rows are one contiguous span of 32 nkb n_e bytes
+// from base (row r of warp w at base + (32 w + r) n_e), too short for
+// whole sectors per row, so the rows are first laid out in order in lin
+// (shared memory, the span's byte k at lin[p0 + k], p0 = base mod 32:
+// global and shared addresses then agree mod 32), then the span goes out
+// as whole 32-byte sectors, one per thread, and its partial first and last
+// sectors (shared with the neighbouring spans) byte by byte.  The whole
+// CTA calls it.
+__device__ __forceinline__ void col_store_short(uint8_t* lin, const uint32_t* tile, uint8_t* base,
+                                                int n_e, int nkb, int wid, int lane) {
+  const uint32_t p0 = (uint32_t)reinterpret_cast<uintptr_t>(base) & 31u;
+  if (wid < nkb) {
+    // the row's n_e tokens are tile bytes 32 .. 32 + n_e - 1
+    const uint4* row = tile_row(const_cast<uint32_t*>(tile), lane);
+    const uint4 h0 = row[2], h1 = row[3];
+    const uint32_t w[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+    uint8_t* const dst = lin + p0 + (32 * wid + lane) * n_e;
+#pragma unroll
+    for (int x = 0; x < 31; ++x)
+      if (x < n_e) dst[x] = (uint8_t)(w[x >> 2] >> (8 * (x & 3)));
+  }
+  __syncthreads();
+  const int len = 32 * nkb * n_e;
+  const int t = (int)threadIdx.x;
+  const int head = (int)((32u - p0) & 31u) < len ? (int)((32u - p0) & 31u) : len;
+  const int tail0 = (int)((p0 + (uint32_t)len) & ~31u) - (int)p0;  // last sector start, span byte
+  const int tail = tail0 > head ? tail0 : head;
+  if (t < (tail - head) >> 5) {  // sector t: span bytes head + 32 t ..
+    const uint4* src = reinterpret_cast<const uint4*>(lin + p0 + head + 32 * t);
+    const uint4 a = src[0], b = src[1];
+    U32x8 o;
+    o.w[0] = a.x; o.w[1] = a.y; o.w[2] = a.z; o.w[3] = a.w;
+    o.w[4] = b.x; o.w[5] = b.y; o.w[6] = b.z; o.w[7] = b.w;
+    st_v8(base + head + 32 * t, o);
+  }
+  if (t < head) base[t] = lin[p0 + t];
+  if (t < len - tail) base[tail + t] = lin[p0 + tail + t];
 }
 
 // Block converted by item `it` of a unit (see the kernel).
@@ -549,13 +585,22 @@ __global__ void __launch_bounds__(kColThreads)
           fp8_t_scales[cols * sp.sofs + (32 * kb + lane) * (sp.send - sp.sofs) + b] =
               ue8m0_to_f32(st);
       }
-      // heads kept at this very block must be visible to the warp before
-      // (heads of an earlier block are, through the barrier above)
-      if (real && last && first && sp.n_e >= 32) __syncthreads();
-      if (active && real) {
-        uint8_t* const base = fp8_t + cols * sp.row0 + 32 * kb * sp.n_e;
-        const uint4* next_head = wid + 1 < nkb ? all_heads + (wid + 1) * (kHeadWords / 4) : nullptr;
-        col_store(tile, heads, next_head, base, sp.n_e, t0, nv, first, last, wid == 0, lane);
+      if (real && sp.n_e < 32) {
+        // a short segment: the CTA's rows through the heads area, in order
+        col_store_short(reinterpret_cast<uint8_t*>(all_heads),
+                        tile,
+                        fp8_t + cols * sp.row0 + 32 * kColGroup * grp * sp.n_e, (int)sp.n_e, nkb,
+                        wid, lane);
+      } else {
+        // heads kept at this very block must be visible to the warp before
+        // (heads of an earlier block are, through the barrier above)
+        if (real && last && first) __syncthreads();
+        if (active && real) {
+          uint8_t* const base = fp8_t + cols * sp.row0 + 32 * kb * sp.n_e;
+          const uint4* next_head =
+              wid + 1 < nkb ? all_heads + (wid + 1) * (kHeadWords / 4) : nullptr;
+          col_store(tile, heads, next_head, base, sp.n_e, t0, nv, first, last, wid == 0, lane);
+        }
       }
       if (active) {
         __syncwarp();

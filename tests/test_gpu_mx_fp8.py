@@ -301,6 +301,37 @@ def test_fp4_to_fp8_col_run_boundaries(sizes, cols, shift):
     assert_bits_equal(o[32 + shift:32 + shift + n], wo, f"fp8_t {sizes[:3]} {cols}")
 
 
+@pytest.mark.parametrize("cols", [128, 384, 1152])
+@pytest.mark.parametrize("shift", [0, 1, 7, 30])
+def test_fp4_to_fp8_col_short_segments(cols, shift):
+    """Segments of 1 .. 31 tokens, whose rows are too short for whole
+    sectors: the kernel lays a CTA's rows out in order in shared memory and
+    writes the span as whole sectors, its two partial ends byte by byte.
+    Every length, empty segments and longer neighbours, feature groups of
+    fewer than eight blocks (cols 128, 384, 1152), output offsets that put
+    the span's start at several positions in a sector; against the oracle
+    bit for bit, with canaries on both sides."""
+    m = fp4()
+    sizes = [0, 200] + list(range(1, 32)) + [0, 5, 0, 31, 140, 3]
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    R = int(off[-1])
+    rng = np.random.default_rng(cols * 31 + shift)
+    packed = rng.integers(0, 256, (R, cols // 2), dtype=np.uint8)
+    scales = rng.integers(110, 140, (R, cols // 32), dtype=np.uint8)
+    segs = m.Segments(torch.from_numpy(off), dev())
+    pk = torch.from_numpy(packed).to(dev())
+    sc = torch.from_numpy(scales).to(dev())
+    n = cols * R
+    out = torch.full((n + 96,), 0x5A, dtype=torch.uint8, device=dev())
+    fts = torch.empty(cols * segs.total_blocks, dtype=torch.float32, device=dev())
+    m.fp4_to_fp8_col(pk, sc, segs, out[32 + shift:32 + shift + n], fts)
+    wo, wsc = ora.fp4_to_fp8_col(packed, scales, off)
+    o = u8(out)
+    assert np.all(o[:32 + shift] == 0x5A) and np.all(o[32 + shift + n:] == 0x5A)
+    assert_bits_equal(o[32 + shift:32 + shift + n], wo, f"fp8_t short {cols} {shift}")
+    assert_bits_equal(to_f32_np(fts), wsc, f"fp8_t scales short {cols} {shift}")
+
+
 @pytest.mark.parametrize("run", [0, 1, 2, 3, 7, 8, 29, 33, 40, 1000])
 def test_fp4_to_fp8_col_any_run_length(run):
     """The column form does not depend on how the token blocks are cut into
