@@ -9,13 +9,20 @@
 // byte in registers, and the receiver unpacks, dequantizes and runs the
 // inverse transform.
 //
-// Layout.  A group of G elements spans L = G/32 consecutive lanes (2, 4 or
-// 8), never leaving its warp: no CTA barrier.  The transform's stages run in
-// the natural (Sylvester) order h = 1, 2, ..., G/2, which the CPU oracle
-// follows, in two phases:
+// The transform's stages run in the natural (Sylvester) order h = 1, 2,
+// ..., G/2, which the CPU oracle follows; each stage is one correctly
+// rounded add and subtract per pair, two pairs per packed f32x2
+// instruction.  A group never leaves its warp: no CTA barrier.
+//
+// Encode layout: a lane holds whole chunk pairs of its group, 64 or 128
+// elements (see the encode section below); G = 64 and 128 exchange nothing
+// between lanes, G = 256 transposes once through a warp-private tile.
+//
+// Decode layout: a group spans L = G/32 consecutive lanes (2, 4 or 8), in
+// two phases:
 //   - phase 1: lane l holds the 32 consecutive elements 32 l .. 32 l + 31 of
-//     the group (staged through shared memory by cp.async), so the sum of
-//     squares and the stages h = 1 .. 16 are in-thread;
+//     the group (its codes staged through shared memory by cp.async), so
+//     the stages h = 1 .. 16 are in-thread;
 //   - a transpose through a warp-private shared-memory tile: lane l then
 //     holds, for every lane i of its group, the 32/L consecutive elements
 //     32 i + l (32/L) .. of i's chunk; the tile's 16-byte units are placed
@@ -24,10 +31,8 @@
 //     per-lane base plus a constant;
 //   - phase 2: the stages h = 32 .. G/2 pair elements of chunks i and
 //     i xor (h/32), now in the same thread.
-// Each stage is one correctly rounded add and subtract per pair, two pairs
-// per packed f32x2 instruction.  The codes (encode) and the values (decode)
-// leave phase 2 as one store per source chunk of 32/L codes or values, the
-// L lanes of a group covering each chunk's row contiguously.
+// The values leave phase 2 as one store per source chunk of 32/L values,
+// the L lanes of a group covering each chunk's row contiguously.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -274,6 +279,16 @@ struct WideTile {
   static constexpr int kBytes = Wide<G>::L > 1 ? 16 * C * 32 : 0;  // per warp
 };
 
+// Threads per CTA of the encode: 256 (two CTAs per SM at about 120
+// registers) for G = 64 and 256; for G = 128, whose lanes hold a whole
+// 128-element group, one CTA of 384 threads at up to 170 registers (12
+// warps per SM; 256 threads at 238 registers gave 8, and ran 4% slower).
+template <int G>
+struct EncThreads {
+  static constexpr int N = G == 128 ? 384 : 256;
+  static constexpr int W = N / 32;
+};
+
 // Input pieces per lane and shared memory of the encode: one staging slot
 // per warp (bf16: 8 or 16 pieces per lane, fp32 twice that), plus for
 // G = 256 the transpose tile.
@@ -282,7 +297,7 @@ struct EncSmem {
   static constexpr int P = Wide<G>::EPL * (kBF16 ? 2 : 4) / 16;
   static constexpr int kSlot = 32 * 16 * P;
   static constexpr int kTile = WideTile<G>::kBytes;
-  static constexpr size_t kSmem = (size_t)kWarps * (kSlot + kTile);
+  static constexpr size_t kSmem = (size_t)EncThreads<G>::W * (kSlot + kTile);
 };
 
 // The lane's chunk pairs from its staged pieces: chunk c's 32 elements are
@@ -384,7 +399,7 @@ __device__ __forceinline__ float group_max(float v) {
 // multiple of L, so a group is entirely inside or entirely past the end).
 // Tile indices are 32-bit (the entry point admits fewer than 2^40 elements).
 template <int G, bool kBF16>
-__global__ void __launch_bounds__(kThreads, Wide<G>::EPL == 128 ? 1 : 2)
+__global__ void __launch_bounds__(EncThreads<G>::N, Wide<G>::EPL == 128 ? 1 : 2)
     encode_kernel(const void* __restrict__ x, int64_t nslices, uint8_t* __restrict__ packed,
                   float* __restrict__ s1_out, float* __restrict__ s2_out, float nz) {
   using W = Wide<G>;
@@ -395,12 +410,12 @@ __global__ void __launch_bounds__(kThreads, Wide<G>::EPL == 128 ? 1 : 2)
   const uint32_t slot =
       (uint32_t)__cvta_generic_to_shared(enc_smem) + (uint32_t)(wid * M::kSlot);
   float4* const tile =
-      reinterpret_cast<float4*>(enc_smem + kWarps * M::kSlot + wid * M::kTile);
+      reinterpret_cast<float4*>(enc_smem + EncThreads<G>::W * M::kSlot + wid * M::kTile);
   const int ntiles = (int)((nslices + 31) >> 5), nfull = (int)(nslices >> 5);
   const int rem = (int)(nslices & 31);
-  const int tstride = (int)gridDim.x * kWarps;
+  const int tstride = (int)gridDim.x * EncThreads<G>::W;
   const int64_t step = (int64_t)tstride * M::kSlot;  // input bytes between a warp's tiles
-  int t = (int)blockIdx.x * kWarps + wid;
+  int t = (int)blockIdx.x * EncThreads<G>::W + wid;
   const uint8_t* src = static_cast<const uint8_t*>(x) + (int64_t)t * M::kSlot;
   auto stage = [&](int tt, const uint8_t* s) {
     if (tt < nfull)
@@ -712,8 +727,8 @@ fp4_status launch_encode_t(const void* x, int64_t nchunks, uint8_t* packed, floa
   static_assert(smem <= 227 * 1024, "one CTA's shared memory must fit an SM");
   if (!allow_dynamic_smem<encode_kernel<G, kBF16>>(smem)) return FP4_ERR_CUDA;
   const int64_t nslices = nchunks / (Wide<G>::EPL / kE);
-  return launch<encode_kernel<G, kBF16>>(nslices, kThreads, smem, s, x, nslices, packed, s1, s2,
-                                         -0.0f);
+  return launch<encode_kernel<G, kBF16>>(nslices, EncThreads<G>::N, smem, s, x, nslices, packed,
+                                         s1, s2, -0.0f);
 }
 
 template <int G>
