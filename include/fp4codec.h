@@ -377,7 +377,7 @@ fp4_status fp4_to_fp8_row(const uint8_t* packed, const uint8_t* scales, int64_t 
  * Alignment: packed 32 bytes, scales and fp8_t_scales 4, the offsets 8;
  * fp8_t may start at any byte (the kernel stores whole 32-byte sectors and
  * writes only the partial sectors at its ends byte by byte).  FP4_ERR_ALIGN
- * otherwise; FP4_ERR_CUDA if the launch fails (it uses about 89 KB of
+ * otherwise; FP4_ERR_CUDA if the launch fails (it uses about 97 KB of
  * shared memory per CTA). */
 fp4_status fp4_to_fp8_col(const uint8_t* packed, const uint8_t* scales, int64_t cols,
                           const int64_t* seg_row_off, const int64_t* seg_scale_off,

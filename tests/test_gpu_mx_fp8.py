@@ -332,6 +332,29 @@ def test_fp4_to_fp8_col_short_segments(cols, shift):
     assert_bits_equal(to_f32_np(fts), wsc, f"fp8_t scales short {cols} {shift}")
 
 
+@pytest.mark.parametrize("nseg", [511, 512, 700])
+def test_fp4_to_fp8_col_many_segments(nseg):
+    """Up to 511 segments the kernel reads the segment offsets from a copy in
+    shared memory, from 512 on from global memory: both paths, with a mix
+    of empty, short, one-block and multi-block segments, against the oracle
+    bit for bit (codes and scales)."""
+    m = fp4()
+    rng = np.random.default_rng(nseg)
+    sizes = rng.choice([0, 1, 5, 31, 32, 33, 100, 128, 129, 300], nseg).tolist()
+    sizes[nseg // 2] = 2000
+    cols = 256
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    R = int(off[-1])
+    packed = rng.integers(0, 256, (R, cols // 2), dtype=np.uint8)
+    scales = rng.integers(110, 140, (R, cols // 32), dtype=np.uint8)
+    segs = m.Segments(torch.from_numpy(off), dev())
+    ft, fts = m.fp4_to_fp8_col(torch.from_numpy(packed).to(dev()),
+                               torch.from_numpy(scales).to(dev()), segs)
+    wo, wsc = ora.fp4_to_fp8_col(packed, scales, off)
+    assert_bits_equal(u8(ft), wo, f"fp8_t {nseg} segments")
+    assert_bits_equal(to_f32_np(fts), wsc, f"fp8_t scales {nseg} segments")
+
+
 @pytest.mark.parametrize("run", [0, 1, 2, 3, 7, 8, 29, 33, 40, 1000])
 def test_fp4_to_fp8_col_any_run_length(run):
     """The column form does not depend on how the token blocks are cut into
