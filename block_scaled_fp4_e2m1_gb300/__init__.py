@@ -9,6 +9,7 @@ from .codec import (Batch, Segments, fp4_blocked_scales_size, fp4_scaled_dequant
                     fp4_scaled_dequantize_dev, fp4_scaled_quantize, fp4_scaled_quantize_amax, fp4_scales_from_blocked, fp4_scales_to_blocked,
                     fp4_seg_scale_offsets, fp4_to_fp8_col, fp4_to_fp8_row,
                     fp4quant_decode, fp4quant_encode, fp8_to_fp4_row, kernel_launches,
+                    wait_timeouts,
                     mxfp4_dequantize, mxfp4_quantize, nvfp4_amax, nvfp4_amax_batched,
                     nvfp4_dequantize, nvfp4_dequantize_batched, nvfp4_qdq, nvfp4_qdq_amax,
                     nvfp4_quantize, nvfp4_quantize_batched, nvfp4_quantize_batched_blocked,
@@ -23,6 +24,7 @@ __all__ = [
     "fp4_scaled_quantize_amax", "fp4_scales_from_blocked",
     "fp4_scales_to_blocked", "fp4_seg_scale_offsets", "fp4_to_fp8_col", "fp4_to_fp8_row",
     "fp4quant_decode", "fp4quant_encode", "fp8_to_fp4_row", "kernel_launches",
+    "wait_timeouts",
     "mxfp4_dequantize", "mxfp4_quantize", "nvfp4_amax", "nvfp4_amax_batched",
     "nvfp4_dequantize", "nvfp4_dequantize_batched", "nvfp4_qdq", "nvfp4_qdq_amax",
     "nvfp4_quantize", "nvfp4_quantize_batched", "nvfp4_quantize_batched_blocked",

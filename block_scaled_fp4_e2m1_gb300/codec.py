@@ -738,3 +738,9 @@ def fp4quant_decode(packed: torch.Tensor, s1: torch.Tensor, s2: torch.Tensor, gr
 
 def kernel_launches() -> int:
     return int(_lib.lib().fp4_kernel_launches())
+
+
+def wait_timeouts() -> int:
+    """Bounded waits in the library's kernels that gave up (0 in a healthy
+    run; see fp4_wait_timeouts in the C header)."""
+    return int(_lib.lib().fp4_wait_timeouts())

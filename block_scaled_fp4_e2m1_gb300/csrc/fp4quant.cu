@@ -33,6 +33,7 @@
 //     i xor (h/32), now in the same thread.
 // The values leave phase 2 as one store per source chunk of 32/L values,
 // the L lanes of a group covering each chunk's row contiguously.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -241,6 +242,65 @@ __device__ __forceinline__ void ring_read(uint32_t slot, int lane, uint4 v[P]) {
 __device__ __forceinline__ float bf16_lo_(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi_(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// ---------------------------------------------------------- TMA staging
+//
+// The bf16 G = 128 encode stages its input with the tensor memory
+// accelerator: per warp tile one elected lane issues bulk tensor copies of
+// 32 rows x 128 bytes (the lanes' slices, two boxes per tile) with the
+// 128-byte swizzle, which leaves each lane's 16-byte chunk j of a box row
+// at chunk j xor (lane mod 8), so the lanes' 128-bit reads are free of bank
+// conflicts; an mbarrier per warp counts the bytes in.  Every wait is
+// bounded: on giving up the warp counts the event in g_wait_timeouts
+// (fp4_wait_timeouts() reads it) and returns.
+
+__device__ unsigned long long g_wait_timeouts;
+
+constexpr uint32_t kWaitSpins = 1u << 22;  // try_wait rounds before giving up
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Box {x, y} of the 2-D tensor map into shared memory at dst; its bytes
+// complete on mbarrier bar.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// Lane's P pieces of a TMA-staged tile in the slot at byte address slot
+// (1024-byte aligned): piece q is chunk q mod 8 of row `lane` of box q / 8.
+template <int P>
+__device__ __forceinline__ void tma_read(uint32_t slot, int lane, uint4 v[P]) {
+  const uint32_t a = slot + 128u * (uint32_t)lane + 16u * (uint32_t)(lane & 7);
+#pragma unroll
+  for (int q = 0; q < P; ++q)
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v[q].x), "=r"(v[q].y), "=r"(v[q].z), "=r"(v[q].w)
+                 : "r"((a + 4096u * (uint32_t)(q >> 3)) ^ (16u * (uint32_t)(q & 7)))
+                 : "memory");
+}
+
 // ------------------------------------------------------------------ encode
 //
 // Each lane holds whole chunk pairs of its group: 64 elements (G = 64 and
@@ -297,8 +357,17 @@ struct EncSmem {
   static constexpr int P = Wide<G>::EPL * (kBF16 ? 2 : 4) / 16;
   static constexpr int kSlot = 32 * 16 * P;
   static constexpr int kTile = WideTile<G>::kBytes;
-  static constexpr size_t kSmem = (size_t)EncThreads<G>::W * (kSlot + kTile);
+  // slots, transpose tiles, one mbarrier per warp, and room to align the
+  // slots to 1024 bytes (the 128-byte swizzle's period)
+  static constexpr size_t kSmem = (size_t)EncThreads<G>::W * (kSlot + kTile + 8) + 1024;
 };
+
+// TMA staging for the bf16 G = 128 encode (measured faster there; the
+// cp.async ring was as fast or faster for the other groups and for fp32).
+template <int G, bool kBF16>
+constexpr bool enc_tma() {
+  return G == 128 && kBF16;
+}
 
 // The lane's chunk pairs from its staged pieces: chunk c's 32 elements are
 // pieces 4c .. 4c + 3 (bf16) or 8c .. 8c + 7 (fp32).
@@ -398,39 +467,78 @@ __device__ __forceinline__ float group_max(float v) {
 // past the end compute on zeros and store nothing (the slice count is a
 // multiple of L, so a group is entirely inside or entirely past the end).
 // Tile indices are 32-bit (the entry point admits fewer than 2^40 elements).
-template <int G, bool kBF16>
+// kTma: the input is staged by TMA through tmap (see above), else by the
+// cp.async ring from x.
+template <int G, bool kBF16, bool kTma>
 __global__ void __launch_bounds__(EncThreads<G>::N, Wide<G>::EPL == 128 ? 1 : 2)
-    encode_kernel(const void* __restrict__ x, int64_t nslices, uint8_t* __restrict__ packed,
-                  float* __restrict__ s1_out, float* __restrict__ s2_out, float nz) {
+    encode_kernel(const __grid_constant__ CUtensorMap tmap, const void* __restrict__ x,
+                  int64_t nslices, uint8_t* __restrict__ packed, float* __restrict__ s1_out,
+                  float* __restrict__ s2_out, float nz) {
   using W = Wide<G>;
   using M = EncSmem<G, kBF16>;
   constexpr int NP = W::NP, L = W::L, B = W::B, P = M::P, NR = 32 * NP;
-  extern __shared__ __align__(512) uint8_t enc_smem[];
+  extern __shared__ __align__(1024) uint8_t enc_smem_raw[];
+  uint8_t* const enc_smem =
+      enc_smem_raw +
+      ((1024u - ((uint32_t)__cvta_generic_to_shared(enc_smem_raw) & 1023u)) & 1023u);
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const uint32_t slot =
       (uint32_t)__cvta_generic_to_shared(enc_smem) + (uint32_t)(wid * M::kSlot);
   float4* const tile =
       reinterpret_cast<float4*>(enc_smem + EncThreads<G>::W * M::kSlot + wid * M::kTile);
+  const uint32_t bar = (uint32_t)__cvta_generic_to_shared(
+      enc_smem + EncThreads<G>::W * (M::kSlot + M::kTile) + 8 * wid);
+  constexpr int KB = P / 8;                   // TMA boxes (4 KB) per tile
+  constexpr int BX = 128 / (kBF16 ? 2 : 4);   // elements per box row
   const int ntiles = (int)((nslices + 31) >> 5), nfull = (int)(nslices >> 5);
   const int rem = (int)(nslices & 31);
   const int tstride = (int)gridDim.x * EncThreads<G>::W;
   const int64_t step = (int64_t)tstride * M::kSlot;  // input bytes between a warp's tiles
   int t = (int)blockIdx.x * EncThreads<G>::W + wid;
   const uint8_t* src = static_cast<const uint8_t*>(x) + (int64_t)t * M::kSlot;
+  if (kTma) {
+    if (lane == 0) {
+      mbar_init(bar, 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+  }
   auto stage = [&](int tt, const uint8_t* s) {
-    if (tt < nfull)
-      ring_copy_full<P>(slot, s + 16 * lane, lane);
-    else if (tt < ntiles)
-      ring_copy<P>(slot, s, (nslices - 32 * (int64_t)tt) * (16 * P), lane);
-    cp_async_commit();
+    if (kTma) {
+      // rows past nslices arrive as zeros
+      if (tt < ntiles && lane == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_expect_tx(bar, KB * 4096);
+#pragma unroll
+        for (int b = 0; b < KB; ++b) tma_load_2d(slot + 4096u * b, &tmap, b * BX, 32 * tt, bar);
+      }
+    } else {
+      if (tt < nfull)
+        ring_copy_full<P>(slot, s + 16 * lane, lane);
+      else if (tt < ntiles)
+        ring_copy<P>(slot, s, (nslices - 32 * (int64_t)tt) * (16 * P), lane);
+      cp_async_commit();
+    }
   };
   const F2 nz2{nz, nz};
+  uint32_t phase = 0;
   stage(t, src);
   for (; t < ntiles; t += tstride, src += step) {
-    cp_async_wait<0>();
-    __syncwarp();
     uint4 v[P];
-    ring_read<P>(slot, lane, v);
+    if (kTma) {
+      for (uint32_t spins = 0; !mbar_try_wait(bar, phase);) {
+        if (++spins > kWaitSpins) {
+          if (lane == 0) atomicAdd(&g_wait_timeouts, 1ull);
+          return;
+        }
+      }
+      phase ^= 1u;
+      tma_read<P>(slot, lane, v);
+    } else {
+      cp_async_wait<0>();
+      __syncwarp();
+      ring_read<P>(slot, lane, v);
+    }
     __syncwarp();  // every lane's reads of the slot before its next copy
     stage(t + tstride, src + step);
     WideRow<G> y;
@@ -720,15 +828,61 @@ __global__ void __launch_bounds__(kThreads, (kBF16Out && G == 256) ? 4 : 1)
   cp_async_wait<0>();
 }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled from the driver (looked up once), or null.
+EncodeTiledFn encode_tiled_fn() {
+  static const EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+// The encode's input as a 2-D tensor for TMA: nslices rows of P 16-byte
+// pieces, read in boxes of 32 rows x 128 bytes with the 128-byte swizzle.
+template <bool kBF16, int P>
+bool encode_tensor_map(CUtensorMap* m, const void* x, int64_t nslices) {
+  const EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return false;
+  constexpr int esize = kBF16 ? 2 : 4;
+  const cuuint64_t gdim[2] = {(cuuint64_t)P * 16 / esize, (cuuint64_t)nslices};
+  const cuuint64_t gstride[1] = {(cuuint64_t)P * 16};
+  const cuuint32_t box[2] = {128 / esize, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+             const_cast<void*>(x), gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int G, bool kBF16>
 fp4_status launch_encode_t(const void* x, int64_t nchunks, uint8_t* packed, float* s1, float* s2,
                            cudaStream_t s) {
   constexpr size_t smem = EncSmem<G, kBF16>::kSmem;
   static_assert(smem <= 227 * 1024, "one CTA's shared memory must fit an SM");
-  if (!allow_dynamic_smem<encode_kernel<G, kBF16>>(smem)) return FP4_ERR_CUDA;
   const int64_t nslices = nchunks / (Wide<G>::EPL / kE);
-  return launch<encode_kernel<G, kBF16>>(nslices, EncThreads<G>::N, smem, s, x, nslices, packed,
-                                         s1, s2, -0.0f);
+  alignas(64) CUtensorMap m = {};
+  if constexpr (enc_tma<G, kBF16>()) {
+    // TMA row coordinates are 32-bit: past 2^31 slices the cp.async ring stages
+    if (nslices < ((int64_t)1 << 31)) {
+      if (!allow_dynamic_smem<encode_kernel<G, kBF16, true>>(smem)) return FP4_ERR_CUDA;
+      if (!encode_tensor_map<kBF16, EncSmem<G, kBF16>::P>(&m, x, nslices)) return FP4_ERR_CUDA;
+      return launch<encode_kernel<G, kBF16, true>>(nslices, EncThreads<G>::N, smem, s, m, x,
+                                                   nslices, packed, s1, s2, -0.0f);
+    }
+  }
+  if (!allow_dynamic_smem<encode_kernel<G, kBF16, false>>(smem)) return FP4_ERR_CUDA;
+  return launch<encode_kernel<G, kBF16, false>>(nslices, EncThreads<G>::N, smem, s, m, x,
+                                                nslices, packed, s1, s2, -0.0f);
 }
 
 template <int G>
@@ -763,6 +917,12 @@ bool group_ok(int g) { return g == 64 || g == 128 || g == 256; }
 using namespace fp4;
 
 extern "C" {
+
+uint64_t fp4_wait_timeouts(void) {
+  unsigned long long v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_wait_timeouts, sizeof(v)) != cudaSuccess) return UINT64_MAX;
+  return (uint64_t)v;
+}
 
 fp4_status fp4quant_encode(const void* x, int dtype, int64_t rows, int64_t cols, int group,
                            uint8_t* packed, float* s1, float* s2, void* stream) {

@@ -67,6 +67,13 @@ const char* fp4_status_string(int status);
 int fp4_abi_version(void);
 /* Number of kernels this library has launched in this process. */
 uint64_t fp4_kernel_launches(void);
+/* Number of bounded waits in this library's kernels that gave up, on the
+ * current device, since the library was loaded (the FP4Quant encode's waits
+ * for its TMA copies).  0 in a healthy run; a warp that gives up skips the
+ * rest of its work, so after a nonzero value the outputs of the launches
+ * since the last read are not to be trusted.  Synchronizes with the device;
+ * UINT64_MAX if the read fails. */
+uint64_t fp4_wait_timeouts(void);
 
 /* ------------------------------------------------------------------ NVFP4
  * [fp4-train] "How it works": 16-element blocks, block scale block_absmax / 6

@@ -34,6 +34,7 @@ def test_header_declares_the_boundary():
                  "fp4_to_fp8_col_runs",
                  "fp4_seg_scale_offsets", "fp4quant_encode", "fp4quant_decode",
                  "fp4_status_string", "fp4_abi_version", "fp4_kernel_launches",
+                 "fp4_wait_timeouts",
                  "fp4_blocked_scales_size", "fp4_scales_to_blocked", "fp4_scales_from_blocked",
                  "nvfp4_quantize_blocked"]:
         assert want in names, want

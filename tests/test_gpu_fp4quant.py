@@ -109,3 +109,30 @@ def test_groups_at_the_fp32_range_ends(G, out_dtype):
         assert_bits_equal(bf16_bits(y)[~nan], ora.bf16_rn(wy)[~nan], "decoded bf16")
     else:
         assert_bits_equal(got[~nan], wy[~nan], "decoded f32")
+
+
+@pytest.mark.parametrize("G", [64, 128, 256])
+@pytest.mark.parametrize("offset", [16, 1040])
+def test_encode_input_inside_a_larger_buffer(G, offset):
+    """The input as a view that starts `offset` bf16 elements (32 and 2080
+    bytes) into a larger device buffer, with a ragged last tile: the G = 128
+    bf16 encode reads it by TMA through a tensor map built on that address,
+    the others by cp.async."""
+    m = fp4()
+    rows, cols = 45, 1024
+    flat = workloads.fp4quant_acts(seed=offset, tokens=rows + 3, hidden=cols,
+                                   device="cpu").to(torch.bfloat16).reshape(-1)
+    d = flat.to(dev())
+    x = d[offset:offset + rows * cols].view(rows, cols)
+    assert x.data_ptr() % 32 == 0
+    packed, s1, s2 = m.fp4quant_encode(x, G)
+    wp, w1, w2 = ora.fp4quant_encode(to_f32_np(flat[offset:offset + rows * cols].view(rows, cols)), G)
+    assert_bits_equal(to_f32_np(s1), w1, "s1")
+    assert_bits_equal(to_f32_np(s2), w2, "s2")
+    assert_bits_equal(u8(packed), wp, "packed")
+
+
+def test_no_bounded_wait_gave_up():
+    """No bounded wait in the library's kernels (the encode's TMA waits) gave
+    up during the tests above."""
+    assert fp4().wait_timeouts() == 0
