@@ -25,6 +25,7 @@ SIGNATURES = {
     "fp4_abi_version": (INT, []),
     "fp4_kernel_launches": (U64, []),
     "fp4_wait_timeouts": (U64, []),
+    "fp4_test_encode_wait_timeout": (INT, [P, I64, I64, P, P, P, P]),
     "nvfp4_amax": (INT, [P, INT, I64, P, P, P]),
     "nvfp4_quantize": (INT, [P, INT, I64, P, INT, U64, U64, INT, P, P, P, P, P]),
     "nvfp4_dequantize": (INT, [P, P, P, I64, P, INT, P]),

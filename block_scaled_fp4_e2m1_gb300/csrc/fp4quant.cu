@@ -255,7 +255,7 @@ __device__ __forceinline__ float bf16_hi_(uint32_t w) { return __uint_as_float(w
 
 __device__ unsigned long long g_wait_timeouts;
 
-constexpr uint32_t kWaitSpins = 1u << 22;  // try_wait rounds before giving up
+constexpr uint32_t kWaitSpins = 1u << 18;  // try_wait rounds before giving up (about 1 s)
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -468,12 +468,13 @@ __device__ __forceinline__ float group_max(float v) {
 // multiple of L, so a group is entirely inside or entirely past the end).
 // Tile indices are 32-bit (the entry point admits fewer than 2^40 elements).
 // kTma: the input is staged by TMA through tmap (see above), else by the
-// cp.async ring from x.
+// cp.async ring from x.  tx_extra is 0 but for the wait test hook
+// (fp4_test_encode_wait_timeout), whose waits never complete.
 template <int G, bool kBF16, bool kTma>
 __global__ void __launch_bounds__(EncThreads<G>::N, Wide<G>::EPL == 128 ? 1 : 2)
     encode_kernel(const __grid_constant__ CUtensorMap tmap, const void* __restrict__ x,
                   int64_t nslices, uint8_t* __restrict__ packed, float* __restrict__ s1_out,
-                  float* __restrict__ s2_out, float nz) {
+                  float* __restrict__ s2_out, float nz, uint32_t tx_extra) {
   using W = Wide<G>;
   using M = EncSmem<G, kBF16>;
   constexpr int NP = W::NP, L = W::L, B = W::B, P = M::P, NR = 32 * NP;
@@ -508,7 +509,7 @@ __global__ void __launch_bounds__(EncThreads<G>::N, Wide<G>::EPL == 128 ? 1 : 2)
       // rows past nslices arrive as zeros
       if (tt < ntiles && lane == 0) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_expect_tx(bar, KB * 4096);
+        mbar_expect_tx(bar, KB * 4096 + tx_extra);
 #pragma unroll
         for (int b = 0; b < KB; ++b) tma_load_2d(slot + 4096u * b, &tmap, b * BX, 32 * tt, bar);
       }
@@ -866,7 +867,7 @@ bool encode_tensor_map(CUtensorMap* m, const void* x, int64_t nslices) {
 
 template <int G, bool kBF16>
 fp4_status launch_encode_t(const void* x, int64_t nchunks, uint8_t* packed, float* s1, float* s2,
-                           cudaStream_t s) {
+                           cudaStream_t s, uint32_t tx_extra = 0) {
   constexpr size_t smem = EncSmem<G, kBF16>::kSmem;
   static_assert(smem <= 227 * 1024, "one CTA's shared memory must fit an SM");
   const int64_t nslices = nchunks / (Wide<G>::EPL / kE);
@@ -877,12 +878,13 @@ fp4_status launch_encode_t(const void* x, int64_t nchunks, uint8_t* packed, floa
       if (!allow_dynamic_smem<encode_kernel<G, kBF16, true>>(smem)) return FP4_ERR_CUDA;
       if (!encode_tensor_map<kBF16, EncSmem<G, kBF16>::P>(&m, x, nslices)) return FP4_ERR_CUDA;
       return launch<encode_kernel<G, kBF16, true>>(nslices, EncThreads<G>::N, smem, s, m, x,
-                                                   nslices, packed, s1, s2, -0.0f);
+                                                   nslices, packed, s1, s2, -0.0f, tx_extra);
     }
   }
   if (!allow_dynamic_smem<encode_kernel<G, kBF16, false>>(smem)) return FP4_ERR_CUDA;
+  if (tx_extra != 0) return FP4_ERR_ARG;  // only the TMA path has the waits
   return launch<encode_kernel<G, kBF16, false>>(nslices, EncThreads<G>::N, smem, s, m, x,
-                                                nslices, packed, s1, s2, -0.0f);
+                                                nslices, packed, s1, s2, -0.0f, 0u);
 }
 
 template <int G>
@@ -917,6 +919,16 @@ bool group_ok(int g) { return g == 64 || g == 128 || g == 256; }
 using namespace fp4;
 
 extern "C" {
+
+fp4_status fp4_test_encode_wait_timeout(const void* x, int64_t rows, int64_t cols,
+                                        uint8_t* packed, float* s1, float* s2, void* stream) {
+  if (rows <= 0 || cols <= 0 || cols % 128 != 0 || rows > ((int64_t)1 << 24) / cols)
+    return FP4_ERR_SHAPE;
+  if (!x || !packed || !s1 || !s2) return FP4_ERR_NULL;
+  if (!aligned(x, 32) || !aligned(packed, 16) || !aligned(s1, 4) || !aligned(s2, 4))
+    return FP4_ERR_ALIGN;
+  return launch_encode_t<128, true>(x, rows * cols / kE, packed, s1, s2, as_stream(stream), 16u);
+}
 
 uint64_t fp4_wait_timeouts(void) {
   unsigned long long v = 0;

@@ -74,6 +74,14 @@ uint64_t fp4_kernel_launches(void);
  * since the last read are not to be trusted.  Synchronizes with the device;
  * UINT64_MAX if the read fails. */
 uint64_t fp4_wait_timeouts(void);
+/* Test hook for the bounded waits: the bf16 G = 128 FP4Quant encode of x
+ * [rows, cols] (cols % 128 == 0, at most 2^24 elements) with its TMA copies
+ * announced 16 bytes longer than they are, so no wait completes: every warp
+ * that has a tile gives up after its wait limit (about a second), adds 1 to
+ * fp4_wait_timeouts() and returns without writing its outputs.  The context
+ * stays usable.  Errors as fp4quant_encode. */
+fp4_status fp4_test_encode_wait_timeout(const void* x, int64_t rows, int64_t cols,
+                                        uint8_t* packed, float* s1, float* s2, void* stream);
 
 /* ------------------------------------------------------------------ NVFP4
  * [fp4-train] "How it works": 16-element blocks, block scale block_absmax / 6

@@ -34,7 +34,7 @@ def test_header_declares_the_boundary():
                  "fp4_to_fp8_col_runs",
                  "fp4_seg_scale_offsets", "fp4quant_encode", "fp4quant_decode",
                  "fp4_status_string", "fp4_abi_version", "fp4_kernel_launches",
-                 "fp4_wait_timeouts",
+                 "fp4_wait_timeouts", "fp4_test_encode_wait_timeout",
                  "fp4_blocked_scales_size", "fp4_scales_to_blocked", "fp4_scales_from_blocked",
                  "nvfp4_quantize_blocked"]:
         assert want in names, want
@@ -132,6 +132,11 @@ def test_mx_fp8_fp4quant_argument_checks(L):
     assert col(A, A, 128, None, A, 2, 10, 2, A, A, None) == 1
     assert col(A, A, 128, A, A, 2, 10, 5, A, A, None) == 3       # too many blocks
     assert col(A, A, 128, A + 4, A, 2, 10, 2, A, A, None) == 2
+    hook = L.fp4_test_encode_wait_timeout
+    assert hook(A, 2, 192, A, A, A, None) == 3                   # cols % 128
+    assert hook(A, 1 << 20, 128, A, A, A, None) == 3             # above 2^24 elements
+    assert hook(A, 2, 256, None, A, A, None) == 1
+    assert hook(MIS, 2, 256, A, A, A, None) == 2
     runs = L.fp4_to_fp8_col_runs
     assert runs(A, A, 128, A, A, 2, 10, 2, -1, A, A, None) == 3      # run_blocks < 0
     assert runs(A, A, 128, A, A, 2, 10, 2, (1 << 20) + 1, A, A, None) == 3

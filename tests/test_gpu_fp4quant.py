@@ -136,3 +136,27 @@ def test_no_bounded_wait_gave_up():
     """No bounded wait in the library's kernels (the encode's TMA waits) gave
     up during the tests above."""
     assert fp4().wait_timeouts() == 0
+
+
+@pytest.mark.timeout(120)
+def test_bounded_wait_gives_up_and_the_context_survives():
+    """The test hook announces the TMA copies of a one-tile bf16 G = 128
+    encode 16 bytes longer than they are, so its one warp's wait never
+    completes: the warp gives up after its limit, the timeout count grows by
+    exactly one, and the next ordinary encode on the same context is exact."""
+    from block_scaled_fp4_e2m1_gb300 import _lib
+    m = fp4()
+    x = workloads.fp4quant_acts(seed=5, tokens=2, hidden=256, device="cpu").to(torch.bfloat16)
+    xd = x.to(dev())
+    packed = torch.zeros(2 * 128, dtype=torch.uint8, device=dev())
+    s1 = torch.zeros(4, dtype=torch.float32, device=dev())
+    s2 = torch.zeros(4, dtype=torch.float32, device=dev())
+    before = m.wait_timeouts()
+    rc = _lib.lib().fp4_test_encode_wait_timeout(xd.data_ptr(), 2, 256, packed.data_ptr(),
+                                                 s1.data_ptr(), s2.data_ptr(),
+                                                 torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert m.wait_timeouts() == before + 1
+    _check(x, 128)
+    assert m.wait_timeouts() == before + 1
