@@ -146,6 +146,16 @@ def test_column_conversion_rejects(calls):
     _raises(calls, codec.fp4_to_fp8_col, pk, sc, segs, fp8_t=z(128 * 300 - 1, U8))
     _raises(calls, codec.fp4_to_fp8_col, pk, sc, segs,
             fp8_t_scales=z(128 * segs.total_blocks, BF16))
+    _raises(calls, codec.fp4_to_fp8_col, pk, sc, segs, run_blocks=-1)
+    _raises(calls, codec.fp4_to_fp8_col, pk, sc, segs, run_blocks=(1 << 20) + 1)
+
+
+def test_column_conversion_run_length_picks_the_entry_point(calls):
+    pk, sc = z(300 * 64, U8).view(300, 64), z(300 * 4, U8)
+    segs = codec.Segments(torch.tensor([0, 100, 300]), "cpu")
+    codec.fp4_to_fp8_col(pk, sc, segs)
+    codec.fp4_to_fp8_col(pk, sc, segs, run_blocks=7)
+    assert calls == ["fp4_to_fp8_col", "fp4_to_fp8_col_runs"]
 
 
 def test_fp4quant_rejects(calls):
