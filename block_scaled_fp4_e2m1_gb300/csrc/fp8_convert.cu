@@ -311,13 +311,18 @@ __device__ __forceinline__ void col_stage(uint8_t* stg, const uint8_t* __restric
   const int64_t t0 = 128 * (fb - p.sofs);
   const int nv = p.n_e - t0 < 128 ? (int)(p.n_e - t0) : 128;
   const int64_t r0 = p.row0 + t0;
+  // copy k moves token tb + 32 k, chunk q: one base address plus k steps
+  const int tb = (int)threadIdx.x >> 3, q = (int)threadIdx.x & 7;
+  const uint8_t* src0 = packed + (r0 + tb) * row_bytes + 16 * (kColGroup * grp + q);
+  const int64_t src_step = 32 * row_bytes;
+  uint8_t* const dst0 = stg + 128 * tb + 16 * (q ^ (tb >> 3));
+  uint8_t* const dst1 = stg + 128 * tb + 16 * (q ^ (tb >> 3) ^ 4);
+  const bool qok = q < nkb;
 #pragma unroll
   for (int k = 0; k < 128 * kColGroup / kColThreads; ++k) {
-    const int idx = (int)threadIdx.x + kColThreads * k;
-    const int t = idx >> 3, q = idx & 7;
-    const bool ok = t < nv && q < nkb;
-    const uint8_t* src = ok ? packed + (r0 + t) * row_bytes + 16 * (kColGroup * grp + q) : packed;
-    cp_async_zfill<16>(stg + 128 * t + 16 * (q ^ ((t >> 3) & 7)), src, ok ? 16 : 0);
+    const bool ok = tb + 32 * k < nv && qok;
+    cp_async_zfill<16>((k & 1 ? dst1 : dst0) + 4096 * k, ok ? src0 + k * src_step : packed,
+                       ok ? 16 : 0);
   }
   {
     // thread (i, g, h) = (tid >> 5, (tid >> 1) & 15, tid & 1): token 8g + i,
