@@ -261,21 +261,21 @@ __device__ __forceinline__ void store_bytes(uint8_t* dst, const uint4* row, int 
 // The segment holding a token block, walked forward block by block.
 struct SegPos {
   int e;
-  int64_t sofs, send;  // its blocks: [sofs, send)
+  int sofs, send;      // its blocks: [sofs, send) (block indices < 2^31)
   int64_t row0, n_e;   // its rows
 };
 
 __device__ __forceinline__ void seg_load(SegPos& p, const int64_t* __restrict__ row_off,
                                          const int64_t* __restrict__ scale_off) {
-  p.sofs = scale_off[p.e];
-  p.send = scale_off[p.e + 1];
+  p.sofs = (int)scale_off[p.e];
+  p.send = (int)scale_off[p.e + 1];
   p.row0 = row_off[p.e];
   p.n_e = row_off[p.e + 1] - p.row0;
 }
 
 // Moves p forward to the segment holding block fb (warp-uniform); false if
 // the offsets end before fb.
-__device__ __forceinline__ bool seg_advance(SegPos& p, int64_t fb, int nseg,
+__device__ __forceinline__ bool seg_advance(SegPos& p, int fb, int nseg,
                                             const int64_t* __restrict__ row_off,
                                             const int64_t* __restrict__ scale_off) {
   while (fb >= p.send && p.e + 1 < nseg) {
@@ -306,9 +306,9 @@ __device__ __forceinline__ void cp_async_zfill(void* smem, const void* gmem, int
 // blocks are zero.
 __device__ __forceinline__ void col_stage(uint8_t* stg, const uint8_t* __restrict__ packed,
                                           const uint8_t* __restrict__ scales, const SegPos& p,
-                                          int64_t fb, int64_t row_bytes, int64_t kblocks, int grp,
+                                          int fb, int64_t row_bytes, int64_t kblocks, int grp,
                                           int nkb) {
-  const int64_t t0 = 128 * (fb - p.sofs);
+  const int64_t t0 = 128 * (int64_t)(fb - p.sofs);
   const int nv = p.n_e - t0 < 128 ? (int)(p.n_e - t0) : 128;
   const int64_t r0 = p.row0 + t0;
   // copy k moves token tb + 32 k, chunk q: one base address plus k steps
@@ -504,8 +504,8 @@ __device__ __forceinline__ void col_store_short(uint8_t* lin, const uint32_t* ti
 }
 
 // Block converted by item `it` of a unit (see the kernel).
-__device__ __forceinline__ int64_t col_item_block(int64_t it, int npre, bool pre_head,
-                                                  const SegPos& p0, int64_t fb0) {
+__device__ __forceinline__ int col_item_block(int it, int npre, bool pre_head,
+                                              const SegPos& p0, int fb0) {
   if (it < npre) return (pre_head && it == 0) ? p0.sofs : fb0 - 1;
   return fb0 + (it - npre);
 }
@@ -513,11 +513,11 @@ __device__ __forceinline__ int64_t col_item_block(int64_t it, int npre, bool pre
 // Stages item `it` into stage it & 1 (nothing past the run or the offsets)
 // and commits its cp.async group; ps follows the staged blocks' segments.
 __device__ __forceinline__ void col_stage_item(
-    int64_t it, int npre, bool pre_head, const SegPos& p0, SegPos& ps, int64_t fb0, int64_t fb1,
+    int it, int npre, bool pre_head, const SegPos& p0, SegPos& ps, int fb0, int fb1,
     uint8_t* stages, const uint8_t* __restrict__ packed, const uint8_t* __restrict__ scales,
     int64_t row_bytes, int64_t kblocks, int grp, int nkb, int nseg,
     const int64_t* __restrict__ row_off, const int64_t* __restrict__ scale_off) {
-  const int64_t fb = col_item_block(it, npre, pre_head, p0, fb0);
+  const int fb = col_item_block(it, npre, pre_head, p0, fb0);
   bool ok = fb < fb1;
   if (ok && it >= npre) ok = seg_advance(ps, fb, nseg, row_off, scale_off);
   if (ok)
@@ -573,13 +573,14 @@ __global__ void __launch_bounds__(kColThreads)
                                                                 : kColGroup);
     const int kb = kColGroup * grp + wid;
     const bool active = wid < nkb;
-    const int64_t fb0 = run * run_len;
-    const int64_t fb1 = fb0 + run_len < total_blocks ? fb0 + run_len : total_blocks;
+    const int fb0 = (int)(run * run_len);
+    const int fb1 = (int)(run * run_len + run_len < total_blocks ? run * run_len + run_len
+                                                                 : total_blocks);
     SegPos p0;
     p0.e = find_segment(seg_scale_off, nseg, fb0);
     seg_load(p0, seg_row_off, seg_scale_off);
     if (!seg_advance(p0, fb0, nseg, seg_row_off, seg_scale_off)) continue;
-    const int64_t blo = fb0 - p0.sofs;  // the run's first block inside its first segment
+    const int blo = fb0 - p0.sofs;  // the run's first block inside its first segment
     const bool pre_head = blo > 1 && p0.send <= fb1 && p0.n_e >= 32;
     const int npre = (pre_head ? 1 : 0) + (blo > 0 ? 1 : 0);
     // item it converts block item_block(it) (items < npre are in segment p0)
@@ -587,17 +588,17 @@ __global__ void __launch_bounds__(kColThreads)
     col_stage_item(0, npre, pre_head, p0, ps, fb0, fb1, stages, packed, scales, row_bytes, kblocks,
                    grp, nkb, nseg, seg_row_off, seg_scale_off);
     SegPos p = p0;
-    for (int64_t it = 0;; ++it) {
+    for (int it = 0;; ++it) {
       cp_async_wait<0>();
       __syncthreads();  // block it is staged; block it - 1 is read
       col_stage_item(it + 1, npre, pre_head, p0, ps, fb0, fb1, stages, packed, scales, row_bytes,
                      kblocks, grp, nkb, nseg, seg_row_off, seg_scale_off);
       const bool real = it >= npre;
-      const int64_t fb = col_item_block(it, npre, pre_head, p0, fb0);
+      const int fb = col_item_block(it, npre, pre_head, p0, fb0);
       if (real && !seg_advance(p, fb, nseg, seg_row_off, seg_scale_off)) break;
       const SegPos sp = real ? p : p0;
-      const int64_t b = fb - sp.sofs;
-      const int64_t t0 = 128 * b;
+      const int b = fb - sp.sofs;
+      const int64_t t0 = 128 * (int64_t)b;
       const int nv = sp.n_e - t0 < 128 ? (int)(sp.n_e - t0) : 128;
       const bool first = b == 0, last = fb + 1 == sp.send;
       const uint8_t* const stg = stages + (it & 1) * kStageBytes;
@@ -605,7 +606,7 @@ __global__ void __launch_bounds__(kColThreads)
         const uint32_t st = col_convert(stg, wid, g, c, lane, first && sp.n_e >= 32, lut2, tile,
                                         heads);
         if (real)
-          fp8_t_scales[cols * sp.sofs + (32 * kb + lane) * (sp.send - sp.sofs) + b] =
+          fp8_t_scales[cols * sp.sofs + (int64_t)(32 * kb + lane) * (sp.send - sp.sofs) + b] =
               ue8m0_to_f32(st);
       }
       if (real && sp.n_e < 32) {
@@ -681,7 +682,8 @@ fp4_status fp4_to_fp8_col_runs(const uint8_t* packed, const uint8_t* scales, int
   if (cols < 0 || cols % 128 != 0 || num_segments < 0 || total_rows < 0 || total_blocks < 0 ||
       run_blocks < 0 || run_blocks > kColRunLimit)
     return FP4_ERR_SHAPE;
-  if (total_blocks > total_rows / 128 + num_segments) return FP4_ERR_SHAPE;
+  if (total_blocks > total_rows / 128 + num_segments || total_blocks >= ((int64_t)1 << 31))
+    return FP4_ERR_SHAPE;
   if (!seg_row_off || !seg_scale_off) return FP4_ERR_NULL;
   const int64_t ntiles = total_blocks * (cols / 128);
   if (ntiles > 0 && (!packed || !scales || !fp8_t || !fp8_t_scales)) return FP4_ERR_NULL;

@@ -387,7 +387,8 @@ fp4_status fp4_to_fp8_row(const uint8_t* packed, const uint8_t* scales, int64_t 
  * (<= 128) tokens for feature block k/32.
  *   packed [total_rows, cols/2], scales [total_rows, cols/32] (as the row form)
  *   seg_row_off, seg_scale_off  device int64 [num_segments + 1]
- *   total_blocks  = seg_scale_off[num_segments] (host copy, sizes the grid)
+ *   total_blocks  = seg_scale_off[num_segments] (host copy, sizes the grid),
+ *                   below 2^31
  *   cols % 128 == 0.  Offsets are trusted: the device reads them as given.
  * Alignment: packed 32 bytes, scales and fp8_t_scales 4, the offsets 8;
  * fp8_t may start at any byte (the kernel stores whole 32-byte sectors and

@@ -131,6 +131,7 @@ def test_mx_fp8_fp4quant_argument_checks(L):
     assert col(A, A, 96, A, A, 2, 10, 2, A, A, None) == 3
     assert col(A, A, 128, None, A, 2, 10, 2, A, A, None) == 1
     assert col(A, A, 128, A, A, 2, 10, 5, A, A, None) == 3       # too many blocks
+    assert col(A, A, 128, A, A, 2, 1 << 40, 1 << 31, A, A, None) == 3  # 2^31 blocks
     assert col(A, A, 128, A + 4, A, 2, 10, 2, A, A, None) == 2
     hook = L.fp4_test_encode_wait_timeout
     assert hook(A, 2, 192, A, A, A, None) == 3                   # cols % 128
