@@ -159,6 +159,8 @@ __global__ void __launch_bounds__(kRowThreads)
 // (col_store_short).
 // One CTA barrier per token block publishes a stage and frees the one read
 // before; a segment of one block adds one between its heads and merges.
+// Token-block indices are 32-bit (the host admits fewer than 2^31 blocks);
+// row offsets stay 64-bit.
 
 constexpr int kColThreads = 256;
 constexpr int kColGroup = kColThreads / 32;  // feature blocks per CTA: one per warp
